@@ -1,0 +1,430 @@
+#!/usr/bin/env python3
+"""Throughput of exact causal attention forward on GB300: bf16, B=1 H=12 N=8192 d=64.
+
+One step is one ``attn_fwd`` call over the whole batch (all 12 heads, every query tile): the
+tcgen05 online-softmax kernel, inputs already resident in device memory. The metric is
+TFLOP/s under the attention pages' convention, 4 * B * H * N^2 * d halved for causal
+("Flash attention in PyTorch, then in Triton", section "Attention by hand": two products,
+two operations each, half of the table masked away).
+
+Timing: W untimed warm-up steps, then exactly K steps between a barrier and a device
+synchronise on both sides. The inputs (50 MB) fit in L2, so a 256 MiB buffer is written
+between steps to flush it; CUDA events on the launching stream bracket each attention
+launch only, and ms_per_step is their mean. SM clocks and clock-event reasons are sampled
+through NVML while the steps run. ``e2e`` repeats the measurement through the same public
+call with pinned host buffers: the host-to-device copy of q, k, v, the kernel and the
+device-to-host copy of o inside each timed step.
+
+Multi-GPU: every rank runs the same workload on its own GPU (independent replicas, weak
+scaling; the path has no exchange step), and rank 0 reports the aggregate over ranks with
+the slowest rank's time. Barrier and max use a gloo group on the host.
+
+``--impl reference`` times the CPU oracle (double precision, all host cores) on the same
+workload instead, each step a bounded sample of query rows, and prints the same line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal attn fwd TFLOP/s, bf16 B1 H12 N8192 d64; % of tensor-core peak"
+UNIT = "TFLOP/s"
+WORKLOAD = {"workload": "causal attention forward, bf16 in/out, fp32 accumulate, B1 H12 N8192 d64",
+            "B": 1, "H": 12, "N": 8192, "d": 64, "causal": True, "dtype": "bf16"}
+SEED = 0xA77E0003
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+L2_FLUSH_BYTES = 256 << 20
+TC_SOURCE = os.path.join(ROOT, "online_softmax_flashattention_gb300", "csrc", "attn_tc.cu")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_tc_bf16_causal_B1H12N8192.md")
+
+
+def workload_flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def row_flops(rows_i, d, N, causal):
+    """Exact flops of a set of query rows: 4 d per visible key (QK^T and PV, mul + add)."""
+    vis = (np.asarray(rows_i, dtype=np.int64) + 1) if causal else np.full(len(rows_i), N)
+    return float(4.0 * d * vis.sum())
+
+
+# ----------------------------------------------------------------------------- peaks, traffic
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return {"bf16_tflops": float(j["bf16_tflops"]), "hbm_gbs": float(j["hbm_gbs"])}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha256():
+    with open(TC_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    try:
+        text = open(TRAFFIC_PROFILE).read()
+    except OSError:
+        return None, "no ncu summary"
+    m_t = re.search(r"^traffic_bytes_per_launch:\s*(\d+)", text, re.M)
+    m_h = re.search(r"^source_sha256:\s*([0-9a-f]{64})", text, re.M)
+    if not m_t or not m_h:
+        return None, "summary lacks traffic or source hash"
+    if m_h.group(1) != source_sha256():
+        return None, "kernel changed since the ncu capture"
+    return int(m_t.group(1)), "ncu capture of this source"
+
+
+# ----------------------------------------------------------------------------- clocks (NVML)
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+            0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+            0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """Reads SM clock and clock-event reasons through NVML every few ms (read-only)."""
+
+    def __init__(self, torch_device):
+        self.ok = False
+        self.samples = []
+        self.reasons = 0
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            import torch
+
+            try:
+                uuid = str(torch.cuda.get_device_properties(torch_device).uuid)
+                uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            except Exception:
+                uuid = ""
+            if not uuid or self.nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+                idx = torch.cuda.current_device() if torch_device is None else torch_device
+                if self.nvml.nvmlDeviceGetHandleByIndex_v2(int(idx), ctypes.byref(self.h)) != 0:
+                    return
+            mx = ctypes.c_uint()
+            got = self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0
+            self.max_mhz = float(mx.value) if got else None
+            fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.reason_fn = fn
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _poll(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(float(clk.value))
+            if self.reason_fn(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
+            time.sleep(0.004)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._poll, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        names = [n for bit, n in _REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class Group:
+    """Host-side barrier and max over ranks (gloo); trivial when world == 1."""
+
+    def __init__(self, world):
+        self.world = world
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group("gloo")
+            self.dist = dist
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.world == 1:
+            return x
+        import torch
+
+        t = torch.tensor([x], dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1:
+            self.dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- inputs
+def make_inputs():
+    import seeded_inputs as si
+
+    w = WORKLOAD
+    return si.qkv(SEED, w["B"], w["H"], w["N"], w["d"], w["dtype"])
+
+
+def cpu_baseline_leg(q, k, v, o_dev_rows_fn, target_s=15.0):
+    """The oracle, as it stands, on a bounded sample of the workload's query rows, timed on
+    this host's cores; the GPU output at the same rows is compared on the side."""
+    import oracle
+    import seeded_inputs as si
+
+    w = WORKLOAD
+    threads = oracle.default_threads()
+    # Calibrate on a few rows, then size the sample to about target_s seconds.
+    rng_rows = si.sample_rows(SEED + 1, w["N"], 64)
+    cal = np.concatenate([h * w["N"] + rng_rows[: 8] for h in range(w["H"])])
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, w["causal"], rows=cal, threads=threads)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    per_row = dt / len(cal)
+    per_head = int(max(4, min(w["N"], target_s / per_row / w["H"])))
+    rows = si.sample_rows(SEED + 2, w["N"], per_head)
+    flat = np.concatenate([h * w["N"] + rows for h in range(w["B"] * w["H"])])
+    t0 = time.perf_counter()
+    ref = oracle.attn_fwd(q, k, v, w["causal"], rows=flat, threads=threads)
+    secs = time.perf_counter() - t0
+    fl = row_flops(np.tile(rows, w["B"] * w["H"]), w["d"], w["N"], w["causal"])
+    got = o_dev_rows_fn(flat)
+    err = float(np.max(np.abs(got - ref)))
+    return ({"value": fl / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+             "sample": f"{len(rows)} seeded query rows per head x {w['B'] * w['H']} heads "
+                       f"({len(flat)} rows, {fl:.3e} flop) of the timed workload, {secs:.1f} s"},
+            {"rows_checked": int(len(flat)), "max_abs_err": err, "tolerance": 2e-2, "pass": bool(err <= 2e-2)})
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local):
+    import torch
+
+    import online_softmax_flashattention_gb300 as fa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    grp = Group(world)
+    w = WORKLOAD
+    q, k, v = make_inputs()
+    tdt = torch.bfloat16
+    qh, kh, vh = (torch.from_numpy(x).to(tdt).pin_memory() for x in (q, k, v))
+    qd, kd, vd = (x.to(dev) for x in (qh, kh, vh))
+    od = torch.empty_like(qd)
+    oh = torch.empty_like(qh).pin_memory()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flop = workload_flops(w["B"], w["H"], w["N"], w["d"], w["causal"])
+
+    # Correct before timed: one run, checked against the oracle in the CPU-baseline leg below.
+    fa.attn_fwd(qd, kd, vd, causal=True, out=od)
+    torch.cuda.synchronize(dev)
+    if fa.attn_device_status(clear=True, device=dev) != 0:
+        raise RuntimeError("device-side timeout in the first run")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fa.attn_fwd(qd, kd, vd, causal=True, out=od)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    grp.barrier()
+    torch.cuda.synchronize(dev)
+    with sampler:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            fa.attn_fwd(qd, kd, vd, causal=True, out=od)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    grp.barrier()
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.fmean(launch_ms)
+    ms_max = grp.max(ms)
+    status = fa.attn_device_status(clear=True, device=dev)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed steps")
+
+    # e2e through the same public call with host buffers.
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        qd.copy_(qh, non_blocking=True); kd.copy_(kh, non_blocking=True); vd.copy_(vh, non_blocking=True)
+        fa.attn_fwd(qd, kd, vd, causal=True, out=od)
+        oh.copy_(od, non_blocking=True)
+    grp.barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        e_starts[i].record(stream)
+        qd.copy_(qh, non_blocking=True); kd.copy_(kh, non_blocking=True); vd.copy_(vh, non_blocking=True)
+        fa.attn_fwd(qd, kd, vd, causal=True, out=od)
+        oh.copy_(od, non_blocking=True)
+        e_ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    grp.barrier()
+    e2e_ms = grp.max(statistics.fmean(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)))
+    h2d = 3 * qh.numel() * qh.element_size()
+    d2h = oh.numel() * oh.element_size()
+
+    # Materialised ablation: bytes and time, once, outside the timed region.
+    ablation = None
+    if rank == 0 and not args.no_ablation:
+        ws_bytes = fa.attn_materialized_workspace_bytes(w["B"], w["H"], w["N"])
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        om = torch.empty_like(qd)
+        fa.attn_fwd_materialized(qd, kd, vd, causal=True, workspace=ws, out=om)
+        torch.cuda.synchronize(dev)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(3):
+            fa.attn_fwd_materialized(qd, kd, vd, causal=True, workspace=ws, out=om)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        mat_ms = a0.elapsed_time(a1) / 3
+        diff = float((om.float() - od.float()).abs().max())
+        bh, n, d = w["B"] * w["H"], w["N"], w["d"]
+        ablation = {"materialized_ms": mat_ms, "materialized_tflops": flop / (mat_ms * 1e-3) / 1e12,
+                    "score_bytes": 5 * 4 * n * n * bh, "online_floor_bytes": 4 * 2 * n * d * bh,
+                    "workspace_bytes": ws_bytes, "max_abs_diff_vs_flash": diff}
+        del ws, om
+
+    cpu = parity = None
+    if rank == 0 and not args.no_cpu_baseline:
+        o_rows = od.float().cpu().numpy().reshape(-1, w["d"]).astype(np.float64)
+        cpu, parity = cpu_baseline_leg(q, k, v, lambda flat: o_rows[flat], args.cpu_seconds)
+
+    grp.close()
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    achieved = flop / (ms * 1e-3) / 1e12
+    traffic, traffic_src = recorded_traffic()
+    value = world * flop / (ms_max * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded i.i.d. N(0,1), rounded to bf16)",
+        "config": {**WORKLOAD, "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": UNIT,
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 dense (burst)", "traffic_source": traffic_src,
+                     "algorithmic_flop_per_launch": flop},
+        "e2e": {"value": world * flop / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+        "cpu_baseline": cpu,
+        "parity": parity,
+        "ablation": ablation,
+        "launch_ms": {"min": min(launch_ms), "median": statistics.median(launch_ms), "max": max(launch_ms)},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    """The CPU oracle on the same workload: each step a bounded sample of query rows."""
+    if rank != 0:
+        return
+    import oracle
+    import seeded_inputs as si
+
+    w = WORKLOAD
+    q, k, v = make_inputs()
+    threads = oracle.default_threads()
+    budget = args.reference_seconds / max(1, args.steps + args.warmup)
+    cal_rows = si.sample_rows(SEED + 3, w["N"], 32)
+    cal = np.concatenate([h * w["N"] + cal_rows for h in range(w["H"])])
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, w["causal"], rows=cal, threads=threads)
+    per_row = max(time.perf_counter() - t0, 1e-4) / len(cal)
+    per_head = int(max(1, min(w["N"], budget / per_row / (w["B"] * w["H"]))))
+    times, flops = [], []
+    for step in range(args.warmup + args.steps):
+        rows = si.sample_rows(SEED + 100 + step, w["N"], per_head)
+        flat = np.concatenate([h * w["N"] + rows for h in range(w["B"] * w["H"])])
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v, w["causal"], rows=flat, threads=threads)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            flops.append(row_flops(np.tile(rows, w["B"] * w["H"]), w["d"], w["N"], w["causal"]))
+    value = sum(flops) / sum(times) / 1e12
+    sample = (f"each step: {per_head} seeded query rows per head x {w['B'] * w['H']} heads of the workload "
+              f"(double-precision oracle, {threads} threads)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.fmean(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded i.i.d. N(0,1), rounded to bf16)", "config": dict(WORKLOAD),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
+    ap.add_argument("--reference-seconds", type=float, default=90.0, help="reference arm budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ablation", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

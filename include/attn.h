@@ -1,0 +1,122 @@
+/*
+ * attn.h — C ABI of libattn.so: exact scaled-dot-product attention forward on GB300
+ * (sm_103a), computed tile by tile with the online-softmax recurrence.
+ *
+ * Operation (all entry points). For every batch b < B, head h < H and query row i < N:
+ *
+ *     o[b,h,i,:] = sum_{j in vis(i)} softmax_j( q[b,h,i,:] . k[b,h,j,:] / sqrt(d) ) * v[b,h,j,:]
+ *
+ * with vis(i) = {0 .. N-1}, or {0 .. i} when causal (the diagonal is kept). This is the
+ * definition on the "Flash attention in PyTorch, then in Triton" page, section "Attention's
+ * table of scores"; the tiled evaluation with a running maximum, running denominator and
+ * running output is the online softmax of its section "Flash attention" and of attention.cu
+ * (attentionOnline). The scale 1/sqrt(d) is fixed, as in both pages.
+ *
+ * Layout. q, k, v and o are contiguous row-major [B, H, N, d] device arrays of one element
+ * type (dtype). Element (b,h,i,e) lives at offset ((b*H + h)*N + i)*d + e.
+ *
+ * Ownership and synchronisation. The caller owns every buffer and the stream. Calls are
+ * stream-ordered and asynchronous: they validate, enqueue on `stream` (a cudaStream_t;
+ * NULL is the legacy default stream) and return. The library keeps no state between calls
+ * apart from per-device caches of device properties and driver entry points, and is safe
+ * to call from several host threads. attn_fwd allocates no device memory.
+ *
+ * Errors. Every entry point returns an attn_status_t and never exits the process.
+ * Argument checks happen before any launch; a non-OK status means nothing was enqueued.
+ * Faults that happen on the device surface at the caller's next synchronisation, as for
+ * any CUDA call. A device-side wait that exceeds its time limit stops the kernel, leaves
+ * o partly written and records ATTN_ERR_TIMEOUT, which attn_device_status() reports.
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_F32 = 0,  /* float32 in and out; FFMA path with fp32 accumulation */
+    ATTN_BF16 = 1, /* bfloat16 in and out; tcgen05 tensor cores, fp32 accumulation */
+    ATTN_F16 = 2   /* float16 in and out; tcgen05 tensor cores, fp32 accumulation */
+} attn_dtype_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1, /* null pointer with work to do, negative size, causal not 0/1 */
+    ATTN_ERR_UNSUPPORTED = 2, /* d != 64, unknown dtype, or a size beyond the stated limits */
+    ATTN_ERR_ALIGN = 3,       /* a tensor or workspace pointer not 16-byte aligned */
+    ATTN_ERR_ALIAS = 4,       /* o overlaps q, k, v (or the workspace overlaps a tensor) */
+    ATTN_ERR_DEVICE = 5,      /* current device is not compute capability 10.3, or a CUDA
+                                 query failed */
+    ATTN_ERR_LAUNCH = 6,      /* the kernel launch itself failed (cudaGetLastError) */
+    ATTN_ERR_TIMEOUT = 7,     /* a device-side wait ran out its time limit (see attn_device_status) */
+    ATTN_ERR_WORKSPACE = 8    /* workspace null or smaller than one head needs */
+} attn_status_t;
+
+/* Largest N accepted by every entry point (2^30 rows per head). */
+#define ATTN_MAX_N ((int64_t)1 << 30)
+
+/*
+ * attn_fwd — the flash (online-softmax) forward. N x N scores never reach device memory.
+ *
+ *   q, k, v : const device pointers, [B, H, N, d] of dtype, 16-byte aligned
+ *   o       : device pointer, [B, H, N, d] of dtype, 16-byte aligned, must not overlap
+ *             q, k or v; every element is written
+ *   B, H, N : sizes >= 0, N <= ATTN_MAX_N, B*H < 2^31. B*H == 0 or N == 0 is a successful
+ *             no-op (pointers may then be NULL)
+ *   d       : head width; only 64 is supported (ATTN_ERR_UNSUPPORTED otherwise)
+ *   causal  : 0 (every key visible) or 1 (key j visible to query i iff j <= i)
+ *   dtype   : attn_dtype_t. bf16/f16 inputs are multiplied on tcgen05 tensor cores with
+ *             fp32 accumulation; the probabilities are rounded to the input type before
+ *             they weigh v, and o is rounded to nearest even. f32 runs on FFMA.
+ *   stream  : cudaStream_t (may be NULL)
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, int64_t B, int64_t H,
+             int64_t N, int64_t d, int causal, int dtype, void* stream);
+
+/*
+ * attn_fwd_materialized — the same result by the materialised path of attention.cu
+ * (scoresQKt, softmaxRows, weightedV): S = q k^T / sqrt(d) with masked entries set to
+ * -inf, written in full as fp32; a three-pass safe softmax that writes exp(S - rowmax) to
+ * a second N x N buffer and the row totals to a vector; then o = (P v) / rowtotal.
+ * Kept as an ablation that moves 5 * 4 * N^2 bytes of scores per head.
+ *
+ *   workspace       : device pointer, 256-byte aligned, caller-owned scratch; it must not
+ *                     overlap q, k, v or o. Contents on entry are ignored and on exit are
+ *                     unspecified.
+ *   workspace_bytes : its size. At least attn_materialized_workspace_bytes(1, 1, N) (one
+ *                     head); heads are processed in groups of as many as fit, so
+ *                     attn_materialized_workspace_bytes(B, H, N) processes all at once.
+ *   other arguments : as attn_fwd; every dtype is computed in fp32 arithmetic.
+ */
+int attn_fwd_materialized(const void* q, const void* k, const void* v, void* o, void* workspace,
+                          size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t d,
+                          int causal, int dtype, void* stream);
+
+/* Bytes of workspace attn_fwd_materialized needs to process all B*H heads in one group:
+ * B*H * (two N x N fp32 buffers + N fp32 row totals), each rounded up to 256 bytes.
+ * Returns 0 for negative sizes or on overflow. */
+size_t attn_materialized_workspace_bytes(int64_t B, int64_t H, int64_t N);
+
+/*
+ * attn_device_status — synchronises `stream`, then reports whether any kernel of this
+ * library on the current device recorded a device-side wait timeout since the flag was
+ * last cleared. Returns ATTN_OK or ATTN_ERR_TIMEOUT (ATTN_ERR_DEVICE if a CUDA call
+ * fails). clear != 0 resets the flag.
+ */
+int attn_device_status(void* stream, int clear);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char* attn_status_string(int status);
+
+/* ABI version of this header: (major << 16) | minor. */
+int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

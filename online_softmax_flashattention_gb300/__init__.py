@@ -1,0 +1,160 @@
+"""Python binding of libattn.so — exact attention forward with the online softmax on GB300.
+
+The names mirror the C ABI in ``include/attn.h``; this module only marshals arguments
+(torch tensors to device pointers, the current torch stream to ``cudaStream_t``). Every step
+of the computation runs in the library's CUDA kernels. There is no CPU or PyTorch fallback:
+if the library has not been built, importing works but every call raises
+:class:`AttnLibraryMissing`.
+
+    import torch, online_softmax_flashattention_gb300 as fa
+    o = fa.attn_fwd(q, k, v, causal=True)        # q, k, v: cuda [B, H, N, 64], same dtype
+
+Build with ``python -m online_softmax_flashattention_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "ATTN_F32", "ATTN_BF16", "ATTN_F16", "AttnError", "AttnLibraryMissing", "library_path",
+    "attn_fwd", "attn_fwd_materialized", "attn_materialized_workspace_bytes", "attn_device_status",
+    "attn_status_string", "attn_abi_version", "raw",
+]
+
+ATTN_F32, ATTN_BF16, ATTN_F16 = 0, 1, 2
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_ALIGN",
+          4: "ATTN_ERR_ALIAS", 5: "ATTN_ERR_DEVICE", 6: "ATTN_ERR_LAUNCH", 7: "ATTN_ERR_TIMEOUT",
+          8: "ATTN_ERR_WORKSPACE"}
+_DTYPES = {torch.float32: ATTN_F32, torch.bfloat16: ATTN_BF16, torch.float16: ATTN_F16}
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_lib", "libattn.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnLibraryMissing(RuntimeError):
+    """libattn.so has not been built in this checkout."""
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({attn_status_string(status)})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def raw():
+    """The loaded ctypes library, with argument types declared (for C-ABI level tests)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise AttnLibraryMissing(
+                    f"{_LIB_PATH} is missing: build it with `python -m online_softmax_flashattention_gb300.build`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            vp, i64, ci, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+            lib.attn_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ci, ci, vp]
+            lib.attn_fwd.restype = ci
+            lib.attn_fwd_materialized.argtypes = [vp, vp, vp, vp, vp, sz, i64, i64, i64, i64, ci, ci, vp]
+            lib.attn_fwd_materialized.restype = ci
+            lib.attn_materialized_workspace_bytes.argtypes = [i64, i64, i64]
+            lib.attn_materialized_workspace_bytes.restype = sz
+            lib.attn_device_status.argtypes = [vp, ci]
+            lib.attn_device_status.restype = ci
+            lib.attn_status_string.argtypes = [ci]
+            lib.attn_status_string.restype = ctypes.c_char_p
+            lib.attn_abi_version.argtypes = []
+            lib.attn_abi_version.restype = ci
+            _lib = lib
+    return _lib
+
+
+def attn_status_string(status: int) -> str:
+    return raw().attn_status_string(int(status)).decode()
+
+
+def attn_abi_version() -> int:
+    return int(raw().attn_abi_version())
+
+
+def _check(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [B, H, N, d]")
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if q.dtype != k.dtype or q.dtype != v.dtype or q.dtype not in _DTYPES:
+        raise TypeError("q, k, v must share one dtype among float32, bfloat16, float16")
+    if q.device != k.device or q.device != v.device:
+        raise ValueError("q, k, v must be on one device")
+
+
+def _stream(dev, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+             out: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """o = softmax(q k^T / sqrt(d) + causal mask) v, by the online (flash) kernels."""
+    _check(q, k, v)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or out.device != q.device or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    B, H, N, d = q.shape
+    lib = raw()
+    with torch.cuda.device(q.device):
+        st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, d,
+                          int(bool(causal)), _DTYPES[q.dtype], _stream(q.device, stream))
+    if st != 0:
+        raise AttnError(st, "attn_fwd")
+    return out
+
+
+def attn_materialized_workspace_bytes(B: int, H: int, N: int) -> int:
+    return int(raw().attn_materialized_workspace_bytes(B, H, N))
+
+
+def attn_fwd_materialized(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                          workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                          stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """The same result through the materialised N x N path (ablation). ``workspace`` is a
+    uint8 CUDA tensor; when omitted one big enough for all heads at once is allocated."""
+    _check(q, k, v)
+    B, H, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = torch.empty(max(1, attn_materialized_workspace_bytes(B, H, N)), dtype=torch.uint8,
+                                device=q.device)
+    lib = raw()
+    with torch.cuda.device(q.device):
+        st = lib.attn_fwd_materialized(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                       B, H, N, d, int(bool(causal)), _DTYPES[q.dtype],
+                                       _stream(q.device, stream))
+    if st != 0:
+        raise AttnError(st, "attn_fwd_materialized")
+    return out
+
+
+def attn_device_status(clear: bool = True, stream: torch.cuda.Stream | None = None,
+                       device: torch.device | int | None = None) -> int:
+    """Synchronises the stream and returns ATTN_OK (0) or ATTN_ERR_TIMEOUT (7)."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index or 0)
+    with torch.cuda.device(dev):
+        return int(raw().attn_device_status(_stream(dev, stream), int(bool(clear))))

@@ -1,0 +1,160 @@
+// The C ABI of libattn.so (declared in include/attn.h): argument checks, dispatch to the
+// fp32 (FFMA) or bf16/fp16 (tcgen05) online kernels or to the materialised ablation, and
+// status reporting. Nothing here allocates device memory.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "attn.h"
+#include "attn_internal.h"
+
+namespace {
+
+constexpr int64_t kHeadDim = 64;
+
+size_t elem_size(int dtype) { return dtype == ATTN_F32 ? 4 : 2; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// Host-side fault injection for tests: ATTN_FAULT=launch makes every entry point report a
+// launch failure after its argument checks, without launching anything.
+bool inject_launch_fault() {
+    const char* f = std::getenv("ATTN_FAULT");
+    return f != nullptr && std::strcmp(f, "launch") == 0;
+}
+
+// Common checks of attn_fwd and attn_fwd_materialized. On success *bh and *bytes hold
+// B*H and the size of one tensor; *skip is set when there is no work.
+int check_common(const void* q, const void* k, const void* v, const void* o, int64_t B, int64_t H,
+                 int64_t N, int64_t d, int causal, int dtype, int64_t* bh, size_t* bytes,
+                 bool* skip) {
+    if (B < 0 || H < 0 || N < 0 || d < 0) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_UNSUPPORTED;
+    if (d != kHeadDim) return ATTN_ERR_UNSUPPORTED;
+    if (N > ATTN_MAX_N) return ATTN_ERR_UNSUPPORTED;
+    if (B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    if (BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+    *bh = BH;
+    *skip = (BH == 0 || N == 0);
+    if (*skip) return ATTN_OK;
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return ATTN_ERR_ALIGN;
+    *bytes = static_cast<size_t>(BH) * static_cast<size_t>(N) * kHeadDim * elem_size(dtype);
+    if (overlap(o, *bytes, q, *bytes) || overlap(o, *bytes, k, *bytes) || overlap(o, *bytes, v, *bytes))
+        return ATTN_ERR_ALIAS;
+    return ATTN_OK;
+}
+
+// The kernels are built for sm_103a only; any other device is refused up front.
+int check_device(int* num_sms) {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return ATTN_ERR_DEVICE;
+    if (major != 10 || minor != 3) return ATTN_ERR_DEVICE;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, int64_t B, int64_t H,
+             int64_t N, int64_t d, int causal, int dtype, void* stream) {
+    int64_t BH = 0;
+    size_t bytes = 0;
+    bool skip = false;
+    int st = check_common(q, k, v, o, B, H, N, d, causal, dtype, &BH, &bytes, &skip);
+    if (st != ATTN_OK || skip) return st;
+    int num_sms = 0;
+    if ((st = check_device(&num_sms)) != ATTN_OK) return st;
+    if (inject_launch_fault()) return ATTN_ERR_LAUNCH;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == ATTN_F32)
+        return attn::launch_fwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                    static_cast<const float*>(v), static_cast<float*>(o), BH, N,
+                                    causal != 0, num_sms, s);
+    return attn::launch_fwd_tc(q, k, v, o, BH, N, causal != 0, dtype == ATTN_BF16, num_sms, s);
+}
+
+size_t attn_materialized_workspace_bytes(int64_t B, int64_t H, int64_t N) {
+    if (B < 0 || H < 0 || N < 0 || B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return 0;
+    const size_t per = attn::materialized_head_bytes(N);
+    if (per == 0 && N != 0) return 0;
+    const size_t bh = static_cast<size_t>(B) * static_cast<size_t>(H);
+    if (bh != 0 && per > SIZE_MAX / bh) return 0;
+    return per * bh;
+}
+
+int attn_fwd_materialized(const void* q, const void* k, const void* v, void* o, void* workspace,
+                          size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t d,
+                          int causal, int dtype, void* stream) {
+    int64_t BH = 0;
+    size_t bytes = 0;
+    bool skip = false;
+    int st = check_common(q, k, v, o, B, H, N, d, causal, dtype, &BH, &bytes, &skip);
+    if (st != ATTN_OK || skip) return st;
+    const size_t per = attn::materialized_head_bytes(N);
+    if (per == 0) return ATTN_ERR_UNSUPPORTED;
+    if (workspace == nullptr || workspace_bytes < per) return ATTN_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return ATTN_ERR_ALIGN;
+    if (overlap(workspace, workspace_bytes, q, bytes) || overlap(workspace, workspace_bytes, k, bytes) ||
+        overlap(workspace, workspace_bytes, v, bytes) || overlap(workspace, workspace_bytes, o, bytes))
+        return ATTN_ERR_ALIAS;
+    int num_sms = 0;
+    if ((st = check_device(&num_sms)) != ATTN_OK) return st;
+    if (inject_launch_fault()) return ATTN_ERR_LAUNCH;
+    int64_t group = static_cast<int64_t>(workspace_bytes / per);
+    if (group > BH) group = BH;
+    if (group > 65535) group = 65535;
+    const size_t head_elems = static_cast<size_t>(N) * kHeadDim;
+    const size_t esz = elem_size(dtype);
+    for (int64_t h0 = 0; h0 < BH; h0 += group) {
+        const int64_t hc = (BH - h0 < group) ? (BH - h0) : group;
+        const size_t off = static_cast<size_t>(h0) * head_elems * esz;
+        st = attn::launch_materialized(static_cast<const uint8_t*>(q) + off,
+                                       static_cast<const uint8_t*>(k) + off,
+                                       static_cast<const uint8_t*>(v) + off,
+                                       static_cast<uint8_t*>(o) + off, workspace, per, hc, N,
+                                       causal != 0, dtype, static_cast<cudaStream_t>(stream));
+        if (st != ATTN_OK) return st;
+    }
+    return ATTN_OK;
+}
+
+int attn_device_status(void* stream, int clear) {
+    unsigned err = 0;
+    const int st = attn::tc_device_error(static_cast<cudaStream_t>(stream), clear != 0, &err);
+    if (st != ATTN_OK) return st;
+    return err ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+const char* attn_status_string(int status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or causal not 0/1)";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim must be 64; dtype f32/bf16/f16; size limits)";
+        case ATTN_ERR_ALIGN: return "pointer not aligned (tensors 16 bytes, workspace 256 bytes)";
+        case ATTN_ERR_ALIAS: return "output or workspace overlaps another buffer";
+        case ATTN_ERR_DEVICE: return "current device is not sm_103 or a CUDA query failed";
+        case ATTN_ERR_LAUNCH: return "kernel launch failed";
+        case ATTN_ERR_TIMEOUT: return "a device-side wait ran out its time limit";
+        case ATTN_ERR_WORKSPACE: return "workspace missing or smaller than one head needs";
+        default: return "unknown status";
+    }
+}
+
+int attn_abi_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

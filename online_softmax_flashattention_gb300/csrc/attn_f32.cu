@@ -1,0 +1,220 @@
+// Online-softmax attention forward for float32 on CUDA cores (FFMA).
+//
+// Same operation and recurrence as the tensor-core kernel: per query row a running max m,
+// a running denominator l and a running output, rescaled by exp(m_old - m_new) when a key
+// tile raises the max (attention.cu, attentionOnline and its "online-update" step; "Flash
+// attention in PyTorch, then in Triton", section "Flash attention"). Scores are kept in
+// base-2 units, s * log2(e) / sqrt(d), so every exponential is an exp2 ("A kernel in
+// Triton"). Causal key tiles past a block's last query are skipped and ragged N is guarded
+// on every load and store (the page's kernel masks rows and keys past T).
+//
+// Layout per CTA: BM query rows (64, or 32 when the grid would not fill the GPU) against
+// key tiles of 64, d = 64, BM/4 x 16 threads. Thread (ty, tx) holds a 4 x 4 score
+// micro-tile — rows ty*4 + i, keys tx + 16 j — and a 4 x 4 output micro-tile — rows ty*4 + i,
+// dims tx*4 + j. Rows of shared tiles are padded to 68 floats so that every float4 read of a
+// key row, every P store and every V read is free of bank conflicts. The 16 threads that
+// share a row sit in one half-warp, so row max and row sum are 4-step xor shuffles.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kD = 64;
+constexpr int kBN = 64;
+constexpr int kLd = 68;  // padded row stride (floats) of every shared tile
+
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int BM>
+__global__ void __launch_bounds__(BM * 4)
+    attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
+                        const float* __restrict__ v, float* __restrict__ o, int N, int BH,
+                        int nblk, int causal, float c) {
+    constexpr int kThreads = BM * 4;
+    extern __shared__ float4 smem4[];
+    float* const Qs = reinterpret_cast<float*>(smem4);
+    float* const Ks = Qs + BM * kLd;
+    float* const Vs = Ks + kBN * kLd;
+    float* const Ps = Vs + kBN * kLd;
+
+    const int tid = threadIdx.x;
+    const int tx = tid & 15;
+    const int ty = tid >> 4;
+    const int bh = static_cast<int>(blockIdx.x % static_cast<unsigned>(BH));
+    const int slot = static_cast<int>(blockIdx.x / static_cast<unsigned>(BH));
+    const int blk = causal ? (nblk - 1 - slot) : slot;
+    const int row0 = blk * BM;
+    const int64_t head = static_cast<int64_t>(bh) * N * kD;
+    const float* qh = q + head;
+    const float* kh = k + head;
+    const float* vh = v + head;
+
+    // Q tile, rows >= N read as zero.
+    for (int idx = tid; idx < BM * 16; idx += kThreads) {
+        const int r = idx >> 4, e4 = idx & 15;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row0 + r < N) val = *reinterpret_cast<const float4*>(qh + static_cast<int64_t>(row0 + r) * kD + 4 * e4);
+        *reinterpret_cast<float4*>(Qs + r * kLd + 4 * e4) = val;
+    }
+
+    float m[4], l[4], acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    }
+
+    const int kend = causal ? min(N, row0 + BM) : N;
+    const int ntiles = (kend + kBN - 1) / kBN;
+    for (int t = 0; t < ntiles; ++t) {
+        const int kbase = t * kBN;
+        __syncthreads();  // the previous tile's products are done with Ks, Vs and Ps
+        for (int idx = tid; idx < kBN * 16; idx += kThreads) {
+            const int r = idx >> 4, e4 = idx & 15;
+            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+            if (kbase + r < N) {
+                const int64_t off = static_cast<int64_t>(kbase + r) * kD + 4 * e4;
+                kv = *reinterpret_cast<const float4*>(kh + off);
+                vv = *reinterpret_cast<const float4*>(vh + off);
+            }
+            *reinterpret_cast<float4*>(Ks + r * kLd + 4 * e4) = kv;
+            *reinterpret_cast<float4*>(Vs + r * kLd + 4 * e4) = vv;
+        }
+        __syncthreads();
+
+        // S micro-tile: rows ty*4+i, keys tx+16j.
+        float s[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+#pragma unroll 4
+        for (int e = 0; e < kD; e += 4) {
+            float4 qa[4], kb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) qa[i] = *reinterpret_cast<const float4*>(Qs + (ty * 4 + i) * kLd + e);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) kb[j] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * j) * kLd + e);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    s[i][j] = fmaf(qa[i].x, kb[j].x, s[i][j]);
+                    s[i][j] = fmaf(qa[i].y, kb[j].y, s[i][j]);
+                    s[i][j] = fmaf(qa[i].z, kb[j].z, s[i][j]);
+                    s[i][j] = fmaf(qa[i].w, kb[j].w, s[i][j]);
+                }
+        }
+
+        // Mask keys past N and, when causal, keys after the query.
+        if (kbase + kBN > N || (causal && kbase + kBN - 1 > row0)) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int row = row0 + ty * 4 + i;
+                const int lim = causal ? min(row + 1, N) : N;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (kbase + tx + 16 * j >= lim) s[i][j] = -INFINITY;
+            }
+        }
+
+        // Online update per row.
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float mx = fmaxf(fmaxf(s[i][0], s[i][1]), fmaxf(s[i][2], s[i][3]));
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float m_new = fmaxf(m[i], mx * c);
+            const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = ex2f(m[i] - m_ref);
+            float ps = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float pv = ex2f(fmaf(s[i][j], c, -m_ref));
+                ps += pv;
+                Ps[(ty * 4 + i) * kLd + tx + 16 * j] = pv;
+            }
+            l[i] = l[i] * alpha + ps;  // this thread's share of the row total
+            m[i] = m_ref;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] *= alpha;
+        }
+        __syncthreads();
+
+        // O micro-tile += P V: rows ty*4+i, dims tx*4+j.
+#pragma unroll 4
+        for (int kk = 0; kk < kBN; kk += 4) {
+            float4 pa[4], vb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pa[i] = *reinterpret_cast<const float4*>(Ps + (ty * 4 + i) * kLd + kk);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) vb[u] = *reinterpret_cast<const float4*>(Vs + (kk + u) * kLd + 4 * tx);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float pw[4] = {pa[i].x, pa[i].y, pa[i].z, pa[i].w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    acc[i][0] = fmaf(pw[u], vb[u].x, acc[i][0]);
+                    acc[i][1] = fmaf(pw[u], vb[u].y, acc[i][1]);
+                    acc[i][2] = fmaf(pw[u], vb[u].z, acc[i][2]);
+                    acc[i][3] = fmaf(pw[u], vb[u].w, acc[i][3]);
+                }
+            }
+        }
+    }
+
+    // Row totals across the 16 threads of the row, then O / l.
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float tot = l[i];
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        const int row = row0 + ty * 4 + i;
+        if (row < N) {
+            const float inv = 1.f / tot;
+            *reinterpret_cast<float4*>(o + head + static_cast<int64_t>(row) * kD + 4 * tx) =
+                make_float4(acc[i][0] * inv, acc[i][1] * inv, acc[i][2] * inv, acc[i][3] * inv);
+        }
+    }
+}
+
+template <int BM>
+int launch_bm(const float* q, const float* k, const float* v, float* o, int64_t BH, int64_t N,
+              bool causal, cudaStream_t stream) {
+    const int smem = (2 * BM + 2 * kBN) * kLd * static_cast<int>(sizeof(float));
+    if (cudaFuncSetAttribute(attn_fwd_f32_kernel<BM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+        return ATTN_ERR_LAUNCH;
+    const int64_t nblk = (N + BM - 1) / BM;
+    const int64_t blocks = nblk * BH;
+    if (blocks > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+    const float c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
+    attn_fwd_f32_kernel<BM><<<static_cast<unsigned>(blocks), BM * 4, smem, stream>>>(
+        q, k, v, o, static_cast<int>(N), static_cast<int>(BH), static_cast<int>(nblk), causal ? 1 : 0, c);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+int launch_fwd_f32(const float* q, const float* k, const float* v, float* o, int64_t BH, int64_t N,
+                   bool causal, int num_sms, cudaStream_t stream) {
+    if (N > 0x7FFFFFFFll - 64 || BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+    // Small problems use 32-row blocks so that more SMs get work.
+    const int64_t blocks64 = ((N + 63) / 64) * BH;
+    if (blocks64 < 2 * static_cast<int64_t>(num_sms))
+        return launch_bm<32>(q, k, v, o, BH, N, causal, stream);
+    return launch_bm<64>(q, k, v, o, BH, N, causal, stream);
+}
+
+}  // namespace attn

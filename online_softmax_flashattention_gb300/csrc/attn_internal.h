@@ -1,0 +1,35 @@
+// Internal launchers behind the C ABI. Each validates nothing (attn_capi.cu has already
+// checked every argument) and returns an attn_status_t.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "attn.h"
+
+namespace attn {
+
+// Online-softmax forward on FFMA for float32 tensors ([BH, N, 64] contiguous).
+int launch_fwd_f32(const float* q, const float* k, const float* v, float* o, int64_t BH, int64_t N,
+                   bool causal, int num_sms, cudaStream_t stream);
+
+// Online-softmax forward on tcgen05 tensor cores for bf16 (bf16 = true) or fp16 tensors.
+int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, int64_t BH, int64_t N,
+                  bool causal, bool bf16, int num_sms, cudaStream_t stream);
+
+// Reads (and optionally clears) the tensor-core kernel's device error word after
+// synchronising `stream`. *err receives the word.
+int tc_device_error(cudaStream_t stream, bool clear, unsigned* err);
+
+// Materialised path: scores, three-pass softmax, weighted values, for `heads` heads whose
+// scratch starts at `ws` (per-head stride `head_ws_bytes`).
+int launch_materialized(const void* q, const void* k, const void* v, void* o, void* ws,
+                        size_t head_ws_bytes, int64_t heads, int64_t N, bool causal, int dtype,
+                        cudaStream_t stream);
+
+// Per-head scratch of the materialised path: S and P (N x N fp32 each) and N row totals,
+// each region rounded up to 256 bytes. Returns 0 on overflow.
+size_t materialized_head_bytes(int64_t N);
+
+}  // namespace attn

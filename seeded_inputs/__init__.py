@@ -24,6 +24,11 @@ q, k and v (streams 0, 1, 2) are independent. Arrays are produced in chunks to b
 
 from __future__ import annotations
 
+import ctypes
+import os
+import subprocess
+import threading
+
 import numpy as np
 
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
@@ -64,8 +69,54 @@ def uniform01(seed: int, stream: int, start: int, count: int) -> np.ndarray:
     return ((x >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
 
 
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_GEN_SRC = os.path.join(_HERE, "gen.c")
+_GEN_LIB = os.path.join(_HERE, "_build", "libseeded_inputs.so")
+_gen_lock = threading.Lock()
+_gen = None
+
+
+def _gen_lib():
+    """The C implementation of the same generator (gen.c), compiled with gcc on first use."""
+    global _gen
+    with _gen_lock:
+        if _gen is None:
+            os.makedirs(os.path.dirname(_GEN_LIB), exist_ok=True)
+            if not os.path.exists(_GEN_LIB) or os.path.getmtime(_GEN_LIB) < os.path.getmtime(_GEN_SRC):
+                tmp = _GEN_LIB + f".{os.getpid()}.tmp"
+                subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                                "-o", tmp, _GEN_SRC, "-lm"], check=True)
+                os.replace(tmp, _GEN_LIB)
+            lib = ctypes.CDLL(_GEN_LIB)
+            lib.si_normal_f32.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int64,
+                                          ctypes.POINTER(ctypes.c_float), ctypes.c_int]
+            lib.si_normal_f32.restype = ctypes.c_int
+            _gen = lib
+    return _gen
+
+
 def normal_f32(seed: int, stream: int, count: int) -> np.ndarray:
-    """``count`` i.i.d. N(0, 1) samples rounded to float32 (Box-Muller, both branches)."""
+    """``count`` i.i.d. N(0, 1) samples rounded to float32 (Box-Muller, both branches).
+
+    Runs the C implementation on all host cores; :func:`normal_f32_numpy` is the same
+    definition in numpy, kept as its cross-check.
+    """
+    out = np.empty(count, dtype=np.float32)
+    if count == 0:
+        return out
+    try:
+        threads = max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        threads = os.cpu_count() or 1
+    st = _gen_lib().si_normal_f32(int(seed) & 0xFFFFFFFFFFFFFFFF, int(stream), count,
+                                  out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), threads)
+    if st != 0:
+        raise RuntimeError("si_normal_f32 failed")
+    return out
+
+
+def normal_f32_numpy(seed: int, stream: int, count: int) -> np.ndarray:
+    """The generator in numpy (the definition that ``gen.c`` implements)."""
     out = np.empty(count, dtype=np.float32)
     pairs = (count + 1) // 2
     done = 0

@@ -1,0 +1,94 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function declared in
+include/attn.h, and rejects bad arguments before touching a device."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import online_softmax_flashattention_gb300 as fa
+from online_softmax_flashattention_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.raw()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for want in ("attn_fwd", "attn_fwd_materialized", "attn_materialized_workspace_bytes",
+                 "attn_device_status", "attn_status_string", "attn_abi_version"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_version_and_status_strings(lib):
+    assert fa.attn_abi_version() >> 16 == 1
+    for code in range(9):
+        s = fa.attn_status_string(code)
+        assert s and s != "unknown status"
+    assert fa.attn_status_string(99) == "unknown status"
+
+
+P = 0x10000  # a 16-byte aligned non-null address; never dereferenced by these calls
+
+
+@pytest.mark.parametrize("args,want", [
+    ((P, P, P, P * 9, -1, 1, 8, 64, 0, 1), 1),            # negative B
+    ((P, P, P, P * 9, 1, 1, 8, 64, 2, 1), 1),             # causal not 0/1
+    ((P, P, P, P * 9, 1, 1, 8, 32, 0, 1), 2),             # d != 64
+    ((P, P, P, P * 9, 1, 1, 8, 64, 0, 7), 2),             # unknown dtype
+    ((P, P, P, P * 9, 1, 1, (1 << 30) + 1, 64, 0, 1), 2),  # N beyond the limit
+    ((None, P, P, P * 9, 1, 1, 8, 64, 0, 1), 1),          # null q with work to do
+    ((P + 2, P, P, P * 9, 1, 1, 8, 64, 0, 1), 3),         # misaligned q
+    ((P, P, P, P + 64, 1, 1, 8, 64, 0, 1), 4),            # o overlaps q
+    ((None, None, None, None, 0, 3, 8, 64, 1, 1), 0),     # B = 0: no-op
+    ((None, None, None, None, 2, 3, 0, 64, 1, 0), 0),     # N = 0: no-op
+])
+def test_argument_checks_before_any_device_work(lib, args, want):
+    assert lib.attn_fwd(*args, None) == want
+
+
+def test_materialized_workspace_checks(lib):
+    per = lib.attn_materialized_workspace_bytes(1, 1, 100)
+    assert per == 2 * ((100 * 100 * 4 + 255) // 256 * 256) + (400 + 255) // 256 * 256
+    assert lib.attn_materialized_workspace_bytes(2, 3, 100) == 6 * per
+    assert lib.attn_materialized_workspace_bytes(-1, 3, 100) == 0
+    ws = 0x4000000
+    assert lib.attn_fwd_materialized(P, P, P, P * 9, None, per, 1, 1, 100, 64, 0, 1, None) == 8
+    assert lib.attn_fwd_materialized(P, P, P, P * 9, ws, per - 1, 1, 1, 100, 64, 0, 1, None) == 8
+    assert lib.attn_fwd_materialized(P, P, P, P * 9, ws + 16, per, 1, 1, 100, 64, 0, 1, None) == 3
+    assert lib.attn_fwd_materialized(P, P, P, P * 9, P, per, 1, 1, 100, 64, 0, 1, None) == 4
+
+
+def test_binding_has_no_fallback_when_library_missing(monkeypatch, tmp_path):
+    monkeypatch.setattr(fa, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(fa, "_lib", None)
+    with pytest.raises(fa.AttnLibraryMissing):
+        fa.raw()
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="needs a machine without a GPU")
+def test_valid_call_without_gpu_reports_device_error(lib):
+    assert lib.attn_fwd(P, P * 3, P * 5, P * 9, 1, 1, 8, 64, 0, 1, None) == 5

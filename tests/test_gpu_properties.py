@@ -1,0 +1,138 @@
+"""GPU properties that hold exactly at any size: single-key identity, causality, run-to-run
+determinism, guard bands around the output, the materialised ablation against the oracle
+and against the flash path, and the C-ABI error statuses on a real device."""
+
+import ctypes
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import online_softmax_flashattention_gb300 as fa
+import seeded_inputs as si
+from attn_testlib import CONFIG_SEED, check, gpu_attn, page_gate_fraction, to_dev
+
+pytestmark = pytest.mark.gpu
+DTYPES = ["f32", "bf16", "f16"]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("causal", [False, True])
+def test_single_key_returns_v_bit_exactly(dtype, causal):
+    q, k, v = si.qkv(3, 3, 5, 1, 64, dtype)
+    got = gpu_attn(q, k, v, dtype, causal)
+    assert np.array_equal(got, v.astype(np.float64))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_empty_problems_are_no_ops(dtype):
+    z = torch.empty(1, 2, 0, 64, device="cuda", dtype={"f32": torch.float32, "bf16": torch.bfloat16,
+                                                        "f16": torch.float16}[dtype])
+    assert fa.attn_fwd(z, z, z, causal=True).shape == z.shape
+    z2 = z.new_empty(0, 3, 16, 64)
+    assert fa.attn_fwd(z2, z2, z2).shape == z2.shape
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("t", [0, 100, 127, 128, 300])
+def test_causal_rows_ignore_later_keys_bit_exactly(dtype, t):
+    N = 515
+    q, k, v = si.qkv(17, 1, 2, N, 64, dtype)
+    k2, v2 = k.copy(), v.copy()
+    k2[:, :, t + 1:], v2[:, :, t + 1:] = si.qkv(18, 1, 2, N, 64, dtype)[1:][0][:, :, t + 1:], \
+        si.qkv(18, 1, 2, N, 64, dtype)[2][:, :, t + 1:]
+    a = gpu_attn(q, k, v, dtype, True)
+    b = gpu_attn(q, k2, v2, dtype, True)
+    assert np.array_equal(a[:, :, : t + 1], b[:, :, : t + 1])
+    assert not np.array_equal(a[:, :, t + 1:], b[:, :, t + 1:])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("causal", [False, True])
+def test_runs_are_bit_identical(dtype, causal):
+    q, k, v = si.qkv(23, 2, 3, 700, 64, dtype)
+    a = gpu_attn(q, k, v, dtype, causal)
+    b = gpu_attn(q, k, v, dtype, causal)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("N", [1, 129, 1000])
+def test_output_guard_band_and_full_coverage(dtype, N):
+    B, H = 2, 3
+    q, k, v = si.qkv(29, B, H, N, 64, dtype)
+    qd, kd, vd = (to_dev(x, dtype) for x in (q, k, v))
+    n = B * H * N * 64
+    slack = 4096
+    buf = torch.full((n + 2 * slack,), float("nan"), device="cuda", dtype=qd.dtype)
+    out = buf[slack: slack + n].view(B, H, N, 64)
+    fa.attn_fwd(qd, kd, vd, causal=True, out=out)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:slack]).all() and torch.isnan(buf[slack + n:]).all()
+    assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 100, 256, 1000])
+def test_materialized_path_matches_oracle_and_flash(dtype, causal, N):
+    q, k, v = si.qkv(CONFIG_SEED[2] + N, 2, 3, N, 64, dtype)
+    ref = oracle.attn_fwd(q, k, v, causal)
+    mat = gpu_attn(q, k, v, dtype, causal, path="materialized")
+    check(mat, ref, dtype, N, "materialized")
+    flash = gpu_attn(q, k, v, dtype, causal)
+    if dtype == "f32":
+        # attention.cu's pair check: the two GPU paths against each other under the gate.
+        assert page_gate_fraction(flash, mat, N) <= 1.0
+    else:
+        assert np.max(np.abs(flash - mat)) <= 4e-2
+
+
+def test_materialized_small_workspace_runs_heads_in_groups():
+    B, H, N = 2, 3, 300
+    q, k, v = si.qkv(31, B, H, N, 64, "f32")
+    qd, kd, vd = (to_dev(x, "f32") for x in (q, k, v))
+    per = fa.attn_materialized_workspace_bytes(1, 1, N)
+    ws = torch.empty(2 * per + 100, dtype=torch.uint8, device="cuda")  # two heads per group
+    got = fa.attn_fwd_materialized(qd, kd, vd, causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    check(got.double().cpu().numpy(), oracle.attn_fwd(q, k, v, True), "f32", N, "grouped")
+
+
+def test_non_default_stream():
+    q, k, v = si.qkv(37, 1, 4, 512, 64, "bf16")
+    qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o = fa.attn_fwd(qd, kd, vd, causal=True)
+    s.synchronize()
+    check(o.double().cpu().numpy(), oracle.attn_fwd(q, k, v, True), "bf16", 512, "stream")
+
+
+def test_error_statuses_on_device():
+    lib = fa.raw()
+    x = torch.zeros(1, 1, 64, 64, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros_like(x)
+    base = (x.data_ptr(), x.data_ptr(), x.data_ptr(), y.data_ptr())
+    assert lib.attn_fwd(*base, 1, 1, 64, 64, 0, 1, None) == 0
+    assert lib.attn_fwd(base[0] + 2, *base[1:], 1, 1, 60, 64, 0, 1, None) == 3
+    assert lib.attn_fwd(*base[:3], base[0], 1, 1, 64, 64, 0, 1, None) == 4
+    assert lib.attn_fwd(*base, 1, 1, 64, 128, 0, 1, None) == 2
+    with pytest.raises(fa.AttnError):
+        fa.attn_fwd(x, x, x, out=x)
+    torch.cuda.synchronize()
+    assert fa.attn_device_status(clear=True) == 0
+
+
+def test_injected_launch_fault_is_reported(monkeypatch):
+    x = torch.zeros(1, 1, 64, 64, dtype=torch.float16, device="cuda")
+    monkeypatch.setenv("ATTN_FAULT", "launch")
+    with pytest.raises(fa.AttnError) as ei:
+        fa.attn_fwd(x, x, x)
+    assert ei.value.status == 6
+    monkeypatch.delenv("ATTN_FAULT")
+    fa.attn_fwd(x, x, x)
+    torch.cuda.synchronize()

@@ -22,6 +22,16 @@ def test_streams_are_deterministic_and_distinct():
     assert np.array_equal(si.normal_f32(7, 0, 4000)[:1001], a)
 
 
+def test_c_generator_matches_numpy_definition():
+    # Same arithmetic; the two libm implementations may differ in a last double bit, which
+    # can move a float32 rounding by one ulp in about one element in 2**29.
+    c = si.normal_f32(12, 2, 200001)
+    n = si.normal_f32_numpy(12, 2, 200001)
+    diff = np.flatnonzero(c != n)
+    assert len(diff) <= 2
+    assert np.all(np.abs(c[diff] - n[diff]) <= np.spacing(np.abs(n[diff])))
+
+
 def test_normal_moments():
     x = si.normal_f32(3, 2, 1 << 20).astype(np.float64)
     assert abs(x.mean()) < 5e-3
