@@ -14,6 +14,11 @@
 // (section "The online softmax, in PyTorch"); ragged N is masked on keys and clipped on
 // stores.
 //
+// The reference m only has to be the same for l and O, not the exact running maximum:
+// any common reference gives the same O / l. The kernel therefore keeps a stale maximum
+// until a tile exceeds it by more than 2^8 (then probabilities stay below 256, well inside
+// bf16/fp16 and fp32 range), which makes the O rescale rare instead of nearly every tile.
+//
 // GB300 mapping (a fresh design; the pages' kernels target sm_75 CUDA cores and a Triton
 // kernel on sm_89):
 //   * One CTA owns two query tiles A and B of 128 rows (rows 256c .. 256c+255 of one head)
@@ -21,15 +26,16 @@
 //     256 queries.
 //   * Warp 8 issues TMA loads (128-byte swizzle) into a 3-stage K/V ring guarded by
 //     full/empty mbarriers. Warp 9 owns the tensor memory and issues every tcgen05.mma from
-//     one thread. Warps 0-3 (tile A) and 4-7 (tile B) are the softmax warpgroups: thread t
-//     of a group owns query row t, which is TMEM lane t, so row reductions need no shuffles.
+//     one thread, in whatever order their inputs become ready. Warps 0-3 (tile A) and 4-7
+//     (tile B) are the softmax warpgroups: thread t of a group owns query row t, which is
+//     TMEM lane t, so row reductions need no shuffles. The third warpgroup (warps 8-11)
+//     gives up registers so the softmax groups can hold a whole row of scores.
 //   * Tensor memory (512 columns x 128 lanes x 32 bit): S_A, S_B fp32 scores (128 columns
 //     each), O_A, O_B fp32 outputs (64 each), P_A, P_B probabilities as 16-bit pairs (64
 //     each). S = Q K^T runs with both operands in shared memory; O += P V takes P from
 //     tensor memory and V (dims contiguous, "MN-major") from shared memory.
-//   * The MMA thread issues S_X(j+1) as soon as softmax X has copied S_X(j) into registers,
-//     so the next QK^T overlaps the exponentials; while one group is in its softmax the
-//     tensor core works on the other group's products.
+//   * S_X(j+1) is issued as soon as softmax X has copied S_X(j) into registers, so the
+//     next QK^T overlaps the exponentials, and the two groups' products interleave.
 //   * Every mbarrier wait is bounded. A wait that exceeds its deadline sets the device
 //     error word and an abort flag; all roles then leave their loops, drain copies and MMAs
 //     still in flight (with a deadline of their own), free tensor memory and return.
@@ -49,34 +55,46 @@ namespace {
 constexpr int kD = 64;
 constexpr int kBM = 128;  // query rows per tile = TMEM lanes
 constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kStages = 3;
+constexpr int kKStages = 4;  // K ring depth (QK^T reads K one step ahead)
+constexpr int kVStages = 3;  // V ring depth
 constexpr int kTileBytes = kBM * kD * 2;  // 16 KiB per 128 x 64 tile of 16-bit values
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kSIssuerWarp = 9;   // also owns the tensor memory
+constexpr int kPVIssuerWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // + 128 * tile
 constexpr uint32_t kColO = 256;  // + 64 * tile
 constexpr uint32_t kColP = 384;  // + 64 * tile
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s for any single wait
 constexpr uint64_t kDrainTimeoutNs = 100000000ull;  // 100 ms to drain after an abort
+constexpr unsigned kPollSleepNs = 32;  // MMA issuers' back-off between unproductive polls
+constexpr float kLazyLog2 = 8.f;  // keep a stale max until a tile exceeds it by 2^8
+constexpr float kLazyBound = 256.f;  // 2^kLazyLog2
+// Register split: launch at 168 per thread (384 x 168 = 64512); the third warpgroup
+// drops to 56 and the two softmax groups rise to 224 (256 x 224 + 128 x 56 = 64512).
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsSoftmax = 224;
+constexpr int kRegsOther = 56;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch,
+              "register split must fit the launch allocation");
 
 // Shared-memory layout (byte offsets from a 1024-byte aligned base).
 constexpr int kOffQ = 0;                                   // 2 tiles
-constexpr int kOffK = kOffQ + 2 * kTileBytes;              // kStages tiles
-constexpr int kOffV = kOffK + kStages * kTileBytes;        // kStages tiles
-constexpr int kOffBar = kOffV + kStages * kTileBytes;      // mbarriers, 8 bytes each
-// barrier indices
+constexpr int kOffK = kOffQ + 2 * kTileBytes;              // kKStages tiles
+constexpr int kOffV = kOffK + kKStages * kTileBytes;       // kVStages tiles
+constexpr int kOffBar = kOffV + kVStages * kTileBytes;     // mbarriers, 8 bytes each
 constexpr int kBarQFull = 0;
 constexpr int kBarKFull = 1;
-constexpr int kBarVFull = kBarKFull + kStages;
-constexpr int kBarKvEmpty = kBarVFull + kStages;
-constexpr int kBarSFull = kBarKvEmpty + kStages;  // 2
-constexpr int kBarSFree = kBarSFull + 2;          // 2
-constexpr int kBarPFull = kBarSFree + 2;          // 2
-constexpr int kBarOReady = kBarPFull + 2;         // 2
-constexpr int kBarMmaDone = kBarOReady + 2;
-constexpr int kNumBars = kBarMmaDone + 1;
+constexpr int kBarKEmpty = kBarKFull + kKStages;
+constexpr int kBarVFull = kBarKEmpty + kKStages;
+constexpr int kBarVEmpty = kBarVFull + kVStages;
+constexpr int kBarSFull = kBarVEmpty + kVStages;  // [2] S_X(j) computed
+constexpr int kBarSFree = kBarSFull + 2;          // [2] softmax X copied S_X(j) out (4 warps)
+constexpr int kBarPFull = kBarSFree + 2;          // [2] softmax X wrote P_X(j) (4 warps)
+constexpr int kBarOReady = kBarPFull + 2;         // [2] PV_X(j) done: O_X stable, P_X reusable
+constexpr int kBarDrain = kBarOReady + 2;         // [2] every MMA of issuer 0 (S) / 1 (PV) done
+constexpr int kNumBars = kBarDrain + 2;
 constexpr int kOffSlot = kOffBar + 8 * kNumBars;  // TMEM base address written by tcgen05.alloc
 constexpr int kOffAbort = kOffSlot + 4;
 constexpr int kSmemUsed = kOffAbort + 4;
@@ -106,6 +124,194 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag) {
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     const bool ok = mbar_wait(bar, parity, abort_flag, kWaitTimeoutNs);
     return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t* r) {
+    ATTN_TMEM_ST_X32(taddr, r);
+}
+
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// Row maximum of 128 scores as eight independent chains of 3-input max, then a tree.
+__device__ __forceinline__ float row_max128(const float (&s)[kBN]) {
+    float mx[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) mx[g] = fmax3(s[g], s[g + 8], s[g + 16]);
+#pragma unroll
+    for (int t = 3; t < 15; t += 2)
+#pragma unroll
+        for (int g = 0; g < 8; ++g) mx[g] = fmax3(mx[g], s[g + 8 * t], s[g + 8 * t + 8]);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) mx[g] = fmaxf(mx[g], s[g + 120]);
+    return fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+}
+
+// p = 2^(s * c - m) for the 128 scores of a row, packed to 16-bit pairs (round to nearest
+// even) in `pk`; returns the fp32 sum of the unrounded p (four independent partial sums).
+template <bool BF16>
+__device__ __forceinline__ float row_exp2_t(const uint32_t (&su)[kBN], float2 c2, float2 negm,
+                                            uint32_t (&pk)[kBN / 2]) {
+    float2 acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kBN / 2; ++i) {
+        const float2 t = ffma2(make_float2(__uint_as_float(su[2 * i]), __uint_as_float(su[2 * i + 1])), c2, negm);
+        const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+        acc[i & 3] = fadd2(acc[i & 3], pp);
+        pk[i] = pack2<BF16>(pp.x, pp.y);
+    }
+    const float2 at = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+    return at.x + at.y;
+}
+
+// One softmax warpgroup's view: its lanes of S_X, O_X, P_X and its barriers.
+struct SoftmaxCtx {
+    uint32_t tS, tO, tP;
+    uint32_t bar_s_full, bar_s_free, bar_p_full, bar_o_ready;
+    volatile int* abort_flag;
+    float c;    // log2(e) / sqrt(d)
+    int limit;  // keys >= limit are masked for this row
+    int lane;
+};
+
+__device__ __forceinline__ void load_s(const SoftmaxCtx& cx, uint32_t (&su)[kBN]) {
+    tc_fence_after();
+    ATTN_TMEM_LD_X32(cx.tS + 0, (su + 0));
+    ATTN_TMEM_LD_X32(cx.tS + 32, (su + 32));
+    ATTN_TMEM_LD_X32(cx.tS + 64, (su + 64));
+    ATTN_TMEM_LD_X32(cx.tS + 96, (su + 96));
+}
+
+__device__ __forceinline__ void release_s(const SoftmaxCtx& cx) {
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (cx.lane == 0) mbar_arrive(cx.bar_s_free);
+}
+
+// One key tile of the online softmax for this thread's query row: scores in `su`, running
+// reference m and denominator l. Writes P(j) to tensor memory, rescales O when the
+// reference moves, starts loading S(j+1) and signals the MMA issuers. Returns false when a
+// wait timed out or the CTA is aborting (the result is the same in all lanes of a warp).
+template <bool BF16, bool kMasked>
+__device__ __forceinline__ bool softmax_step(const SoftmaxCtx& cx, uint32_t (&su)[kBN], float& m,
+                                             float& l, int j, int nX) {
+    // The scores stay in the registers tcgen05.ld filled (as bit patterns); masked keys get
+    // the bit pattern of -inf.
+    if constexpr (kMasked) {
+        const int nvalid = cx.limit - j * kBN;
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) su[i] = (i < nvalid) ? su[i] : 0xFF800000u;
+    }
+    const float c = cx.c;
+    const float2 c2 = make_float2(c, c);
+    // Optimistic pass: exponentials against the current (possibly stale) reference m. If
+    // some p exceeded 2^kLazyLog2 (the lazy rule would then move m), the tile's sum of p
+    // would exceed 2^kLazyLog2 too; so a sum within that bound proves m may stay, and only
+    // otherwise (or on the first tile) the row maximum is computed and p redone if m moves.
+    uint32_t pk[kBN / 2];
+    float tile_sum = INFINITY;
+    if (m != -INFINITY) tile_sum = row_exp2_t<BF16>(su, c2, make_float2(-m, -m), pk);
+    float alpha = 1.f;
+    if (!(tile_sum <= kLazyBound)) {
+        float s[kBN];
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(su[i]);
+        const float mt = row_max128(s) * c;
+        if (mt > m + kLazyLog2) {
+            alpha = ex2_approx(m - mt);  // 0 on the first tile (m = -inf)
+            m = mt;
+            l *= alpha;
+        }
+        // A row with every key masked so far keeps a zero reference (no inf - inf).
+        const float m_use = (m == -INFINITY) ? 0.f : m;
+        if (alpha != 1.f || tile_sum == INFINITY || tile_sum != tile_sum)
+            tile_sum = row_exp2_t<BF16>(su, c2, make_float2(-m_use, -m_use), pk);
+    }
+    bool rescale = false;
+    if (j > 0) {
+        if (!warp_wait(cx.bar_o_ready, (j - 1) & 1, cx.abort_flag)) return false;
+        tc_fence_after();
+        rescale = __any_sync(0xffffffffu, alpha != 1.f);
+    }
+    tmem_st_x32(cx.tP, pk);
+    tmem_st_x32(cx.tP + 32, pk + 32);
+    if (rescale) {
+        // O <- alpha * O (rare: only when some row of this warp moved its reference); done in
+        // 16-column pieces so it adds few registers to the step.
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+            uint32_t ou[16];
+            tmem_ld_x16(cx.tO + 16 * h, ou);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                const float2 v = fmul2(make_float2(__uint_as_float(ou[i]), __uint_as_float(ou[i + 1])), a2);
+                ou[i] = __float_as_uint(v.x);
+                ou[i + 1] = __float_as_uint(v.y);
+            }
+            tmem_st_x16(cx.tO + 16 * h, ou);
+        }
+    }
+    l += tile_sum;
+    const bool more = j + 1 < nX;
+    bool ok = true;
+    if (more) {  // the next scores start moving while P drains
+        ok = warp_wait(cx.bar_s_full, (j + 1) & 1, cx.abort_flag);
+        if (ok) load_s(cx, su);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (cx.lane == 0) mbar_arrive(cx.bar_p_full);
+    if (more && ok) release_s(cx);
+    return ok;
+}
+
+// S_X(j) = Q_X K_j^T : M=128, N=128, K=64 as four K=16 steps (32 bytes each).
+template <bool BF16>
+__device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sQx, uint32_t sKs, int X, uint32_t bar_s_full) {
+    constexpr uint32_t kIdescQK = idesc_f16(BF16, kBM, kBN, false, false);
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint64_t a = smem_desc_sw128(sQx + 32 * kk, 16, 1024);
+        const uint64_t b = smem_desc_sw128(sKs + 32 * kk, 16, 1024);
+        umma_ss(tmem + kColS + 128u * X, a, b, kIdescQK, kk > 0 ? 1u : 0u);
+    }
+    umma_commit(bar_s_full);
+}
+
+// O_X += P_X V_j : M=128, N=64, K=128 as eight K=16 steps (16 keys = 2048 bytes of V), P from
+// tensor memory.
+template <bool BF16>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sVs, int X, bool accumulate, uint32_t bar_o_ready) {
+    constexpr uint32_t kIdescPV = idesc_f16(BF16, kBM, kD, false, true);
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+        const uint64_t b = smem_desc_sw128(sVs + 2048 * kk, 16, 1024);
+        umma_ts(tmem + kColO + 64u * X, tmem + kColP + 64u * X + 8u * kk, b, kIdescPV,
+                (accumulate || kk > 0) ? 1u : 0u);
+    }
+    umma_commit(bar_o_ready);
 }
 
 template <bool BF16>
@@ -140,25 +346,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nB = (rowB < N) ? (p.causal ? min(nkv, rowB / kBN + 1) : nkv) : 0;
     const int nmax = max(nA, nB);
 
-    // ---- setup: barriers (thread 0), tensor memory (MMA warp) ----
+    // ---- setup: barriers (thread 0), tensor memory (S-issuer warp) ----
     if (threadIdx.x == 0) {
         mbar_init(bar(kBarQFull), 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(bar(kBarKFull + s), 1);
+            mbar_init(bar(kBarKEmpty + s), 2);  // one release per query tile
+        }
+        for (int s = 0; s < kVStages; ++s) {
             mbar_init(bar(kBarVFull + s), 1);
-            mbar_init(bar(kBarKvEmpty + s), 1);
+            mbar_init(bar(kBarVEmpty + s), 2);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(kBarSFull + x), 1);
             mbar_init(bar(kBarSFree + x), 4);
             mbar_init(bar(kBarPFull + x), 4);
             mbar_init(bar(kBarOReady + x), 1);
+            mbar_init(bar(kBarDrain + x), 1);
         }
-        mbar_init(bar(kBarMmaDone), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kSIssuerWarp) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -169,244 +378,192 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 8) {
         // =========================== softmax warpgroups ===========================
+        regs_increase<kRegsSoftmax>();
         const int X = warp >> 2;
         const int nX = X ? nB : nA;
-        const int r0 = X ? rowB : rowA;
-        const int trow = ((warp & 3) << 5) + lane;
-        const int row = r0 + trow;
+        const int row = (X ? rowB : rowA) + ((warp & 3) << 5) + lane;
         const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) << 5) << 16;
-        const uint32_t tS = tmem + lane_addr + kColS + 128u * X;
-        const uint32_t tO = tmem + lane_addr + kColO + 64u * X;
-        const uint32_t tP = tmem + lane_addr + kColP + 64u * X;
-        const float c = p.scale_log2;
-        const int limit = p.causal ? min(row + 1, N) : N;  // keys >= limit are masked
-
-        float m = -INFINITY;  // running max of scaled scores (base-2 units)
-        float l = 0.f;        // running denominator, relative to m
+        const SoftmaxCtx cx{tmem + lane_addr + kColS + 128u * X, tmem + lane_addr + kColO + 64u * X,
+                            tmem + lane_addr + kColP + 64u * X, bar(kBarSFull + X), bar(kBarSFree + X),
+                            bar(kBarPFull + X), bar(kBarOReady + X), abort_flag, p.scale_log2,
+                            p.causal ? min(row + 1, N) : N, lane};
+        float m = -INFINITY;  // reference max of scaled scores (base-2 units), possibly stale
+        float l = 0.f;        // running denominator relative to m
         bool ok = true;
-        for (int j = 0; j < nX; ++j) {
-            if (!warp_wait(bar(kBarSFull + X), j & 1, abort_flag)) {
-                raise_abort(abort_flag);
-                ok = false;
-                break;
+        // `su` holds the scores of the tile about to be used; S(j+1) is copied out of tensor
+        // memory while P(j) drains (software pipelining).
+        uint32_t su[kBN];
+        if (nX > 0) {
+            ok = warp_wait(cx.bar_s_full, 0, abort_flag);
+            if (ok) {
+                load_s(cx, su);
+                release_s(cx);
             }
-            tc_fence_after();
-            uint32_t su[kBN];
-            ATTN_TMEM_LD_X32(tS + 0, (su + 0));
-            ATTN_TMEM_LD_X32(tS + 32, (su + 32));
-            ATTN_TMEM_LD_X32(tS + 64, (su + 64));
-            ATTN_TMEM_LD_X32(tS + 96, (su + 96));
-            tmem_ld_wait();
-            float s[kBN];
-#pragma unroll
-            for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(su[i]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarSFree + X));
-
-            const int kbase = j * kBN;
-            if (kbase + kBN > limit || kbase + kBN > N) {
-#pragma unroll
-                for (int i = 0; i < kBN; ++i)
-                    if (kbase + i >= limit) s[i] = -INFINITY;
-            }
-            float mx = s[0];
-#pragma unroll
-            for (int i = 1; i + 1 < kBN; i += 2) mx = fmax3(mx, s[i], s[i + 1]);
-            mx = fmaxf(mx, s[kBN - 1]);
-            const float m_new = fmaxf(m, mx * c);
-            // A row with every key masked so far keeps a zero reference so no inf - inf occurs.
-            const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ex2_approx(m - m_ref);
-            const float neg = -m_ref;
-
-            bool rescale = false;
-            if (j > 0) {
-                // O and P are still in use by the previous PV product until it completes.
-                if (!warp_wait(bar(kBarOReady + X), (j - 1) & 1, abort_flag)) {
-                    raise_abort(abort_flag);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                rescale = __any_sync(0xffffffffu, alpha != 1.f);
-            }
-            float rs = 0.f;
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2_approx(fmaf(s[32 * h + 2 * i], c, neg));
-                    const float p1 = ex2_approx(fmaf(s[32 * h + 2 * i + 1], c, neg));
-                    rs += p0 + p1;
-                    pk[i] = pack2<BF16>(p0, p1);
-                }
-                asm volatile(
-                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,"
-                    "%10,%11,%12,%13,%14,%15,%16};" ::"r"(tP + 16 * h),
-                    "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]),
-                    "r"(pk[6]), "r"(pk[7]), "r"(pk[8]), "r"(pk[9]), "r"(pk[10]), "r"(pk[11]),
-                    "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
-                    : "memory");
-            }
-            if (rescale) {
-                // O <- alpha * O, after the scores are spent so both never occupy registers.
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t ou[32];
-                    ATTN_TMEM_LD_X32(tO + 32 * h, ou);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) ou[i] = __float_as_uint(__uint_as_float(ou[i]) * alpha);
-                    ATTN_TMEM_ST_X32(tO + 32 * h, ou);
-                }
-            }
-            l = l * alpha + rs;
-            m = m_ref;
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarPFull + X));
         }
+        // Only a query tile's last key tile can hold masked keys (the causal diagonal or
+        // keys past N), so the loop runs mask-free and the last step is peeled off.
+        for (int j = 0; ok && j + 1 < nX; ++j) ok = softmax_step<BF16, false>(cx, su, m, l, j, nX);
+        if (ok && nX > 0) ok = softmax_step<BF16, true>(cx, su, m, l, nX - 1, nX);
 
         // ---- epilogue: O / l, rounded to the output type, rows >= N not stored ----
         if (ok && nX > 0) {
-            if (warp_wait(bar(kBarOReady + X), (nX - 1) & 1, abort_flag)) {
+            if (warp_wait(cx.bar_o_ready, (nX - 1) & 1, abort_flag)) {
                 tc_fence_after();
                 const float inv = 1.f / l;
-                using elem = uint16_t;
-                elem* const orow = reinterpret_cast<elem*>(p.o) +
-                                   (static_cast<int64_t>(bh) * N + row) * kD;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t ou[32];
-                    ATTN_TMEM_LD_X32(tO + 32 * h, ou);
+                uint16_t* const orow = reinterpret_cast<uint16_t*>(p.o) +
+                                       (static_cast<int64_t>(bh) * N + row) * kD;
+#pragma unroll 1
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t ou[16];
+                    tmem_ld_x16(cx.tO + 16 * h, ou);
                     tmem_ld_wait();
-                    uint32_t pk[16];
+                    uint32_t pk[8];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
+                    for (int i = 0; i < 8; ++i)
                         pk[i] = pack2<BF16>(__uint_as_float(ou[2 * i]) * inv,
                                             __uint_as_float(ou[2 * i + 1]) * inv);
                     if (row < N) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * h);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        uint4* dst = reinterpret_cast<uint4*>(orow + 16 * h);
+                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                     }
                 }
             } else {
-                raise_abort(abort_flag);
+                ok = false;
             }
         }
-    } else if (warp == kProducerWarp) {
-        // =============================== TMA producer ===============================
-        if (lane == 0) {
+        if (!ok) raise_abort(abort_flag);
+    } else {
+        regs_decrease<kRegsOther>();
+        if (warp == kProducerWarp && lane == 0) {
+            // =============================== TMA producer ===============================
             prefetch_tmap(&tmap_q);
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
             mbar_arrive_expect_tx(bar(kBarQFull), (nB > 0 ? 2 : 1) * kTileBytes);
             tma_load_3d(sQ, &tmap_q, 0, rowA, bh, bar(kBarQFull));
             if (nB > 0) tma_load_3d(sQ + kTileBytes, &tmap_q, 0, rowB, bh, bar(kBarQFull));
-            int issued = 0;
-            for (int j = 0; j < nmax; ++j) {
-                const int s = j % kStages;
-                if (!mbar_wait(bar(kBarKvEmpty + s), ((j / kStages) & 1) ^ 1, abort_flag,
-                               kWaitTimeoutNs)) {
-                    raise_abort(abort_flag);
+            // K runs ahead of V: K_j is needed by S(j) a step before V_j is needed by PV(j).
+            int kissued = 0, vissued = 0;
+            bool ok = true;
+            for (int j = 0; ok && j < nmax; ++j) {
+                const int sk = j % kKStages;
+                if (!(ok = mbar_wait(bar(kBarKEmpty + sk), ((j / kKStages) & 1) ^ 1, abort_flag, kWaitTimeoutNs)))
                     break;
+                mbar_arrive_expect_tx(bar(kBarKFull + sk), kTileBytes);
+                tma_load_3d(sK + sk * kTileBytes, &tmap_k, 0, j * kBN, bh, bar(kBarKFull + sk));
+                kissued = j + 1;
+                for (; vissued < j; ++vissued) {  // V_{j-1} after K_j
+                    const int sv = vissued % kVStages;
+                    if (!(ok = mbar_wait(bar(kBarVEmpty + sv), ((vissued / kVStages) & 1) ^ 1, abort_flag,
+                                         kWaitTimeoutNs)))
+                        break;
+                    mbar_arrive_expect_tx(bar(kBarVFull + sv), kTileBytes);
+                    tma_load_3d(sV + sv * kTileBytes, &tmap_v, 0, vissued * kBN, bh, bar(kBarVFull + sv));
                 }
-                mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
-                tma_load_3d(sK + s * kTileBytes, &tmap_k, 0, j * kBN, bh, bar(kBarKFull + s));
-                mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
-                tma_load_3d(sV + s * kTileBytes, &tmap_v, 0, j * kBN, bh, bar(kBarVFull + s));
-                issued = j + 1;
             }
+            for (; ok && vissued < nmax; ++vissued) {
+                const int sv = vissued % kVStages;
+                if (!(ok = mbar_wait(bar(kBarVEmpty + sv), ((vissued / kVStages) & 1) ^ 1, abort_flag,
+                                     kWaitTimeoutNs)))
+                    break;
+                mbar_arrive_expect_tx(bar(kBarVFull + sv), kTileBytes);
+                tma_load_3d(sV + sv * kTileBytes, &tmap_v, 0, vissued * kBN, bh, bar(kBarVFull + sv));
+            }
+            if (!ok) raise_abort(abort_flag);
             // Every copy issued must have landed before the CTA may exit. In normal operation
             // they were all consumed already and these waits return at once.
             mbar_wait(bar(kBarQFull), 0, nullptr, kDrainTimeoutNs);
-            for (int j = max(0, issued - kStages); j < issued; ++j) {
-                const int s = j % kStages;
-                mbar_wait(bar(kBarKFull + s), (j / kStages) & 1, nullptr, kDrainTimeoutNs);
-                mbar_wait(bar(kBarVFull + s), (j / kStages) & 1, nullptr, kDrainTimeoutNs);
-            }
-        }
-    } else {
-        // ================================ MMA issuer ================================
-        if (lane == 0) {
-            constexpr uint32_t kIdescQK = idesc_f16(BF16, kBM, kBN, false, false);
-            constexpr uint32_t kIdescPV = idesc_f16(BF16, kBM, kD, false, true);
+            for (int j = max(0, kissued - kKStages); j < kissued; ++j)
+                mbar_wait(bar(kBarKFull + j % kKStages), (j / kKStages) & 1, nullptr, kDrainTimeoutNs);
+            for (int j = max(0, vissued - kVStages); j < vissued; ++j)
+                mbar_wait(bar(kBarVFull + j % kVStages), (j / kVStages) & 1, nullptr, kDrainTimeoutNs);
+        } else if (warp == kSIssuerWarp && lane == 0) {
+            // ============================ S issuer: QK^T ============================
+            // S_X(j) goes out as soon as K_j has landed and (j > 0) softmax X has copied
+            // S_X(j-1) out of tensor memory; the two tiles progress independently. Each tile
+            // releases K_j once (twice when the other tile does not read K_j).
             bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, kWaitTimeoutNs);
-            bool issued_any = false;
-
-            // S_X(j) = Q_X K_j^T : M=128, N=128, K=64 as four K=16 steps (32 bytes each)
-            auto issue_s = [&](int X, int j) {
-                const int s = j % kStages;
+            int ns0 = 0, ns1 = 0;
+            uint64_t idle_since = 0;
+            uint32_t polls = 0;
+            while (ok && (ns0 < nA || ns1 < nB)) {
+                bool progressed = false;
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint64_t a = smem_desc_sw128(sQ + X * kTileBytes + 32 * kk, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(sK + s * kTileBytes + 32 * kk, 16, 1024);
-                    umma_ss(tmem + kColS + 128u * X, a, b, kIdescQK, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(bar(kBarSFull + X));
-                issued_any = true;
-            };
-            // O_X += P_X V_j : M=128, N=64, K=128 as eight K=16 steps (16 keys = 2048 bytes of V)
-            auto issue_pv = [&](int X, int j) {
-                const int s = j % kStages;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t b = smem_desc_sw128(sV + s * kTileBytes + 2048 * kk, 16, 1024);
-                    umma_ts(tmem + kColO + 64u * X, tmem + kColP + 64u * X + 8u * kk, b, kIdescPV,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                umma_commit(bar(kBarOReady + X));
-                issued_any = true;
-            };
-
-            if (ok && nmax > 0) {
-                ok = mbar_wait(bar(kBarKFull + 0), 0, abort_flag, kWaitTimeoutNs);
-                if (ok) {
-                    tc_fence_after();
-                    if (nA > 0) issue_s(0, 0);
-                    if (nB > 0) issue_s(1, 0);
-                }
-            }
-            for (int j = 0; ok && j < nmax; ++j) {
-                const int s = j % kStages;
-                const int s1 = (j + 1) % kStages;
-                for (int X = 0; X < 2 && ok; ++X) {
-                    if (j + 1 < (X ? nB : nA)) {
-                        ok = mbar_wait(bar(kBarKFull + s1), ((j + 1) / kStages) & 1, abort_flag,
-                                       kWaitTimeoutNs) &&
-                             mbar_wait(bar(kBarSFree + X), j & 1, abort_flag, kWaitTimeoutNs);
-                        if (!ok) break;
+                for (int X = 0; X < 2; ++X) {
+                    int& j = X ? ns1 : ns0;
+                    const int nX = X ? nB : nA, nO = X ? nA : nB;
+                    if (j < nX && mbar_test(bar(kBarKFull + j % kKStages), (j / kKStages) & 1) &&
+                        (j == 0 || mbar_test(bar(kBarSFree + X), (j - 1) & 1))) {
                         tc_fence_after();
-                        issue_s(X, j + 1);
-                    }
-                    if (j < (X ? nB : nA)) {
-                        ok = mbar_wait(bar(kBarVFull + s), (j / kStages) & 1, abort_flag,
-                                       kWaitTimeoutNs) &&
-                             mbar_wait(bar(kBarPFull + X), j & 1, abort_flag, kWaitTimeoutNs);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(X, j);
+                        issue_s<BF16>(tmem, sQ + X * kTileBytes, sK + (j % kKStages) * kTileBytes, X,
+                                      bar(kBarSFull + X));
+                        umma_commit(bar(kBarKEmpty + j % kKStages));
+                        if (j >= nO) umma_commit(bar(kBarKEmpty + j % kKStages));
+                        ++j;
+                        progressed = true;
                     }
                 }
-                if (ok) umma_commit(bar(kBarKvEmpty + s));
+                if (progressed) {
+                    idle_since = 0;
+                } else {
+                    // Nothing ready: yield the issue slots to the softmax warps for a moment.
+                    __nanosleep(kPollSleepNs);
+                    if ((++polls & 15u) == 0) {
+                        const uint64_t now = global_timer_ns();
+                        if (idle_since == 0) idle_since = now;
+                        if (*abort_flag || now - idle_since > kWaitTimeoutNs) ok = false;
+                    }
+                }
             }
             if (!ok) raise_abort(abort_flag);
-            // No MMA may still be running when the tensor memory is released.
-            if (issued_any) {
-                umma_commit(bar(kBarMmaDone));
-                mbar_wait(bar(kBarMmaDone), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+            umma_commit(bar(kBarDrain + 0));  // no S product may still run at teardown
+            mbar_wait(bar(kBarDrain + 0), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+        } else if (warp == kPVIssuerWarp && lane == 0) {
+            // ============================== PV issuer ==============================
+            // PV_X(j) goes out as soon as V_j has landed and softmax X has written P_X(j); the
+            // two tiles progress independently and each releases V_j as above.
+            bool ok = true;
+            int np0 = 0, np1 = 0;
+            uint64_t idle_since = 0;
+            uint32_t polls = 0;
+            while (ok && (np0 < nA || np1 < nB)) {
+                bool progressed = false;
+#pragma unroll
+                for (int X = 0; X < 2; ++X) {
+                    int& j = X ? np1 : np0;
+                    const int nX = X ? nB : nA, nO = X ? nA : nB;
+                    if (j < nX && mbar_test(bar(kBarVFull + j % kVStages), (j / kVStages) & 1) &&
+                        mbar_test(bar(kBarPFull + X), j & 1)) {
+                        tc_fence_after();
+                        issue_pv<BF16>(tmem, sV + (j % kVStages) * kTileBytes, X, j > 0, bar(kBarOReady + X));
+                        umma_commit(bar(kBarVEmpty + j % kVStages));
+                        if (j >= nO) umma_commit(bar(kBarVEmpty + j % kVStages));
+                        ++j;
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    idle_since = 0;
+                } else {
+                    // Nothing ready: yield the issue slots to the softmax warps for a moment.
+                    __nanosleep(kPollSleepNs);
+                    if ((++polls & 15u) == 0) {
+                        const uint64_t now = global_timer_ns();
+                        if (idle_since == 0) idle_since = now;
+                        if (*abort_flag || now - idle_since > kWaitTimeoutNs) ok = false;
+                    }
+                }
             }
+            if (!ok) raise_abort(abort_flag);
+            umma_commit(bar(kBarDrain + 1));  // no PV product may still run at teardown
+            mbar_wait(bar(kBarDrain + 1), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kSIssuerWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -454,6 +611,12 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, bool bf1
 template <bool BF16>
 int launch_impl(const void* q, const void* k, const void* v, void* o, int64_t BH, int64_t N,
                 bool causal, cudaStream_t stream) {
+    // The register split assumes the launch allocation; a smaller one could leave the
+    // softmax groups waiting for registers forever, so it is refused instead.
+    cudaFuncAttributes fattr;
+    if (cudaFuncGetAttributes(&fattr, attn_fwd_tc_kernel<BF16>) != cudaSuccess ||
+        fattr.numRegs < kRegsLaunch)
+        return ATTN_ERR_LAUNCH;
     CUtensorMap mq, mk, mv;
     if (!make_map(&mq, q, BH, N, BF16) || !make_map(&mk, k, BH, N, BF16) ||
         !make_map(&mv, v, BH, N, BF16))

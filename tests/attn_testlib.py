@@ -4,7 +4,10 @@ the tolerance rules.
 Tolerances (spec contract, with the attention.cu gate reported beside it):
 * fp32: max |got - ref| <= 1e-5 * N * max |ref|  (the K-scaled rule with K = N);
   attention.cu's own gate |got - ref| <= atol + rtol |ref| with rtol = max(1e-5, 4 * 2^-23 *
-  sqrt(N)), atol = rtol * max |ref| is computed too, and must also hold.
+  sqrt(N)), atol = rtol * max |ref| is computed too, and must also hold — except for q, k
+  scaled x8 (logit std ~64), where fp32 rounding of the scores alone exceeds it (PyTorch's
+  own fp32 attention scores 1.08 on the same inputs); there the Triton page's rule applies
+  instead: the error is at most twice PyTorch's fp32 error against the same reference.
 * bf16 / fp16: max |got - ref| <= 2e-2, against the double oracle on the same rounded inputs.
 Non-finite output fails outright.
 """
@@ -51,7 +54,8 @@ def page_gate_fraction(got: np.ndarray, ref: np.ndarray, N: int) -> float:
     return float(np.max(np.abs(got - ref) / (atol + rtol * np.abs(ref))))
 
 
-def check(got: np.ndarray, ref: np.ndarray, dtype: str, N: int, what: str = "") -> dict:
+def check(got: np.ndarray, ref: np.ndarray, dtype: str, N: int, what: str = "",
+          page_gate: bool = True) -> dict:
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     err = np.abs(got - ref)
@@ -63,7 +67,8 @@ def check(got: np.ndarray, ref: np.ndarray, dtype: str, N: int, what: str = "") 
         rep["bound"] = bound
         rep["gate_fraction"] = page_gate_fraction(got, ref, N)
         assert max_err <= bound, f"{what}: fp32 max err {max_err:.3e} > {bound:.3e}"
-        assert rep["gate_fraction"] <= 1.0, f"{what}: attention.cu gate fraction {rep['gate_fraction']:.3f}"
+        if page_gate:
+            assert rep["gate_fraction"] <= 1.0, f"{what}: attention.cu gate fraction {rep['gate_fraction']:.3f}"
     else:
         rep["bound"] = 2e-2
         if max_err > 2e-2:
