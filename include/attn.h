@@ -102,6 +102,33 @@ int attn_fwd_materialized(const void* q, const void* k, const void* v, void* o, 
 size_t attn_materialized_workspace_bytes(int64_t B, int64_t H, int64_t N);
 
 /*
+ * attn_fwd_materialized_noalloc — the materialised path of attn_fwd_materialized with no
+ * workspace argument and no allocation of any kind. (The attention pages have no counterpart:
+ * this is a convenience of this library.) It is meant for callers that cannot allocate
+ * device memory or hand over a scratch buffer — for example code running under an allocator
+ * it does not own, or on a path that must not call cudaMalloc/cudaFree because those can
+ * synchronise the device.
+ *
+ *   Scratch: a fixed array of ATTN_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU
+ *            that loads the library holds it until the process exits. Heads run in groups of
+ *            as many as fit.
+ *   Limit:   N <= ATTN_NOALLOC_MAX_N (one head's scores and probabilities must fit the
+ *            array); larger N returns ATTN_ERR_UNSUPPORTED and launches nothing.
+ *   Set-up:  the first call on a device looks up the array's device address
+ *            (cudaGetSymbolAddress) with that device current; make that first call before
+ *            capturing a stream into a graph.
+ *   Sharing: all calls use the same array, which keeps the previous call's contents (no call
+ *            depends on them: everything is written before it is read). Calls whose kernels
+ *            overlap on the GPU — unordered streams, several host threads — race on it.
+ *   Other arguments, layout and errors: as attn_fwd.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+#define ATTN_NOALLOC_MAX_N ((int64_t)2896)
+int attn_fwd_materialized_noalloc(const void* q, const void* k, const void* v, void* o, int64_t B,
+                                  int64_t H, int64_t N, int64_t d, int causal, int dtype,
+                                  void* stream);
+
+/*
  * attn_device_status — synchronises `stream`, then reports whether any kernel of this
  * library on the current device recorded a device-side wait timeout since the flag was
  * last cleared. Returns ATTN_OK or ATTN_ERR_TIMEOUT (ATTN_ERR_DEVICE if a CUDA call

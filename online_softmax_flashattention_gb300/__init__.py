@@ -24,7 +24,8 @@ import torch
 __all__ = [
     "ATTN_F32", "ATTN_BF16", "ATTN_F16", "AttnError", "AttnLibraryMissing", "library_path",
     "attn_fwd", "attn_fwd_materialized", "attn_materialized_workspace_bytes", "attn_device_status",
-    "attn_status_string", "attn_abi_version", "raw",
+    "attn_status_string", "attn_abi_version", "raw", "attn_fwd_materialized_noalloc",
+    "ATTN_NOALLOC_MAX_N",
 ]
 
 ATTN_F32, ATTN_BF16, ATTN_F16 = 0, 1, 2
@@ -158,3 +159,31 @@ def attn_device_status(clear: bool = True, stream: torch.cuda.Stream | None = No
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index or 0)
     with torch.cuda.device(dev):
         return int(raw().attn_device_status(_stream(dev, stream), int(bool(clear))))
+
+
+ATTN_NOALLOC_MAX_N = 2896  # include/attn.h: largest N whose per-head scratch fits the fixed array
+
+
+def attn_fwd_materialized_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                                  out: torch.Tensor | None = None,
+                                  stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """The materialised path without a workspace: its scratch is a fixed array inside the
+    library, so the library allocates nothing. Meant for callers that cannot allocate device
+    memory. ``out`` may be passed to avoid the one allocation this Python wrapper would
+    otherwise make for the result. N must not exceed ``ATTN_NOALLOC_MAX_N``; concurrent calls
+    whose kernels overlap on the GPU share the scratch and race."""
+    _check(q, k, v)
+    B, H, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    lib = raw()
+    fn = lib.attn_fwd_materialized_noalloc
+    vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    fn.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ci, ci, vp]
+    fn.restype = ci
+    with torch.cuda.device(q.device):
+        st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, d, int(bool(causal)),
+                _DTYPES[q.dtype], _stream(q.device, stream))
+    if st != 0:
+        raise AttnError(st, "attn_fwd_materialized_noalloc")
+    return out
