@@ -407,6 +407,24 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """The timed kernel on the timed workload, a few launches and nothing else: the command
+    that ncu captures (``ncu ... python bench.py --profile``)."""
+    import torch
+
+    import online_softmax_flashattention_gb300 as fa
+
+    q, k, v = make_inputs()
+    qd, kd, vd = (torch.from_numpy(x).to("cuda").to(torch.bfloat16) for x in (q, k, v))
+    od = torch.empty_like(qd)
+    for _ in range(args.profile_launches):
+        fa.attn_fwd(qd, kd, vd, causal=True, out=od)
+    torch.cuda.synchronize()
+    if fa.attn_device_status(clear=True) != 0:
+        raise RuntimeError("device-side timeout")
+    print(f"profile: {args.profile_launches} launches of attn_fwd on {WORKLOAD['workload']}")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -417,10 +435,14 @@ def main(argv=None):
     ap.add_argument("--reference-seconds", type=float, default=90.0, help="reference arm budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
+    ap.add_argument("--profile", action="store_true", help="only launch the timed kernel (for ncu)")
+    ap.add_argument("--profile-launches", type=int, default=4)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     rank, world, local = dist_env()
+    if args.profile:
+        return run_profile(args)
     if args.impl == "reference":
         return run_reference(args, rank, world)
     return run_ours(args, rank, world, local)

@@ -44,6 +44,8 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "attn_internal.h"
@@ -76,8 +78,9 @@ constexpr float kLazyBound = 256.f;  // 2^kLazyLog2
 constexpr int kRegsLaunch = 168;
 constexpr int kRegsSoftmax = 224;
 constexpr int kRegsOther = 56;
-static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch,
+static_assert(2 * 128 * kRegsSoftmax + (kThreads - 2 * 128) * kRegsOther <= kThreads * kRegsLaunch,
               "register split must fit the launch allocation");
+static_assert(kThreads * kRegsLaunch <= 65536, "launch allocation must fit the register file");
 
 // Shared-memory layout (byte offsets from a 1024-byte aligned base).
 constexpr int kOffQ = 0;                                   // 2 tiles
@@ -615,16 +618,25 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, int64_t BH
     // softmax groups waiting for registers forever, so it is refused instead.
     cudaFuncAttributes fattr;
     if (cudaFuncGetAttributes(&fattr, attn_fwd_tc_kernel<BF16>) != cudaSuccess ||
-        fattr.numRegs < kRegsLaunch)
+        fattr.numRegs < kRegsLaunch) {
+        if (std::getenv("ATTN_DEBUG"))
+            std::fprintf(stderr, "attn: kernel has %d registers per thread, the register split needs %d\n",
+                         fattr.numRegs, kRegsLaunch);
         return ATTN_ERR_LAUNCH;
+    }
     CUtensorMap mq, mk, mv;
     if (!make_map(&mq, q, BH, N, BF16) || !make_map(&mk, k, BH, N, BF16) ||
         !make_map(&mv, v, BH, N, BF16))
         return ATTN_ERR_DEVICE;
     // The attribute is per device; setting it on every call is cheap and thread-safe.
-    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
+    const cudaError_t aerr = cudaFuncSetAttribute(attn_fwd_tc_kernel<BF16>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (aerr != cudaSuccess) {
+        if (std::getenv("ATTN_DEBUG"))
+            std::fprintf(stderr, "attn: cannot grant %d bytes of shared memory: %s\n", kSmemBytes,
+                         cudaGetErrorString(aerr));
         return ATTN_ERR_LAUNCH;
+    }
     TcParams prm;
     prm.o = o;
     prm.N = static_cast<int>(N);
@@ -636,7 +648,10 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, int64_t BH
     if (blocks > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     attn_fwd_tc_kernel<BF16><<<static_cast<unsigned>(blocks), kThreads, kSmemBytes, stream>>>(
         mq, mk, mv, prm);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess && std::getenv("ATTN_DEBUG"))
+        std::fprintf(stderr, "attn: tensor-core kernel launch failed: %s\n", cudaGetErrorString(err));
+    return err == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 }  // namespace

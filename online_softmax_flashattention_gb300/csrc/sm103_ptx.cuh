@@ -79,6 +79,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Shared-memory counter with acquire-release ordering: the thread that brings the count to a
+// multiple of n knows every earlier arrival (and what each did before arriving) happened.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+    return old;
+}
+
 // ---------------------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), completion counted in bytes on an mbarrier
 // ---------------------------------------------------------------------------------------
