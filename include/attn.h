@@ -78,6 +78,24 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, int64_t B, in
              int64_t N, int64_t d, int causal, int dtype, void* stream);
 
 /*
+ * attn_fwd_lse — attn_fwd that also stores each row's log-sum-exp, the log of the sum the
+ * softmax divides by, which a backward pass needs to rebuild the probabilities from the
+ * scores. Following the "Flash attention in PyTorch, then in Triton" page (section
+ * "Backwards, and training with it": the forward kernel "stores each row's log-sum-exp,
+ * which in our powers of two is m plus log two of l"), it is kept in base 2:
+ *
+ *     lse[b,h,i] = log2( sum_{j in vis(i)} exp( q[b,h,i,:] . k[b,h,j,:] / sqrt(d) ) )
+ *
+ * (multiply by ln 2 for the natural-log value).
+ *
+ *   lse            : device pointer, float32 [B, H, N] contiguous, 4-byte aligned, must not
+ *                    overlap q, k, v or o; every element is written
+ *   other arguments: as attn_fwd; o is bit-identical to what attn_fwd writes.
+ */
+int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                 int64_t H, int64_t N, int64_t d, int causal, int dtype, void* stream);
+
+/*
  * attn_fwd_materialized — the same result by the materialised path of attention.cu
  * (scoresQKt, softmaxRows, weightedV): S = q k^T / sqrt(d) with masked entries set to
  * -inf, written in full as fp32; a three-pass safe softmax that writes exp(S - rowmax) to
@@ -139,7 +157,7 @@ int attn_device_status(void* stream, int clear);
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* attn_status_string(int status);
 
-/* ABI version of this header: (major << 16) | minor. */
+/* ABI version of this header: (major << 16) | minor (1.1 added attn_fwd_lse). */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

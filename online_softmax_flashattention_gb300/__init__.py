@@ -25,7 +25,7 @@ __all__ = [
     "ATTN_F32", "ATTN_BF16", "ATTN_F16", "AttnError", "AttnLibraryMissing", "library_path",
     "attn_fwd", "attn_fwd_materialized", "attn_materialized_workspace_bytes", "attn_device_status",
     "attn_status_string", "attn_abi_version", "raw", "attn_fwd_materialized_noalloc",
-    "ATTN_NOALLOC_MAX_N",
+    "ATTN_NOALLOC_MAX_N", "attn_fwd_lse",
 ]
 
 ATTN_F32, ATTN_BF16, ATTN_F16 = 0, 1, 2
@@ -66,6 +66,8 @@ def raw():
             vp, i64, ci, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ci, ci, vp]
             lib.attn_fwd.restype = ci
+            lib.attn_fwd_lse.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ci, ci, vp]
+            lib.attn_fwd_lse.restype = ci
             lib.attn_fwd_materialized.argtypes = [vp, vp, vp, vp, vp, sz, i64, i64, i64, i64, ci, ci, vp]
             lib.attn_fwd_materialized.restype = ci
             lib.attn_materialized_workspace_bytes.argtypes = [i64, i64, i64]
@@ -124,6 +126,30 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
     if st != 0:
         raise AttnError(st, "attn_fwd")
     return out
+
+
+def attn_fwd_lse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                 stream: torch.cuda.Stream | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """``(o, lse)``: the flash forward and each row's base-2 log-sum-exp,
+    ``lse[b, h, i] = log2(sum_j exp(q_i . k_j / sqrt(d)))`` (float32 ``[B, H, N]``)."""
+    _check(q, k, v)
+    B, H, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or out.device != q.device or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    elif lse.shape != (B, H, N) or lse.dtype != torch.float32 or lse.device != q.device or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, N] on q's device")
+    lib = raw()
+    with torch.cuda.device(q.device):
+        st = lib.attn_fwd_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                              B, H, N, d, int(bool(causal)), _DTYPES[q.dtype], _stream(q.device, stream))
+    if st != 0:
+        raise AttnError(st, "attn_fwd_lse")
+    return out, lse
 
 
 def attn_materialized_workspace_bytes(B: int, H: int, N: int) -> int:

@@ -72,20 +72,32 @@ extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, int64_t B, int64_t H,
              int64_t N, int64_t d, int causal, int dtype, void* stream) {
+    return attn_fwd_lse(q, k, v, o, nullptr, B, H, N, d, causal, dtype, stream);
+}
+
+int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                 int64_t H, int64_t N, int64_t d, int causal, int dtype, void* stream) {
     int64_t BH = 0;
     size_t bytes = 0;
     bool skip = false;
     int st = check_common(q, k, v, o, B, H, N, d, causal, dtype, &BH, &bytes, &skip);
     if (st != ATTN_OK || skip) return st;
+    if (lse != nullptr) {
+        if (!aligned(lse, 4)) return ATTN_ERR_ALIGN;
+        const size_t lbytes = static_cast<size_t>(BH) * static_cast<size_t>(N) * sizeof(float);
+        if (overlap(lse, lbytes, q, bytes) || overlap(lse, lbytes, k, bytes) || overlap(lse, lbytes, v, bytes) ||
+            overlap(lse, lbytes, o, bytes))
+            return ATTN_ERR_ALIAS;
+    }
     int num_sms = 0;
     if ((st = check_device(&num_sms)) != ATTN_OK) return st;
     if (inject_launch_fault()) return ATTN_ERR_LAUNCH;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == ATTN_F32)
         return attn::launch_fwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
-                                    static_cast<const float*>(v), static_cast<float*>(o), BH, N,
+                                    static_cast<const float*>(v), static_cast<float*>(o), lse, BH, N,
                                     causal != 0, num_sms, s);
-    return attn::launch_fwd_tc(q, k, v, o, BH, N, causal != 0, dtype == ATTN_BF16, num_sms, s);
+    return attn::launch_fwd_tc(q, k, v, o, lse, BH, N, causal != 0, dtype == ATTN_BF16, num_sms, s);
 }
 
 size_t attn_materialized_workspace_bytes(int64_t B, int64_t H, int64_t N) {
@@ -155,6 +167,6 @@ const char* attn_status_string(int status) {
     }
 }
 
-int attn_abi_version(void) { return (1 << 16) | 0; }
+int attn_abi_version(void) { return (1 << 16) | 1; }
 
 }  // extern "C"

@@ -14,6 +14,9 @@
 // dims tx*4 + j. Rows of shared tiles are padded to 68 floats so that every float4 read of a
 // key row, every P store and every V read is free of bank conflicts. The 16 threads that
 // share a row sit in one half-warp, so row max and row sum are 4-step xor shuffles.
+// With an `lse` pointer each row's log-sum-exp is stored too, in base 2 as the page's
+// forward kernel keeps it for the backward pass (m + log2 l, "Backwards, and training with
+// it").
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -37,8 +40,8 @@ __device__ __forceinline__ float ex2f(float x) {
 template <int BM>
 __global__ void __launch_bounds__(BM * 4)
     attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
-                        const float* __restrict__ v, float* __restrict__ o, int N, int BH,
-                        int nblk, int causal, float c) {
+                        const float* __restrict__ v, float* __restrict__ o, float* __restrict__ lse,
+                        int N, int BH, int nblk, int causal, float c) {
     constexpr int kThreads = BM * 4;
     extern __shared__ float4 smem4[];
     float* const Qs = reinterpret_cast<float*>(smem4);
@@ -185,13 +188,14 @@ __global__ void __launch_bounds__(BM * 4)
             const float inv = 1.f / tot;
             *reinterpret_cast<float4*>(o + head + static_cast<int64_t>(row) * kD + 4 * tx) =
                 make_float4(acc[i][0] * inv, acc[i][1] * inv, acc[i][2] * inv, acc[i][3] * inv);
+            if (lse != nullptr && tx == 0) lse[static_cast<int64_t>(bh) * N + row] = m[i] + log2f(tot);
         }
     }
 }
 
 template <int BM>
-int launch_bm(const float* q, const float* k, const float* v, float* o, int64_t BH, int64_t N,
-              bool causal, cudaStream_t stream) {
+int launch_bm(const float* q, const float* k, const float* v, float* o, float* lse, int64_t BH,
+              int64_t N, bool causal, cudaStream_t stream) {
     const int smem = (2 * BM + 2 * kBN) * kLd * static_cast<int>(sizeof(float));
     if (cudaFuncSetAttribute(attn_fwd_f32_kernel<BM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
@@ -201,20 +205,20 @@ int launch_bm(const float* q, const float* k, const float* v, float* o, int64_t 
     if (blocks > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     const float c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
     attn_fwd_f32_kernel<BM><<<static_cast<unsigned>(blocks), BM * 4, smem, stream>>>(
-        q, k, v, o, static_cast<int>(N), static_cast<int>(BH), static_cast<int>(nblk), causal ? 1 : 0, c);
+        q, k, v, o, lse, static_cast<int>(N), static_cast<int>(BH), static_cast<int>(nblk), causal ? 1 : 0, c);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 }  // namespace
 
-int launch_fwd_f32(const float* q, const float* k, const float* v, float* o, int64_t BH, int64_t N,
-                   bool causal, int num_sms, cudaStream_t stream) {
+int launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int64_t BH,
+                   int64_t N, bool causal, int num_sms, cudaStream_t stream) {
     if (N > 0x7FFFFFFFll - 64 || BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     // Small problems use 32-row blocks so that more SMs get work.
     const int64_t blocks64 = ((N + 63) / 64) * BH;
     if (blocks64 < 2 * static_cast<int64_t>(num_sms))
-        return launch_bm<32>(q, k, v, o, BH, N, causal, stream);
-    return launch_bm<64>(q, k, v, o, BH, N, causal, stream);
+        return launch_bm<32>(q, k, v, o, lse, BH, N, causal, stream);
+    return launch_bm<64>(q, k, v, o, lse, BH, N, causal, stream);
 }
 
 }  // namespace attn

@@ -36,6 +36,9 @@
 //     tensor memory and V (dims contiguous, "MN-major") from shared memory.
 //   * S_X(j+1) is issued as soon as softmax X has copied S_X(j) into registers, so the
 //     next QK^T overlaps the exponentials, and the two groups' products interleave.
+//   * With an `lse` pointer the epilogue also stores each row's log-sum-exp in base 2,
+//     m + log2 l, as the page's forward kernel keeps it for the backward pass ("Backwards,
+//     and training with it"); any common reference m gives the same value.
 //   * Every mbarrier wait is bounded. A wait that exceeds its deadline sets the device
 //     error word and an abort flag; all roles then leave their loops, drain copies and MMAs
 //     still in flight (with a deadline of their own), free tensor memory and return.
@@ -110,6 +113,7 @@ __device__ unsigned int g_tc_error = 0;
 
 struct TcParams {
     void* o;
+    float* lse;  // null, or [BH, N] base-2 log-sum-exps
     int N;
     int BH;
     int num_pairs;
@@ -431,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                     }
                 }
+                if (p.lse != nullptr && row < N) p.lse[static_cast<int64_t>(bh) * N + row] = m + log2f(l);
             } else {
                 ok = false;
             }
@@ -612,8 +617,8 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, bool bf1
 }
 
 template <bool BF16>
-int launch_impl(const void* q, const void* k, const void* v, void* o, int64_t BH, int64_t N,
-                bool causal, cudaStream_t stream) {
+int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
+                int64_t N, bool causal, cudaStream_t stream) {
     // The register split assumes the launch allocation; a smaller one could leave the
     // softmax groups waiting for registers forever, so it is refused instead.
     cudaFuncAttributes fattr;
@@ -639,6 +644,7 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, int64_t BH
     }
     TcParams prm;
     prm.o = o;
+    prm.lse = lse;
     prm.N = static_cast<int>(N);
     prm.BH = static_cast<int>(BH);
     prm.num_pairs = static_cast<int>((N + 2 * kBM - 1) / (2 * kBM));
@@ -656,11 +662,11 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, int64_t BH
 
 }  // namespace
 
-int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, int64_t BH, int64_t N,
-                  bool causal, bool bf16, int /*num_sms*/, cudaStream_t stream) {
+int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
+                  int64_t N, bool causal, bool bf16, int /*num_sms*/, cudaStream_t stream) {
     if (N > 0x7FFFFFFFll - 2 * kBM || BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
-    return bf16 ? launch_impl<true>(q, k, v, o, BH, N, causal, stream)
-                : launch_impl<false>(q, k, v, o, BH, N, causal, stream);
+    return bf16 ? launch_impl<true>(q, k, v, o, lse, BH, N, causal, stream)
+                : launch_impl<false>(q, k, v, o, lse, BH, N, causal, stream);
 }
 
 int tc_device_error(cudaStream_t stream, bool clear, unsigned* err) {

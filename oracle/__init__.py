@@ -12,6 +12,9 @@ Functions:
   ``q, k, v`` are float32 numpy arrays ``[B, H, N, d]`` holding the exact device values.
   ``rows`` is an optional array of flat row ids ``bh * N + i``; the result is ``[len(rows), d]``
   (or ``[B, H, N, d]`` when ``rows`` is None).
+* ``attn_fwd_lse(q, k, v, causal, rows=None, threads=None)`` — the same rows and, per row, the
+  base-2 log-sum-exp of its scores, ``log2(sum_j exp(s_j))`` ("m plus log two of l", section
+  "Backwards, and training with it"); returns ``(o, lse)``.
 * ``attn_weights(q, k, causal, i)`` — the normalised softmax weights of one row of one head.
 
 Definitions follow the "Flash attention in PyTorch, then in Triton" page ("Attention's table
@@ -56,6 +59,9 @@ def _load():
             lib.oracle_attn_fwd.argtypes = [fp, fp, fp, i64, i64, i64, i64, ctypes.c_int,
                                             ctypes.POINTER(ctypes.c_int64), i64, dp, ctypes.c_int]
             lib.oracle_attn_fwd.restype = ctypes.c_int
+            lib.oracle_attn_fwd_lse.argtypes = [fp, fp, fp, i64, i64, i64, i64, ctypes.c_int,
+                                                ctypes.POINTER(ctypes.c_int64), i64, dp, dp, ctypes.c_int]
+            lib.oracle_attn_fwd_lse.restype = ctypes.c_int
             lib.oracle_attn_weights.argtypes = [fp, fp, i64, i64, ctypes.c_int, i64, dp]
             lib.oracle_attn_weights.restype = ctypes.c_int
             _lib = lib
@@ -74,7 +80,7 @@ def _f32(a: np.ndarray) -> np.ndarray:
     return a
 
 
-def attn_fwd(q, k, v, causal: bool, rows=None, threads: int | None = None) -> np.ndarray:
+def _run(q, k, v, causal, rows, threads, want_lse):
     lib = _load()
     q, k, v = _f32(q), _f32(k), _f32(v)
     if q.ndim != 4 or q.shape != k.shape or q.shape != v.shape:
@@ -82,19 +88,31 @@ def attn_fwd(q, k, v, causal: bool, rows=None, threads: int | None = None) -> np
     B, H, N, d = q.shape
     threads = threads or default_threads()
     fp = ctypes.POINTER(ctypes.c_float)
+    dp = ctypes.POINTER(ctypes.c_double)
     if rows is None:
         out = np.empty((B, H, N, d), dtype=np.float64)
+        lse = np.empty((B, H, N), dtype=np.float64) if want_lse else None
         rp, nrows = None, B * H * N
     else:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         out = np.empty((rows.shape[0], d), dtype=np.float64)
+        lse = np.empty(rows.shape[0], dtype=np.float64) if want_lse else None
         rp, nrows = rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), rows.shape[0]
-    st = lib.oracle_attn_fwd(q.ctypes.data_as(fp), k.ctypes.data_as(fp), v.ctypes.data_as(fp),
-                             B, H, N, d, int(bool(causal)), rp, nrows,
-                             out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(threads))
+    st = lib.oracle_attn_fwd_lse(q.ctypes.data_as(fp), k.ctypes.data_as(fp), v.ctypes.data_as(fp),
+                                 B, H, N, d, int(bool(causal)), rp, nrows, out.ctypes.data_as(dp),
+                                 lse.ctypes.data_as(dp) if want_lse else None, int(threads))
     if st != 0:
         raise RuntimeError(f"oracle_attn_fwd failed with status {st}")
-    return out
+    return out, lse
+
+
+def attn_fwd(q, k, v, causal: bool, rows=None, threads: int | None = None) -> np.ndarray:
+    return _run(q, k, v, causal, rows, threads, False)[0]
+
+
+def attn_fwd_lse(q, k, v, causal: bool, rows=None, threads: int | None = None):
+    """Rows of the output and their base-2 log-sum-exps ``log2(sum_j exp(s_j))``."""
+    return _run(q, k, v, causal, rows, threads, True)
 
 
 def attn_weights(q, k, causal: bool, i: int) -> np.ndarray:

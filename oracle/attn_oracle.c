@@ -20,6 +20,11 @@
  *   3. w_j = exp(s_j - m),  L = sum_j w_j
  *   4. o[i,e] = (sum_j w_j * v[j,e]) / L
  *
+ * The row's log-sum-exp, which the forward pass keeps for the backward pass, is the log of
+ * the sum the softmax divides by. The page keeps it in powers of two, "m plus log two of l"
+ * ("Backwards, and training with it"), i.e. log2(sum_j exp(s_j)):
+ *   5. lse2 = (m + log(L)) / ln(2)
+ *
  * Inputs are float32 arrays that hold exactly the values the device reads (bf16/fp16
  * values widen to float32 exactly); every product and sum is in double. The only
  * parallelism is over independent rows (pthreads); each row's arithmetic is sequential
@@ -43,13 +48,16 @@ typedef struct {
     const int64_t* rows; /* flat ids r = bh * N + i; NULL means all rows in order */
     int64_t nrows;
     double* o;
+    double* lse; /* NULL, or one double per row */
     int tid, nthreads;
     int status;
 } oracle_job;
 
-/* One query row: fills o_row[0..d). s and acc are scratch of N and d doubles. */
+/* One query row: fills o_row[0..d) and, if lse_row is not NULL, the row's base-2
+ * log-sum-exp. s and acc are scratch of N and d doubles. */
 static void oracle_row(const float* qh, const float* kh, const float* vh, int64_t N, int64_t d,
-                       int causal, int64_t i, double* s, double* acc, double* o_row) {
+                       int causal, int64_t i, double* s, double* acc, double* o_row,
+                       double* lse_row) {
     const double scale = 1.0 / sqrt((double)d);
     const int64_t visible = causal ? i + 1 : N;
     double best = -HUGE_VAL;
@@ -72,6 +80,7 @@ static void oracle_row(const float* qh, const float* kh, const float* vh, int64_
         for (int64_t e = 0; e < d; ++e) acc[e] += w * (double)vh[j * d + e];
     }
     for (int64_t e = 0; e < d; ++e) o_row[e] = acc[e] / total;
+    if (lse_row) *lse_row = (best + log(total)) / log(2.0);
 }
 
 static void* oracle_worker(void* arg) {
@@ -91,7 +100,7 @@ static void* oracle_worker(void* arg) {
         const int64_t bh = r / job->N;
         const int64_t i = r % job->N;
         oracle_row(job->q + bh * head, job->k + bh * head, job->v + bh * head, job->N, job->d,
-                   job->causal, i, s, acc, job->o + t * job->d);
+                   job->causal, i, s, acc, job->o + t * job->d, job->lse ? job->lse + t : NULL);
     }
     free(s);
     free(acc);
@@ -105,12 +114,13 @@ static void* oracle_worker(void* arg) {
  *   rows     : flat row ids bh * N + i (0 <= bh < B*H, 0 <= i < N), or NULL for all rows
  *   nrows    : length of rows (ignored when rows is NULL: all B*H*N rows)
  *   o        : nrows x d doubles, row t holds the output of rows[t]
+ *   lse      : NULL, or nrows doubles: lse[t] = log2 of the softmax denominator of rows[t]
  *   nthreads : worker threads (>= 1)
  * Returns 0 on success, -1 on a bad argument, -2 when memory or threads run out.
  */
-int oracle_attn_fwd(const float* q, const float* k, const float* v, int64_t B, int64_t H,
-                    int64_t N, int64_t d, int causal, const int64_t* rows, int64_t nrows,
-                    double* o, int nthreads) {
+int oracle_attn_fwd_lse(const float* q, const float* k, const float* v, int64_t B, int64_t H,
+                        int64_t N, int64_t d, int causal, const int64_t* rows, int64_t nrows,
+                        double* o, double* lse, int nthreads) {
     if (B < 0 || H < 0 || N < 0 || d <= 0 || (causal != 0 && causal != 1) || nthreads < 1)
         return -1;
     const int64_t BH = B * H;
@@ -131,7 +141,7 @@ int oracle_attn_fwd(const float* q, const float* k, const float* v, int64_t B, i
     }
     int started = 0, status = 0;
     for (int t = 0; t < nthreads; ++t) {
-        jobs[t] = (oracle_job){q, k, v, N, d, BH, causal, rows, nrows, o, t, nthreads, -1};
+        jobs[t] = (oracle_job){q, k, v, N, d, BH, causal, rows, nrows, o, lse, t, nthreads, -1};
         if (t == 0) continue; /* thread 0's share runs on the caller */
         if (pthread_create(&th[t], NULL, oracle_worker, &jobs[t]) != 0) {
             status = -2;
@@ -146,6 +156,13 @@ int oracle_attn_fwd(const float* q, const float* k, const float* v, int64_t B, i
     free(jobs);
     free(th);
     return status;
+}
+
+/* The same without log-sum-exps. */
+int oracle_attn_fwd(const float* q, const float* k, const float* v, int64_t B, int64_t H,
+                    int64_t N, int64_t d, int causal, const int64_t* rows, int64_t nrows,
+                    double* o, int nthreads) {
+    return oracle_attn_fwd_lse(q, k, v, B, H, N, d, causal, rows, nrows, o, NULL, nthreads);
 }
 
 /*

@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_header_declares_the_abi():
     names = declared_functions()
-    for want in ("attn_fwd", "attn_fwd_materialized", "attn_materialized_workspace_bytes",
+    for want in ("attn_fwd", "attn_fwd_lse", "attn_fwd_materialized", "attn_materialized_workspace_bytes",
                  "attn_device_status", "attn_status_string", "attn_abi_version"):
         assert want in names
 
@@ -45,6 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_status_strings(lib):
     assert fa.attn_abi_version() >> 16 == 1
+    assert fa.attn_abi_version() & 0xFFFF >= 1  # 1.1: attn_fwd_lse
     for code in range(9):
         s = fa.attn_status_string(code)
         assert s and s != "unknown status"
@@ -70,6 +71,21 @@ def test_argument_checks_before_any_device_work(lib, args, want):
     assert lib.attn_fwd(*args, None) == want
 
 
+@pytest.mark.parametrize("lse,want", [
+    (P * 20 + 2, 3),   # lse not 4-byte aligned
+    (P + 16, 4),       # lse overlaps q
+    (P * 9 + 64, 4),   # lse overlaps o
+])
+def test_lse_argument_checks(lib, lse, want):
+    # q, k, v, o: 1 x 1 x 8 x 64 bf16 = 1 KiB each at P, 3P, 5P, 9P
+    assert lib.attn_fwd_lse(P, P * 3, P * 5, P * 9, lse, 1, 1, 8, 64, 0, 1, None) == want
+
+
+def test_lse_shares_the_forward_checks(lib):
+    assert lib.attn_fwd_lse(P, P, P, P * 9, P * 20, 1, 1, 8, 32, 0, 1, None) == 2       # d != 64
+    assert lib.attn_fwd_lse(None, None, None, None, None, 0, 1, 8, 64, 0, 1, None) == 0  # no work
+
+
 def test_materialized_workspace_checks(lib):
     per = lib.attn_materialized_workspace_bytes(1, 1, 100)
     assert per == 2 * ((100 * 100 * 4 + 255) // 256 * 256) + (400 + 255) // 256 * 256
@@ -92,3 +108,4 @@ def test_binding_has_no_fallback_when_library_missing(monkeypatch, tmp_path):
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="needs a machine without a GPU")
 def test_valid_call_without_gpu_reports_device_error(lib):
     assert lib.attn_fwd(P, P * 3, P * 5, P * 9, 1, 1, 8, 64, 0, 1, None) == 5
+    assert lib.attn_fwd_lse(P, P * 3, P * 5, P * 9, P * 20, 1, 1, 8, 64, 0, 1, None) == 5
