@@ -16,6 +16,9 @@ Functions:
   base-2 log-sum-exp of its scores, ``log2(sum_j exp(s_j))`` ("m plus log two of l", section
   "Backwards, and training with it"); returns ``(o, lse)``.
 * ``attn_weights(q, k, causal, i)`` — the normalised softmax weights of one row of one head.
+* ``attn_bwd(q, k, v, dout, causal, threads=None)`` — ``(dq, dk, dv)`` in float64, the
+  gradients of exact attention for the output gradient ``dout`` (``attn_bwd_oracle.c``,
+  following the steps of the page's section "Backwards, and training with it").
 
 Definitions follow the "Flash attention in PyTorch, then in Triton" page ("Attention's table
 of scores", "Attention by hand") and attention.cu's CPU reference ("CPU reference in double").
@@ -32,6 +35,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
+_BWD_SRC = os.path.join(_HERE, "attn_bwd_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD, "liboracle.so")
 CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread"]
@@ -43,9 +47,10 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile the oracle library with gcc if it is missing or older than its source."""
     os.makedirs(_BUILD, exist_ok=True)
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_BWD_SRC))
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
         tmp = _LIB + f".{os.getpid()}.tmp"
-        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, _BWD_SRC, "-lm"], check=True)
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -64,6 +69,9 @@ def _load():
             lib.oracle_attn_fwd_lse.restype = ctypes.c_int
             lib.oracle_attn_weights.argtypes = [fp, fp, i64, i64, ctypes.c_int, i64, dp]
             lib.oracle_attn_weights.restype = ctypes.c_int
+            lib.oracle_attn_bwd.argtypes = [fp, fp, fp, fp, i64, i64, i64, i64, ctypes.c_int, dp, dp, dp,
+                                            ctypes.c_int]
+            lib.oracle_attn_bwd.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -127,3 +135,21 @@ def attn_weights(q, k, causal: bool, i: int) -> np.ndarray:
     if st != 0:
         raise RuntimeError(f"oracle_attn_weights failed with status {st}")
     return w
+
+
+def attn_bwd(q, k, v, dout, causal: bool, threads: int | None = None):
+    """``(dq, dk, dv)`` float64 ``[B, H, N, d]``: gradients of exact attention for ``dout``."""
+    lib = _load()
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    if q.ndim != 4 or any(t.shape != q.shape for t in (k, v, dout)):
+        raise ValueError("q, k, v, dout must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    outs = [np.empty((B, H, N, d), dtype=np.float64) for _ in range(3)]
+    fp = ctypes.POINTER(ctypes.c_float)
+    dp = ctypes.POINTER(ctypes.c_double)
+    st = lib.oracle_attn_bwd(q.ctypes.data_as(fp), k.ctypes.data_as(fp), v.ctypes.data_as(fp),
+                             dout.ctypes.data_as(fp), B, H, N, d, int(bool(causal)),
+                             *(x.ctypes.data_as(dp) for x in outs), int(threads or default_threads()))
+    if st != 0:
+        raise RuntimeError(f"oracle_attn_bwd failed with status {st}")
+    return tuple(outs)
