@@ -96,6 +96,31 @@ int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* ls
                  int64_t H, int64_t N, int64_t d, int causal, int dtype, void* stream);
 
 /*
+ * attn_bwd — gradients of the loss with respect to q, k and v, given its gradient with
+ * respect to the output, dout: the backward pass of the "Flash attention in PyTorch, then in
+ * Triton" page, section "Backwards, and training with it". With S = q k^T / sqrt(d) (masked
+ * when causal) and P = softmax(S) rebuilt from the scores and the forward's log-sum-exps,
+ *
+ *     dv = P^T dout,   dP = dout v^T,   delta_i = sum_e dout[i,e] o[i,e],
+ *     dS = P * (dP - delta),   dq = dS k / sqrt(d),   dk = dS^T q / sqrt(d).
+ *
+ * Two kernels as on the page (one program per key block writes dk and dv, one per query block
+ * writes dq), so no program adds into another's rows; arithmetic is fp32 for every dtype,
+ * results are rounded to dtype (RNE). Nothing is allocated.
+ *
+ *   q, k, v, o, dout : const device pointers, [B, H, N, d] of dtype, 16-byte aligned; o is the
+ *                      forward's output for these q, k, v (from attn_fwd_lse)
+ *   lse              : const device pointer, float32 [B, H, N], 16-byte aligned: the base-2
+ *                      log-sum-exps attn_fwd_lse stored for the same q, k
+ *   dq, dk, dv       : device pointers, [B, H, N, d] of dtype, 16-byte aligned; they must not
+ *                      overlap each other or any input; every element is written
+ *   other arguments  : as attn_fwd (same checks and status codes)
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N,
+             int64_t d, int causal, int dtype, void* stream);
+
+/*
  * attn_fwd_materialized — the same result by the materialised path of attention.cu
  * (scoresQKt, softmaxRows, weightedV): S = q k^T / sqrt(d) with masked entries set to
  * -inf, written in full as fp32; a three-pass safe softmax that writes exp(S - rowmax) to
@@ -157,7 +182,7 @@ int attn_device_status(void* stream, int clear);
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* attn_status_string(int status);
 
-/* ABI version of this header: (major << 16) | minor (1.1 added attn_fwd_lse). */
+/* ABI version of this header: (major << 16) | minor (1.1 added attn_fwd_lse, 1.2 attn_bwd). */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

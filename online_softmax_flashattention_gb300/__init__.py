@@ -25,7 +25,7 @@ __all__ = [
     "ATTN_F32", "ATTN_BF16", "ATTN_F16", "AttnError", "AttnLibraryMissing", "library_path",
     "attn_fwd", "attn_fwd_materialized", "attn_materialized_workspace_bytes", "attn_device_status",
     "attn_status_string", "attn_abi_version", "raw", "attn_fwd_materialized_noalloc",
-    "ATTN_NOALLOC_MAX_N", "attn_fwd_lse",
+    "ATTN_NOALLOC_MAX_N", "attn_fwd_lse", "attn_bwd",
 ]
 
 ATTN_F32, ATTN_BF16, ATTN_F16 = 0, 1, 2
@@ -68,6 +68,8 @@ def raw():
             lib.attn_fwd.restype = ci
             lib.attn_fwd_lse.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ci, ci, vp]
             lib.attn_fwd_lse.restype = ci
+            lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ci, ci, vp]
+            lib.attn_bwd.restype = ci
             lib.attn_fwd_materialized.argtypes = [vp, vp, vp, vp, vp, sz, i64, i64, i64, i64, ci, ci, vp]
             lib.attn_fwd_materialized.restype = ci
             lib.attn_materialized_workspace_bytes.argtypes = [i64, i64, i64]
@@ -150,6 +152,30 @@ def attn_fwd_lse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool
     if st != 0:
         raise AttnError(st, "attn_fwd_lse")
     return out, lse
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, dout: torch.Tensor,
+             lse: torch.Tensor, causal: bool = False,
+             stream: torch.cuda.Stream | None = None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """``(dq, dk, dv)``: gradients for the output gradient ``dout``, given the forward's ``o``
+    and base-2 log-sum-exps ``lse`` from :func:`attn_fwd_lse` on the same ``q, k, v``."""
+    _check(q, k, v)
+    B, H, N, d = q.shape
+    for name, t in (("o", o), ("dout", dout)):
+        if not isinstance(t, torch.Tensor) or t.shape != q.shape or t.dtype != q.dtype or t.device != q.device \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor like q")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or lse.device != q.device or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, N] on q's device")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    lib = raw()
+    with torch.cuda.device(q.device):
+        st = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, int(bool(causal)),
+                          _DTYPES[q.dtype], _stream(q.device, stream))
+    if st != 0:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_materialized_workspace_bytes(B: int, H: int, N: int) -> int:

@@ -100,6 +100,36 @@ int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* ls
     return attn::launch_fwd_tc(q, k, v, o, lse, BH, N, causal != 0, dtype == ATTN_BF16, num_sms, s);
 }
 
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N,
+             int64_t d, int causal, int dtype, void* stream) {
+    int64_t BH = 0;
+    size_t bytes = 0;
+    bool skip = false;
+    // q, k, v and o get the forward's checks (o plays the output's part, so it may not alias
+    // q, k or v); then the backward's own tensors.
+    int st = check_common(q, k, v, o, B, H, N, d, causal, dtype, &BH, &bytes, &skip);
+    if (st != ATTN_OK || skip) return st;
+    if (!dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(dout, 16) || !aligned(lse, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+        return ATTN_ERR_ALIGN;
+    const size_t lbytes = static_cast<size_t>(BH) * static_cast<size_t>(N) * sizeof(float);
+    const void* ins[6] = {q, k, v, o, dout, lse};
+    const size_t in_bytes[6] = {bytes, bytes, bytes, bytes, bytes, lbytes};
+    void* outs[3] = {dq, dk, dv};
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 6; ++b)
+            if (overlap(outs[a], bytes, ins[b], in_bytes[b])) return ATTN_ERR_ALIAS;
+        for (int b = a + 1; b < 3; ++b)
+            if (overlap(outs[a], bytes, outs[b], bytes)) return ATTN_ERR_ALIAS;
+    }
+    int num_sms = 0;
+    if ((st = check_device(&num_sms)) != ATTN_OK) return st;
+    if (inject_launch_fault()) return ATTN_ERR_LAUNCH;
+    return attn::launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal != 0, dtype,
+                            static_cast<cudaStream_t>(stream));
+}
+
 size_t attn_materialized_workspace_bytes(int64_t B, int64_t H, int64_t N) {
     if (B < 0 || H < 0 || N < 0 || B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return 0;
     const size_t per = attn::materialized_head_bytes(N);
@@ -167,6 +197,6 @@ const char* attn_status_string(int status) {
     }
 }
 
-int attn_abi_version(void) { return (1 << 16) | 1; }
+int attn_abi_version(void) { return (1 << 16) | 2; }
 
 }  // extern "C"
