@@ -105,8 +105,11 @@ int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* ls
  *     dS = P * (dP - delta),   dq = dS k / sqrt(d),   dk = dS^T q / sqrt(d).
  *
  * Two kernels as on the page (one program per key block writes dk and dv, one per query block
- * writes dq), so no program adds into another's rows; arithmetic is fp32 for every dtype,
- * results are rounded to dtype (RNE). Nothing is allocated.
+ * writes dq), so no program adds into another's rows. bf16/fp16 run on tcgen05 tensor cores
+ * (products with bf16/fp16 operands and fp32 accumulation; P and dS are rounded to dtype before
+ * the products that take them, as the forward rounds P); f32 runs on FFMA in fp32. Results are
+ * rounded to dtype (RNE). Nothing is allocated. A device-side wait timeout is reported by
+ * attn_device_status like the forward's.
  *
  *   q, k, v, o, dout : const device pointers, [B, H, N, d] of dtype, 16-byte aligned; o is the
  *                      forward's output for these q, k, v (from attn_fwd_lse)

@@ -1,4 +1,5 @@
-// Backward pass of exact attention on CUDA cores, fp32 arithmetic for every input type.
+// Backward pass of exact attention for float32 tensors on CUDA cores (FFMA). The bf16/fp16
+// backward runs on tensor cores (attn_bwd_tc.cu) with the same two-kernel structure.
 //
 // Given the output gradient dO, the forward's output O and each row's base-2 log-sum-exp
 // (lse2 = m + log2 l, kept by attn_fwd_lse), the gradients follow the "Flash attention in
@@ -368,17 +369,11 @@ int launch_t(const void* q, const void* k, const void* v, const void* o, const v
 
 }  // namespace
 
-int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-               void* dq, void* dk, void* dv, int64_t BH, int64_t N, bool causal, int dtype, cudaStream_t stream) {
+int launch_bwd_f32(const float* q, const float* k, const float* v, const float* o, const float* dout,
+                   const float* lse, float* dq, float* dk, float* dv, int64_t BH, int64_t N, bool causal,
+                   cudaStream_t stream) {
     if (N > 0x7FFFFFFFll - kB || BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
-    switch (dtype) {
-        case ATTN_F32:
-            return launch_t<float>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream);
-        case ATTN_BF16:
-            return launch_t<__nv_bfloat16>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream);
-        default:
-            return launch_t<__half>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream);
-    }
+    return launch_t<float>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream);
 }
 
 }  // namespace attn

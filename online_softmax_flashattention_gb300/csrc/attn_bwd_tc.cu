@@ -1,0 +1,681 @@
+// Backward pass of exact attention for bf16 / fp16 on GB300 (sm_103a) tensor cores.
+//
+// The gradients follow the "Flash attention in PyTorch, then in Triton" page, section
+// "Backwards, and training with it": P is made again from the scores and each row's base-2
+// log-sum-exp (lse2 = m + log2 l, kept by the forward), then
+//   dV = P^T dO,  dP = dO V^T,  delta_i = sum_e dO[i,e] O[i,e],  dS = P (dP - delta),
+//   dQ = dS K / sqrt(d),  dK = dS^T Q / sqrt(d).
+// As on the page the work is split into two kernels so that no program adds into another's
+// rows: one CTA per block of 128 keys keeps dK and dV while the blocks of 128 queries that see
+// those keys go past; one CTA per block of 128 queries keeps dQ while its key blocks go past.
+// Both recompute the scores and dP (the page's trade: no atomics, that work done twice).
+//
+// GB300 mapping. Every product is a tcgen05.mma (bf16/fp16 operands, fp32 accumulate) with
+// the forward kernel's two shapes: SS (both operands K-major tiles as TMA writes them, 128-byte
+// swizzle) and TS (A from tensor memory, B an MN-major tile).
+//   dK/dV kernel, per query block, with the keys in the 128 TMEM lanes:
+//     S^T = K Q^T (SS), dP^T = V dO^T (SS)               -> TMEM, 128 columns each
+//     the four "softmax" warps (thread = key) make P^T and dS^T = P^T (dP^T - delta) in
+//     registers and store them to TMEM as 16-bit pairs
+//     dV += P^T dO (TS, B = dO tile MN-major), dK += dS^T Q (TS, B = Q tile MN-major)
+//   dQ kernel, per key block, with the queries in the lanes:
+//     S = Q K^T (SS), dP = dO V^T (SS); dS = P (dP - delta) -> TMEM; dQ += dS K (TS, B = K)
+// Tensor memory (512 columns): dK/dV kernel S^T 0, dP^T 128, P^T 256, dS^T 320, dV 384, dK 448;
+// dQ kernel S 0, dP 128, dS 256, dQ 320. The next block's S and dP products go out as soon as
+// the softmax warps have copied the current ones out, so they overlap the elementwise work.
+// delta is computed from the dO and O tiles in shared memory (the dK/dV kernel loads O for
+// that) and lse is read per block, so the call allocates nothing.
+//
+// Roles: warps 0-3 elementwise (thread = TMEM lane), warp 4 TMA producer, warp 5 MMA issuer
+// and tensor-memory owner. Every mbarrier wait is bounded; on expiry the kernel sets the
+// shared device error word (reported by attn_device_status), drains and returns.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kD = 64;
+constexpr int kBlk = 128;                   // queries or keys per block = TMEM lanes
+constexpr int kTile = kBlk * kD * 2;        // 16 KiB: one 128 x 64 tile of 16-bit values
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+constexpr uint64_t kDrainTimeoutNs = 100000000ull;
+
+__device__ unsigned int g_bwd_error = 0;
+
+struct BwdParams {
+    void* grad0;  // dk (kv kernel) or dq (q kernel)
+    void* grad1;  // dv (kv kernel)
+    const void* o;
+    const float* lse;
+    int N;
+    int BH;
+    int nblk;
+    int causal;
+    float c;      // log2(e) / sqrt(d)
+    float scale;  // 1 / sqrt(d)
+};
+
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicOr(&g_bwd_error, 1u);
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, kWaitTimeoutNs);
+    return __all_sync(0xffffffffu, ok);
+}
+
+
+// Element (row r, column e) of a 128-row x 64 tile written by TMA with the 128-byte swizzle:
+// 16-byte chunks of a row are permuted by row % 8.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int e) {
+    return static_cast<uint32_t>(r * 128 + ((((e >> 3) ^ (r & 7)) << 4)) + ((e & 7) << 1));
+}
+
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+    if constexpr (BF16) {
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    } else {
+        __half2 h = *reinterpret_cast<__half2*>(&u);
+        return __half22float2(h);
+    }
+}
+
+// sum_e a[r,e] b[r,e] over one row of two swizzled tiles (fp32 accumulation).
+template <bool BF16>
+__device__ __forceinline__ float row_dot(const uint8_t* a, const uint8_t* b, int r) {
+    float acc = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t off = sw128_offset(r, ch * 8);
+        const uint4 x = *reinterpret_cast<const uint4*>(a + off);
+        const uint4 y = *reinterpret_cast<const uint4*>(b + off);
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 u = unpack2<BF16>(xs[i]), v = unpack2<BF16>(ys[i]);
+            acc = fmaf(u.x, v.x, acc);
+            acc = fmaf(u.y, v.y, acc);
+        }
+    }
+    return acc;
+}
+
+// 128 x 128 product over K = 64 (four K=16 steps) of two K-major tiles into TMEM columns `d`.
+template <bool BF16>
+__device__ __forceinline__ void mma_ss_128x128(uint32_t d, uint32_t sA, uint32_t sB) {
+    constexpr uint32_t kIdesc = idesc_f16(BF16, kBlk, kBlk, false, false);
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk)
+        umma_ss(d, smem_desc_sw128(sA + 32 * kk, 16, 1024), smem_desc_sw128(sB + 32 * kk, 16, 1024), kIdesc,
+                kk > 0 ? 1u : 0u);
+}
+
+// 128 x 64 product over K = 128 with A (128 lanes x 128 16-bit values) in TMEM columns `a`
+// and B an MN-major 128 x 64 tile (rows = K), accumulated into TMEM columns `d`.
+template <bool BF16>
+__device__ __forceinline__ void mma_ts_128x64(uint32_t d, uint32_t a, uint32_t sB, bool accumulate) {
+    constexpr uint32_t kIdesc = idesc_f16(BF16, kBlk, kD, false, true);
+#pragma unroll
+    for (int kk = 0; kk < kBlk / 16; ++kk)
+        umma_ts(d, a + 8u * kk, smem_desc_sw128(sB + 2048 * kk, 16, 1024), kIdesc, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// ================================ dK, dV: one CTA per key block ================================
+// Shared memory: K, V tiles, then two stages of (Q, dO, O) tiles, then per-block lse and
+// delta (double-buffered by block parity), then mbarriers.
+constexpr int kvOffK = 0;
+constexpr int kvOffV = kTile;
+constexpr int kvOffStage = 2 * kTile;          // stage s: Q at +0, dO at +kTile, O at +2 kTile
+constexpr int kvStageBytes = 3 * kTile;
+constexpr int kvOffRow = kvOffStage + 2 * kvStageBytes;  // lse[2][128], delta[2][128] floats
+constexpr int kvOffBar = kvOffRow + 4 * kBlk * 4;
+enum { kvKV = 0, kvQFull = 1, kvQEmpty = 3, kvSFull = 5, kvDPFull, kvSdPFree, kvPdSFull, kvDone, kvDrain,
+       kvRows, kvNumBars };  // kvRows: the four elementwise warps wrote this block's lse and delta
+constexpr int kvOffSlot = kvOffBar + 8 * kvNumBars;
+constexpr int kvOffAbort = kvOffSlot + 4;
+constexpr int kvSmem = kvOffAbort + 4 + 1024;
+static_assert(kvSmem <= 227 * 1024, "shared memory budget");
+constexpr uint32_t kvColS = 0, kvColDP = 128, kvColP = 256, kvColDS = 320, kvColDV = 384, kvColDK = 448;
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                            const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const gbase = smem_raw + (base - raw);
+    auto bar = [&](int i) -> uint32_t { return base + kvOffBar + 8u * static_cast<uint32_t>(i); };
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + kvOffSlot);
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + kvOffAbort);
+    float* const lse_s = reinterpret_cast<float*>(gbase + kvOffRow);     // [2][128]
+    float* const delta_s = lse_s + 2 * kBlk;                              // [2][128]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = p.N;
+    const int bh = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.BH));
+    const int kblk = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.BH));  // block 0 sees most queries
+    const int k0 = kblk * kBlk;
+    const int qb0 = p.causal ? kblk : 0;  // the first query block that sees these keys
+    const int nq = p.nblk - qb0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(kvKV), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(kvQFull + s), 1);
+            mbar_init(bar(kvQEmpty + s), 1);
+        }
+        mbar_init(bar(kvSFull), 1);
+        mbar_init(bar(kvDPFull), 1);
+        mbar_init(bar(kvSdPFree), 4);
+        mbar_init(bar(kvPdSFull), 4);
+        mbar_init(bar(kvDone), 1);
+        mbar_init(bar(kvDrain), 1);
+        mbar_init(bar(kvRows), 4);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        // ===================== elementwise warps: thread = key (TMEM lane) =====================
+        const int r = threadIdx.x;  // key row within the block, = TMEM lane
+        const int key = k0 + r;
+        const uint32_t t = tmem + (static_cast<uint32_t>(warp << 5) << 16);
+        bool ok = true;
+        for (int i = 0; ok && i < nq; ++i) {
+            const int st = i & 1, q0 = (qb0 + i) * kBlk;
+            // This block's lse and delta (thread r handles query q0 + r).
+            if (!(ok = warp_wait(bar(kvQFull + st), (i >> 1) & 1, abort_flag))) break;
+            const uint8_t* stage = gbase + kvOffStage + st * kvStageBytes;
+            const bool qin = q0 + r < N;
+            lse_s[st * kBlk + r] = qin ? p.lse[static_cast<int64_t>(bh) * N + q0 + r] : 0.f;
+            delta_s[st * kBlk + r] = qin ? row_dot<BF16>(stage + kTile, stage + 2 * kTile, r) : 0.f;
+            // All four warps' rows written (a bounded wait, unlike a named barrier, so a warp that
+            // gave up cannot leave the others waiting forever).
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kvRows));
+            if (!(ok = warp_wait(bar(kvRows), i & 1, abort_flag))) break;
+            const float* ls = lse_s + st * kBlk;
+            const float* dl = delta_s + st * kBlk;
+            if (!(ok = warp_wait(bar(kvSFull), i & 1, abort_flag))) break;
+            if (!(ok = warp_wait(bar(kvDPFull), i & 1, abort_flag))) break;
+            tc_fence_after();
+            // The previous block's dV/dK products read P^T and dS^T: wait before overwriting.
+            if (i > 0 && !(ok = warp_wait(bar(kvDone), (i - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {  // 32 queries at a time
+                uint32_t s[32], dp[32];
+                ATTN_TMEM_LD_X32(t + kvColS + 32 * ch, s);
+                ATTN_TMEM_LD_X32(t + kvColDP + 32 * ch, dp);
+                tmem_ld_wait();
+                uint32_t pp[16], ds[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    float pv[2], dv[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int col = ch * 32 + 2 * u + h;
+                        const int query = q0 + col;
+                        const bool vis = query < N && key < N && (!p.causal || key <= query);
+                        const float pr = vis ? ex2_approx(fmaf(__uint_as_float(s[2 * u + h]), p.c, -ls[col])) : 0.f;
+                        pv[h] = pr;
+                        dv[h] = pr * (__uint_as_float(dp[2 * u + h]) - dl[col]);
+                    }
+                    pp[u] = pack2<BF16>(pv[0], pv[1]);
+                    ds[u] = pack2<BF16>(dv[0], dv[1]);
+                }
+                tmem_st_x16(t + kvColP + 16 * ch, pp);
+                tmem_st_x16(t + kvColDS + 16 * ch, ds);
+            }
+            // S^T and dP^T are copied out: the next block's products may overwrite them.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kvSdPFree));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kvPdSFull));
+        }
+        // ---- epilogue: dK * scale and dV, rounded to the output type; keys >= N not stored ----
+        if (ok && nq > 0) {
+            if ((ok = warp_wait(bar(kvDone), (nq - 1) & 1, abort_flag))) {
+                tc_fence_after();
+                uint16_t* const dk = reinterpret_cast<uint16_t*>(p.grad0) + (static_cast<int64_t>(bh) * N + key) * kD;
+                uint16_t* const dv = reinterpret_cast<uint16_t*>(p.grad1) + (static_cast<int64_t>(bh) * N + key) * kD;
+#pragma unroll 1
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t a[16], b[16];
+                    tmem_ld_x16(t + kvColDK + 16 * h, a);
+                    tmem_ld_x16(t + kvColDV + 16 * h, b);
+                    tmem_ld_wait();
+                    uint32_t pa[8], pb[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        pa[i] = pack2<BF16>(__uint_as_float(a[2 * i]) * p.scale, __uint_as_float(a[2 * i + 1]) * p.scale);
+                        pb[i] = pack2<BF16>(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
+                    }
+                    if (key < N) {
+                        uint4* x = reinterpret_cast<uint4*>(dk + 16 * h);
+                        x[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+                        x[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
+                        uint4* y = reinterpret_cast<uint4*>(dv + 16 * h);
+                        y[0] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
+                        y[1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
+                    }
+                }
+            }
+        }
+        if (!ok) raise_abort(abort_flag);
+    } else if (warp == kProducerWarp && lane == 0) {
+        // =============================== TMA producer ===============================
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_o);
+        prefetch_tmap(&tm_do);
+        mbar_arrive_expect_tx(bar(kvKV), 2 * kTile);
+        tma_load_3d(base + kvOffK, &tm_k, 0, k0, bh, bar(kvKV));
+        tma_load_3d(base + kvOffV, &tm_v, 0, k0, bh, bar(kvKV));
+        bool ok = true;
+        int issued = 0;
+        for (int i = 0; i < nq; ++i) {
+            const int st = i & 1, q0 = (qb0 + i) * kBlk;
+            if (!(ok = mbar_wait(bar(kvQEmpty + st), ((i >> 1) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
+            const uint32_t stage = base + kvOffStage + st * kvStageBytes;
+            mbar_arrive_expect_tx(bar(kvQFull + st), 3 * kTile);
+            tma_load_3d(stage, &tm_q, 0, q0, bh, bar(kvQFull + st));
+            tma_load_3d(stage + kTile, &tm_do, 0, q0, bh, bar(kvQFull + st));
+            tma_load_3d(stage + 2 * kTile, &tm_o, 0, q0, bh, bar(kvQFull + st));
+            issued = i + 1;
+        }
+        if (!ok) raise_abort(abort_flag);
+        // Every copy must land before the CTA exits (normally they were all consumed).
+        mbar_wait(bar(kvKV), 0, nullptr, kDrainTimeoutNs);
+        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
+            mbar_wait(bar(kvQFull + (i & 1)), (i >> 1) & 1, nullptr, kDrainTimeoutNs);
+    } else if (warp == kMmaWarp && lane == 0) {
+        // ================================ MMA issuer ================================
+        // S^T(0), dP^T(0); then per block i: S^T(i+1), dP^T(i+1) once block i's were copied
+        // out, and dV, dK += block i's P^T dO, dS^T Q once P^T and dS^T are in TMEM.
+        bool ok = mbar_wait(bar(kvKV), 0, abort_flag, kWaitTimeoutNs);
+        auto issue_sdp = [&](int i) {
+            const uint32_t stage = base + kvOffStage + (i & 1) * kvStageBytes;
+            if (!mbar_wait(bar(kvQFull + (i & 1)), (i >> 1) & 1, abort_flag, kWaitTimeoutNs)) return false;
+            tc_fence_after();
+            mma_ss_128x128<BF16>(tmem + kvColS, base + kvOffK, stage);           // S^T = K Q^T
+            umma_commit(bar(kvSFull));
+            mma_ss_128x128<BF16>(tmem + kvColDP, base + kvOffV, stage + kTile);  // dP^T = V dO^T
+            umma_commit(bar(kvDPFull));
+            return true;
+        };
+        if (ok && nq > 0) ok = issue_sdp(0);
+        for (int i = 0; ok && i < nq; ++i) {
+            if (i + 1 < nq) {
+                if (!(ok = mbar_wait(bar(kvSdPFree), i & 1, abort_flag, kWaitTimeoutNs))) break;
+                if (!(ok = issue_sdp(i + 1))) break;
+            }
+            if (!(ok = mbar_wait(bar(kvPdSFull), i & 1, abort_flag, kWaitTimeoutNs))) break;
+            tc_fence_after();
+            const uint32_t stage = base + kvOffStage + (i & 1) * kvStageBytes;
+            mma_ts_128x64<BF16>(tmem + kvColDV, tmem + kvColP, stage + kTile, i > 0);  // dV += P^T dO
+            mma_ts_128x64<BF16>(tmem + kvColDK, tmem + kvColDS, stage, i > 0);          // dK += dS^T Q
+            umma_commit(bar(kvDone));
+            umma_commit(bar(kvQEmpty + (i & 1)));
+        }
+        if (!ok) raise_abort(abort_flag);
+        umma_commit(bar(kvDrain));
+        mbar_wait(bar(kvDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ================================== dQ: one CTA per query block ==================================
+constexpr int qOffQ = 0;
+constexpr int qOffDO = kTile;
+constexpr int qOffKV = 2 * kTile;               // stage s: K at +0, V at +kTile
+constexpr int qStageBytes = 2 * kTile;
+constexpr int qStages = 3;
+constexpr int qOffBar = qOffKV + qStages * qStageBytes;
+enum { qQ = 0, qKVFull = 1, qKVEmpty = qKVFull + qStages, qSFull = qKVEmpty + qStages, qDPFull, qSdPFree, qDSFull,
+       qDone, qDrain, qNumBars };
+constexpr int qOffSlot = qOffBar + 8 * qNumBars;
+constexpr int qOffAbort = qOffSlot + 4;
+constexpr int qSmem = qOffAbort + 4 + 1024;
+static_assert(qSmem <= 227 * 1024, "shared memory budget");
+constexpr uint32_t qColS = 0, qColDP = 128, qColDS = 256, qColDQ = 320;
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                          const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const gbase = smem_raw + (base - raw);
+    auto bar = [&](int i) -> uint32_t { return base + qOffBar + 8u * static_cast<uint32_t>(i); };
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + qOffSlot);
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + qOffAbort);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = p.N;
+    const int bh = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.BH));
+    const int slot = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.BH));
+    const int qblk = p.causal ? (p.nblk - 1 - slot) : slot;  // heaviest causal blocks first
+    const int q0 = qblk * kBlk;
+    const int nk = p.causal ? qblk + 1 : p.nblk;  // keys up to the block's last query
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(qQ), 1);
+        for (int s = 0; s < qStages; ++s) {
+            mbar_init(bar(qKVFull + s), 1);
+            mbar_init(bar(qKVEmpty + s), 1);
+        }
+        mbar_init(bar(qSFull), 1);
+        mbar_init(bar(qDPFull), 1);
+        mbar_init(bar(qSdPFree), 4);
+        mbar_init(bar(qDSFull), 4);
+        mbar_init(bar(qDone), 1);
+        mbar_init(bar(qDrain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        // ==================== elementwise warps: thread = query (TMEM lane) ====================
+        const int r = threadIdx.x;
+        const int query = q0 + r;
+        const bool qin = query < N;
+        const uint32_t t = tmem + (static_cast<uint32_t>(warp << 5) << 16);
+        bool ok = warp_wait(bar(qQ), 0, abort_flag);
+        // delta = dO . O for this row (O read from global), and the row's lse.
+        float delta = 0.f, l2 = 0.f;
+        if (ok && qin) {
+            const uint8_t* dO = gbase + qOffDO;
+            const uint16_t* orow = reinterpret_cast<const uint16_t*>(p.o) + (static_cast<int64_t>(bh) * N + query) * kD;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const uint4 x = *reinterpret_cast<const uint4*>(dO + sw128_offset(r, ch * 8));
+                const uint4 y = *reinterpret_cast<const uint4*>(orow + ch * 8);
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 u = unpack2<BF16>(xs[i]), v = unpack2<BF16>(ys[i]);
+                    delta = fmaf(u.x, v.x, delta);
+                    delta = fmaf(u.y, v.y, delta);
+                }
+            }
+            l2 = p.lse[static_cast<int64_t>(bh) * N + query];
+        }
+        for (int j = 0; ok && j < nk; ++j) {
+            const int k0 = j * kBlk;
+            if (!(ok = warp_wait(bar(qSFull), j & 1, abort_flag))) break;
+            if (!(ok = warp_wait(bar(qDPFull), j & 1, abort_flag))) break;
+            tc_fence_after();
+            // The previous block's dQ product reads dS: wait before overwriting it.
+            if (j > 0 && !(ok = warp_wait(bar(qDone), (j - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {  // 32 keys at a time
+                uint32_t s[32], dp[32];
+                ATTN_TMEM_LD_X32(t + qColS + 32 * ch, s);
+                ATTN_TMEM_LD_X32(t + qColDP + 32 * ch, dp);
+                tmem_ld_wait();
+                uint32_t ds[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    float dv[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int key = k0 + ch * 32 + 2 * u + h;
+                        const bool vis = qin && key < N && (!p.causal || key <= query);
+                        const float pr = vis ? ex2_approx(fmaf(__uint_as_float(s[2 * u + h]), p.c, -l2)) : 0.f;
+                        dv[h] = pr * (__uint_as_float(dp[2 * u + h]) - delta);
+                    }
+                    ds[u] = pack2<BF16>(dv[0], dv[1]);
+                }
+                tmem_st_x16(t + qColDS + 16 * ch, ds);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(qSdPFree));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(qDSFull));
+        }
+        // ---- epilogue: dQ * scale, rounded to the output type; rows >= N not stored ----
+        if (ok && nk > 0) {
+            if ((ok = warp_wait(bar(qDone), (nk - 1) & 1, abort_flag))) {
+                tc_fence_after();
+                uint16_t* const dq = reinterpret_cast<uint16_t*>(p.grad0) + (static_cast<int64_t>(bh) * N + query) * kD;
+#pragma unroll 1
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t a[16];
+                    tmem_ld_x16(t + qColDQ + 16 * h, a);
+                    tmem_ld_wait();
+                    uint32_t pa[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        pa[i] = pack2<BF16>(__uint_as_float(a[2 * i]) * p.scale, __uint_as_float(a[2 * i + 1]) * p.scale);
+                    if (qin) {
+                        uint4* x = reinterpret_cast<uint4*>(dq + 16 * h);
+                        x[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+                        x[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
+                    }
+                }
+            }
+        }
+        if (!ok) raise_abort(abort_flag);
+    } else if (warp == kProducerWarp && lane == 0) {
+        // =============================== TMA producer ===============================
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_do);
+        mbar_arrive_expect_tx(bar(qQ), 2 * kTile);
+        tma_load_3d(base + qOffQ, &tm_q, 0, q0, bh, bar(qQ));
+        tma_load_3d(base + qOffDO, &tm_do, 0, q0, bh, bar(qQ));
+        bool ok = true;
+        int issued = 0;
+        for (int j = 0; j < nk; ++j) {
+            const int st = j % qStages;
+            if (!(ok = mbar_wait(bar(qKVEmpty + st), ((j / qStages) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
+            const uint32_t stage = base + qOffKV + st * qStageBytes;
+            mbar_arrive_expect_tx(bar(qKVFull + st), 2 * kTile);
+            tma_load_3d(stage, &tm_k, 0, j * kBlk, bh, bar(qKVFull + st));
+            tma_load_3d(stage + kTile, &tm_v, 0, j * kBlk, bh, bar(qKVFull + st));
+            issued = j + 1;
+        }
+        if (!ok) raise_abort(abort_flag);
+        mbar_wait(bar(qQ), 0, nullptr, kDrainTimeoutNs);
+        for (int j = (issued > qStages ? issued - qStages : 0); j < issued; ++j)
+            mbar_wait(bar(qKVFull + j % qStages), (j / qStages) & 1, nullptr, kDrainTimeoutNs);
+    } else if (warp == kMmaWarp && lane == 0) {
+        // ================================ MMA issuer ================================
+        bool ok = mbar_wait(bar(qQ), 0, abort_flag, kWaitTimeoutNs);
+        auto issue_sdp = [&](int j) {
+            const int st = j % qStages;
+            const uint32_t stage = base + qOffKV + st * qStageBytes;
+            if (!mbar_wait(bar(qKVFull + st), (j / qStages) & 1, abort_flag, kWaitTimeoutNs)) return false;
+            tc_fence_after();
+            mma_ss_128x128<BF16>(tmem + qColS, base + qOffQ, stage);             // S = Q K^T
+            umma_commit(bar(qSFull));
+            mma_ss_128x128<BF16>(tmem + qColDP, base + qOffDO, stage + kTile);   // dP = dO V^T
+            umma_commit(bar(qDPFull));
+            return true;
+        };
+        if (ok && nk > 0) ok = issue_sdp(0);
+        for (int j = 0; ok && j < nk; ++j) {
+            if (j + 1 < nk) {
+                if (!(ok = mbar_wait(bar(qSdPFree), j & 1, abort_flag, kWaitTimeoutNs))) break;
+                if (!(ok = issue_sdp(j + 1))) break;
+            }
+            if (!(ok = mbar_wait(bar(qDSFull), j & 1, abort_flag, kWaitTimeoutNs))) break;
+            tc_fence_after();
+            const uint32_t stage = base + qOffKV + (j % qStages) * qStageBytes;
+            mma_ts_128x64<BF16>(tmem + qColDQ, tmem + qColDS, stage, j > 0);  // dQ += dS K
+            umma_commit(bar(qDone));
+            umma_commit(bar(qKVEmpty + j % qStages));
+        }
+        if (!ok) raise_abort(abort_flag);
+        umma_commit(bar(qDrain));
+        mbar_wait(bar(qDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------ host side ------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<EncodeTiledFn>(ptr);
+        return static_cast<EncodeTiledFn>(nullptr);
+    }();
+    return fn;
+}
+
+// [BH][N][64] 16-bit tensor; boxes of 128 rows x 64 values, 128-byte swizzle; rows past N of
+// a head are out of bounds (zero-filled), never the next head's.
+bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, bool bf16) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(N) * kD * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kBlk), 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+               const_cast<void*>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool BF16>
+int launch_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                void* dq, void* dk, void* dv, int64_t BH, int64_t N, bool causal, cudaStream_t stream) {
+    CUtensorMap mq, mk, mv, mo, mdo;
+    if (!make_map(&mq, q, BH, N, BF16) || !make_map(&mk, k, BH, N, BF16) || !make_map(&mv, v, BH, N, BF16) ||
+        !make_map(&mo, o, BH, N, BF16) || !make_map(&mdo, dout, BH, N, BF16))
+        return ATTN_ERR_DEVICE;
+    if (cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kvSmem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, qSmem) !=
+            cudaSuccess)
+        return ATTN_ERR_LAUNCH;
+    BwdParams prm;
+    prm.o = o;
+    prm.lse = lse;
+    prm.N = static_cast<int>(N);
+    prm.BH = static_cast<int>(BH);
+    prm.nblk = static_cast<int>((N + kBlk - 1) / kBlk);
+    prm.causal = causal ? 1 : 0;
+    prm.c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
+    prm.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(kD)));
+    const int64_t blocks = static_cast<int64_t>(prm.nblk) * BH;
+    if (blocks > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+    prm.grad0 = dk;
+    prm.grad1 = dv;
+    attn_bwd_dkdv_tc_kernel<BF16><<<static_cast<unsigned>(blocks), kThreads, kvSmem, stream>>>(mq, mk, mv, mo, mdo, prm);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+    prm.grad0 = dq;
+    prm.grad1 = nullptr;
+    attn_bwd_dq_tc_kernel<BF16><<<static_cast<unsigned>(blocks), kThreads, qSmem, stream>>>(mq, mk, mv, mdo, prm);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+int launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, int64_t BH, int64_t N, bool causal, bool bf16, cudaStream_t stream) {
+    if (N > 0x7FFFFFFFll - kBlk || BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+    return bf16 ? launch_impl<true>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream)
+                : launch_impl<false>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream);
+}
+
+int bwd_tc_device_error(bool clear, unsigned* err) {
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_bwd_error, sizeof(v)) != cudaSuccess) return ATTN_ERR_DEVICE;
+    if (clear && v != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_bwd_error, &zero, sizeof(zero)) != cudaSuccess) return ATTN_ERR_DEVICE;
+    }
+    *err = v;
+    return ATTN_OK;
+}
+
+}  // namespace attn

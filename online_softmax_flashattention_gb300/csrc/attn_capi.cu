@@ -126,8 +126,13 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
     int num_sms = 0;
     if ((st = check_device(&num_sms)) != ATTN_OK) return st;
     if (inject_launch_fault()) return ATTN_ERR_LAUNCH;
-    return attn::launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal != 0, dtype,
-                            static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == ATTN_F32)
+        return attn::launch_bwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                    static_cast<const float*>(v), static_cast<const float*>(o),
+                                    static_cast<const float*>(dout), lse, static_cast<float*>(dq),
+                                    static_cast<float*>(dk), static_cast<float*>(dv), BH, N, causal != 0, s);
+    return attn::launch_bwd_tc(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal != 0, dtype == ATTN_BF16, s);
 }
 
 size_t attn_materialized_workspace_bytes(int64_t B, int64_t H, int64_t N) {
@@ -176,10 +181,11 @@ int attn_fwd_materialized(const void* q, const void* k, const void* v, void* o, 
 }
 
 int attn_device_status(void* stream, int clear) {
-    unsigned err = 0;
-    const int st = attn::tc_device_error(static_cast<cudaStream_t>(stream), clear != 0, &err);
+    unsigned err = 0, berr = 0;
+    int st = attn::tc_device_error(static_cast<cudaStream_t>(stream), clear != 0, &err);
     if (st != ATTN_OK) return st;
-    return err ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    if ((st = attn::bwd_tc_device_error(clear != 0, &berr)) != ATTN_OK) return st;
+    return (err || berr) ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 const char* attn_status_string(int status) {

@@ -20,11 +20,18 @@ int launch_fwd_f32(const float* q, const float* k, const float* v, float* o, flo
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
                   int64_t N, bool causal, bool bf16, int num_sms, cudaStream_t stream);
 
-// Backward pass (two FFMA kernels, fp32 arithmetic) for float32, bf16 or fp16 tensors:
-// dq, dk, dv from q, k, v, the forward's o, the output gradient dout and the forward's base-2
-// log-sum-exps lse ([BH, N] float32).
-int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-               void* dq, void* dk, void* dv, int64_t BH, int64_t N, bool causal, int dtype, cudaStream_t stream);
+// Backward pass for float32 tensors (two FFMA kernels): dq, dk, dv from q, k, v, the forward's
+// o, the output gradient dout and the forward's base-2 log-sum-exps lse ([BH, N] float32).
+int launch_bwd_f32(const float* q, const float* k, const float* v, const float* o, const float* dout,
+                   const float* lse, float* dq, float* dk, float* dv, int64_t BH, int64_t N, bool causal,
+                   cudaStream_t stream);
+
+// The same for bf16 (bf16 = true) or fp16 tensors on tcgen05 tensor cores (two kernels).
+int launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, int64_t BH, int64_t N, bool causal, bool bf16, cudaStream_t stream);
+
+// Reads (and optionally clears) the tensor-core backward kernels' device error word.
+int bwd_tc_device_error(bool clear, unsigned* err);
 
 // Reads (and optionally clears) the tensor-core kernel's device error word after
 // synchronising `stream`. *err receives the word.
