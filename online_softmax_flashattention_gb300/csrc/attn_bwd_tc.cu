@@ -172,6 +172,43 @@ constexpr int kvSmem = kvOffAbort + 4 + 1024;
 static_assert(kvSmem <= 227 * 1024, "shared memory budget");
 constexpr uint32_t kvColS = 0, kvColDP = 128, kvColP = 256, kvColDS = 320, kvColDV = 384, kvColDK = 448;
 
+
+// One 32-query chunk of the dK/dV kernel's elementwise step for this thread's key: P^T and
+// dS^T = P^T (dP^T - delta) from S^T and dP^T in TMEM, stored back as 16-bit pairs. The
+// queries' lse and delta come from shared memory four at a time.
+template <bool BF16, bool kMasked>
+__device__ __forceinline__ void kv_chunk(uint32_t t, int ch, const float* ls, const float* dl, float c, int key,
+                                         int q0, int N, int causal) {
+    uint32_t s[32], dp[32];
+    ATTN_TMEM_LD_X32(t + kvColS + 32 * ch, s);
+    ATTN_TMEM_LD_X32(t + kvColDP + 32 * ch, dp);
+    tmem_ld_wait();
+    uint32_t pp[16], ds[16];
+#pragma unroll
+    for (int u4 = 0; u4 < 8; ++u4) {
+        const float4 lv = *reinterpret_cast<const float4*>(ls + ch * 32 + 4 * u4);
+        const float4 dv4 = *reinterpret_cast<const float4*>(dl + ch * 32 + 4 * u4);
+        const float lq[4] = {lv.x, lv.y, lv.z, lv.w}, dq[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+        float pv[4], dv[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            float pr = ex2_approx(fmaf(__uint_as_float(s[4 * u4 + h]), c, -lq[h]));
+            if constexpr (kMasked) {
+                const int query = q0 + ch * 32 + 4 * u4 + h;
+                if (!(query < N && key < N && (!causal || key <= query))) pr = 0.f;
+            }
+            pv[h] = pr;
+            dv[h] = pr * (__uint_as_float(dp[4 * u4 + h]) - dq[h]);
+        }
+        pp[2 * u4] = pack2<BF16>(pv[0], pv[1]);
+        pp[2 * u4 + 1] = pack2<BF16>(pv[2], pv[3]);
+        ds[2 * u4] = pack2<BF16>(dv[0], dv[1]);
+        ds[2 * u4 + 1] = pack2<BF16>(dv[2], dv[3]);
+    }
+    tmem_st_x16(t + kvColP + 16 * ch, pp);
+    tmem_st_x16(t + kvColDS + 16 * ch, ds);
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -247,30 +284,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The previous block's dV/dK products read P^T and dS^T: wait before overwriting.
             if (i > 0 && !(ok = warp_wait(bar(kvDone), (i - 1) & 1, abort_flag))) break;
             tc_fence_after();
+            // Only the causal diagonal block and ragged edges need a mask.
+            const bool masked = (p.causal && qb0 + i == kblk) || q0 + kBlk > N || k0 + kBlk > N;
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {  // 32 queries at a time
-                uint32_t s[32], dp[32];
-                ATTN_TMEM_LD_X32(t + kvColS + 32 * ch, s);
-                ATTN_TMEM_LD_X32(t + kvColDP + 32 * ch, dp);
-                tmem_ld_wait();
-                uint32_t pp[16], ds[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    float pv[2], dv[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int col = ch * 32 + 2 * u + h;
-                        const int query = q0 + col;
-                        const bool vis = query < N && key < N && (!p.causal || key <= query);
-                        const float pr = vis ? ex2_approx(fmaf(__uint_as_float(s[2 * u + h]), p.c, -ls[col])) : 0.f;
-                        pv[h] = pr;
-                        dv[h] = pr * (__uint_as_float(dp[2 * u + h]) - dl[col]);
-                    }
-                    pp[u] = pack2<BF16>(pv[0], pv[1]);
-                    ds[u] = pack2<BF16>(dv[0], dv[1]);
-                }
-                tmem_st_x16(t + kvColP + 16 * ch, pp);
-                tmem_st_x16(t + kvColDS + 16 * ch, ds);
+                if (masked)
+                    kv_chunk<BF16, true>(t, ch, ls, dl, p.c, key, q0, N, p.causal);
+                else
+                    kv_chunk<BF16, false>(t, ch, ls, dl, p.c, key, q0, N, p.causal);
             }
             // S^T and dP^T are copied out: the next block's products may overwrite them.
             tc_fence_before();
@@ -396,6 +417,34 @@ constexpr int qSmem = qOffAbort + 4 + 1024;
 static_assert(qSmem <= 227 * 1024, "shared memory budget");
 constexpr uint32_t qColS = 0, qColDP = 128, qColDS = 256, qColDQ = 320;
 
+
+// One 32-key chunk of the dQ kernel's elementwise step for this thread's query: dS = P (dP -
+// delta) from S and dP in TMEM, stored back as 16-bit pairs.
+template <bool BF16, bool kMasked>
+__device__ __forceinline__ void q_chunk(uint32_t t, int ch, float l2, float delta, float c, int query, int k0, int N,
+                                        int causal) {
+    uint32_t s[32], dp[32];
+    ATTN_TMEM_LD_X32(t + qColS + 32 * ch, s);
+    ATTN_TMEM_LD_X32(t + qColDP + 32 * ch, dp);
+    tmem_ld_wait();
+    uint32_t ds[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        float dv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float pr = ex2_approx(fmaf(__uint_as_float(s[2 * u + h]), c, -l2));
+            if constexpr (kMasked) {
+                const int key = k0 + ch * 32 + 2 * u + h;
+                if (!(query < N && key < N && (!causal || key <= query))) pr = 0.f;
+            }
+            dv[h] = pr * (__uint_as_float(dp[2 * u + h]) - delta);
+        }
+        ds[u] = pack2<BF16>(dv[0], dv[1]);
+    }
+    tmem_st_x16(t + qColDS + 16 * ch, ds);
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -475,26 +524,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The previous block's dQ product reads dS: wait before overwriting it.
             if (j > 0 && !(ok = warp_wait(bar(qDone), (j - 1) & 1, abort_flag))) break;
             tc_fence_after();
+            const bool masked = (p.causal && j == qblk) || q0 + kBlk > N || k0 + kBlk > N;
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {  // 32 keys at a time
-                uint32_t s[32], dp[32];
-                ATTN_TMEM_LD_X32(t + qColS + 32 * ch, s);
-                ATTN_TMEM_LD_X32(t + qColDP + 32 * ch, dp);
-                tmem_ld_wait();
-                uint32_t ds[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    float dv[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int key = k0 + ch * 32 + 2 * u + h;
-                        const bool vis = qin && key < N && (!p.causal || key <= query);
-                        const float pr = vis ? ex2_approx(fmaf(__uint_as_float(s[2 * u + h]), p.c, -l2)) : 0.f;
-                        dv[h] = pr * (__uint_as_float(dp[2 * u + h]) - delta);
-                    }
-                    ds[u] = pack2<BF16>(dv[0], dv[1]);
-                }
-                tmem_st_x16(t + qColDS + 16 * ch, ds);
+                if (masked)
+                    q_chunk<BF16, true>(t, ch, l2, delta, p.c, query, k0, N, p.causal);
+                else
+                    q_chunk<BF16, false>(t, ch, l2, delta, p.c, query, k0, N, p.causal);
             }
             tc_fence_before();
             __syncwarp();
