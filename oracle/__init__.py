@@ -16,6 +16,9 @@ Functions:
   base-2 log-sum-exp of its scores, ``log2(sum_j exp(s_j))`` ("m plus log two of l", section
   "Backwards, and training with it"); returns ``(o, lse)``.
 * ``attn_weights(q, k, causal, i)`` — the normalised softmax weights of one row of one head.
+* ``attn_fwd_kv(q, k, v, causal)`` — ``(o, lse)`` for Nq queries (``q`` ``[B, H, Nq, d]``) against
+  Nk >= Nq keys (``k, v`` ``[B, H, Nk, d]``), the queries being the last Nq positions: when causal,
+  query i sees keys ``0 .. Nk - Nq + i`` (the key-value cache case).
 * ``attn_bwd(q, k, v, dout, causal, threads=None)`` — ``(dq, dk, dv)`` in float64, the
   gradients of exact attention for the output gradient ``dout`` (``attn_bwd_oracle.c``,
   following the steps of the page's section "Backwards, and training with it").
@@ -72,6 +75,8 @@ def _load():
             lib.oracle_attn_bwd.argtypes = [fp, fp, fp, fp, i64, i64, i64, i64, ctypes.c_int, dp, dp, dp,
                                             ctypes.c_int]
             lib.oracle_attn_bwd.restype = ctypes.c_int
+            lib.oracle_attn_fwd_kv.argtypes = [fp, fp, fp, i64, i64, i64, i64, i64, ctypes.c_int, dp, dp]
+            lib.oracle_attn_fwd_kv.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -153,3 +158,23 @@ def attn_bwd(q, k, v, dout, causal: bool, threads: int | None = None):
     if st != 0:
         raise RuntimeError(f"oracle_attn_bwd failed with status {st}")
     return tuple(outs)
+
+
+def attn_fwd_kv(q, k, v, causal: bool):
+    """``(o, lse)`` float64: Nq queries against Nk >= Nq keys, the queries being the last Nq
+    positions (causal: query i sees keys ``0 .. Nk - Nq + i``); lse in base 2."""
+    lib = _load()
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    if q.ndim != 4 or k.shape != v.shape or k.ndim != 4 or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [B, H, Nq, d] and k, v [B, H, Nk, d]")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    o = np.empty((B, H, Nq, d), dtype=np.float64)
+    lse = np.empty((B, H, Nq), dtype=np.float64)
+    fp = ctypes.POINTER(ctypes.c_float)
+    dp = ctypes.POINTER(ctypes.c_double)
+    st = lib.oracle_attn_fwd_kv(q.ctypes.data_as(fp), k.ctypes.data_as(fp), v.ctypes.data_as(fp), B, H, Nq, Nk, d,
+                                int(bool(causal)), o.ctypes.data_as(dp), lse.ctypes.data_as(dp))
+    if st != 0:
+        raise RuntimeError(f"oracle_attn_fwd_kv failed with status {st}")
+    return o, lse

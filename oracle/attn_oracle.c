@@ -192,3 +192,58 @@ int oracle_attn_weights(const float* q, const float* k, int64_t N, int64_t d, in
     for (int64_t j = 0; j < visible; ++j) w[j] /= total;
     return 0;
 }
+
+/*
+ * The key-value cache case: Nq new queries against Nk >= Nq keys, the queries being the last
+ * Nq positions of the sequence. The "Flash attention in PyTorch, then in Triton" page names
+ * this case ("with a cache, the queries are a few new tokens against all the keys") without
+ * giving its mask; read plainly, query i sits at position Nk - Nq + i and, when causal, sees
+ * the keys up to and including that position (all of the cache and the new tokens up to
+ * itself). With Nq = Nk this is the ordinary causal mask. Per query row the arithmetic is
+ * steps 1-5 above.
+ *   q : float32 [B, H, Nq, d];  k, v : float32 [B, H, Nk, d]
+ *   o : double [B, H, Nq, d];   lse : NULL or double [B, H, Nq] (base 2)
+ */
+int oracle_attn_fwd_kv(const float* q, const float* k, const float* v, int64_t B, int64_t H, int64_t Nq,
+                       int64_t Nk, int64_t d, int causal, double* o, double* lse) {
+    if (B < 0 || H < 0 || Nq < 0 || Nk < Nq || d <= 0 || (causal != 0 && causal != 1)) return -1;
+    const int64_t BH = B * H;
+    if (BH == 0 || Nq == 0) return 0;
+    if (!q || !k || !v || !o) return -1;
+    const double scale = 1.0 / sqrt((double)d);
+    double* s = (double*)malloc(sizeof(double) * (size_t)Nk);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!s || !acc) {
+        free(s);
+        free(acc);
+        return -2;
+    }
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        const float* qh = q + bh * Nq * d;
+        const float* kh = k + bh * Nk * d;
+        const float* vh = v + bh * Nk * d;
+        for (int64_t i = 0; i < Nq; ++i) {
+            const int64_t visible = causal ? (Nk - Nq + i + 1) : Nk;
+            double best = -HUGE_VAL;
+            for (int64_t j = 0; j < visible; ++j) {
+                double dot = 0.0;
+                for (int64_t e = 0; e < d; ++e) dot += (double)qh[i * d + e] * (double)kh[j * d + e];
+                s[j] = dot * scale;
+                if (s[j] > best) best = s[j];
+            }
+            double total = 0.0;
+            for (int64_t j = 0; j < visible; ++j) {
+                s[j] = exp(s[j] - best);
+                total += s[j];
+            }
+            for (int64_t e = 0; e < d; ++e) acc[e] = 0.0;
+            for (int64_t j = 0; j < visible; ++j)
+                for (int64_t e = 0; e < d; ++e) acc[e] += s[j] * (double)vh[j * d + e];
+            for (int64_t e = 0; e < d; ++e) o[(bh * Nq + i) * d + e] = acc[e] / total;
+            if (lse) lse[bh * Nq + i] = (best + log(total)) / log(2.0);
+        }
+    }
+    free(s);
+    free(acc);
+    return 0;
+}
