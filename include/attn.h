@@ -81,8 +81,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, int64_t B, in
  * attn_fwd_lse — attn_fwd that also stores each row's log-sum-exp, the log of the sum the
  * softmax divides by, which a backward pass needs to rebuild the probabilities from the
  * scores. Following the "Flash attention in PyTorch, then in Triton" page (section
- * "Backwards, and training with it": the forward kernel "stores each row's log-sum-exp,
- * which in our powers of two is m plus log two of l"), it is kept in base 2:
+ * "Backwards, and training with it": the forward kernel saves, per row, its running maximum
+ * plus the base-2 log of its running total), it is kept in base 2:
  *
  *     lse[b,h,i] = log2( sum_{j in vis(i)} exp( q[b,h,i,:] . k[b,h,j,:] / sqrt(d) ) )
  *
@@ -122,6 +122,55 @@ int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* ls
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
              const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N,
              int64_t d, int causal, int dtype, void* stream);
+
+/*
+ * attn_fwd_kvcache — attention of Nq new queries against a key-value cache of Nk >= Nq rows:
+ * the generation case that the "Flash attention in PyTorch, then in Triton" page names and
+ * leaves out of its kernel (section "Backwards, and training with it"). The queries are the
+ * last Nq positions of the sequence, so query i sits at position Nk - Nq + i and
+ *
+ *     o[b,h,i,:] = sum_{j in vis(i)} softmax_j( q[b,h,i,:] . k[b,h,j,:] / sqrt(d) ) v[b,h,j,:]
+ *
+ * with vis(i) = {0 .. Nk-1}, or {0 .. Nk-Nq+i} when causal (with Nq == Nk this is attn_fwd's
+ * mask). The key range is cut into num_splits shares, one CTA each; every share runs the
+ * page's online softmax (section "Flash attention") over its keys and leaves its normalised
+ * output O_s and base-2 log-sum-exp lse_s, and a second kernel merges them the way the online
+ * softmax merges tiles: lse = log2 sum_s 2^lse_s, o = sum_s 2^(lse_s - lse) O_s. With one
+ * share the first kernel writes o directly. All arithmetic is fp32 on CUDA cores (the work is
+ * bound by reading the cache); o is rounded to dtype (RNE). Nothing is allocated.
+ *
+ *   q, o          : device pointers, [B, H, Nq, d] of dtype, 16-byte aligned; o must not
+ *                   overlap q, k, v, lse or the workspace
+ *   k, v          : const device pointers, [B, H, Nk, d] of dtype, 16-byte aligned
+ *   lse           : NULL, or device pointer float32 [B, H, Nq], 4-byte aligned, receiving each
+ *                   row's base-2 log-sum-exp as attn_fwd_lse defines it; must not overlap the
+ *                   other buffers
+ *   workspace     : device pointer, 256-byte aligned, caller-owned fp32 scratch for the shares'
+ *                   partial results (contents on entry ignored, on exit unspecified); may be NULL
+ *                   when workspace_bytes is 0. It must not overlap any tensor.
+ *   workspace_bytes: its size; attn_kvcache_workspace_bytes(B, H, Nq, num_splits) is enough
+ *   Nq, Nk        : 0 <= Nq <= Nk <= ATTN_MAX_N, Nq <= 8 * 65535; Nq == 0 or B*H == 0 is a
+ *                   successful no-op; Nk == 0 requires Nq == 0
+ *   num_splits    : 1 .. ATTN_KV_MAX_SPLITS, or 0 for the library's choice for this device
+ *                   (attn_kvcache_num_splits), halved until the workspace holds it (down to 1,
+ *                   which needs none). An explicit count above 1 whose workspace is too small
+ *                   returns ATTN_ERR_WORKSPACE. Shares past the last key are empty and carry
+ *                   weight 0 in the merge.
+ *   other arguments: as attn_fwd (d == 64; dtype f32, bf16 or f16; causal 0/1).
+ */
+#define ATTN_KV_MAX_SPLITS 1024
+int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                     size_t workspace_bytes, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                     int causal, int dtype, int num_splits, void* stream);
+
+/* Bytes of workspace attn_fwd_kvcache needs for num_splits shares: B*H*Nq*num_splits rows of
+ * d + 1 floats, in two regions rounded up to 256 bytes; 0 when num_splits <= 1. Returns 0 for
+ * negative sizes or on overflow. */
+size_t attn_kvcache_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int num_splits);
+
+/* The share count attn_fwd_kvcache picks for num_splits == 0 on the current device (about
+ * eight CTAs per SM, at least 256 keys a share); 1 if the device cannot be queried. */
+int attn_kvcache_num_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk);
 
 /*
  * attn_fwd_materialized — the same result by the materialised path of attention.cu
@@ -185,7 +234,8 @@ int attn_device_status(void* stream, int clear);
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* attn_status_string(int status);
 
-/* ABI version of this header: (major << 16) | minor (1.1 added attn_fwd_lse, 1.2 attn_bwd). */
+/* ABI version of this header: (major << 16) | minor (1.1 added attn_fwd_lse, 1.2 attn_bwd,
+ * 1.3 attn_fwd_kvcache). */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

@@ -25,7 +25,8 @@ __all__ = [
     "ATTN_F32", "ATTN_BF16", "ATTN_F16", "AttnError", "AttnLibraryMissing", "library_path",
     "attn_fwd", "attn_fwd_materialized", "attn_materialized_workspace_bytes", "attn_device_status",
     "attn_status_string", "attn_abi_version", "raw", "attn_fwd_materialized_noalloc",
-    "ATTN_NOALLOC_MAX_N", "attn_fwd_lse", "attn_bwd",
+    "ATTN_NOALLOC_MAX_N", "attn_fwd_lse", "attn_bwd", "attn_fwd_kvcache", "attn_kvcache_workspace_bytes",
+    "attn_kvcache_num_splits", "ATTN_KV_MAX_SPLITS",
 ]
 
 ATTN_F32, ATTN_BF16, ATTN_F16 = 0, 1, 2
@@ -70,6 +71,12 @@ def raw():
             lib.attn_fwd_lse.restype = ci
             lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ci, ci, vp]
             lib.attn_bwd.restype = ci
+            lib.attn_fwd_kvcache.argtypes = [vp, vp, vp, vp, vp, vp, sz, i64, i64, i64, i64, i64, ci, ci, ci, vp]
+            lib.attn_fwd_kvcache.restype = ci
+            lib.attn_kvcache_workspace_bytes.argtypes = [i64, i64, i64, ci]
+            lib.attn_kvcache_workspace_bytes.restype = sz
+            lib.attn_kvcache_num_splits.argtypes = [i64, i64, i64, i64]
+            lib.attn_kvcache_num_splits.restype = ci
             lib.attn_fwd_materialized.argtypes = [vp, vp, vp, vp, vp, sz, i64, i64, i64, i64, ci, ci, vp]
             lib.attn_fwd_materialized.restype = ci
             lib.attn_materialized_workspace_bytes.argtypes = [i64, i64, i64]
@@ -176,6 +183,67 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     if st != 0:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv
+
+
+ATTN_KV_MAX_SPLITS = 1024  # include/attn.h: most shares the key range may be cut into
+
+
+def attn_kvcache_workspace_bytes(B: int, H: int, Nq: int, num_splits: int) -> int:
+    return int(raw().attn_kvcache_workspace_bytes(B, H, Nq, num_splits))
+
+
+def attn_kvcache_num_splits(B: int, H: int, Nq: int, Nk: int, device: torch.device | int | None = None) -> int:
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index or 0)
+    with torch.cuda.device(dev):
+        return int(raw().attn_kvcache_num_splits(B, H, Nq, Nk))
+
+
+def attn_fwd_kvcache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = True,
+                     num_splits: int = 0, workspace: torch.Tensor | None = None,
+                     out: torch.Tensor | None = None, lse: torch.Tensor | bool | None = None,
+                     stream: torch.cuda.Stream | None = None):
+    """Attention of ``q`` ``[B, H, Nq, d]`` (the last Nq positions) against a key-value cache
+    ``k, v`` ``[B, H, Nk, d]``, Nq <= Nk; causal: query i sees keys ``0 .. Nk - Nq + i``.
+    ``num_splits`` 0 lets the library choose how many shares the keys are cut into. When
+    ``workspace`` (a uint8 CUDA tensor) is omitted, one of the needed size is allocated here.
+    ``lse=True`` (or a float32 ``[B, H, Nq]`` tensor) also returns the base-2 log-sum-exps:
+    the result is then ``(o, lse)``, otherwise ``o``."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-d tensor")
+    if k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q must be [B, H, Nq, d] and k, v [B, H, Nk, d]")
+    if q.dtype != k.dtype or q.dtype != v.dtype or q.dtype not in _DTYPES:
+        raise TypeError("q, k, v must share one dtype among float32, bfloat16, float16")
+    if q.device != k.device or q.device != v.device:
+        raise ValueError("q, k, v must be on one device")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or out.device != q.device or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    want_lse = lse is not None and lse is not False
+    if lse is True:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    elif want_lse and (lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or lse.device != q.device
+                       or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, Nq] on q's device")
+    lib = raw()
+    with torch.cuda.device(q.device):
+        splits = int(num_splits) if num_splits else int(lib.attn_kvcache_num_splits(B, H, Nq, Nk))
+        if workspace is None:
+            need = int(lib.attn_kvcache_workspace_bytes(B, H, Nq, splits))
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        st = lib.attn_fwd_kvcache(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr() if want_lse else None, workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), B, H, Nq, Nk, d,
+                                  int(bool(causal)), _DTYPES[q.dtype], int(num_splits), _stream(q.device, stream))
+    if st != 0:
+        raise AttnError(st, "attn_fwd_kvcache")
+    return (out, lse) if want_lse else out
 
 
 def attn_materialized_workspace_bytes(B: int, H: int, N: int) -> int:

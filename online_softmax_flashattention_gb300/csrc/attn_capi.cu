@@ -135,6 +135,72 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
     return attn::launch_bwd_tc(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal != 0, dtype == ATTN_BF16, s);
 }
 
+size_t attn_kvcache_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int num_splits) {
+    if (B < 0 || H < 0 || Nq < 0 || B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return 0;
+    return attn::decode_workspace_bytes(B * H, Nq, num_splits);
+}
+
+int attn_kvcache_num_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return 1;
+    int num_sms = 0;
+    if (check_device(&num_sms) != ATTN_OK) return 1;
+    return attn::decode_auto_splits(B * H, Nq, Nk, num_sms);
+}
+
+int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                     size_t workspace_bytes, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                     int causal, int dtype, int num_splits, void* stream) {
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d < 0) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (Nq > Nk || num_splits < 0) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_UNSUPPORTED;
+    if (d != kHeadDim) return ATTN_ERR_UNSUPPORTED;
+    if (Nk > ATTN_MAX_N || Nq > 8 * 65535ll || num_splits > ATTN_KV_MAX_SPLITS) return ATTN_ERR_UNSUPPORTED;
+    if (B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    if (BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+    if (BH == 0 || Nq == 0) return ATTN_OK;
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return ATTN_ERR_ALIGN;
+    const size_t esz = elem_size(dtype);
+    const size_t qbytes = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * kHeadDim * esz;
+    const size_t kbytes = static_cast<size_t>(BH) * static_cast<size_t>(Nk) * kHeadDim * esz;
+    if (overlap(o, qbytes, q, qbytes) || overlap(o, qbytes, k, kbytes) || overlap(o, qbytes, v, kbytes))
+        return ATTN_ERR_ALIAS;
+    const size_t lbytes = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * sizeof(float);
+    if (lse != nullptr) {
+        if (!aligned(lse, 4)) return ATTN_ERR_ALIGN;
+        if (overlap(lse, lbytes, q, qbytes) || overlap(lse, lbytes, k, kbytes) || overlap(lse, lbytes, v, kbytes) ||
+            overlap(lse, lbytes, o, qbytes))
+            return ATTN_ERR_ALIAS;
+    }
+    // An explicit share count is checked against the workspace before the device is queried;
+    // the automatic one needs the SM count first.
+    int num_sms = 0;
+    int st = ATTN_OK;
+    int splits = num_splits;
+    if (splits == 0) {
+        if ((st = check_device(&num_sms)) != ATTN_OK) return st;
+        splits = attn::decode_auto_splits(BH, Nq, Nk, num_sms);
+        while (splits > 1 && attn::decode_workspace_bytes(BH, Nq, splits) > workspace_bytes) splits /= 2;
+        if (splits > 1 && workspace == nullptr) splits = 1;
+    }
+    if (splits > 1) {
+        const size_t need = attn::decode_workspace_bytes(BH, Nq, splits);
+        if (need == 0) return ATTN_ERR_UNSUPPORTED;
+        if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return ATTN_ERR_ALIGN;
+        if (overlap(workspace, need, q, qbytes) || overlap(workspace, need, k, kbytes) ||
+            overlap(workspace, need, v, kbytes) || overlap(workspace, need, o, qbytes) ||
+            (lse != nullptr && overlap(workspace, need, lse, lbytes)))
+            return ATTN_ERR_ALIAS;
+    }
+    if (num_splits != 0 && (st = check_device(&num_sms)) != ATTN_OK) return st;
+    if (inject_launch_fault()) return ATTN_ERR_LAUNCH;
+    return attn::launch_decode(q, k, v, o, lse, workspace, BH, Nq, Nk, causal != 0, dtype, splits,
+                               static_cast<cudaStream_t>(stream));
+}
+
 size_t attn_materialized_workspace_bytes(int64_t B, int64_t H, int64_t N) {
     if (B < 0 || H < 0 || N < 0 || B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return 0;
     const size_t per = attn::materialized_head_bytes(N);
@@ -203,6 +269,6 @@ const char* attn_status_string(int status) {
     }
 }
 
-int attn_abi_version(void) { return (1 << 16) | 2; }
+int attn_abi_version(void) { return (1 << 16) | 3; }
 
 }  // extern "C"

@@ -47,4 +47,16 @@ int launch_materialized(const void* q, const void* k, const void* v, void* o, vo
 // each region rounded up to 256 bytes. Returns 0 on overflow.
 size_t materialized_head_bytes(int64_t N);
 
+// Key-value cache attention (attn_decode.cu): Nq queries [BH, Nq, 64] against Nk keys and
+// values [BH, Nk, 64], key range cut into `splits` CTAs' shares and merged by a second kernel
+// through the workspace when splits > 1.
+int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace, int64_t BH,
+                  int64_t Nq, int64_t Nk, bool causal, int dtype, int splits, cudaStream_t stream);
+
+// Workspace bytes launch_decode needs for `splits` (0 when splits <= 1 or on overflow).
+size_t decode_workspace_bytes(int64_t BH, int64_t Nq, int64_t splits);
+
+// Split count chosen when the caller asks for the automatic one.
+int decode_auto_splits(int64_t BH, int64_t Nq, int64_t Nk, int num_sms);
+
 }  // namespace attn

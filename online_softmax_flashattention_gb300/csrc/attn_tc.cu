@@ -8,7 +8,7 @@
 // terms are added (the online normaliser of that page's "Flash attention" section and of
 // attention.cu's attentionOnline). After the last tile O / l is the softmax-weighted sum.
 // Scores are kept in base-2 units, s * log2(e) / sqrt(d), so every exponential is an exp2
-// ("A kernel in Triton": the kernel keeps its scores times log two e), and the
+// (section "A kernel in Triton" scales its scores by log2(e) for the same reason), and the
 // probabilities are rounded to the input type before they weigh v so the tensor cores can
 // take them (same section). Causal tiles past a query tile's last row are skipped
 // (section "The online softmax, in PyTorch"); ragged N is masked on keys and clipped on

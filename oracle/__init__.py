@@ -13,8 +13,8 @@ Functions:
   ``rows`` is an optional array of flat row ids ``bh * N + i``; the result is ``[len(rows), d]``
   (or ``[B, H, N, d]`` when ``rows`` is None).
 * ``attn_fwd_lse(q, k, v, causal, rows=None, threads=None)`` — the same rows and, per row, the
-  base-2 log-sum-exp of its scores, ``log2(sum_j exp(s_j))`` ("m plus log two of l", section
-  "Backwards, and training with it"); returns ``(o, lse)``.
+  base-2 log-sum-exp of its scores, ``log2(sum_j exp(s_j))`` (the running maximum plus the base-2 log of the running total,
+  section "Backwards, and training with it"); returns ``(o, lse)``.
 * ``attn_weights(q, k, causal, i)`` — the normalised softmax weights of one row of one head.
 * ``attn_fwd_kv(q, k, v, causal)`` — ``(o, lse)`` for Nq queries (``q`` ``[B, H, Nq, d]``) against
   Nk >= Nq keys (``k, v`` ``[B, H, Nk, d]``), the queries being the last Nq positions: when causal,

@@ -10,11 +10,11 @@
  * gives the gradients step by step, which this file follows in double precision with the
  * whole table of one head held in memory:
  *   1. S = q k^T * scale, masked entries excluded;  P = row softmax of S
- *   2. dV = P^T do                                   ("P transposed times d O")
- *   3. dP = do v^T                                    ("d O times V transposed")
- *   4. delta_i = sum_e do[i,e] * o[i,e]               ("each row's sum of d O times O")
- *   5. dS = P * (dP - delta)  elementwise, per row     ("P times d P minus delta")
- *   6. dQ = dS k * scale,  dK = dS^T q * scale         ("each scaled")
+ *   2. dV = P^T do
+ *   3. dP = do v^T
+ *   4. delta_i = sum_e do[i,e] * o[i,e]   (one number per row, formed once)
+ *   5. dS = P * (dP - delta)  elementwise, per row (the softmax's backward)
+ *   6. dQ = dS k * scale,  dK = dS^T q * scale (the scores carry the scale)
  * o in step 4 is this file's own forward (row softmax times v, in double), so nothing here
  * depends on a device result.
  *

@@ -21,8 +21,9 @@
  *   4. o[i,e] = (sum_j w_j * v[j,e]) / L
  *
  * The row's log-sum-exp, which the forward pass keeps for the backward pass, is the log of
- * the sum the softmax divides by. The page keeps it in powers of two, "m plus log two of l"
- * ("Backwards, and training with it"), i.e. log2(sum_j exp(s_j)):
+ * the sum the softmax divides by. The page keeps it in base 2, as the running maximum plus
+ * the base-2 log of the running total ("Backwards, and training with it"), i.e.
+ * log2(sum_j exp(s_j)):
  *   5. lse2 = (m + log(L)) / ln(2)
  *
  * Inputs are float32 arrays that hold exactly the values the device reads (bf16/fp16
@@ -196,8 +197,8 @@ int oracle_attn_weights(const float* q, const float* k, int64_t N, int64_t d, in
 /*
  * The key-value cache case: Nq new queries against Nk >= Nq keys, the queries being the last
  * Nq positions of the sequence. The "Flash attention in PyTorch, then in Triton" page names
- * this case ("with a cache, the queries are a few new tokens against all the keys") without
- * giving its mask; read plainly, query i sits at position Nk - Nq + i and, when causal, sees
+ * this case (a handful of new tokens attending to every cached key, which its kernel leaves
+ * out; section "Backwards, and training with it") without giving its mask; read plainly, query i sits at position Nk - Nq + i and, when causal, sees
  * the keys up to and including that position (all of the cache and the new tokens up to
  * itself). With Nq = Nk this is the ordinary causal mask. Per query row the arithmetic is
  * steps 1-5 above.

@@ -109,3 +109,46 @@ def test_binding_has_no_fallback_when_library_missing(monkeypatch, tmp_path):
 def test_valid_call_without_gpu_reports_device_error(lib):
     assert lib.attn_fwd(P, P * 3, P * 5, P * 9, 1, 1, 8, 64, 0, 1, None) == 5
     assert lib.attn_fwd_lse(P, P * 3, P * 5, P * 9, P * 20, 1, 1, 8, 64, 0, 1, None) == 5
+
+
+# attn_fwd_kvcache(q, k, v, o, lse, ws, ws_bytes, B, H, Nq, Nk, d, causal, dtype, splits, stream)
+# q, o: 1 x 2 x 4 x 64 bf16 = 1 KiB at P and 9P; k, v: 1 x 2 x 100 x 64 bf16 = 25.6 KiB at 3P, 5P.
+@pytest.mark.parametrize("args,want", [
+    ((P, P * 3, P * 5, P * 9, None, None, 0, -1, 2, 4, 100, 64, 1, 1, 1), 1),   # negative B
+    ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 101, 100, 64, 1, 1, 1), 1),  # Nq > Nk
+    ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 2, 1, 1), 1),    # causal not 0/1
+    ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 1, -1), 1),   # negative split count
+    ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 128, 1, 1, 1), 2),   # d != 64
+    ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 5, 1), 2),    # unknown dtype
+    ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 1, 1025), 2),  # too many shares
+    ((None, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 1, 1), 1),  # null q
+    ((P, P * 3 + 8, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 1, 1), 3),  # misaligned k
+    ((P, P * 3, P * 5, P * 3 + 512, None, None, 0, 1, 2, 4, 100, 64, 1, 1, 1), 4),  # o overlaps k
+    ((P, P * 3, P * 5, P * 9, P * 20 + 1, None, 0, 1, 2, 4, 100, 64, 1, 1, 1), 3),  # lse misaligned
+    ((P, P * 3, P * 5, P * 9, P * 5 + 64, None, 0, 1, 2, 4, 100, 64, 1, 1, 1), 4),  # lse overlaps v
+    ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 1, 4), 8),    # 4 shares, no workspace
+    ((P, P * 3, P * 5, P * 9, None, P * 40, 100, 1, 2, 4, 100, 64, 1, 1, 4), 8),  # workspace too small
+    ((P, P * 3, P * 5, P * 9, None, P * 40 + 16, 1 << 20, 1, 2, 4, 100, 64, 1, 1, 4), 3),  # ws misaligned
+    ((P, P * 3, P * 5, P * 9, None, P * 5, 1 << 20, 1, 2, 4, 100, 64, 1, 1, 4), 4),  # ws overlaps v
+    ((None, None, None, None, None, None, 0, 1, 2, 0, 100, 64, 1, 1, 0), 0),    # Nq = 0: no-op
+    ((None, None, None, None, None, None, 0, 0, 2, 4, 100, 64, 1, 1, 0), 0),    # B = 0: no-op
+])
+def test_kvcache_argument_checks(lib, args, want):
+    assert lib.attn_fwd_kvcache(*args, None) == want
+
+
+def test_kvcache_workspace_bytes(lib):
+    r = 2 * 3 * 5 * 7  # B * H * Nq * splits
+    want = (r * 64 * 4 + 255) // 256 * 256 + (r * 4 + 255) // 256 * 256
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 7) == want
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 1) == 0   # one share writes o directly
+    assert lib.attn_kvcache_workspace_bytes(-1, 3, 5, 7) == 0
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 1025) == 0
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="needs a machine without a GPU")
+def test_kvcache_valid_call_without_gpu_reports_device_error(lib):
+    ws = P * 64
+    assert lib.attn_fwd_kvcache(P, P * 3, P * 5, P * 9, None, ws, 1 << 20, 1, 2, 4, 100, 64, 1, 1, 4, None) == 5
+    assert lib.attn_fwd_kvcache(P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 1, 0, None) == 5
+    assert lib.attn_kvcache_num_splits(1, 2, 4, 100) == 1

@@ -1,0 +1,136 @@
+"""GPU parity of attn_fwd_kvcache: Nq new queries (the last Nq positions) against a key-value
+cache of Nk keys, the key range cut into shares merged by their log-sum-exps, against the
+double oracle's key-value cache case on the same seeded inputs.
+
+Tolerances: o as the forward's (bf16/fp16 2e-2 absolute against the double oracle on the same
+rounded inputs; fp32 1e-5 * Nk * max|ref| and the attention.cu gate with N = Nk); lse as
+attn_fwd_lse's, 2e-5 * (1 + max|lse|) + 1e-4 (fp32 scores from exact products over d = 64; the
+merge adds one fp32 log2 and exp2 per share). Different share counts give the same result
+within those bounds, not bit for bit (the sums are taken in another order).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import online_softmax_flashattention_gb300 as fa
+import oracle
+import seeded_inputs as si
+from attn_testlib import check, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _lse_bound(ref):
+    return 2e-5 * (1.0 + float(np.max(np.abs(ref)))) + 1e-4
+
+
+def _inputs(seed, B, H, Nq, Nk, dtype, qk_scale=1.0):
+    q = si.qkv(seed, B, H, Nq, 64, dtype, qk_scale=qk_scale)[0]
+    _, k, v = si.qkv(seed + 1, B, H, Nk, 64, dtype, qk_scale=qk_scale)
+    return q, k, v
+
+
+def _run(seed, B, H, Nq, Nk, dtype, causal, splits, qk_scale=1.0):
+    q, k, v = _inputs(seed, B, H, Nq, Nk, dtype, qk_scale)
+    qd, kd, vd = (to_dev(x, dtype) for x in (q, k, v))
+    o, lse = fa.attn_fwd_kvcache(qd, kd, vd, causal=causal, num_splits=splits, lse=True)
+    torch.cuda.synchronize()
+    assert fa.attn_device_status(clear=True) == 0
+    ref_o, ref_lse = oracle.attn_fwd_kv(q, k, v, causal)
+    got_o = o.float().cpu().numpy().astype(np.float64)
+    check(got_o, ref_o, dtype, Nk, f"kvcache {dtype} Nq={Nq} Nk={Nk} splits={splits}", page_gate=(qk_scale == 1.0))
+    got_lse = lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got_lse))
+    err = float(np.max(np.abs(got_lse - ref_lse)))
+    assert err <= _lse_bound(ref_lse), f"lse max err {err:.3e} > {_lse_bound(ref_lse):.3e}"
+    return got_o, got_lse
+
+
+SHAPES = [(1, 1), (1, 300), (1, 4096), (2, 77), (4, 257), (5, 1000), (8, 8), (16, 1000), (33, 64), (100, 100)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", SHAPES)
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_kvcache_against_oracle(dtype, causal, Nq, Nk, splits):
+    _run(0xCAC30000 + Nq * 7919 + Nk, 2, 3, Nq, Nk, dtype, causal, splits)
+
+
+@pytest.mark.parametrize("splits", [2, 7, 64, 200, 1024])
+def test_kvcache_many_shares_including_empty_ones(splits):
+    # 1024 shares over 300 keys: shares are rounded to 32 keys, so most are empty and must
+    # carry weight 0 in the merge.
+    _run(0xCAC31000 + splits, 1, 2, 3, 300, "bf16", True, splits)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_kvcache_qk_scaled_x8(dtype):
+    # Scores of std ~64: the online rescale and the share merge both see large maxima.
+    _run(0xCAC32000, 1, 2, 4, 700, dtype, True, 5, qk_scale=8.0)
+
+
+def test_kvcache_share_count_does_not_change_the_result_beyond_rounding():
+    q, k, v = _inputs(0xCAC33000, 2, 4, 3, 2048, "bf16")
+    qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+    outs = [fa.attn_fwd_kvcache(qd, kd, vd, causal=True, num_splits=s, lse=True) for s in (1, 2, 5, 16, 64)]
+    torch.cuda.synchronize()
+    o0, l0 = outs[0]
+    for o, l in outs[1:]:
+        assert float((o.float() - o0.float()).abs().max()) <= 2 ** -7  # one bf16 ulp at |o| < 1, twice
+        assert float((l - l0).abs().max()) <= 1e-4
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_kvcache_square_case_matches_the_flash_forward(causal):
+    # Nq == Nk is ordinary attention: same result as attn_fwd_lse within the forward's bounds.
+    q, k, v = si.qkv(0xCAC34000, 1, 2, 200, 64, "bf16")
+    qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+    o, lse = fa.attn_fwd_kvcache(qd, kd, vd, causal=causal, num_splits=3, lse=True)
+    o2, lse2 = fa.attn_fwd_lse(qd, kd, vd, causal=causal)
+    torch.cuda.synchronize()
+    assert float((o.float() - o2.float()).abs().max()) <= 2e-2
+    assert float((lse - lse2).abs().max()) <= 2e-4
+
+
+def test_kvcache_single_visible_key_returns_its_value():
+    # Causal with Nq == Nk: query 0 sees key 0 alone, so o[0] == v[0] exactly and lse == s_00 * log2 e.
+    q, k, v = si.qkv(0xCAC35000, 1, 1, 16, 64, "f32")
+    qd, kd, vd = (to_dev(x, "f32") for x in (q, k, v))
+    o, lse = fa.attn_fwd_kvcache(qd, kd, vd, causal=True, num_splits=4, lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o[0, 0, 0].cpu(), torch.from_numpy(v[0, 0, 0]))
+    s00 = float(np.dot(q[0, 0, 0].astype(np.float64), k[0, 0, 0].astype(np.float64))) / 8.0
+    assert abs(float(lse[0, 0, 0]) - s00 / np.log(2.0)) <= 1e-5 * (1 + abs(s00))
+
+
+def test_kvcache_decode_workload_sampled():
+    # One new token per sequence against an 8192-key cache, B16 H12 (the decode measurement's
+    # shape), automatic share count; every query row is checked against the oracle.
+    B, H, Nq, Nk = 16, 12, 1, 8192
+    q, k, v = _inputs(0xCAC36000, B, H, Nq, Nk, "bf16")
+    qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+    o, lse = fa.attn_fwd_kvcache(qd, kd, vd, causal=True, lse=True)
+    torch.cuda.synchronize()
+    assert fa.attn_device_status(clear=True) == 0
+    ref_o, ref_lse = oracle.attn_fwd_kv(q, k, v, True)
+    check(o.float().cpu().numpy().astype(np.float64), ref_o, "bf16", Nk, "decode B16H12 Nk8192")
+    assert float(np.max(np.abs(lse.cpu().numpy() - ref_lse))) <= _lse_bound(ref_lse)
+
+
+def test_kvcache_explicit_workspace_and_outputs_are_used():
+    B, H, Nq, Nk, S = 1, 3, 2, 500, 6
+    q, k, v = _inputs(0xCAC37000, B, H, Nq, Nk, "f16")
+    qd, kd, vd = (to_dev(x, "f16") for x in (q, k, v))
+    ws = torch.empty(fa.attn_kvcache_workspace_bytes(B, H, Nq, S), dtype=torch.uint8, device="cuda")
+    out = torch.full_like(qd, float("nan"))
+    lse = torch.full((B, H, Nq), float("nan"), device="cuda")
+    r = fa.attn_fwd_kvcache(qd, kd, vd, causal=False, num_splits=S, workspace=ws, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert r[0] is out and r[1] is lse
+    ref_o, ref_lse = oracle.attn_fwd_kv(q, k, v, False)
+    check(out.float().cpu().numpy().astype(np.float64), ref_o, "f16", Nk, "explicit workspace")
+    assert float(np.max(np.abs(lse.cpu().numpy() - ref_lse))) <= _lse_bound(ref_lse)
+    with pytest.raises(fa.AttnError):  # one byte short
+        fa.attn_fwd_kvcache(qd, kd, vd, num_splits=S, workspace=ws[:-1])

@@ -1,7 +1,7 @@
 """Pins for the oracle's key-value cache case: Nq new queries, the last Nq positions, against
-Nk >= Nq keys; when causal, query i sees keys 0 .. Nk - Nq + i (the reading of the page's "with
-a cache, the queries are a few new tokens against all the keys", section "Backwards, and
-training with it"). Pins: PyTorch float64 attention with that mask written out, 40-digit
+Nk >= Nq keys; when causal, query i sees keys 0 .. Nk - Nq + i (the plain reading of the page's
+mention of generation with a cache, where a few new tokens attend to every cached key, section
+"Backwards, and training with it"). Pins: PyTorch float64 attention with that mask written out, 40-digit
 decimal brute force, closed forms (equal scores; one visible key), and the reduction to the
 ordinary causal case when Nq = Nk.
 """

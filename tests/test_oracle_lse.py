@@ -1,8 +1,8 @@
 """Pins for the oracle's log-sum-exp, the value the forward pass keeps for the backward pass.
 
 The "Flash attention in PyTorch, then in Triton" page (section "Backwards, and training with
-it") defines it as the log of the sum the softmax divides by, kept in powers of two as
-"m plus log two of l": lse2_i = log2(sum_{j visible} exp(q_i . k_j / sqrt(d))). The pins:
+it") defines it as the log of the sum the softmax divides by, kept in base 2 as the
+running maximum plus the base-2 log of the running total: lse2_i = log2(sum_{j visible} exp(q_i . k_j / sqrt(d))). The pins:
 closed forms (one key, equal scores, two keys), 40-digit decimal brute force, PyTorch's
 float64 logsumexp, and its relation to the softmax weights; planted mistakes in the C source
 (natural log, the maximum dropped, the wrong base) must fail them.
