@@ -19,6 +19,11 @@ Multi-GPU: every rank runs the same workload on its own GPU (independent replica
 scaling; the path has no exchange step), and rank 0 reports the aggregate over ranks with
 the slowest rank's time. Barrier and max use a gloo group on the host.
 
+Beside the headline line's keys, ``decode`` reports the key-value cache path
+(``attn_fwd_kvcache``) on one new token per sequence against an 8192-key cache, B16 H12 d64
+bf16: GB/s of algorithmic bytes (K and V read once, q read, o written) against the measured
+HBM copy bandwidth, 50 calls back to back (K and V, 403 MB, exceed L2, so nothing is flushed).
+
 ``--impl reference`` times the CPU oracle (double precision, all host cores) on the same
 workload instead, each step a bounded sample of query rows, and prints the same line.
 """
@@ -51,6 +56,12 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 L2_FLUSH_BYTES = 256 << 20
 TC_SOURCE = os.path.join(ROOT, "online_softmax_flashattention_gb300", "csrc", "attn_tc.cu")
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_tc_bf16_causal_B1H12N8192.md")
+# Key-value cache decode, reported beside the headline: one new token per sequence against an
+# 8192-key cache, B16 H12 d64 bf16 (K and V: 403 MB, larger than L2).
+DECODE = {"workload": "key-value cache decode, bf16, B16 H12 Nq1 Nk8192 d64 (one new token per sequence)",
+          "B": 16, "H": 12, "Nq": 1, "Nk": 8192, "d": 64, "causal": True, "dtype": "bf16"}
+DECODE_SOURCE = os.path.join(ROOT, "online_softmax_flashattention_gb300", "csrc", "attn_decode.cu")
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "attn_decode_bf16_B16H12Nq1Nk8192.md")
 
 
 def workload_flops(B, H, N, d, causal):
@@ -75,24 +86,31 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_sha256():
-    with open(TC_SOURCE, "rb") as f:
+def source_sha256(path=None):
+    with open(path or TC_SOURCE, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def recorded_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+def recorded_traffic(profile=None, source=None):
+    """DRAM bytes per launch from a committed ncu summary (the forward's by default), if it
+    matches the current source."""
+    profile = profile or TRAFFIC_PROFILE
     try:
-        text = open(TRAFFIC_PROFILE).read()
+        text = open(profile).read()
     except OSError:
         return None, "no ncu summary"
     m_t = re.search(r"^traffic_bytes_per_launch:\s*(\d+)", text, re.M)
     m_h = re.search(r"^source_sha256:\s*([0-9a-f]{64})", text, re.M)
     if not m_t or not m_h:
         return None, "summary lacks traffic or source hash"
-    if m_h.group(1) != source_sha256():
+    if m_h.group(1) != source_sha256(source):
         return None, "kernel changed since the ncu capture"
     return int(m_t.group(1)), "ncu capture of this source"
+
+
+def decode_bytes(B, H, Nq, Nk, d, esz=2):
+    """Algorithmic bytes of one decode call: K and V read once, q read, o written."""
+    return esz * B * H * (2 * Nk * d + 2 * Nq * d)
 
 
 # ----------------------------------------------------------------------------- clocks (NVML)
@@ -239,6 +257,98 @@ def cpu_baseline_leg(q, k, v, o_dev_rows_fn, target_s=15.0):
             {"rows_checked": int(len(flat)), "max_abs_err": err, "tolerance": 2e-2, "pass": bool(err <= 2e-2)})
 
 
+def make_decode_inputs(dev):
+    """Seeded N(0,1) inputs of the decode workload, drawn on the device (403 MB)."""
+    import torch
+
+    w = DECODE
+    g = torch.Generator(device=dev).manual_seed(SEED + 11)
+    q = torch.randn(w["B"], w["H"], w["Nq"], w["d"], generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn(w["B"], w["H"], w["Nk"], w["d"], generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn(w["B"], w["H"], w["Nk"], w["d"], generator=g, device=dev).to(torch.bfloat16)
+    return q, k, v
+
+
+def decode_cpu_leg(q, k, v, o, lse, target_s=10.0):
+    """The oracle on a bounded sample of the decode workload's heads, timed on this host's
+    cores; the GPU's o and lse at the same heads are compared on the side."""
+    import oracle
+
+    w = DECODE
+    bh = w["B"] * w["H"]
+    qf = q.float().reshape(bh, w["Nq"], w["d"])
+    kf = k.float().reshape(bh, w["Nk"], w["d"])
+    vf = v.float().reshape(bh, w["Nk"], w["d"])
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.attn_fwd_kv(qf[:1, None].cpu().numpy(), kf[:1, None].cpu().numpy(), vf[:1, None].cpu().numpy(), True)
+    per_head = max(time.perf_counter() - t0, 1e-4)
+    n = int(max(2, min(bh, target_s / per_head)))
+    heads = np.unique(np.linspace(0, bh - 1, n).astype(np.int64))
+    idx = __import__("torch").from_numpy(heads).to(q.device)
+    qs, ks, vs = (x.index_select(0, idx)[None].cpu().numpy() for x in (qf, kf, vf))
+    t0 = time.perf_counter()
+    ref_o, ref_lse = oracle.attn_fwd_kv(qs, ks, vs, True)
+    secs = time.perf_counter() - t0
+    got_o = o.float().reshape(bh, w["Nq"], w["d"]).index_select(0, idx).cpu().numpy()
+    got_l = lse.reshape(bh, w["Nq"]).index_select(0, idx).cpu().numpy()
+    err_o = float(np.max(np.abs(got_o - ref_o[0])))
+    err_l = float(np.max(np.abs(got_l - ref_lse[0])))
+    tol_l = 2e-5 * (1.0 + float(np.max(np.abs(ref_lse)))) + 1e-4
+    nbytes = decode_bytes(1, len(heads), w["Nq"], w["Nk"], w["d"])
+    return ({"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+             "sample": f"{len(heads)} of {bh} heads of the decode workload (every query row), {secs:.1f} s"},
+            {"heads_checked": int(len(heads)), "max_abs_err_o": err_o, "tolerance_o": 2e-2,
+             "max_abs_err_lse": err_l, "tolerance_lse": tol_l, "pass": bool(err_o <= 2e-2 and err_l <= tol_l)})
+
+
+def decode_leg(dev, stream, steps, warmup, with_cpu, cpu_seconds):
+    """The key-value cache path on the decode workload: K steps back to back between two events
+    (inputs larger than L2, so no flush), balanced plan (num_splits = 0)."""
+    import torch
+
+    import online_softmax_flashattention_gb300 as fa
+
+    w = DECODE
+    q, k, v = make_decode_inputs(dev)
+    ws_bytes = fa.attn_kvcache_workspace_bytes(w["B"], w["H"], w["Nq"], w["Nk"], 0, torch.bfloat16, device=dev)
+    ws = torch.empty(max(1, ws_bytes), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(w["B"], w["H"], w["Nq"], dtype=torch.float32, device=dev)
+    call = lambda: fa.attn_fwd_kvcache(q, k, v, causal=True, workspace=ws, out=o, lse=lse, stream=stream)
+    call()
+    torch.cuda.synchronize(dev)
+    if fa.attn_device_status(clear=True, device=dev) != 0:
+        raise RuntimeError("device-side timeout in the first decode run")
+    for _ in range(warmup):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if fa.attn_device_status(clear=True, device=dev) != 0:
+        raise RuntimeError("device-side timeout in the timed decode runs")
+    us = e0.elapsed_time(e1) / steps * 1e3
+    nbytes = decode_bytes(w["B"], w["H"], w["Nq"], w["Nk"], w["d"])
+    peaks, peak_src = load_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    traffic, traffic_src = recorded_traffic(DECODE_PROFILE, DECODE_SOURCE)
+    out = {"config": dict(DECODE), "steps": steps, "us_per_step": us, "value": gbs, "unit": "GB/s",
+           "l2": "not flushed: K and V (403 MB) exceed L2; steps run back to back",
+           "launches_per_step": 2 if ws_bytes > 0 else 1,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"], "traffic": traffic,
+                        "peak_source": f"{peak_src} HBM copy", "traffic_source": traffic_src,
+                        "algorithmic_bytes_per_launch": nbytes}}
+    if with_cpu:
+        out["cpu_baseline"], out["parity"] = decode_cpu_leg(q, k, v, o, lse, cpu_seconds)
+    del q, k, v, o, lse, ws
+    return out
+
+
 # ----------------------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local):
     import torch
@@ -333,9 +443,9 @@ def run_ours(args, rank, world, local):
         del ws, om
 
     # Backward pass on the same workload (attn_fwd_lse, then attn_bwd with a seeded output
-    # gradient), once, outside the timed region. Algorithmic work: five products where the
-    # forward does two ("Backwards, and training with it"), i.e. 2.5x the forward's flop; the
-    # two tensor-core kernels recompute S and dP, so they execute seven (3.5x).
+    # gradient), once, outside the timed region. Algorithmic work: five products against the
+    # forward's two (section "Backwards, and training with it"), i.e. 2.5x the forward's flop;
+    # the two tensor-core kernels recompute S and dP, so they execute seven (3.5x).
     backward = None
     if rank == 0 and not args.no_ablation:
         dout = torch.randn(qd.shape, generator=torch.Generator(device=dev).manual_seed(SEED + 7),
@@ -360,6 +470,10 @@ def run_ours(args, rank, world, local):
                                  "executed_frac": executed / (bwd_ms * 1e-3) / 1e12 / peak,
                                  "peak_source": "measured bf16 dense (burst)"}}
         del dout, ob, lse
+
+    decode = None
+    if rank == 0 and not args.no_ablation:
+        decode = decode_leg(dev, stream, 50, args.warmup, not args.no_cpu_baseline, min(args.cpu_seconds, 10.0))
 
     cpu = parity = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -391,6 +505,7 @@ def run_ours(args, rank, world, local):
         "parity": parity,
         "ablation": ablation,
         "backward": backward,
+        "decode": decode,
         "launch_ms": {"min": min(launch_ms), "median": statistics.median(launch_ms), "max": max(launch_ms)},
     }
     print(json.dumps(line), flush=True)
@@ -444,6 +559,19 @@ def run_profile(args):
 
     import online_softmax_flashattention_gb300 as fa
 
+    if args.profile_kernel == "decode":
+        w = DECODE
+        q, k, v = make_decode_inputs(torch.device("cuda", 0))
+        nb = fa.attn_kvcache_workspace_bytes(w["B"], w["H"], w["Nq"], w["Nk"], 0, torch.bfloat16)
+        ws = torch.empty(max(1, nb), dtype=torch.uint8, device="cuda")
+        o = torch.empty_like(q)
+        for _ in range(args.profile_launches):
+            fa.attn_fwd_kvcache(q, k, v, causal=True, workspace=ws, out=o)
+        torch.cuda.synchronize()
+        if fa.attn_device_status(clear=True) != 0:
+            raise RuntimeError("device-side timeout")
+        print(f"profile: {args.profile_launches} calls of attn_fwd_kvcache on {w['workload']}")
+        return
     q, k, v = make_inputs()
     qd, kd, vd = (torch.from_numpy(x).to("cuda").to(torch.bfloat16) for x in (q, k, v))
     od = torch.empty_like(qd)
@@ -467,6 +595,8 @@ def main(argv=None):
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--profile", action="store_true", help="only launch the timed kernel (for ncu)")
     ap.add_argument("--profile-launches", type=int, default=4)
+    ap.add_argument("--profile-kernel", choices=["forward", "decode"], default="forward",
+                    help="which path --profile launches")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

@@ -132,12 +132,13 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  *     o[b,h,i,:] = sum_{j in vis(i)} softmax_j( q[b,h,i,:] . k[b,h,j,:] / sqrt(d) ) v[b,h,j,:]
  *
  * with vis(i) = {0 .. Nk-1}, or {0 .. Nk-Nq+i} when causal (with Nq == Nk this is attn_fwd's
- * mask). The key range is cut into num_splits shares, one CTA each; every share runs the
- * page's online softmax (section "Flash attention") over its keys and leaves its normalised
- * output O_s and base-2 log-sum-exp lse_s, and a second kernel merges them the way the online
- * softmax merges tiles: lse = log2 sum_s 2^lse_s, o = sum_s 2^(lse_s - lse) O_s. With one
- * share the first kernel writes o directly. All arithmetic is fp32 on CUDA cores (the work is
- * bound by reading the cache); o is rounded to dtype (RNE). Nothing is allocated.
+ * mask). The keys of each (head, group of up to 8 queries) are cut into pieces that run on
+ * different CTAs; every piece runs the page's online softmax (section "Flash attention") over
+ * its keys and leaves its normalised output O_p and base-2 log-sum-exp lse_p, and a second
+ * kernel merges the pieces the way the online softmax merges tiles: lse = log2 sum_p 2^lse_p,
+ * o = sum_p 2^(lse_p - lse) O_p. A piece that covers all of its head's keys writes o directly.
+ * All arithmetic is fp32 on CUDA cores (the work is bound by reading the cache); o is rounded
+ * to dtype (RNE). Nothing is allocated.
  *
  *   q, o          : device pointers, [B, H, Nq, d] of dtype, 16-byte aligned; o must not
  *                   overlap q, k, v, lse or the workspace
@@ -145,17 +146,18 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  *   lse           : NULL, or device pointer float32 [B, H, Nq], 4-byte aligned, receiving each
  *                   row's base-2 log-sum-exp as attn_fwd_lse defines it; must not overlap the
  *                   other buffers
- *   workspace     : device pointer, 256-byte aligned, caller-owned fp32 scratch for the shares'
- *                   partial results (contents on entry ignored, on exit unspecified); may be NULL
- *                   when workspace_bytes is 0. It must not overlap any tensor.
- *   workspace_bytes: its size; attn_kvcache_workspace_bytes(B, H, Nq, num_splits) is enough
+ *   workspace     : device pointer, 256-byte aligned, caller-owned fp32 scratch for the pieces'
+ *                   partial results (contents on entry ignored, on exit unspecified); may be
+ *                   NULL when no workspace is needed. It must not overlap any tensor.
+ *   workspace_bytes: its size; attn_kvcache_workspace_bytes(B, H, Nq, Nk, num_splits, dtype)
+ *                   with the same device current is enough; less returns ATTN_ERR_WORKSPACE
  *   Nq, Nk        : 0 <= Nq <= Nk <= ATTN_MAX_N, Nq <= 8 * 65535; Nq == 0 or B*H == 0 is a
- *                   successful no-op; Nk == 0 requires Nq == 0
- *   num_splits    : 1 .. ATTN_KV_MAX_SPLITS, or 0 for the library's choice for this device
- *                   (attn_kvcache_num_splits), halved until the workspace holds it (down to 1,
- *                   which needs none). An explicit count above 1 whose workspace is too small
- *                   returns ATTN_ERR_WORKSPACE. Shares past the last key are empty and carry
- *                   weight 0 in the merge.
+ *                   successful no-op
+ *   num_splits    : 0 — balanced: a persistent grid of as many CTAs as the device holds, each
+ *                   streaming the same number of 128-key tiles (within one) of all heads' keys,
+ *                   cut at head boundaries; 1 .. ATTN_KV_MAX_SPLITS — every (head, query
+ *                   group) is cut into that many equal shares (shares past the last key are
+ *                   empty and carry weight 0 in the merge).
  *   other arguments: as attn_fwd (d == 64; dtype f32, bf16 or f16; causal 0/1).
  */
 #define ATTN_KV_MAX_SPLITS 1024
@@ -163,14 +165,12 @@ int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float
                      size_t workspace_bytes, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
                      int causal, int dtype, int num_splits, void* stream);
 
-/* Bytes of workspace attn_fwd_kvcache needs for num_splits shares: B*H*Nq*num_splits rows of
- * d + 1 floats, in two regions rounded up to 256 bytes; 0 when num_splits <= 1. Returns 0 for
- * negative sizes or on overflow. */
-size_t attn_kvcache_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int num_splits);
-
-/* The share count attn_fwd_kvcache picks for num_splits == 0 on the current device (about
- * eight CTAs per SM, at least 256 keys a share); 1 if the device cannot be queried. */
-int attn_kvcache_num_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk);
+/* Bytes of workspace attn_fwd_kvcache needs: B*H*Nq*P rows of d + 1 floats in two regions
+ * rounded up to 256 bytes, where P is num_splits, or for num_splits == 0 the most pieces the
+ * balanced plan gives one head on the current device; 0 when every head is a single piece.
+ * Returns 0 also for invalid sizes or dtype, on overflow, or (num_splits == 0) when the
+ * current device cannot be queried. */
+size_t attn_kvcache_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int num_splits, int dtype);
 
 /*
  * attn_fwd_materialized — the same result by the materialised path of attention.cu

@@ -26,7 +26,7 @@ __all__ = [
     "attn_fwd", "attn_fwd_materialized", "attn_materialized_workspace_bytes", "attn_device_status",
     "attn_status_string", "attn_abi_version", "raw", "attn_fwd_materialized_noalloc",
     "ATTN_NOALLOC_MAX_N", "attn_fwd_lse", "attn_bwd", "attn_fwd_kvcache", "attn_kvcache_workspace_bytes",
-    "attn_kvcache_num_splits", "ATTN_KV_MAX_SPLITS",
+    "ATTN_KV_MAX_SPLITS",
 ]
 
 ATTN_F32, ATTN_BF16, ATTN_F16 = 0, 1, 2
@@ -73,10 +73,8 @@ def raw():
             lib.attn_bwd.restype = ci
             lib.attn_fwd_kvcache.argtypes = [vp, vp, vp, vp, vp, vp, sz, i64, i64, i64, i64, i64, ci, ci, ci, vp]
             lib.attn_fwd_kvcache.restype = ci
-            lib.attn_kvcache_workspace_bytes.argtypes = [i64, i64, i64, ci]
+            lib.attn_kvcache_workspace_bytes.argtypes = [i64, i64, i64, i64, ci, ci]
             lib.attn_kvcache_workspace_bytes.restype = sz
-            lib.attn_kvcache_num_splits.argtypes = [i64, i64, i64, i64]
-            lib.attn_kvcache_num_splits.restype = ci
             lib.attn_fwd_materialized.argtypes = [vp, vp, vp, vp, vp, sz, i64, i64, i64, i64, ci, ci, vp]
             lib.attn_fwd_materialized.restype = ci
             lib.attn_materialized_workspace_bytes.argtypes = [i64, i64, i64]
@@ -188,14 +186,16 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
 ATTN_KV_MAX_SPLITS = 1024  # include/attn.h: most shares the key range may be cut into
 
 
-def attn_kvcache_workspace_bytes(B: int, H: int, Nq: int, num_splits: int) -> int:
-    return int(raw().attn_kvcache_workspace_bytes(B, H, Nq, num_splits))
-
-
-def attn_kvcache_num_splits(B: int, H: int, Nq: int, Nk: int, device: torch.device | int | None = None) -> int:
-    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index or 0)
+def attn_kvcache_workspace_bytes(B: int, H: int, Nq: int, Nk: int, num_splits: int = 0,
+                                 dtype: torch.dtype = torch.bfloat16, device: torch.device | int | None = None) -> int:
+    """Workspace bytes :func:`attn_fwd_kvcache` needs; for ``num_splits == 0`` (balanced) the plan
+    depends on the device, which is queried with ``device`` current."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index or 0) \
+        if num_splits == 0 else None
+    if dev is None:
+        return int(raw().attn_kvcache_workspace_bytes(B, H, Nq, Nk, num_splits, _DTYPES[dtype]))
     with torch.cuda.device(dev):
-        return int(raw().attn_kvcache_num_splits(B, H, Nq, Nk))
+        return int(raw().attn_kvcache_workspace_bytes(B, H, Nq, Nk, num_splits, _DTYPES[dtype]))
 
 
 def attn_fwd_kvcache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = True,
@@ -204,10 +204,10 @@ def attn_fwd_kvcache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: 
                      stream: torch.cuda.Stream | None = None):
     """Attention of ``q`` ``[B, H, Nq, d]`` (the last Nq positions) against a key-value cache
     ``k, v`` ``[B, H, Nk, d]``, Nq <= Nk; causal: query i sees keys ``0 .. Nk - Nq + i``.
-    ``num_splits`` 0 lets the library choose how many shares the keys are cut into. When
-    ``workspace`` (a uint8 CUDA tensor) is omitted, one of the needed size is allocated here.
-    ``lse=True`` (or a float32 ``[B, H, Nq]`` tensor) also returns the base-2 log-sum-exps:
-    the result is then ``(o, lse)``, otherwise ``o``."""
+    ``num_splits`` 0 balances the keys of all heads over the whole GPU; S >= 1 cuts every head
+    into S shares. When ``workspace`` (a uint8 CUDA tensor) is omitted, one of the needed size
+    is allocated here. ``lse=True`` (or a float32 ``[B, H, Nq]`` tensor) also returns the base-2
+    log-sum-exps: the result is then ``(o, lse)``, otherwise ``o``."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
             raise TypeError(f"{name} must be a CUDA tensor")
@@ -233,9 +233,8 @@ def attn_fwd_kvcache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: 
         raise ValueError("lse must be a contiguous float32 tensor [B, H, Nq] on q's device")
     lib = raw()
     with torch.cuda.device(q.device):
-        splits = int(num_splits) if num_splits else int(lib.attn_kvcache_num_splits(B, H, Nq, Nk))
         if workspace is None:
-            need = int(lib.attn_kvcache_workspace_bytes(B, H, Nq, splits))
+            need = int(lib.attn_kvcache_workspace_bytes(B, H, Nq, Nk, int(num_splits), _DTYPES[q.dtype]))
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
         st = lib.attn_fwd_kvcache(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                   lse.data_ptr() if want_lse else None, workspace.data_ptr(),

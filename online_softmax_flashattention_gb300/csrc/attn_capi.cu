@@ -135,16 +135,12 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
     return attn::launch_bwd_tc(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal != 0, dtype == ATTN_BF16, s);
 }
 
-size_t attn_kvcache_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int num_splits) {
-    if (B < 0 || H < 0 || Nq < 0 || B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return 0;
-    return attn::decode_workspace_bytes(B * H, Nq, num_splits);
-}
-
-int attn_kvcache_num_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk) {
-    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return 1;
+size_t attn_kvcache_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int num_splits, int dtype) {
+    if (B < 0 || H < 0 || Nq < 0 || Nk < Nq || B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return 0;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16 && dtype != ATTN_F16) return 0;
     int num_sms = 0;
-    if (check_device(&num_sms) != ATTN_OK) return 1;
-    return attn::decode_auto_splits(B * H, Nq, Nk, num_sms);
+    if (num_splits == 0 && check_device(&num_sms) != ATTN_OK) return 0;
+    return attn::decode_workspace_bytes(B * H, Nq, Nk, num_splits, dtype, num_sms);
 }
 
 int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
@@ -175,18 +171,14 @@ int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float
             return ATTN_ERR_ALIAS;
     }
     // An explicit share count is checked against the workspace before the device is queried;
-    // the automatic one needs the SM count first.
+    // the balanced plan needs the SM count and the kernel's occupancy first.
     int num_sms = 0;
     int st = ATTN_OK;
-    int splits = num_splits;
-    if (splits == 0) {
-        if ((st = check_device(&num_sms)) != ATTN_OK) return st;
-        splits = attn::decode_auto_splits(BH, Nq, Nk, num_sms);
-        while (splits > 1 && attn::decode_workspace_bytes(BH, Nq, splits) > workspace_bytes) splits /= 2;
-        if (splits > 1 && workspace == nullptr) splits = 1;
-    }
-    if (splits > 1) {
-        const size_t need = attn::decode_workspace_bytes(BH, Nq, splits);
+    if (num_splits == 0 && (st = check_device(&num_sms)) != ATTN_OK) return st;
+    const size_t need = attn::decode_workspace_bytes(BH, Nq, Nk, num_splits, dtype, num_sms);
+    // (A balanced plan of one piece per segment needs none; the launch re-checks the size.)
+    const bool needs_ws = num_splits > 1 || (num_splits == 0 && need > 0);
+    if (needs_ws) {
         if (need == 0) return ATTN_ERR_UNSUPPORTED;
         if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
         if (!aligned(workspace, 256)) return ATTN_ERR_ALIGN;
@@ -197,8 +189,8 @@ int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float
     }
     if (num_splits != 0 && (st = check_device(&num_sms)) != ATTN_OK) return st;
     if (inject_launch_fault()) return ATTN_ERR_LAUNCH;
-    return attn::launch_decode(q, k, v, o, lse, workspace, BH, Nq, Nk, causal != 0, dtype, splits,
-                               static_cast<cudaStream_t>(stream));
+    return attn::launch_decode(q, k, v, o, lse, workspace, workspace_bytes, BH, Nq, Nk, causal != 0, dtype,
+                               num_splits, num_sms, static_cast<cudaStream_t>(stream));
 }
 
 size_t attn_materialized_workspace_bytes(int64_t B, int64_t H, int64_t N) {
@@ -247,11 +239,12 @@ int attn_fwd_materialized(const void* q, const void* k, const void* v, void* o, 
 }
 
 int attn_device_status(void* stream, int clear) {
-    unsigned err = 0, berr = 0;
+    unsigned err = 0, berr = 0, derr = 0;
     int st = attn::tc_device_error(static_cast<cudaStream_t>(stream), clear != 0, &err);
     if (st != ATTN_OK) return st;
     if ((st = attn::bwd_tc_device_error(clear != 0, &berr)) != ATTN_OK) return st;
-    return (err || berr) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    if ((st = attn::decode_device_error(clear != 0, &derr)) != ATTN_OK) return st;
+    return (err || berr || derr) ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 const char* attn_status_string(int status) {

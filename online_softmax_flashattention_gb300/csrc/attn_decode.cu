@@ -1,25 +1,41 @@
 // Key-value cache attention (decode): Nq new queries, the last Nq positions of a sequence,
-// against Nk >= Nq cached keys and values, with the key range split across CTAs and the
-// partial results merged by their log-sum-exps.
+// against Nk >= Nq cached keys and values, with the key range cut into pieces that run on
+// different CTAs and are merged by their log-sum-exps.
 //
 // The "Flash attention in PyTorch, then in Triton" page names this case and leaves it out of
 // its kernel (section "Backwards, and training with it": generation with a cache, where a few
 // new tokens attend to every cached key). Query i sits at position Nk - Nq + i; when causal it
-// sees keys 0 .. Nk - Nq + i. Each split runs the page's online softmax ("Flash attention": a running
-// maximum, denominator and output per query, rescaled when a tile raises the maximum) over
-// its share of the keys and leaves (O_s / l_s, lse2_s = m_s + log2 l_s); the combine step
-// merges the splits the way the online softmax merges tiles:
-//     lse2 = log2 sum_s 2^lse2_s,   O = sum_s 2^(lse2_s - lse2) O_s.
-// A query sees few keys per byte it reads (one product of d terms per cached row of 2d
-// values), so the work is bound by reading the cache from HBM; the kernel streams each K and
-// V row once per query group with 16-byte loads and keeps the arithmetic on CUDA cores.
+// sees keys 0 .. Nk - Nq + i. Each piece runs the page's online softmax (section "Flash
+// attention": a running maximum, denominator and output per query, rescaled when a tile raises
+// the maximum) over its keys and leaves (O_p / l_p, lse2_p = m_p + log2 l_p); the merge kernel
+// combines the pieces the way the online softmax combines tiles:
+//     lse2 = log2 sum_p 2^lse2_p,   O = sum_p 2^(lse2_p - lse2) O_p.
+// A query does one product of d terms per cached row of 2d values, so the work is bound by
+// reading the cache from HBM. The kernel streams K and V once per group of up to eight
+// queries through a ring of shared-memory stages filled by TMA, and keeps the arithmetic on
+// CUDA cores.
 //
-// Layout per CTA (bh, split, query group of QG queries): 4 warps, each taking 32 keys at a
-// time, one key per lane. Scores: the lane forms q_i . k_j for its key and the group's QG
-// queries (queries pre-scaled by log2(e)/sqrt(d) in shared memory). Online update per query
-// over the warp's 32 keys (shuffle max), then the weighted values: lane L accumulates O_i for
-// dims 2L, 2L+1, reading each value row coalesced and taking p_ij from lane j by shuffle. The
-// four warps' states merge in shared memory at the end.
+// Work split. The queries are cut into groups of QG (1, 2, 4 or 8); a segment is one
+// (head, query group) with Tn tiles of 128 keys. Two ways to cut segments into pieces:
+//   balanced (num_splits == 0): the grid is persistent (as many CTAs as fit on the GPU, or
+//     fewer when there is less work) and CTA c takes the contiguous run of tiles
+//     [c G / C, (c+1) G / C) of all G = segments * Tn tiles, cut at segment boundaries, so
+//     every CTA streams the same number of tiles (within one) whatever B*H is;
+//   explicit (num_splits = S >= 1): every segment is cut into S equal shares, handed out to
+//     the CTAs round robin.
+// A piece that covers a whole segment writes o and lse directly; the others write fp32
+// partials to the workspace for the merge kernel.
+//
+// CTA layout: four consumer warps and one producer warp. The producer's first lane walks the
+// same pieces as the consumers and, per tile, waits for a free stage and issues the K and V
+// tile loads (128 rows x 64 values, 128-byte swizzle; fp32 rows are two 32-value halves).
+// Consumer warp w takes rows 32w .. 32w+31 of each tile, one key per lane: scores against the
+// group's queries (pre-scaled by log2(e)/sqrt(d), in warp-private shared memory), a warp-wide
+// online update per query, then the weighted values with lane L owning dims 2L, 2L+1 and the
+// probabilities read back from shared memory. At the end of a piece the four warps' states
+// merge through shared memory. Every wait is bounded: on a timeout the kernel records an
+// error, stops, and the producer waits for its loads in flight before the CTA exits.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -29,13 +45,20 @@
 #include <cstdint>
 
 #include "attn_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace attn {
 namespace {
 
 constexpr int kD = 64;
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
+constexpr int kCW = 4;                  // consumer warps
+constexpr int kThreads = 32 * (kCW + 1);
+constexpr int kRows = 32 * kCW;         // keys per tile
+constexpr int kProducerWarp = kCW;
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+constexpr uint64_t kDrainTimeoutNs = 100000000ull;
+
+__device__ unsigned int g_decode_error = 0;
 
 __device__ __forceinline__ float ex2f(float x) {
     float y;
@@ -43,37 +66,35 @@ __device__ __forceinline__ float ex2f(float x) {
     return y;
 }
 
-// Eight consecutive elements as fp32.
 template <typename T>
-__device__ __forceinline__ void load8(const T* p, float (&f)[8]);
+struct Elem;
 template <>
-__device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
-    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
-    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+struct Elem<float> {
+    static constexpr int kStages = 3;
+    static constexpr int kHalves = 2;  // a 64-value fp32 row is two 128-byte boxes
+};
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr int kStages = 3;
+    static constexpr int kHalves = 1;
+};
+template <>
+struct Elem<__half> {
+    static constexpr int kStages = 3;
+    static constexpr int kHalves = 1;
+};
+
+template <typename T>
+__device__ __forceinline__ float2 to_f2(uint32_t u);
+template <>
+__device__ __forceinline__ float2 to_f2<__nv_bfloat16>(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
 }
 template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&f)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-}
-template <>
-__device__ __forceinline__ void load8<__half>(const __half* p, float (&f)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-        f[2 * i] = x.x;
-        f[2 * i + 1] = x.y;
-    }
+__device__ __forceinline__ float2 to_f2<__half>(uint32_t u) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&u));
 }
 
-// Two consecutive elements as fp32 (for the value rows, lane L reads dims 2L, 2L+1).
 template <typename T>
 __device__ __forceinline__ float2 load2(const T* p);
 template <>
@@ -90,7 +111,9 @@ __device__ __forceinline__ float2 load2<__half>(const __half* p) {
 template <typename T>
 __device__ __forceinline__ void store2(T* p, float a, float b);
 template <>
-__device__ __forceinline__ void store2<float>(float* p, float a, float b) { *reinterpret_cast<float2*>(p) = make_float2(a, b); }
+__device__ __forceinline__ void store2<float>(float* p, float a, float b) {
+    *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
 template <>
 __device__ __forceinline__ void store2<__nv_bfloat16>(__nv_bfloat16* p, float a, float b) {
     *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
@@ -102,262 +125,600 @@ __device__ __forceinline__ void store2<__half>(__half* p, float a, float b) {
 
 struct DecodeParams {
     const void* q;
-    const void* k;
-    const void* v;
-    void* o;          // written directly when splits == 1
-    float* lse;       // null, or [BH, Nq] (direct mode)
-    float* part_o;    // [BH][Nq][splits][64] when splits > 1
-    float* part_lse;  // [BH][Nq][splits]
-    int Nq, Nk, BH, splits, chunk, causal;
-    float c;  // log2(e) / sqrt(d)
+    void* o;
+    float* lse;       // null, or [BH, Nq]
+    float* part_o;    // [BH * Nq][P][64]
+    float* part_lse;  // [BH * Nq][P]
+    int Nq, Nk, BH;
+    int groups;           // query groups per head
+    int Tn;               // tiles of kRows keys per segment
+    int causal;
+    int explicit_splits;  // S >= 1: every segment in S shares; 0: balanced
+    int tps;              // explicit: tiles per share
+    int P;                // slot stride of the partials (S, or most pieces a segment can have)
+    int C;                // CTAs in the grid
+    int64_t G;            // balanced: segments * Tn
+    float c;              // log2(e) / sqrt(d)
 };
+
+struct Piece {
+    int bh, g0, ng;  // head, first query of the group, queries in the group
+    int t0, t1;      // tiles [t0, t1) of the segment, already clipped to the visible keys
+    int ke;          // the segment's visible keys end before ke
+    int slot, nslots;
+};
+
+// Balanced mode: the CTA whose run holds global tile t.
+__device__ __host__ __forceinline__ int64_t owner_of(int64_t t, int64_t C, int64_t G) {
+    return ((t + 1) * C - 1) / G;
+}
+
+// The k-th piece of CTA `cta`; false once the CTA has no more.
+template <int QG>
+__device__ __forceinline__ bool get_piece(const DecodeParams& p, int cta, int k, Piece& pc) {
+    int64_t seg;
+    int t0, t1;
+    if (p.explicit_splits > 0) {
+        const int64_t idx = static_cast<int64_t>(cta) + static_cast<int64_t>(k) * p.C;
+        const int64_t nseg = static_cast<int64_t>(p.BH) * p.groups;
+        if (idx >= nseg * p.explicit_splits) return false;
+        seg = idx / p.explicit_splits;
+        const int share = static_cast<int>(idx % p.explicit_splits);
+        t0 = min(p.Tn, share * p.tps);
+        t1 = min(p.Tn, t0 + p.tps);
+        pc.slot = share;
+        pc.nslots = p.explicit_splits;
+    } else {
+        const int64_t A = static_cast<int64_t>(cta) * p.G / p.C;
+        const int64_t Bend = (static_cast<int64_t>(cta) + 1) * p.G / p.C;
+        if (A >= Bend) return false;
+        seg = A / p.Tn + k;
+        const int64_t s0 = seg * p.Tn;
+        if (s0 >= Bend) return false;
+        const int64_t a = max(A, s0), b = min(Bend, s0 + p.Tn);
+        t0 = static_cast<int>(a - s0);
+        t1 = static_cast<int>(b - s0);
+        const int64_t first = owner_of(s0, p.C, p.G), last = owner_of(s0 + p.Tn - 1, p.C, p.G);
+        pc.slot = static_cast<int>(cta - first);
+        pc.nslots = static_cast<int>(last - first + 1);
+    }
+    pc.bh = static_cast<int>(seg / p.groups);
+    pc.g0 = static_cast<int>(seg % p.groups) * QG;
+    pc.ng = min(QG, p.Nq - pc.g0);
+    pc.ke = p.causal ? min(p.Nk, p.Nk - p.Nq + pc.g0 + pc.ng) : p.Nk;
+    const int tv = (pc.ke + kRows - 1) / kRows;  // tiles holding a visible key
+    pc.t0 = min(t0, tv);
+    pc.t1 = min(t1, tv);
+    return true;
+}
+
+template <typename T, int QG>
+struct Smem {
+    static constexpr int kHalves = Elem<T>::kHalves;
+    static constexpr int kStages = Elem<T>::kStages;
+    static constexpr int kTileBytes = kRows * kD * static_cast<int>(sizeof(T));  // one of K, V
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kRing = kStages * kStageBytes;
+    static constexpr int kQs = kRing;                    // [kCW][QG][64] f32
+    static constexpr int kPs = kQs + kCW * QG * kD * 4;  // [kCW][QG][32] f32
+    static constexpr int kMl = kPs + kCW * QG * 32 * 4;  // [kCW][QG] m, then [kCW][QG] l
+    static constexpr int kBars = kMl + 2 * kCW * QG * 4; // full[S], empty[S], mFull, mFree
+    static constexpr int kAbort = kBars + (2 * kStages + 2) * 8;
+    static constexpr int kBytes = kAbort + 16;
+    static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
+};
+
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicOr(&g_decode_error, 1u);
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, kWaitTimeoutNs);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Byte offset of the 16-byte chunk `ch` of row r in a tile of 128-byte rows written with the
+// 128-byte swizzle (the chunks of a row are permuted by row % 8).
+__device__ __forceinline__ uint32_t sw_chunk(int r, int ch) {
+    return static_cast<uint32_t>(r * 128 + ((ch ^ (r & 7)) << 4));
+}
 
 template <typename T, int QG>
 __global__ void __launch_bounds__(kThreads)
-    attn_decode_split_kernel(const DecodeParams p) {
-    __shared__ float qs[QG][kD];
-    __shared__ float wm[kWarps][QG], wl[kWarps][QG];
-    __shared__ float wo[kWarps][QG][kD];
+    attn_decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                       const DecodeParams p) {
+    using L = Smem<T, QG>;
+    constexpr int S = L::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t base = smem_u32(smem);
+    auto full = [&](int s) { return base + L::kBars + 8 * s; };
+    auto empty = [&](int s) { return base + L::kBars + 8 * (S + s); };
+    const uint32_t mFull = base + L::kBars + 8 * (2 * S), mFree = mFull + 8;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int split = blockIdx.y;
-    const int g0 = blockIdx.z * QG;  // first query of the group
-    const int ng = min(QG, p.Nq - g0);
-    const T* const qh = static_cast<const T*>(p.q) + static_cast<int64_t>(bh) * p.Nq * kD;
-    const T* const kh = static_cast<const T*>(p.k) + static_cast<int64_t>(bh) * p.Nk * kD;
-    const T* const vh = static_cast<const T*>(p.v) + static_cast<int64_t>(bh) * p.Nk * kD;
-
-    // The group's queries, scaled so that scores come out in base-2 units.
-    for (int idx = threadIdx.x; idx < QG * kD; idx += kThreads) {
-        const int i = idx / kD, e = idx % kD;
-        float val = 0.f;
-        if (i < ng) {
-            float f[8];
-            load8<T>(qh + static_cast<int64_t>(g0 + i) * kD + (e & ~7), f);
-            val = f[e & 7] * p.c;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kCW);
         }
-        qs[i][e] = val;
+        mbar_init(mFull, kCW);
+        mbar_init(mFree, kCW);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x == 32 * kProducerWarp) {
+        prefetch_tmap(&mk);
+        prefetch_tmap(&mv);
     }
     __syncthreads();
+    // Let the merge kernel (launched with programmatic stream serialisation) get onto the GPU
+    // now; it waits for this grid to finish before it reads anything.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int cta = blockIdx.x;
 
-    // Keys of this split, and the last key any query of the group may see.
-    const int ks = split * p.chunk;
-    int ke = min(p.Nk, ks + p.chunk);
-    if (p.causal) ke = min(ke, p.Nk - p.Nq + g0 + ng);
-    float m[QG], l[QG], acc[QG][2];
+    if (warp == kProducerWarp) {
+        if (lane != 0) return;
+        int nt = 0;  // tiles issued by this CTA
+        bool ok = true;
+        Piece pc;
+        for (int k = 0; ok && get_piece<QG>(p, cta, k, pc); ++k) {
+            for (int t = pc.t0; t < pc.t1; ++t, ++nt) {
+                const int s = nt % S;
+                if (!(ok = mbar_wait(empty(s), ((nt / S) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
+                const uint32_t dst = base + s * L::kStageBytes;
+                mbar_arrive_expect_tx(full(s), L::kStageBytes);
 #pragma unroll
-    for (int i = 0; i < QG; ++i) {
-        m[i] = -INFINITY;
-        l[i] = 0.f;
-        acc[i][0] = acc[i][1] = 0.f;
-    }
-    for (int base = ks + 32 * warp; base < ke; base += 32 * kWarps) {
-        const int j = base + lane;
-        // scores of key j against the group's queries
-        float s[QG];
-#pragma unroll
-        for (int i = 0; i < QG; ++i) s[i] = 0.f;
-        if (j < ke) {
-            const T* krow = kh + static_cast<int64_t>(j) * kD;
-#pragma unroll
-            for (int c8 = 0; c8 < kD; c8 += 8) {
-                float f[8];
-                load8<T>(krow + c8, f);
-#pragma unroll
-                for (int i = 0; i < QG; ++i) {
-                    const float4 a = *reinterpret_cast<const float4*>(&qs[i][c8]);
-                    const float4 b = *reinterpret_cast<const float4*>(&qs[i][c8 + 4]);
-                    s[i] = fmaf(a.x, f[0], s[i]);
-                    s[i] = fmaf(a.y, f[1], s[i]);
-                    s[i] = fmaf(a.z, f[2], s[i]);
-                    s[i] = fmaf(a.w, f[3], s[i]);
-                    s[i] = fmaf(b.x, f[4], s[i]);
-                    s[i] = fmaf(b.y, f[5], s[i]);
-                    s[i] = fmaf(b.z, f[6], s[i]);
-                    s[i] = fmaf(b.w, f[7], s[i]);
+                for (int h = 0; h < L::kHalves; ++h) {
+                    const uint32_t hoff = h * (L::kTileBytes / L::kHalves);
+                    tma_load_3d(dst + hoff, &mk, h * 32, t * kRows, pc.bh, full(s));
+                    tma_load_3d(dst + L::kTileBytes + hoff, &mv, h * 32, t * kRows, pc.bh, full(s));
                 }
             }
         }
-        float pr[QG];
-#pragma unroll
-        for (int i = 0; i < QG; ++i) {
-            const bool vis = j < ke && i < ng && (!p.causal || j <= p.Nk - p.Nq + g0 + i);
-            const float sc = vis ? s[i] : -INFINITY;
-            float mx = sc;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float m_new = fmaxf(m[i], mx);
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // no inf - inf on empty rows
-            const float alpha = ex2f(m[i] - m_use);
-            pr[i] = ex2f(sc - m_use);
-            l[i] = l[i] * alpha + pr[i];  // this lane's share of the row total
-            acc[i][0] *= alpha;
-            acc[i][1] *= alpha;
-            m[i] = m_new;
-        }
-        // weighted values: lane L owns dims 2L, 2L+1
-        const int nk = min(32, ke - base);
-#pragma unroll 8
-        for (int kk = 0; kk < nk; ++kk) {
-            const float2 vv = load2<T>(vh + static_cast<int64_t>(base + kk) * kD + 2 * lane);
+        if (!ok) raise_abort(abort_flag);
+        // Wait for the loads still in flight so that none lands after the CTA has exited.
+        for (int u = max(0, nt - S); u < nt; ++u)
+            mbar_wait(full(u % S), (u / S) & 1, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+        return;
+    }
+
+    // ------------------------------------ consumers ------------------------------------
+    float* qs = reinterpret_cast<float*>(smem + L::kQs) + warp * QG * kD;  // this warp's queries, scaled
+    float* ps = reinterpret_cast<float*>(smem + L::kPs) + warp * QG * 32;  // this warp's probabilities
+    float* ml = reinterpret_cast<float*>(smem + L::kMl);                    // m [kCW][QG], l [kCW][QG]
+    const int tid = threadIdx.x;  // 0 .. 32*kCW - 1
+    int nt = 0;  // tiles consumed by this CTA
+    bool ok = true;
+    Piece pc;
+    for (int k = 0; get_piece<QG>(p, cta, k, pc); ++k) {
+        // The previous piece's merge read every warp's qs; wait until all are done with it.
+        if (k > 0 && !(ok = warp_wait(mFree, (k - 1) & 1, abort_flag))) break;
+        {
+            const T* qh = static_cast<const T*>(p.q) + (static_cast<int64_t>(pc.bh) * p.Nq + pc.g0) * kD;
 #pragma unroll
             for (int i = 0; i < QG; ++i) {
-                const float w = __shfl_sync(0xffffffffu, pr[i], kk);
-                acc[i][0] = fmaf(w, vv.x, acc[i][0]);
-                acc[i][1] = fmaf(w, vv.y, acc[i][1]);
+                float2 x = make_float2(0.f, 0.f);
+                if (i < pc.ng) x = load2<T>(qh + i * kD + 2 * lane);
+                *reinterpret_cast<float2*>(qs + i * kD + 2 * lane) = make_float2(x.x * p.c, x.y * p.c);
+            }
+            __syncwarp();
+        }
+        float m[QG], l[QG], acc[QG][2];
+#pragma unroll
+        for (int i = 0; i < QG; ++i) {
+            m[i] = -INFINITY;
+            l[i] = 0.f;
+            acc[i][0] = acc[i][1] = 0.f;
+        }
+        const int qpos0 = p.Nk - p.Nq + pc.g0;  // position of the group's first query
+        for (int t = pc.t0; t < pc.t1; ++t, ++nt) {
+            const int s = nt % S;
+            if (!(ok = warp_wait(full(s), (nt / S) & 1, abort_flag))) break;
+            const uint8_t* kt = smem + s * L::kStageBytes;
+            const uint8_t* vt = kt + L::kTileBytes;
+            const int r = 32 * warp + lane;
+            const int j = t * kRows + r;
+            // ---- scores of key j against the group's queries ----
+            constexpr int NA = QG >= 4 ? 1 : 4 / QG;  // independent partial sums per query
+            float sa[QG][NA];
+#pragma unroll
+            for (int i = 0; i < QG; ++i)
+#pragma unroll
+                for (int a = 0; a < NA; ++a) sa[i][a] = 0.f;
+            if constexpr (L::kHalves == 1) {
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(kt + sw_chunk(r, ch));
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float2 kf = to_f2<T>(w[h]);
+#pragma unroll
+                        for (int i = 0; i < QG; ++i) {
+                            const float2 qv = *reinterpret_cast<const float2*>(qs + i * kD + ch * 8 + 2 * h);
+                            sa[i][(2 * h) % NA] = fmaf(qv.x, kf.x, sa[i][(2 * h) % NA]);
+                            sa[i][(2 * h + 1) % NA] = fmaf(qv.y, kf.y, sa[i][(2 * h + 1) % NA]);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int ch = 0; ch < 16; ++ch) {
+                    const float4 kf =
+                        *reinterpret_cast<const float4*>(kt + (ch >> 3) * (L::kTileBytes / 2) + sw_chunk(r, ch & 7));
+#pragma unroll
+                    for (int i = 0; i < QG; ++i) {
+                        const float4 qv = *reinterpret_cast<const float4*>(qs + i * kD + ch * 4);
+                        sa[i][0 % NA] = fmaf(qv.x, kf.x, sa[i][0 % NA]);
+                        sa[i][1 % NA] = fmaf(qv.y, kf.y, sa[i][1 % NA]);
+                        sa[i][2 % NA] = fmaf(qv.z, kf.z, sa[i][2 % NA]);
+                        sa[i][3 % NA] = fmaf(qv.w, kf.w, sa[i][3 % NA]);
+                    }
+                }
+            }
+            // ---- online update per query, probabilities to shared memory ----
+#pragma unroll
+            for (int i = 0; i < QG; ++i) {
+                float sc = 0.f;
+#pragma unroll
+                for (int a = 0; a < NA; ++a) sc += sa[i][a];
+                const bool vis = j < pc.ke && i < pc.ng && (!p.causal || j <= qpos0 + i);
+                sc = vis ? sc : -INFINITY;
+                float mx = sc;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const float m_new = fmaxf(m[i], mx);
+                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // no inf - inf on empty rows
+                const float alpha = ex2f(m[i] - m_use);
+                const float pr = ex2f(sc - m_use);
+                l[i] = fmaf(l[i], alpha, pr);  // this lane's share of the row total
+                acc[i][0] *= alpha;
+                acc[i][1] *= alpha;
+                m[i] = m_new;
+                ps[i * 32 + lane] = pr;
+            }
+            __syncwarp();
+            // ---- weighted values: lane L owns dims 2L, 2L+1 ----
+            const int nk = min(32, pc.ke - (t * kRows + 32 * warp));  // rows of this warp with a visible key
+#pragma unroll
+            for (int k4 = 0; k4 < 32; k4 += 4) {
+                if (k4 >= nk) break;
+                float4 pp[QG];
+#pragma unroll
+                for (int i = 0; i < QG; ++i) pp[i] = *reinterpret_cast<const float4*>(ps + i * 32 + k4);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int rr = 32 * warp + k4 + u;
+                    float2 vv;
+                    if constexpr (L::kHalves == 1) {
+                        const uint32_t w =
+                            *reinterpret_cast<const uint32_t*>(vt + sw_chunk(rr, lane >> 2) + ((lane & 3) << 2));
+                        vv = to_f2<T>(w);
+                    } else {
+                        vv = *reinterpret_cast<const float2*>(vt + (lane >> 4) * (L::kTileBytes / 2) +
+                                                              sw_chunk(rr, (lane & 15) >> 1) + ((lane & 1) << 3));
+                    }
+#pragma unroll
+                    for (int i = 0; i < QG; ++i) {
+                        const float w = u == 0 ? pp[i].x : u == 1 ? pp[i].y : u == 2 ? pp[i].z : pp[i].w;
+                        acc[i][0] = fmaf(w, vv.x, acc[i][0]);
+                        acc[i][1] = fmaf(w, vv.y, acc[i][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            mbar_arrive_elect(empty(s));
+        }
+        if (!ok) break;
+        // ---- merge the four warps' states: this warp's O into its qs, m and l beside ----
+#pragma unroll
+        for (int i = 0; i < QG; ++i) {
+            float tl = l[i];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) tl += __shfl_xor_sync(0xffffffffu, tl, off);
+            *reinterpret_cast<float2*>(qs + i * kD + 2 * lane) = make_float2(acc[i][0], acc[i][1]);
+            if (lane == 0) {
+                ml[warp * QG + i] = m[i];
+                ml[kCW * QG + warp * QG + i] = tl;
             }
         }
-    }
-    // The warp's totals, then the four warps' states merged in shared memory.
+        __syncwarp();
+        mbar_arrive_elect(mFull);
+        if (!(ok = warp_wait(mFull, k & 1, abort_flag))) break;
+        const float* qall = reinterpret_cast<const float*>(smem + L::kQs);
+        for (int it = tid; it < QG * 32; it += 32 * kCW) {
+            const int i = it >> 5, d2 = 2 * (it & 31);
+            if (i >= pc.ng) continue;
+            float mm = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < QG; ++i) {
-        float t = l[i];
+            for (int w = 0; w < kCW; ++w) mm = fmaxf(mm, ml[w * QG + i]);
+            const float m_use = (mm == -INFINITY) ? 0.f : mm;
+            float lt = 0.f, o0 = 0.f, o1 = 0.f;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-        if (lane == 0) {
-            wm[warp][i] = m[i];
-            wl[warp][i] = t;
+            for (int w = 0; w < kCW; ++w) {
+                const float f = ex2f(ml[w * QG + i] - m_use);
+                const float2 ow = *reinterpret_cast<const float2*>(qall + (w * QG + i) * kD + d2);
+                lt = fmaf(ml[kCW * QG + w * QG + i], f, lt);
+                o0 = fmaf(ow.x, f, o0);
+                o1 = fmaf(ow.y, f, o1);
+            }
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const float lse2 = lt > 0.f ? mm + log2f(lt) : -INFINITY;  // -inf: no visible key here
+            const int64_t row = static_cast<int64_t>(pc.bh) * p.Nq + pc.g0 + i;
+            if (pc.nslots == 1) {
+                store2<T>(static_cast<T*>(p.o) + row * kD + d2, o0 * inv, o1 * inv);
+                if (p.lse != nullptr && d2 == 0) p.lse[row] = lse2;
+            } else {
+                float* po = p.part_o + (row * p.P + pc.slot) * kD;
+                *reinterpret_cast<float2*>(po + d2) = make_float2(o0 * inv, o1 * inv);
+                if (d2 == 0) p.part_lse[row * p.P + pc.slot] = lse2;
+            }
         }
-        *reinterpret_cast<float2*>(&wo[warp][i][2 * lane]) = make_float2(acc[i][0], acc[i][1]);
+        __syncwarp();
+        mbar_arrive_elect(mFree);
     }
-    __syncthreads();
-    // Thread t of the first QG*32 threads finishes query t/32, dims 2(t%32), 2(t%32)+1.
-    for (int item = threadIdx.x; item < QG * 32; item += kThreads) {
-        const int i = item >> 5, d2 = 2 * (item & 31);
-        if (i >= ng) continue;
-        float mm = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, wm[w][i]);
-        const float m_use = (mm == -INFINITY) ? 0.f : mm;
-        float lt = 0.f, o0 = 0.f, o1 = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float f = ex2f(wm[w][i] - m_use);
-            lt = fmaf(wl[w][i], f, lt);
-            o0 = fmaf(wo[w][i][d2], f, o0);
-            o1 = fmaf(wo[w][i][d2 + 1], f, o1);
-        }
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        const float lse2 = lt > 0.f ? mm + log2f(lt) : -INFINITY;  // -inf: no key of this split visible
-        const int64_t row = static_cast<int64_t>(bh) * p.Nq + g0 + i;
-        if (p.splits == 1) {
-            store2<T>(static_cast<T*>(p.o) + row * kD + d2, o0 * inv, o1 * inv);
-            if (p.lse != nullptr && d2 == 0) p.lse[row] = lse2;
-        } else {
-            float* po = p.part_o + (row * p.splits + split) * kD;
-            po[d2] = o0 * inv;
-            po[d2 + 1] = o1 * inv;
-            if (d2 == 0) p.part_lse[row * p.splits + split] = lse2;
-        }
-    }
+    if (!ok) raise_abort(abort_flag);
 }
 
-// One warp per query row: merge the splits by their log-sum-exps.
-template <typename T>
-__global__ void __launch_bounds__(128) attn_decode_combine_kernel(const DecodeParams p, int64_t rows) {
+// One warp per query row: merge the row's pieces by their log-sum-exps. Rows whose segment is
+// a single piece were written by the main kernel and are skipped. Lane s holds piece s's
+// log-sum-exp and weight (pieces in rounds of 32), so the loads of a round are independent.
+template <typename T, int QG>
+__global__ void __launch_bounds__(128) attn_decode_merge_kernel(const DecodeParams p, int64_t rows) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the main kernel's writes are visible
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
-    const float* pl = p.part_lse + row * p.splits;
-    float mx = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) mx = fmaxf(mx, pl[s]);
-    float w_tot = 0.f, o0 = 0.f, o1 = 0.f;
-    for (int s = 0; s < p.splits; ++s) {
-        if (pl[s] == -INFINITY) continue;  // a split with no visible key
-        const float w = ex2f(pl[s] - mx);
-        const float2 ov = *reinterpret_cast<const float2*>(p.part_o + (row * p.splits + s) * kD + 2 * lane);
-        w_tot += w;
-        o0 = fmaf(w, ov.x, o0);
-        o1 = fmaf(w, ov.y, o1);
+    const int bh = static_cast<int>(row / p.Nq), qi = static_cast<int>(row % p.Nq);
+    int n;
+    if (p.explicit_splits > 0) {
+        n = p.explicit_splits;
+    } else {
+        const int64_t s0 = (static_cast<int64_t>(bh) * p.groups + qi / QG) * p.Tn;
+        n = static_cast<int>(owner_of(s0 + p.Tn - 1, p.C, p.G) - owner_of(s0, p.C, p.G) + 1);
     }
+    if (n == 1) return;
+    const float* pl = p.part_lse + row * p.P;
+    const float* po = p.part_o + row * p.P * kD + 2 * lane;
+    float mx = -INFINITY;
+    for (int s0 = 0; s0 < n; s0 += 32) mx = fmaxf(mx, s0 + lane < n ? pl[s0 + lane] : -INFINITY);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float w_tot = 0.f, o0 = 0.f, o1 = 0.f;
+    for (int s0 = 0; s0 < n; s0 += 32) {
+        const float ls = s0 + lane < n ? pl[s0 + lane] : -INFINITY;
+        const float w = ls == -INFINITY ? 0.f : ex2f(ls - mx);  // a piece with no visible key weighs 0
+        w_tot += w;
+        const int m = min(32, n - s0);
+#pragma unroll 8
+        for (int u = 0; u < m; ++u) {
+            const float wu = __shfl_sync(0xffffffffu, w, u);
+            const float2 ov = *reinterpret_cast<const float2*>(po + (s0 + u) * kD);
+            o0 = fmaf(wu, ov.x, o0);
+            o1 = fmaf(wu, ov.y, o1);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) w_tot += __shfl_xor_sync(0xffffffffu, w_tot, off);
     const float inv = 1.f / w_tot;  // every row sees at least one key, so w_tot >= 1
     store2<T>(static_cast<T*>(p.o) + row * kD + 2 * lane, o0 * inv, o1 * inv);
     if (p.lse != nullptr && lane == 0) p.lse[row] = mx + log2f(w_tot);
 }
 
-template <typename T>
-int launch_t(DecodeParams prm, int64_t groups, int qg, cudaStream_t stream) {
-    const dim3 grid(static_cast<unsigned>(prm.BH), static_cast<unsigned>(prm.splits), static_cast<unsigned>(groups));
-    switch (qg) {
-        case 1: attn_decode_split_kernel<T, 1><<<grid, kThreads, 0, stream>>>(prm); break;
-        case 2: attn_decode_split_kernel<T, 2><<<grid, kThreads, 0, stream>>>(prm); break;
-        case 4: attn_decode_split_kernel<T, 4><<<grid, kThreads, 0, stream>>>(prm); break;
-        default: attn_decode_split_kernel<T, 8><<<grid, kThreads, 0, stream>>>(prm); break;
+// ------------------------------------------ host side ------------------------------------------
+int queries_per_group(int64_t Nq) { return Nq <= 1 ? 1 : Nq <= 2 ? 2 : Nq <= 4 ? 4 : 8; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<EncodeTiledFn>(ptr);
+        return static_cast<EncodeTiledFn>(nullptr);
+    }();
+    return fn;
+}
+
+// [BH][Nk][64] tensor; boxes of kRows rows x 128 bytes (64 16-bit values, or 32 fp32 values
+// — an fp32 row takes two boxes), 128-byte swizzle; rows past Nk of a head are out of bounds
+// (zero-filled), never the next head's.
+bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t Nk, int dtype) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t esz = dtype == ATTN_F32 ? 4 : 2;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(Nk), static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {kD * esz, static_cast<cuuint64_t>(Nk) * kD * esz};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(kRows), 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = dtype == ATTN_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, int QG>
+int ctas_per_sm() {
+    static int n = [] {
+        int v = 0;
+        if (cudaFuncSetAttribute(attn_decode_kernel<T, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Smem<T, QG>::kAlloc) != cudaSuccess)
+            return 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, attn_decode_kernel<T, QG>, kThreads,
+                                                          Smem<T, QG>::kAlloc) != cudaSuccess)
+            return 0;
+        return v;
+    }();
+    return n;
+}
+
+int ctas_per_sm_for(int dtype, int qg) {
+    switch (dtype) {
+        case ATTN_F32:
+            return qg == 1 ? ctas_per_sm<float, 1>() : qg == 2 ? ctas_per_sm<float, 2>()
+                   : qg == 4 ? ctas_per_sm<float, 4>() : ctas_per_sm<float, 8>();
+        case ATTN_BF16:
+            return qg == 1 ? ctas_per_sm<__nv_bfloat16, 1>() : qg == 2 ? ctas_per_sm<__nv_bfloat16, 2>()
+                   : qg == 4 ? ctas_per_sm<__nv_bfloat16, 4>() : ctas_per_sm<__nv_bfloat16, 8>();
+        default:
+            return qg == 1 ? ctas_per_sm<__half, 1>() : qg == 2 ? ctas_per_sm<__half, 2>()
+                   : qg == 4 ? ctas_per_sm<__half, 4>() : ctas_per_sm<__half, 8>();
     }
+}
+
+// The grid and slot layout of one call. The workspace query and the launch both build it, so
+// they agree on P.
+struct Plan {
+    int qg, groups, Tn, C, P, tps;
+    int64_t G;
+    bool merge;  // some segment has more than one piece
+};
+
+bool make_plan(int64_t BH, int64_t Nq, int64_t Nk, int splits, int num_sms, int per_sm, Plan* pl) {
+    pl->qg = queries_per_group(Nq);
+    pl->groups = static_cast<int>((Nq + pl->qg - 1) / pl->qg);
+    pl->Tn = static_cast<int>((Nk + kRows - 1) / kRows);
+    const int64_t segs = BH * pl->groups;
+    const int64_t slots = static_cast<int64_t>(std::max(1, num_sms)) * std::max(1, per_sm);
+    if (splits > 0) {
+        pl->tps = (pl->Tn + splits - 1) / splits;
+        pl->P = splits;
+        pl->G = 0;
+        pl->C = static_cast<int>(std::min<int64_t>(slots, segs * splits));
+        pl->merge = splits > 1;
+    } else {
+        pl->tps = 0;
+        pl->G = segs * pl->Tn;
+        pl->C = static_cast<int>(std::min<int64_t>(slots, pl->G));
+        // Every CTA run holds at least floor(G / C) tiles, so a segment of Tn tiles meets at
+        // most ceil((Tn - 1) / run) + 1 runs.
+        const int64_t run = pl->G / pl->C;
+        pl->P = static_cast<int>(std::min<int64_t>(pl->C, (pl->Tn - 1 + run - 1) / run + 1));
+        pl->merge = pl->P > 1;
+    }
+    return pl->C >= 1;
+}
+
+template <typename T, int QG>
+int launch_t(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& prm, bool merge, cudaStream_t stream) {
+    attn_decode_kernel<T, QG><<<static_cast<unsigned>(prm.C), kThreads, Smem<T, QG>::kAlloc, stream>>>(mk, mv, prm);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
-    if (prm.splits > 1) {
+    if (merge) {
         const int64_t rows = static_cast<int64_t>(prm.BH) * prm.Nq;
-        attn_decode_combine_kernel<T><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(prm, rows);
-        if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+        // Programmatic stream serialisation: the merge grid may start while the main grid runs
+        // (it is released by the main kernel's launch_dependents) and waits in griddepcontrol.wait
+        // until that grid has completed and its memory is visible.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, attn_decode_merge_kernel<T, QG>, prm, rows) != cudaSuccess) return ATTN_ERR_LAUNCH;
     }
     return ATTN_OK;
 }
 
-}  // namespace
+template <typename T>
+int launch_qg(int qg, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& prm, bool merge,
+              cudaStream_t stream) {
+    switch (qg) {
+        case 1: return launch_t<T, 1>(mk, mv, prm, merge, stream);
+        case 2: return launch_t<T, 2>(mk, mv, prm, merge, stream);
+        case 4: return launch_t<T, 4>(mk, mv, prm, merge, stream);
+        default: return launch_t<T, 8>(mk, mv, prm, merge, stream);
+    }
+}
 
-namespace {
-
-int queries_per_group(int64_t Nq) { return Nq <= 1 ? 1 : Nq <= 2 ? 2 : Nq <= 4 ? 4 : 8; }
-
-}  // namespace
-
-size_t decode_workspace_bytes(int64_t BH, int64_t Nq, int64_t splits) {
-    if (BH <= 0 || Nq <= 0 || splits <= 1 || splits > ATTN_KV_MAX_SPLITS) return 0;
-    if (BH > 0x7FFFFFFFll || Nq > ATTN_MAX_N) return 0;
-    // rows * splits * 65 floats stays below 2^31 * 2^30 * 2^10 * 2^7 < 2^64 only for sizes the
-    // launcher accepts; check in double first.
-    const double need = static_cast<double>(BH) * static_cast<double>(Nq) * static_cast<double>(splits) * (kD + 1) * 4.0;
+size_t partial_bytes(int64_t BH, int64_t Nq, int64_t P) {
+    const double need = static_cast<double>(BH) * static_cast<double>(Nq) * static_cast<double>(P) * (kD + 1) * 4.0;
     if (need > 9.0e18) return 0;
-    const size_t r = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * static_cast<size_t>(splits);
-    const size_t o_bytes = (r * kD * sizeof(float) + 255) / 256 * 256;
-    const size_t l_bytes = (r * sizeof(float) + 255) / 256 * 256;
-    return o_bytes + l_bytes;
+    const size_t r = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * static_cast<size_t>(P);
+    return (r * kD * sizeof(float) + 255) / 256 * 256 + (r * sizeof(float) + 255) / 256 * 256;
 }
 
-int decode_auto_splits(int64_t BH, int64_t Nq, int64_t Nk, int num_sms) {
-    if (BH <= 0 || Nq <= 0 || Nk <= 0) return 1;
-    const int64_t groups = (Nq + queries_per_group(Nq) - 1) / queries_per_group(Nq);
-    const int64_t ctas = BH * groups;
-    const int64_t target = 8 * static_cast<int64_t>(num_sms);  // about eight CTAs of four warps per SM
-    int64_t want = (target + ctas - 1) / ctas;
-    want = std::min<int64_t>(want, std::max<int64_t>(1, Nk / 256));  // at least 256 keys per split
-    want = std::min<int64_t>(want, ATTN_KV_MAX_SPLITS);
-    return static_cast<int>(std::max<int64_t>(want, 1));
+}  // namespace
+
+size_t decode_workspace_bytes(int64_t BH, int64_t Nq, int64_t Nk, int splits, int dtype, int num_sms) {
+    if (BH <= 0 || Nq <= 0 || Nk <= 0 || splits < 0 || splits > ATTN_KV_MAX_SPLITS) return 0;
+    if (BH > 0x7FFFFFFFll || Nq > ATTN_MAX_N || Nk > ATTN_MAX_N) return 0;
+    if (splits == 1) return 0;
+    if (splits > 1) return partial_bytes(BH, Nq, splits);
+    const int per_sm = ctas_per_sm_for(dtype, queries_per_group(Nq));
+    if (per_sm <= 0) return 0;
+    Plan pl;
+    if (!make_plan(BH, Nq, Nk, 0, num_sms, per_sm, &pl)) return 0;
+    return pl.merge ? partial_bytes(BH, Nq, pl.P) : 0;
 }
 
-int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace, int64_t BH,
-                  int64_t Nq, int64_t Nk, bool causal, int dtype, int splits, cudaStream_t stream) {
-    if (Nk > ATTN_MAX_N || BH > 0x7FFFFFFFll || splits < 1 || splits > ATTN_KV_MAX_SPLITS) return ATTN_ERR_UNSUPPORTED;
+int decode_device_error(bool clear, unsigned* err) {
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_decode_error, sizeof(v)) != cudaSuccess) return ATTN_ERR_DEVICE;
+    if (clear && v != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_decode_error, &zero, sizeof(zero)) != cudaSuccess) return ATTN_ERR_DEVICE;
+    }
+    *err = v;
+    return ATTN_OK;
+}
+
+int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                  size_t workspace_bytes, int64_t BH, int64_t Nq, int64_t Nk, bool causal, int dtype, int splits,
+                  int num_sms, cudaStream_t stream) {
+    if (Nk > ATTN_MAX_N || BH > 0x7FFFFFFFll || splits < 0 || splits > ATTN_KV_MAX_SPLITS) return ATTN_ERR_UNSUPPORTED;
     const int qg = queries_per_group(Nq);
-    const int64_t groups = (Nq + qg - 1) / qg;
-    if (groups > 65535) return ATTN_ERR_UNSUPPORTED;
+    const int per_sm = ctas_per_sm_for(dtype, qg);
+    if (per_sm <= 0) return ATTN_ERR_LAUNCH;
+    Plan pl;
+    if (!make_plan(BH, Nq, Nk, splits, num_sms, per_sm, &pl)) return ATTN_ERR_UNSUPPORTED;
+    if (BH * pl.groups > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     DecodeParams prm;
     prm.q = q;
-    prm.k = k;
-    prm.v = v;
     prm.o = o;
     prm.lse = lse;
     prm.Nq = static_cast<int>(Nq);
     prm.Nk = static_cast<int>(Nk);
     prm.BH = static_cast<int>(BH);
-    prm.splits = splits;
-    prm.chunk = static_cast<int>(((Nk + splits - 1) / splits + 31) / 32 * 32);
+    prm.groups = pl.groups;
+    prm.Tn = pl.Tn;
     prm.causal = causal ? 1 : 0;
+    prm.explicit_splits = splits;
+    prm.tps = pl.tps;
+    prm.P = pl.P;
+    prm.C = pl.C;
+    prm.G = pl.G;
     prm.c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
-    if (splits > 1) {
-        const size_t r = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * static_cast<size_t>(splits);
+    prm.part_o = nullptr;
+    prm.part_lse = nullptr;
+    if (pl.merge) {
+        const size_t need = partial_bytes(BH, Nq, pl.P);
+        if (need == 0) return ATTN_ERR_UNSUPPORTED;
+        if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+        const size_t r = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * static_cast<size_t>(pl.P);
         prm.part_o = static_cast<float*>(workspace);
         prm.part_lse =
             reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + (r * kD * sizeof(float) + 255) / 256 * 256);
-    } else {
-        prm.part_o = nullptr;
-        prm.part_lse = nullptr;
     }
+    CUtensorMap mk, mv;
+    if (!make_map(&mk, k, BH, Nk, dtype) || !make_map(&mv, v, BH, Nk, dtype)) return ATTN_ERR_DEVICE;
     switch (dtype) {
-        case ATTN_F32: return launch_t<float>(prm, groups, qg, stream);
-        case ATTN_BF16: return launch_t<__nv_bfloat16>(prm, groups, qg, stream);
-        default: return launch_t<__half>(prm, groups, qg, stream);
+        case ATTN_F32: return launch_qg<float>(qg, mk, mv, prm, pl.merge, stream);
+        case ATTN_BF16: return launch_qg<__nv_bfloat16>(qg, mk, mv, prm, pl.merge, stream);
+        default: return launch_qg<__half>(qg, mk, mv, prm, pl.merge, stream);
     }
 }
 

@@ -110,3 +110,16 @@ def test_reference_arm_prints_one_line(capsys, monkeypatch):
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "TFLOP/s"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_decode_bytes_count_k_v_once_and_q_o():
+    # bf16: K and V (Nk x d each) read once per head, q read and o written (Nq x d each).
+    assert bench.decode_bytes(16, 12, 1, 8192, 64) == 2 * 16 * 12 * (2 * 8192 * 64 + 2 * 64)
+    assert bench.decode_bytes(1, 1, 4, 100, 64, esz=4) == 4 * (2 * 100 * 64 + 2 * 4 * 64)
+
+
+def test_decode_traffic_record_is_keyed_to_the_decode_source(tmp_path):
+    prof = tmp_path / "d.md"
+    prof.write_text(f"traffic_bytes_per_launch: 777\nsource_sha256: {bench.source_sha256(bench.DECODE_SOURCE)}\n")
+    assert bench.recorded_traffic(str(prof), bench.DECODE_SOURCE) == (777, "ncu capture of this source")
+    assert bench.recorded_traffic(str(prof), bench.TC_SOURCE)[0] is None

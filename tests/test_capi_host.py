@@ -140,10 +140,12 @@ def test_kvcache_argument_checks(lib, args, want):
 def test_kvcache_workspace_bytes(lib):
     r = 2 * 3 * 5 * 7  # B * H * Nq * splits
     want = (r * 64 * 4 + 255) // 256 * 256 + (r * 4 + 255) // 256 * 256
-    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 7) == want
-    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 1) == 0   # one share writes o directly
-    assert lib.attn_kvcache_workspace_bytes(-1, 3, 5, 7) == 0
-    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 1025) == 0
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 7, 1) == want
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 1, 1) == 0   # one share writes o directly
+    assert lib.attn_kvcache_workspace_bytes(-1, 3, 5, 100, 7, 1) == 0
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 4, 7, 1) == 0     # Nq > Nk
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 1025, 1) == 0
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 7, 9) == 0   # unknown dtype
 
 
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="needs a machine without a GPU")
@@ -151,4 +153,4 @@ def test_kvcache_valid_call_without_gpu_reports_device_error(lib):
     ws = P * 64
     assert lib.attn_fwd_kvcache(P, P * 3, P * 5, P * 9, None, ws, 1 << 20, 1, 2, 4, 100, 64, 1, 1, 4, None) == 5
     assert lib.attn_fwd_kvcache(P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 1, 0, None) == 5
-    assert lib.attn_kvcache_num_splits(1, 2, 4, 100) == 1
+    assert lib.attn_kvcache_workspace_bytes(1, 2, 4, 100, 0, 1) == 0  # balanced plan needs the device

@@ -60,7 +60,7 @@ def test_kvcache_against_oracle(dtype, causal, Nq, Nk, splits):
 
 @pytest.mark.parametrize("splits", [2, 7, 64, 200, 1024])
 def test_kvcache_many_shares_including_empty_ones(splits):
-    # 1024 shares over 300 keys: shares are rounded to 32 keys, so most are empty and must
+    # 1024 shares over 300 keys: shares are whole 128-key tiles, so most are empty and must
     # carry weight 0 in the merge.
     _run(0xCAC31000 + splits, 1, 2, 3, 300, "bf16", True, splits)
 
@@ -105,9 +105,19 @@ def test_kvcache_single_visible_key_returns_its_value():
     assert abs(float(lse[0, 0, 0]) - s00 / np.log(2.0)) <= 1e-5 * (1 + abs(s00))
 
 
+@pytest.mark.parametrize("B,H,Nq,Nk", [(1, 1, 1, 100), (1, 2, 1, 100000), (3, 5, 2, 3000), (64, 12, 1, 300),
+                                       (2, 3, 40, 5000), (1, 1, 9, 129)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_kvcache_balanced_plan_over_head_boundaries(B, H, Nq, Nk, causal):
+    # The balanced plan cuts the tiles of all heads into equal runs, so runs start and end
+    # inside heads (several pieces per head, merged) or hold several whole heads (written
+    # directly); tiny cases give fewer tiles than CTAs.
+    _run(0xCAC38000 + B * 1000 + Nq * 10 + Nk, B, H, Nq, Nk, "bf16", causal, 0)
+
+
 def test_kvcache_decode_workload_sampled():
     # One new token per sequence against an 8192-key cache, B16 H12 (the decode measurement's
-    # shape), automatic share count; every query row is checked against the oracle.
+    # shape), balanced plan; every query row is checked against the oracle.
     B, H, Nq, Nk = 16, 12, 1, 8192
     q, k, v = _inputs(0xCAC36000, B, H, Nq, Nk, "bf16")
     qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
@@ -123,7 +133,7 @@ def test_kvcache_explicit_workspace_and_outputs_are_used():
     B, H, Nq, Nk, S = 1, 3, 2, 500, 6
     q, k, v = _inputs(0xCAC37000, B, H, Nq, Nk, "f16")
     qd, kd, vd = (to_dev(x, "f16") for x in (q, k, v))
-    ws = torch.empty(fa.attn_kvcache_workspace_bytes(B, H, Nq, S), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(fa.attn_kvcache_workspace_bytes(B, H, Nq, Nk, S, torch.float16), dtype=torch.uint8, device="cuda")
     out = torch.full_like(qd, float("nan"))
     lse = torch.full((B, H, Nq), float("nan"), device="cuda")
     r = fa.attn_fwd_kvcache(qd, kd, vd, causal=False, num_splits=S, workspace=ws, out=out, lse=lse)
