@@ -30,15 +30,16 @@ bool inject_launch_fault() {
     return f != nullptr && std::strcmp(f, "launch") == 0;
 }
 
-// Common checks of attn_fwd and attn_fwd_materialized. On success *bh and *bytes hold
-// B*H and the size of one tensor; *skip is set when there is no work.
+// Common checks of the entry points over [B, H, N, d] tensors. On success *bh and *bytes
+// hold B*H and the size of one tensor; *skip is set when there is no work. d = 128 is
+// accepted only where `wide` is set (the forward entry points).
 int check_common(const void* q, const void* k, const void* v, const void* o, int64_t B, int64_t H,
                  int64_t N, int64_t d, int causal, int dtype, int64_t* bh, size_t* bytes,
-                 bool* skip) {
+                 bool* skip, bool wide = false) {
     if (B < 0 || H < 0 || N < 0 || d < 0) return ATTN_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
     if (dtype != ATTN_F32 && dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_UNSUPPORTED;
-    if (d != kHeadDim) return ATTN_ERR_UNSUPPORTED;
+    if (d != kHeadDim && !(wide && d == 2 * kHeadDim)) return ATTN_ERR_UNSUPPORTED;
     if (N > ATTN_MAX_N) return ATTN_ERR_UNSUPPORTED;
     if (B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     const int64_t BH = B * H;
@@ -48,7 +49,7 @@ int check_common(const void* q, const void* k, const void* v, const void* o, int
     if (*skip) return ATTN_OK;
     if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return ATTN_ERR_ALIGN;
-    *bytes = static_cast<size_t>(BH) * static_cast<size_t>(N) * kHeadDim * elem_size(dtype);
+    *bytes = static_cast<size_t>(BH) * static_cast<size_t>(N) * static_cast<size_t>(d) * elem_size(dtype);
     if (overlap(o, *bytes, q, *bytes) || overlap(o, *bytes, k, *bytes) || overlap(o, *bytes, v, *bytes))
         return ATTN_ERR_ALIAS;
     return ATTN_OK;
@@ -80,7 +81,7 @@ int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* ls
     int64_t BH = 0;
     size_t bytes = 0;
     bool skip = false;
-    int st = check_common(q, k, v, o, B, H, N, d, causal, dtype, &BH, &bytes, &skip);
+    int st = check_common(q, k, v, o, B, H, N, d, causal, dtype, &BH, &bytes, &skip, true);
     if (st != ATTN_OK || skip) return st;
     if (lse != nullptr) {
         if (!aligned(lse, 4)) return ATTN_ERR_ALIGN;
@@ -95,9 +96,9 @@ int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* ls
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == ATTN_F32)
         return attn::launch_fwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
-                                    static_cast<const float*>(v), static_cast<float*>(o), lse, BH, N,
+                                    static_cast<const float*>(v), static_cast<float*>(o), lse, BH, N, d,
                                     causal != 0, num_sms, s);
-    return attn::launch_fwd_tc(q, k, v, o, lse, BH, N, causal != 0, dtype == ATTN_BF16, num_sms, s);
+    return attn::launch_fwd_tc(q, k, v, o, lse, BH, N, d, causal != 0, dtype == ATTN_BF16, num_sms, s);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -251,7 +252,7 @@ const char* attn_status_string(int status) {
     switch (status) {
         case ATTN_OK: return "ok";
         case ATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or causal not 0/1)";
-        case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim must be 64; dtype f32/bf16/f16; size limits)";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim 64, or 128 for the forward; dtype f32/bf16/f16; size limits)";
         case ATTN_ERR_ALIGN: return "pointer not aligned (tensors 16 bytes, workspace 256 bytes)";
         case ATTN_ERR_ALIAS: return "output or workspace overlaps another buffer";
         case ATTN_ERR_DEVICE: return "current device is not sm_103 or a CUDA query failed";
@@ -262,6 +263,6 @@ const char* attn_status_string(int status) {
     }
 }
 
-int attn_abi_version(void) { return (1 << 16) | 3; }
+int attn_abi_version(void) { return (1 << 16) | 4; }
 
 }  // extern "C"

@@ -9,11 +9,12 @@
 // on every load and store (the page's kernel masks rows and keys past T).
 //
 // Layout per CTA: BM query rows (64, or 32 when the grid would not fill the GPU) against
-// key tiles of 64, d = 64, BM/4 x 16 threads. Thread (ty, tx) holds a 4 x 4 score
-// micro-tile — rows ty*4 + i, keys tx + 16 j — and a 4 x 4 output micro-tile — rows ty*4 + i,
-// dims tx*4 + j. Rows of shared tiles are padded to 68 floats so that every float4 read of a
-// key row, every P store and every V read is free of bank conflicts. The 16 threads that
-// share a row sit in one half-warp, so row max and row sum are 4-step xor shuffles.
+// key tiles of 64, head width D = 64 or 128, BM/4 x 16 threads. Thread (ty, tx) holds a 4 x 4
+// score micro-tile — rows ty*4 + i, keys tx + 16 j — and a 4 x D/16 output micro-tile — rows
+// ty*4 + i, dims 64 g + tx*4 + j. Rows of shared tiles are padded to D + 4 floats so that every
+// float4 read of a key row, every P store and every V read is free of bank conflicts. The 16
+// threads that share a row sit in one half-warp, so row max and row sum are 4-step xor
+// shuffles.
 // With an `lse` pointer each row's log-sum-exp is stored too, in base 2 as the page's
 // forward kernel keeps it for the backward pass (m + log2 l, "Backwards, and training with
 // it").
@@ -27,9 +28,11 @@
 namespace attn {
 namespace {
 
-constexpr int kD = 64;
 constexpr int kBN = 64;
-constexpr int kLd = 68;  // padded row stride (floats) of every shared tile
+
+// Padded row stride (floats) of every shared tile.
+template <int D>
+__host__ __device__ constexpr int ld_of() { return D + 4; }
 
 __device__ __forceinline__ float ex2f(float x) {
     float y;
@@ -37,12 +40,15 @@ __device__ __forceinline__ float ex2f(float x) {
     return y;
 }
 
-template <int BM>
+template <int BM, int D>
 __global__ void __launch_bounds__(BM * 4)
     attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                         const float* __restrict__ v, float* __restrict__ o, float* __restrict__ lse,
                         int N, int BH, int nblk, int causal, float c) {
     constexpr int kThreads = BM * 4;
+    constexpr int kLd = ld_of<D>();
+    constexpr int kD4 = D / 4;   // float4 per row
+    constexpr int kG = D / 64;   // 64-dim groups of this thread's output columns
     extern __shared__ float4 smem4[];
     float* const Qs = reinterpret_cast<float*>(smem4);
     float* const Ks = Qs + BM * kLd;
@@ -56,26 +62,26 @@ __global__ void __launch_bounds__(BM * 4)
     const int slot = static_cast<int>(blockIdx.x / static_cast<unsigned>(BH));
     const int blk = causal ? (nblk - 1 - slot) : slot;
     const int row0 = blk * BM;
-    const int64_t head = static_cast<int64_t>(bh) * N * kD;
+    const int64_t head = static_cast<int64_t>(bh) * N * D;
     const float* qh = q + head;
     const float* kh = k + head;
     const float* vh = v + head;
 
     // Q tile, rows >= N read as zero.
-    for (int idx = tid; idx < BM * 16; idx += kThreads) {
-        const int r = idx >> 4, e4 = idx & 15;
+    for (int idx = tid; idx < BM * kD4; idx += kThreads) {
+        const int r = idx / kD4, e4 = idx % kD4;
         float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (row0 + r < N) val = *reinterpret_cast<const float4*>(qh + static_cast<int64_t>(row0 + r) * kD + 4 * e4);
+        if (row0 + r < N) val = *reinterpret_cast<const float4*>(qh + static_cast<int64_t>(row0 + r) * D + 4 * e4);
         *reinterpret_cast<float4*>(Qs + r * kLd + 4 * e4) = val;
     }
 
-    float m[4], l[4], acc[4][4];
+    float m[4], l[4], acc[4][4 * kG];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         m[i] = -INFINITY;
         l[i] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < 4 * kG; ++j) acc[i][j] = 0.f;
     }
 
     const int kend = causal ? min(N, row0 + BM) : N;
@@ -83,11 +89,11 @@ __global__ void __launch_bounds__(BM * 4)
     for (int t = 0; t < ntiles; ++t) {
         const int kbase = t * kBN;
         __syncthreads();  // the previous tile's products are done with Ks, Vs and Ps
-        for (int idx = tid; idx < kBN * 16; idx += kThreads) {
-            const int r = idx >> 4, e4 = idx & 15;
+        for (int idx = tid; idx < kBN * kD4; idx += kThreads) {
+            const int r = idx / kD4, e4 = idx % kD4;
             float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
             if (kbase + r < N) {
-                const int64_t off = static_cast<int64_t>(kbase + r) * kD + 4 * e4;
+                const int64_t off = static_cast<int64_t>(kbase + r) * D + 4 * e4;
                 kv = *reinterpret_cast<const float4*>(kh + off);
                 vv = *reinterpret_cast<const float4*>(vh + off);
             }
@@ -103,7 +109,7 @@ __global__ void __launch_bounds__(BM * 4)
 #pragma unroll
             for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
 #pragma unroll 4
-        for (int e = 0; e < kD; e += 4) {
+        for (int e = 0; e < D; e += 4) {
             float4 qa[4], kb[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) qa[i] = *reinterpret_cast<const float4*>(Qs + (ty * 4 + i) * kLd + e);
@@ -151,27 +157,32 @@ __global__ void __launch_bounds__(BM * 4)
             l[i] = l[i] * alpha + ps;  // this thread's share of the row total
             m[i] = m_ref;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] *= alpha;
+            for (int j = 0; j < 4 * kG; ++j) acc[i][j] *= alpha;
         }
         __syncthreads();
 
-        // O micro-tile += P V: rows ty*4+i, dims tx*4+j.
+        // O micro-tile += P V: rows ty*4+i, dims 64g + tx*4+j.
 #pragma unroll 4
         for (int kk = 0; kk < kBN; kk += 4) {
-            float4 pa[4], vb[4];
+            float4 pa[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) pa[i] = *reinterpret_cast<const float4*>(Ps + (ty * 4 + i) * kLd + kk);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) vb[u] = *reinterpret_cast<const float4*>(Vs + (kk + u) * kLd + 4 * tx);
+            for (int g = 0; g < kG; ++g) {
+                float4 vb[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float pw[4] = {pa[i].x, pa[i].y, pa[i].z, pa[i].w};
+                for (int u = 0; u < 4; ++u)
+                    vb[u] = *reinterpret_cast<const float4*>(Vs + (kk + u) * kLd + 64 * g + 4 * tx);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    acc[i][0] = fmaf(pw[u], vb[u].x, acc[i][0]);
-                    acc[i][1] = fmaf(pw[u], vb[u].y, acc[i][1]);
-                    acc[i][2] = fmaf(pw[u], vb[u].z, acc[i][2]);
-                    acc[i][3] = fmaf(pw[u], vb[u].w, acc[i][3]);
+                for (int i = 0; i < 4; ++i) {
+                    const float pw[4] = {pa[i].x, pa[i].y, pa[i].z, pa[i].w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        acc[i][4 * g + 0] = fmaf(pw[u], vb[u].x, acc[i][4 * g + 0]);
+                        acc[i][4 * g + 1] = fmaf(pw[u], vb[u].y, acc[i][4 * g + 1]);
+                        acc[i][4 * g + 2] = fmaf(pw[u], vb[u].z, acc[i][4 * g + 2]);
+                        acc[i][4 * g + 3] = fmaf(pw[u], vb[u].w, acc[i][4 * g + 3]);
+                    }
                 }
             }
         }
@@ -186,25 +197,28 @@ __global__ void __launch_bounds__(BM * 4)
         const int row = row0 + ty * 4 + i;
         if (row < N) {
             const float inv = 1.f / tot;
-            *reinterpret_cast<float4*>(o + head + static_cast<int64_t>(row) * kD + 4 * tx) =
-                make_float4(acc[i][0] * inv, acc[i][1] * inv, acc[i][2] * inv, acc[i][3] * inv);
+#pragma unroll
+            for (int g = 0; g < kG; ++g)
+                *reinterpret_cast<float4*>(o + head + static_cast<int64_t>(row) * D + 64 * g + 4 * tx) =
+                    make_float4(acc[i][4 * g] * inv, acc[i][4 * g + 1] * inv, acc[i][4 * g + 2] * inv,
+                                acc[i][4 * g + 3] * inv);
             if (lse != nullptr && tx == 0) lse[static_cast<int64_t>(bh) * N + row] = m[i] + log2f(tot);
         }
     }
 }
 
-template <int BM>
+template <int BM, int D>
 int launch_bm(const float* q, const float* k, const float* v, float* o, float* lse, int64_t BH,
               int64_t N, bool causal, cudaStream_t stream) {
-    const int smem = (2 * BM + 2 * kBN) * kLd * static_cast<int>(sizeof(float));
-    if (cudaFuncSetAttribute(attn_fwd_f32_kernel<BM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const int smem = (2 * BM + 2 * kBN) * ld_of<D>() * static_cast<int>(sizeof(float));
+    if (cudaFuncSetAttribute(attn_fwd_f32_kernel<BM, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
         return ATTN_ERR_LAUNCH;
     const int64_t nblk = (N + BM - 1) / BM;
     const int64_t blocks = nblk * BH;
     if (blocks > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
-    const float c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
-    attn_fwd_f32_kernel<BM><<<static_cast<unsigned>(blocks), BM * 4, smem, stream>>>(
+    const float c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    attn_fwd_f32_kernel<BM, D><<<static_cast<unsigned>(blocks), BM * 4, smem, stream>>>(
         q, k, v, o, lse, static_cast<int>(N), static_cast<int>(BH), static_cast<int>(nblk), causal ? 1 : 0, c);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
@@ -212,13 +226,18 @@ int launch_bm(const float* q, const float* k, const float* v, float* o, float* l
 }  // namespace
 
 int launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int64_t BH,
-                   int64_t N, bool causal, int num_sms, cudaStream_t stream) {
+                   int64_t N, int64_t d, bool causal, int num_sms, cudaStream_t stream) {
     if (N > 0x7FFFFFFFll - 64 || BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     // Small problems use 32-row blocks so that more SMs get work.
     const int64_t blocks64 = ((N + 63) / 64) * BH;
-    if (blocks64 < 2 * static_cast<int64_t>(num_sms))
-        return launch_bm<32>(q, k, v, o, lse, BH, N, causal, stream);
-    return launch_bm<64>(q, k, v, o, lse, BH, N, causal, stream);
+    const bool small = blocks64 < 2 * static_cast<int64_t>(num_sms);
+    if (d == 64)
+        return small ? launch_bm<32, 64>(q, k, v, o, lse, BH, N, causal, stream)
+                     : launch_bm<64, 64>(q, k, v, o, lse, BH, N, causal, stream);
+    if (d == 128)
+        return small ? launch_bm<32, 128>(q, k, v, o, lse, BH, N, causal, stream)
+                     : launch_bm<64, 128>(q, k, v, o, lse, BH, N, causal, stream);
+    return ATTN_ERR_UNSUPPORTED;
 }
 
 }  // namespace attn

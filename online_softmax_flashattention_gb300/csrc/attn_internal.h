@@ -10,15 +10,15 @@
 
 namespace attn {
 
-// Online-softmax forward on FFMA for float32 tensors ([BH, N, 64] contiguous). `lse` is null
-// or receives each row's base-2 log-sum-exp ([BH, N] float32).
+// Online-softmax forward on FFMA for float32 tensors ([BH, N, d] contiguous, d = 64 or 128).
+// `lse` is null or receives each row's base-2 log-sum-exp ([BH, N] float32).
 int launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int64_t BH,
-                   int64_t N, bool causal, int num_sms, cudaStream_t stream);
+                   int64_t N, int64_t d, bool causal, int num_sms, cudaStream_t stream);
 
-// Online-softmax forward on tcgen05 tensor cores for bf16 (bf16 = true) or fp16 tensors;
-// `lse` as above.
+// Online-softmax forward on tcgen05 tensor cores for bf16 (bf16 = true) or fp16 tensors,
+// d = 64 or 128; `lse` as above.
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
-                  int64_t N, bool causal, bool bf16, int num_sms, cudaStream_t stream);
+                  int64_t N, int64_t d, bool causal, bool bf16, int num_sms, cudaStream_t stream);
 
 // Backward pass for float32 tensors (two FFMA kernels): dq, dk, dv from q, k, v, the forward's
 // o, the output gradient dout and the forward's base-2 log-sum-exps lse ([BH, N] float32).

@@ -57,20 +57,16 @@
 namespace attn {
 namespace {
 
-constexpr int kD = 64;
 constexpr int kBM = 128;  // query rows per tile = TMEM lanes
 constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kKStages = 4;  // K ring depth (QK^T reads K one step ahead)
-constexpr int kVStages = 3;  // V ring depth
-constexpr int kTileBytes = kBM * kD * 2;  // 16 KiB per 128 x 64 tile of 16-bit values
+constexpr int kBlockBytes = kBM * 64 * 2;  // one 128-row x 128-byte column block (the swizzle span)
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kSIssuerWarp = 9;   // also owns the tensor memory
 constexpr int kPVIssuerWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // + 128 * tile
-constexpr uint32_t kColO = 256;  // + 64 * tile
-constexpr uint32_t kColP = 384;  // + 64 * tile
+constexpr uint32_t kColO = 256;  // + D * tile
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s for any single wait
 constexpr uint64_t kDrainTimeoutNs = 100000000ull;  // 100 ms to drain after an abort
 constexpr unsigned kPollSleepNs = 32;  // MMA issuers' back-off between unproductive polls
@@ -85,29 +81,47 @@ static_assert(2 * 128 * kRegsSoftmax + (kThreads - 2 * 128) * kRegsOther <= kThr
               "register split must fit the launch allocation");
 static_assert(kThreads * kRegsLaunch <= 65536, "launch allocation must fit the register file");
 
-// Shared-memory layout (byte offsets from a 1024-byte aligned base).
-constexpr int kOffQ = 0;                                   // 2 tiles
-constexpr int kOffK = kOffQ + 2 * kTileBytes;              // kKStages tiles
-constexpr int kOffV = kOffK + kKStages * kTileBytes;       // kVStages tiles
-constexpr int kOffBar = kOffV + kVStages * kTileBytes;     // mbarriers, 8 bytes each
-constexpr int kBarQFull = 0;
-constexpr int kBarKFull = 1;
-constexpr int kBarKEmpty = kBarKFull + kKStages;
-constexpr int kBarVFull = kBarKEmpty + kKStages;
-constexpr int kBarVEmpty = kBarVFull + kVStages;
-constexpr int kBarSFull = kBarVEmpty + kVStages;  // [2] S_X(j) computed
-constexpr int kBarSFree = kBarSFull + 2;          // [2] softmax X copied S_X(j) out (4 warps)
-constexpr int kBarPFull = kBarSFree + 2;          // [2] softmax X wrote P_X(j) (4 warps)
-constexpr int kBarOReady = kBarPFull + 2;         // [2] PV_X(j) done: O_X stable, P_X reusable
-constexpr int kBarDrain = kBarOReady + 2;         // [2] every MMA of issuer 0 (S) / 1 (PV) done
-constexpr int kNumBars = kBarDrain + 2;
-constexpr int kOffSlot = kOffBar + 8 * kNumBars;  // TMEM base address written by tcgen05.alloc
-constexpr int kOffAbort = kOffSlot + 4;
-constexpr int kSmemUsed = kOffAbort + 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
-
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget of one CTA");
-static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+// Everything that depends on the head width D (64 or 128). A tile of 128 rows x D 16-bit
+// values is D/64 column blocks of 128 rows x 128 bytes, each loaded by its own TMA box.
+// Tensor memory: S_X at column 128X, O_X at 256 + D X; P_X (the probabilities as 16-bit
+// pairs, 64 columns) at 384 + 64X for D = 64, and over the first 64 columns of S_X for
+// D = 128, where the S and O of both tiles fill all 512 columns. With P over S, S_X(j+1) may
+// only start once PV_X(j) has read P_X(j).
+template <int D>
+struct Lay {
+    static_assert(D == 64 || D == 128, "head width 64 or 128");
+    static constexpr int kBlocks = D / 64;
+    static constexpr int kTileBytes = kBlocks * kBlockBytes;  // 16 or 32 KiB
+    static constexpr int kKStages = D == 64 ? 4 : 2;  // K ring depth (QK^T reads K one step ahead)
+    static constexpr int kVStages = D == 64 ? 3 : 2;  // V ring depth
+    static constexpr bool kPOverS = D > 64;
+    __host__ __device__ static constexpr uint32_t colP(int X) {
+        return kPOverS ? kColS + 128u * static_cast<uint32_t>(X) : 384u + 64u * static_cast<uint32_t>(X);
+    }
+    // Shared-memory layout (byte offsets from a 1024-byte aligned base).
+    static constexpr int kOffQ = 0;                                // 2 tiles
+    static constexpr int kOffK = kOffQ + 2 * kTileBytes;           // kKStages tiles
+    static constexpr int kOffV = kOffK + kKStages * kTileBytes;    // kVStages tiles
+    static constexpr int kOffBar = kOffV + kVStages * kTileBytes;  // mbarriers, 8 bytes each
+    static constexpr int kBarQFull = 0;
+    static constexpr int kBarKFull = 1;
+    static constexpr int kBarKEmpty = kBarKFull + kKStages;
+    static constexpr int kBarVFull = kBarKEmpty + kKStages;
+    static constexpr int kBarVEmpty = kBarVFull + kVStages;
+    static constexpr int kBarSFull = kBarVEmpty + kVStages;  // [2] S_X(j) computed
+    static constexpr int kBarSFree = kBarSFull + 2;          // [2] softmax X copied S_X(j) out (4 warps)
+    static constexpr int kBarPFull = kBarSFree + 2;          // [2] softmax X wrote P_X(j) (4 warps)
+    static constexpr int kBarOReady = kBarPFull + 2;         // [2] PV_X(j) done: O_X stable, P_X reusable
+    static constexpr int kBarDrain = kBarOReady + 2;         // [2] every MMA of issuer 0 (S) / 1 (PV) done
+    static constexpr int kNumBars = kBarDrain + 2;
+    static constexpr int kOffSlot = kOffBar + 8 * kNumBars;  // TMEM base address written by tcgen05.alloc
+    static constexpr int kOffAbort = kOffSlot + 4;
+    static constexpr int kSmemUsed = kOffAbort + 4;
+    static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget of one CTA");
+    static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+    static_assert(kColO + 2 * D <= kTmemCols && (kPOverS || 384 + 128 <= kTmemCols), "tensor memory budget");
+};
 
 __device__ unsigned int g_tc_error = 0;
 
@@ -218,7 +232,7 @@ __device__ __forceinline__ void release_s(const SoftmaxCtx& cx) {
 // reference m and denominator l. Writes P(j) to tensor memory, rescales O when the
 // reference moves, starts loading S(j+1) and signals the MMA issuers. Returns false when a
 // wait timed out or the CTA is aborting (the result is the same in all lanes of a warp).
-template <bool BF16, bool kMasked>
+template <bool BF16, bool kMasked, int D>
 __device__ __forceinline__ bool softmax_step(const SoftmaxCtx& cx, uint32_t (&su)[kBN], float& m,
                                              float& l, int j, int nX) {
     // The scores stay in the registers tcgen05.ld filled (as bit patterns); masked keys get
@@ -266,7 +280,7 @@ __device__ __forceinline__ bool softmax_step(const SoftmaxCtx& cx, uint32_t (&su
         // 16-column pieces so it adds few registers to the step.
         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
-        for (int h = 0; h < 4; ++h) {
+        for (int h = 0; h < D / 16; ++h) {
             uint32_t ou[16];
             tmem_ld_x16(cx.tO + 16 * h, ou);
             tmem_ld_wait();
@@ -282,61 +296,81 @@ __device__ __forceinline__ bool softmax_step(const SoftmaxCtx& cx, uint32_t (&su
     l += tile_sum;
     const bool more = j + 1 < nX;
     bool ok = true;
-    if (more) {  // the next scores start moving while P drains
-        ok = warp_wait(cx.bar_s_full, (j + 1) & 1, cx.abort_flag);
-        if (ok) load_s(cx, su);
+    if constexpr (Lay<D>::kPOverS) {
+        // P_X(j) sits over S_X's columns, so S_X(j+1) follows PV_X(j): hand P over first.
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (cx.lane == 0) mbar_arrive(cx.bar_p_full);
+        if (more) {
+            ok = warp_wait(cx.bar_s_full, (j + 1) & 1, cx.abort_flag);
+            if (ok) {
+                load_s(cx, su);
+                release_s(cx);
+            }
+        }
+    } else {
+        if (more) {  // the next scores start moving while P drains
+            ok = warp_wait(cx.bar_s_full, (j + 1) & 1, cx.abort_flag);
+            if (ok) load_s(cx, su);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (cx.lane == 0) mbar_arrive(cx.bar_p_full);
+        if (more && ok) release_s(cx);
     }
-    tmem_st_wait();
-    tc_fence_before();
-    __syncwarp();
-    if (cx.lane == 0) mbar_arrive(cx.bar_p_full);
-    if (more && ok) release_s(cx);
     return ok;
 }
 
-// S_X(j) = Q_X K_j^T : M=128, N=128, K=64 as four K=16 steps (32 bytes each).
-template <bool BF16>
+// S_X(j) = Q_X K_j^T : M=128, N=128, K=D as D/16 steps of K=16 (32 bytes of a 128-byte row;
+// steps 4..7 of D = 128 read the second column block).
+template <bool BF16, int D>
 __device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sQx, uint32_t sKs, int X, uint32_t bar_s_full) {
     constexpr uint32_t kIdescQK = idesc_f16(BF16, kBM, kBN, false, false);
 #pragma unroll
-    for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint64_t a = smem_desc_sw128(sQx + 32 * kk, 16, 1024);
-        const uint64_t b = smem_desc_sw128(sKs + 32 * kk, 16, 1024);
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = static_cast<uint32_t>((kk >> 2) * kBlockBytes + 32 * (kk & 3));
+        const uint64_t a = smem_desc_sw128(sQx + off, 16, 1024);
+        const uint64_t b = smem_desc_sw128(sKs + off, 16, 1024);
         umma_ss(tmem + kColS + 128u * X, a, b, kIdescQK, kk > 0 ? 1u : 0u);
     }
     umma_commit(bar_s_full);
 }
 
-// O_X += P_X V_j : M=128, N=64, K=128 as eight K=16 steps (16 keys = 2048 bytes of V), P from
-// tensor memory.
-template <bool BF16>
+// O_X += P_X V_j : M=128, N=D, K=128 as eight K=16 steps (16 keys = 2048 bytes of each V
+// column block), P from tensor memory. V is the MN-major operand (dims contiguous); for D = 128
+// its two 64-dim column blocks are 16 KiB apart, the descriptor's leading byte offset.
+template <bool BF16, int D>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sVs, int X, bool accumulate, uint32_t bar_o_ready) {
-    constexpr uint32_t kIdescPV = idesc_f16(BF16, kBM, kD, false, true);
+    constexpr uint32_t kIdescPV = idesc_f16(BF16, kBM, D, false, true);
+    constexpr uint32_t kLbo = D == 64 ? 16u : static_cast<uint32_t>(kBlockBytes);
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk) {
-        const uint64_t b = smem_desc_sw128(sVs + 2048 * kk, 16, 1024);
-        umma_ts(tmem + kColO + 64u * X, tmem + kColP + 64u * X + 8u * kk, b, kIdescPV,
+        const uint64_t b = smem_desc_sw128(sVs + 2048 * kk, kLbo, 1024);
+        umma_ts(tmem + kColO + static_cast<uint32_t>(D) * X, tmem + Lay<D>::colP(X) + 8u * kk, b, kIdescPV,
                 (accumulate || kk > 0) ? 1u : 0u);
     }
     umma_commit(bar_o_ready);
 }
 
-template <bool BF16>
+template <bool BF16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                        const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
+    using L = Lay<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const gbase = smem_raw + (base - raw);
 
-    const uint32_t sQ = base + kOffQ;
-    const uint32_t sK = base + kOffK;
-    const uint32_t sV = base + kOffV;
-    auto bar = [&](int i) -> uint32_t { return base + kOffBar + 8u * static_cast<uint32_t>(i); };
-    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffSlot);
-    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + kOffAbort);
+    const uint32_t sQ = base + L::kOffQ;
+    const uint32_t sK = base + L::kOffK;
+    const uint32_t sV = base + L::kOffV;
+    auto bar = [&](int i) -> uint32_t { return base + L::kOffBar + 8u * static_cast<uint32_t>(i); };
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kOffSlot);
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + L::kOffAbort);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -355,21 +389,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- setup: barriers (thread 0), tensor memory (S-issuer warp) ----
     if (threadIdx.x == 0) {
-        mbar_init(bar(kBarQFull), 1);
-        for (int s = 0; s < kKStages; ++s) {
-            mbar_init(bar(kBarKFull + s), 1);
-            mbar_init(bar(kBarKEmpty + s), 2);  // one release per query tile
+        mbar_init(bar(L::kBarQFull), 1);
+        for (int s = 0; s < L::kKStages; ++s) {
+            mbar_init(bar(L::kBarKFull + s), 1);
+            mbar_init(bar(L::kBarKEmpty + s), 2);  // one release per query tile
         }
-        for (int s = 0; s < kVStages; ++s) {
-            mbar_init(bar(kBarVFull + s), 1);
-            mbar_init(bar(kBarVEmpty + s), 2);
+        for (int s = 0; s < L::kVStages; ++s) {
+            mbar_init(bar(L::kBarVFull + s), 1);
+            mbar_init(bar(L::kBarVEmpty + s), 2);
         }
         for (int x = 0; x < 2; ++x) {
-            mbar_init(bar(kBarSFull + x), 1);
-            mbar_init(bar(kBarSFree + x), 4);
-            mbar_init(bar(kBarPFull + x), 4);
-            mbar_init(bar(kBarOReady + x), 1);
-            mbar_init(bar(kBarDrain + x), 1);
+            mbar_init(bar(L::kBarSFull + x), 1);
+            mbar_init(bar(L::kBarSFree + x), 4);
+            mbar_init(bar(L::kBarPFull + x), 4);
+            mbar_init(bar(L::kBarOReady + x), 1);
+            mbar_init(bar(L::kBarDrain + x), 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -390,9 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nX = X ? nB : nA;
         const int row = (X ? rowB : rowA) + ((warp & 3) << 5) + lane;
         const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) << 5) << 16;
-        const SoftmaxCtx cx{tmem + lane_addr + kColS + 128u * X, tmem + lane_addr + kColO + 64u * X,
-                            tmem + lane_addr + kColP + 64u * X, bar(kBarSFull + X), bar(kBarSFree + X),
-                            bar(kBarPFull + X), bar(kBarOReady + X), abort_flag, p.scale_log2,
+        const SoftmaxCtx cx{tmem + lane_addr + kColS + 128u * X, tmem + lane_addr + kColO + static_cast<uint32_t>(D) * X,
+                            tmem + lane_addr + L::colP(X), bar(L::kBarSFull + X), bar(L::kBarSFree + X),
+                            bar(L::kBarPFull + X), bar(L::kBarOReady + X), abort_flag, p.scale_log2,
                             p.causal ? min(row + 1, N) : N, lane};
         float m = -INFINITY;  // reference max of scaled scores (base-2 units), possibly stale
         float l = 0.f;        // running denominator relative to m
@@ -409,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Only a query tile's last key tile can hold masked keys (the causal diagonal or
         // keys past N), so the loop runs mask-free and the last step is peeled off.
-        for (int j = 0; ok && j + 1 < nX; ++j) ok = softmax_step<BF16, false>(cx, su, m, l, j, nX);
-        if (ok && nX > 0) ok = softmax_step<BF16, true>(cx, su, m, l, nX - 1, nX);
+        for (int j = 0; ok && j + 1 < nX; ++j) ok = softmax_step<BF16, false, D>(cx, su, m, l, j, nX);
+        if (ok && nX > 0) ok = softmax_step<BF16, true, D>(cx, su, m, l, nX - 1, nX);
 
         // ---- epilogue: O / l, rounded to the output type, rows >= N not stored ----
         if (ok && nX > 0) {
@@ -418,9 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const float inv = 1.f / l;
                 uint16_t* const orow = reinterpret_cast<uint16_t*>(p.o) +
-                                       (static_cast<int64_t>(bh) * N + row) * kD;
+                                       (static_cast<int64_t>(bh) * N + row) * D;
 #pragma unroll 1
-                for (int h = 0; h < 4; ++h) {
+                for (int h = 0; h < D / 16; ++h) {
                     uint32_t ou[16];
                     tmem_ld_x16(cx.tO + 16 * h, ou);
                     tmem_ld_wait();
@@ -448,50 +482,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmap_q);
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
-            mbar_arrive_expect_tx(bar(kBarQFull), (nB > 0 ? 2 : 1) * kTileBytes);
-            tma_load_3d(sQ, &tmap_q, 0, rowA, bh, bar(kBarQFull));
-            if (nB > 0) tma_load_3d(sQ + kTileBytes, &tmap_q, 0, rowB, bh, bar(kBarQFull));
+            mbar_arrive_expect_tx(bar(L::kBarQFull), (nB > 0 ? 2 : 1) * L::kTileBytes);
+#pragma unroll
+            for (int c = 0; c < L::kBlocks; ++c) {
+                tma_load_3d(sQ + c * kBlockBytes, &tmap_q, 64 * c, rowA, bh, bar(L::kBarQFull));
+                if (nB > 0) tma_load_3d(sQ + L::kTileBytes + c * kBlockBytes, &tmap_q, 64 * c, rowB, bh, bar(L::kBarQFull));
+            }
             // K runs ahead of V: K_j is needed by S(j) a step before V_j is needed by PV(j).
             int kissued = 0, vissued = 0;
             bool ok = true;
             for (int j = 0; ok && j < nmax; ++j) {
-                const int sk = j % kKStages;
-                if (!(ok = mbar_wait(bar(kBarKEmpty + sk), ((j / kKStages) & 1) ^ 1, abort_flag, kWaitTimeoutNs)))
+                const int sk = j % L::kKStages;
+                if (!(ok = mbar_wait(bar(L::kBarKEmpty + sk), ((j / L::kKStages) & 1) ^ 1, abort_flag, kWaitTimeoutNs)))
                     break;
-                mbar_arrive_expect_tx(bar(kBarKFull + sk), kTileBytes);
-                tma_load_3d(sK + sk * kTileBytes, &tmap_k, 0, j * kBN, bh, bar(kBarKFull + sk));
+                mbar_arrive_expect_tx(bar(L::kBarKFull + sk), L::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < L::kBlocks; ++c)
+                    tma_load_3d(sK + sk * L::kTileBytes + c * kBlockBytes, &tmap_k, 64 * c, j * kBN, bh,
+                                bar(L::kBarKFull + sk));
                 kissued = j + 1;
                 for (; vissued < j; ++vissued) {  // V_{j-1} after K_j
-                    const int sv = vissued % kVStages;
-                    if (!(ok = mbar_wait(bar(kBarVEmpty + sv), ((vissued / kVStages) & 1) ^ 1, abort_flag,
+                    const int sv = vissued % L::kVStages;
+                    if (!(ok = mbar_wait(bar(L::kBarVEmpty + sv), ((vissued / L::kVStages) & 1) ^ 1, abort_flag,
                                          kWaitTimeoutNs)))
                         break;
-                    mbar_arrive_expect_tx(bar(kBarVFull + sv), kTileBytes);
-                    tma_load_3d(sV + sv * kTileBytes, &tmap_v, 0, vissued * kBN, bh, bar(kBarVFull + sv));
+                    mbar_arrive_expect_tx(bar(L::kBarVFull + sv), L::kTileBytes);
+#pragma unroll
+                    for (int c = 0; c < L::kBlocks; ++c)
+                        tma_load_3d(sV + sv * L::kTileBytes + c * kBlockBytes, &tmap_v, 64 * c, vissued * kBN, bh,
+                                    bar(L::kBarVFull + sv));
                 }
             }
             for (; ok && vissued < nmax; ++vissued) {
-                const int sv = vissued % kVStages;
-                if (!(ok = mbar_wait(bar(kBarVEmpty + sv), ((vissued / kVStages) & 1) ^ 1, abort_flag,
+                const int sv = vissued % L::kVStages;
+                if (!(ok = mbar_wait(bar(L::kBarVEmpty + sv), ((vissued / L::kVStages) & 1) ^ 1, abort_flag,
                                      kWaitTimeoutNs)))
                     break;
-                mbar_arrive_expect_tx(bar(kBarVFull + sv), kTileBytes);
-                tma_load_3d(sV + sv * kTileBytes, &tmap_v, 0, vissued * kBN, bh, bar(kBarVFull + sv));
+                mbar_arrive_expect_tx(bar(L::kBarVFull + sv), L::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < L::kBlocks; ++c)
+                    tma_load_3d(sV + sv * L::kTileBytes + c * kBlockBytes, &tmap_v, 64 * c, vissued * kBN, bh,
+                                bar(L::kBarVFull + sv));
             }
             if (!ok) raise_abort(abort_flag);
             // Every copy issued must have landed before the CTA may exit. In normal operation
             // they were all consumed already and these waits return at once.
-            mbar_wait(bar(kBarQFull), 0, nullptr, kDrainTimeoutNs);
-            for (int j = max(0, kissued - kKStages); j < kissued; ++j)
-                mbar_wait(bar(kBarKFull + j % kKStages), (j / kKStages) & 1, nullptr, kDrainTimeoutNs);
-            for (int j = max(0, vissued - kVStages); j < vissued; ++j)
-                mbar_wait(bar(kBarVFull + j % kVStages), (j / kVStages) & 1, nullptr, kDrainTimeoutNs);
+            mbar_wait(bar(L::kBarQFull), 0, nullptr, kDrainTimeoutNs);
+            for (int j = max(0, kissued - L::kKStages); j < kissued; ++j)
+                mbar_wait(bar(L::kBarKFull + j % L::kKStages), (j / L::kKStages) & 1, nullptr, kDrainTimeoutNs);
+            for (int j = max(0, vissued - L::kVStages); j < vissued; ++j)
+                mbar_wait(bar(L::kBarVFull + j % L::kVStages), (j / L::kVStages) & 1, nullptr, kDrainTimeoutNs);
         } else if (warp == kSIssuerWarp && lane == 0) {
             // ============================ S issuer: QK^T ============================
             // S_X(j) goes out as soon as K_j has landed and (j > 0) softmax X has copied
             // S_X(j-1) out of tensor memory; the two tiles progress independently. Each tile
             // releases K_j once (twice when the other tile does not read K_j).
-            bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, kWaitTimeoutNs);
+            bool ok = mbar_wait(bar(L::kBarQFull), 0, abort_flag, kWaitTimeoutNs);
             int ns0 = 0, ns1 = 0;
             uint64_t idle_since = 0;
             uint32_t polls = 0;
@@ -501,13 +547,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int X = 0; X < 2; ++X) {
                     int& j = X ? ns1 : ns0;
                     const int nX = X ? nB : nA, nO = X ? nA : nB;
-                    if (j < nX && mbar_test(bar(kBarKFull + j % kKStages), (j / kKStages) & 1) &&
-                        (j == 0 || mbar_test(bar(kBarSFree + X), (j - 1) & 1))) {
+                    if (j < nX && mbar_test(bar(L::kBarKFull + j % L::kKStages), (j / L::kKStages) & 1) &&
+                        (j == 0 || (mbar_test(bar(L::kBarSFree + X), (j - 1) & 1) &&
+                                    (!L::kPOverS || mbar_test(bar(L::kBarOReady + X), (j - 1) & 1))))) {
                         tc_fence_after();
-                        issue_s<BF16>(tmem, sQ + X * kTileBytes, sK + (j % kKStages) * kTileBytes, X,
-                                      bar(kBarSFull + X));
-                        umma_commit(bar(kBarKEmpty + j % kKStages));
-                        if (j >= nO) umma_commit(bar(kBarKEmpty + j % kKStages));
+                        issue_s<BF16, D>(tmem, sQ + X * L::kTileBytes, sK + (j % L::kKStages) * L::kTileBytes, X,
+                                      bar(L::kBarSFull + X));
+                        umma_commit(bar(L::kBarKEmpty + j % L::kKStages));
+                        if (j >= nO) umma_commit(bar(L::kBarKEmpty + j % L::kKStages));
                         ++j;
                         progressed = true;
                     }
@@ -525,8 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) raise_abort(abort_flag);
-            umma_commit(bar(kBarDrain + 0));  // no S product may still run at teardown
-            mbar_wait(bar(kBarDrain + 0), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+            umma_commit(bar(L::kBarDrain + 0));  // no S product may still run at teardown
+            mbar_wait(bar(L::kBarDrain + 0), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         } else if (warp == kPVIssuerWarp && lane == 0) {
             // ============================== PV issuer ==============================
             // PV_X(j) goes out as soon as V_j has landed and softmax X has written P_X(j); the
@@ -541,12 +588,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int X = 0; X < 2; ++X) {
                     int& j = X ? np1 : np0;
                     const int nX = X ? nB : nA, nO = X ? nA : nB;
-                    if (j < nX && mbar_test(bar(kBarVFull + j % kVStages), (j / kVStages) & 1) &&
-                        mbar_test(bar(kBarPFull + X), j & 1)) {
+                    if (j < nX && mbar_test(bar(L::kBarVFull + j % L::kVStages), (j / L::kVStages) & 1) &&
+                        mbar_test(bar(L::kBarPFull + X), j & 1)) {
                         tc_fence_after();
-                        issue_pv<BF16>(tmem, sV + (j % kVStages) * kTileBytes, X, j > 0, bar(kBarOReady + X));
-                        umma_commit(bar(kBarVEmpty + j % kVStages));
-                        if (j >= nO) umma_commit(bar(kBarVEmpty + j % kVStages));
+                        issue_pv<BF16, D>(tmem, sV + (j % L::kVStages) * L::kTileBytes, X, j > 0, bar(L::kBarOReady + X));
+                        umma_commit(bar(L::kBarVEmpty + j % L::kVStages));
+                        if (j >= nO) umma_commit(bar(L::kBarVEmpty + j % L::kVStages));
                         ++j;
                         progressed = true;
                     }
@@ -564,8 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) raise_abort(abort_flag);
-            umma_commit(bar(kBarDrain + 1));  // no PV product may still run at teardown
-            mbar_wait(bar(kBarDrain + 1), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+            umma_commit(bar(L::kBarDrain + 1));  // no PV product may still run at teardown
+            mbar_wait(bar(L::kBarDrain + 1), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         }
     }
 
@@ -600,15 +647,16 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// [BH][N][64] 16-bit tensor; boxes of 128 rows x 64 values (128 bytes, the swizzle span).
-bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, bool bf16) {
+// [BH][N][D] 16-bit tensor; boxes of 128 rows x 64 values (128 bytes, the swizzle span), one
+// per 64-dim column block.
+bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t D, bool bf16) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(N),
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
-                                   static_cast<cuuint64_t>(N) * kD * 2};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kBM), 1};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                   static_cast<cuuint64_t>(N) * D * 2};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(kBM), 1};
     const cuuint32_t estride[3] = {1, 1, 1};
     return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                const_cast<void*>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -616,13 +664,14 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, bool bf1
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool BF16>
+template <bool BF16, int D>
 int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
                 int64_t N, bool causal, cudaStream_t stream) {
+    constexpr int kSmemBytes = Lay<D>::kSmemBytes;
     // The register split assumes the launch allocation; a smaller one could leave the
     // softmax groups waiting for registers forever, so it is refused instead.
     cudaFuncAttributes fattr;
-    if (cudaFuncGetAttributes(&fattr, attn_fwd_tc_kernel<BF16>) != cudaSuccess ||
+    if (cudaFuncGetAttributes(&fattr, attn_fwd_tc_kernel<BF16, D>) != cudaSuccess ||
         fattr.numRegs < kRegsLaunch) {
         if (std::getenv("ATTN_DEBUG"))
             std::fprintf(stderr, "attn: kernel has %d registers per thread, the register split needs %d\n",
@@ -630,11 +679,11 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
         return ATTN_ERR_LAUNCH;
     }
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, BH, N, BF16) || !make_map(&mk, k, BH, N, BF16) ||
-        !make_map(&mv, v, BH, N, BF16))
+    if (!make_map(&mq, q, BH, N, D, BF16) || !make_map(&mk, k, BH, N, D, BF16) ||
+        !make_map(&mv, v, BH, N, D, BF16))
         return ATTN_ERR_DEVICE;
     // The attribute is per device; setting it on every call is cheap and thread-safe.
-    const cudaError_t aerr = cudaFuncSetAttribute(attn_fwd_tc_kernel<BF16>,
+    const cudaError_t aerr = cudaFuncSetAttribute(attn_fwd_tc_kernel<BF16, D>,
                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (aerr != cudaSuccess) {
         if (std::getenv("ATTN_DEBUG"))
@@ -649,10 +698,10 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     prm.BH = static_cast<int>(BH);
     prm.num_pairs = static_cast<int>((N + 2 * kBM - 1) / (2 * kBM));
     prm.causal = causal ? 1 : 0;
-    prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
+    prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     const int64_t blocks = static_cast<int64_t>(prm.num_pairs) * BH;
     if (blocks > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
-    attn_fwd_tc_kernel<BF16><<<static_cast<unsigned>(blocks), kThreads, kSmemBytes, stream>>>(
+    attn_fwd_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, kSmemBytes, stream>>>(
         mq, mk, mv, prm);
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess && std::getenv("ATTN_DEBUG"))
@@ -663,10 +712,15 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
 }  // namespace
 
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
-                  int64_t N, bool causal, bool bf16, int /*num_sms*/, cudaStream_t stream) {
+                  int64_t N, int64_t d, bool causal, bool bf16, int /*num_sms*/, cudaStream_t stream) {
     if (N > 0x7FFFFFFFll - 2 * kBM || BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
-    return bf16 ? launch_impl<true>(q, k, v, o, lse, BH, N, causal, stream)
-                : launch_impl<false>(q, k, v, o, lse, BH, N, causal, stream);
+    if (d == 64)
+        return bf16 ? launch_impl<true, 64>(q, k, v, o, lse, BH, N, causal, stream)
+                    : launch_impl<false, 64>(q, k, v, o, lse, BH, N, causal, stream);
+    if (d == 128)
+        return bf16 ? launch_impl<true, 128>(q, k, v, o, lse, BH, N, causal, stream)
+                    : launch_impl<false, 128>(q, k, v, o, lse, BH, N, causal, stream);
+    return ATTN_ERR_UNSUPPORTED;
 }
 
 int tc_device_error(cudaStream_t stream, bool clear, unsigned* err) {

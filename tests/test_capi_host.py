@@ -81,6 +81,18 @@ def test_lse_argument_checks(lib, lse, want):
     assert lib.attn_fwd_lse(P, P * 3, P * 5, P * 9, lse, 1, 1, 8, 64, 0, 1, None) == want
 
 
+def test_head_width_128_is_a_forward_only_width(lib):
+    # d = 128 passes the forward's checks (and then needs the device), the other entry points
+    # refuse it before touching one.
+    if not __import__("torch").cuda.is_available():
+        assert lib.attn_fwd(P, P * 3, P * 5, P * 9, 1, 1, 8, 128, 0, 1, None) == 5
+        assert lib.attn_fwd_lse(P, P * 3, P * 5, P * 9, P * 20, 1, 1, 8, 128, 0, 1, None) == 5
+    assert lib.attn_fwd(P, P * 3, P * 5, P * 9, 1, 1, 8, 96, 0, 1, None) == 2
+    assert lib.attn_fwd(P, P * 3, P * 5, P * 9, 1, 1, 8, 256, 0, 1, None) == 2
+    assert lib.attn_bwd(P, P * 3, P * 5, P * 7, P * 9, P * 11, P * 13, P * 15, P * 17, 1, 1, 8, 128, 0, 1, None) == 2
+    assert lib.attn_fwd_materialized(P, P * 3, P * 5, P * 9, P * 40, 1 << 20, 1, 1, 8, 128, 0, 1, None) == 2
+
+
 def test_lse_shares_the_forward_checks(lib):
     assert lib.attn_fwd_lse(P, P, P, P * 9, P * 20, 1, 1, 8, 32, 0, 1, None) == 2       # d != 64
     assert lib.attn_fwd_lse(None, None, None, None, None, 0, 1, 8, 64, 0, 1, None) == 0  # no work

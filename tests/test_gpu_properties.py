@@ -120,7 +120,8 @@ def test_error_statuses_on_device():
     assert lib.attn_fwd(*base, 1, 1, 64, 64, 0, 1, None) == 0
     assert lib.attn_fwd(base[0] + 2, *base[1:], 1, 1, 60, 64, 0, 1, None) == 3
     assert lib.attn_fwd(*base[:3], base[0], 1, 1, 64, 64, 0, 1, None) == 4
-    assert lib.attn_fwd(*base, 1, 1, 64, 128, 0, 1, None) == 2
+    assert lib.attn_fwd(*base, 1, 1, 64, 96, 0, 1, None) == 2   # head width neither 64 nor 128
+    assert lib.attn_fwd(*base, 1, 1, 32, 128, 0, 1, None) == 0  # d = 128 over the same bytes
     with pytest.raises(fa.AttnError):
         fa.attn_fwd(x, x, x, out=x)
     torch.cuda.synchronize()

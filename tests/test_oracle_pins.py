@@ -128,7 +128,7 @@ def _decimal_attention(q, k, v, causal):
 
 
 @pytest.mark.parametrize("causal", [0, 1])
-@pytest.mark.parametrize("N,d", [(1, 8), (2, 4), (5, 16), (6, 64)])
+@pytest.mark.parametrize("N,d", [(1, 8), (2, 4), (5, 16), (6, 64), (3, 128)])
 def test_matches_decimal_brute_force(causal, N, d):
     q, k, v = si.qkv(41 + N, 1, 1, N, d)
     got = oracle.attn_fwd(q, k, v, causal)[0, 0]
@@ -137,7 +137,8 @@ def test_matches_decimal_brute_force(causal, N, d):
 
 
 @pytest.mark.parametrize("causal", [0, 1])
-@pytest.mark.parametrize("shape", [(2, 3, 1, 64), (2, 3, 100, 64), (1, 2, 257, 64), (1, 1, 33, 16)])
+@pytest.mark.parametrize("shape", [(2, 3, 1, 64), (2, 3, 100, 64), (1, 2, 257, 64), (1, 1, 33, 16),
+                                   (1, 2, 130, 128)])
 @pytest.mark.parametrize("qk_scale", [1.0, 8.0])
 def test_matches_torch_float64_sdpa(causal, shape, qk_scale):
     torch = pytest.importorskip("torch")
