@@ -46,7 +46,7 @@ typedef enum {
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1, /* null pointer with work to do, negative size, causal not 0/1 */
-    ATTN_ERR_UNSUPPORTED = 2, /* d != 64, unknown dtype, or a size beyond the stated limits */
+    ATTN_ERR_UNSUPPORTED = 2, /* head width not taken, unknown dtype, or a size beyond the limits */
     ATTN_ERR_ALIGN = 3,       /* a tensor or workspace pointer not 16-byte aligned */
     ATTN_ERR_ALIAS = 4,       /* o overlaps q, k, v (or the workspace overlaps a tensor) */
     ATTN_ERR_DEVICE = 5,      /* current device is not compute capability 10.3, or a CUDA
@@ -67,7 +67,9 @@ typedef enum {
  *             q, k or v; every element is written
  *   B, H, N : sizes >= 0, N <= ATTN_MAX_N, B*H < 2^31. B*H == 0 or N == 0 is a successful
  *             no-op (pointers may then be NULL)
- *   d       : head width; only 64 is supported (ATTN_ERR_UNSUPPORTED otherwise)
+ *   d       : head width, 64 or 128 (ATTN_ERR_UNSUPPORTED otherwise). The pages fix 64; 128
+ *             is the other common width (scale 1/sqrt(128)). attn_fwd, attn_fwd_lse and
+ *             attn_fwd_kvcache take both; attn_bwd and the materialised path take 64.
  *   causal  : 0 (every key visible) or 1 (key j visible to query i iff j <= i)
  *   dtype   : attn_dtype_t. bf16/f16 inputs are multiplied on tcgen05 tensor cores with
  *             fp32 accumulation; the probabilities are rounded to the input type before
@@ -149,7 +151,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  *   workspace     : device pointer, 256-byte aligned, caller-owned fp32 scratch for the pieces'
  *                   partial results (contents on entry ignored, on exit unspecified); may be
  *                   NULL when no workspace is needed. It must not overlap any tensor.
- *   workspace_bytes: its size; attn_kvcache_workspace_bytes(B, H, Nq, Nk, num_splits, dtype)
+ *   workspace_bytes: its size; attn_kvcache_workspace_bytes(B, H, Nq, Nk, d, num_splits, dtype)
  *                   with the same device current is enough; less returns ATTN_ERR_WORKSPACE
  *   Nq, Nk        : 0 <= Nq <= Nk <= ATTN_MAX_N, Nq <= 8 * 65535; Nq == 0 or B*H == 0 is a
  *                   successful no-op
@@ -158,7 +160,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  *                   cut at head boundaries; 1 .. ATTN_KV_MAX_SPLITS — every (head, query
  *                   group) is cut into that many equal shares (shares past the last key are
  *                   empty and carry weight 0 in the merge).
- *   other arguments: as attn_fwd (d == 64; dtype f32, bf16 or f16; causal 0/1).
+ *   d             : head width, 64 or 128 (scale 1/sqrt(d))
+ *   other arguments: as attn_fwd (dtype f32, bf16 or f16; causal 0/1).
  */
 #define ATTN_KV_MAX_SPLITS 1024
 int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
@@ -170,7 +173,8 @@ int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float
  * balanced plan gives one head on the current device; 0 when every head is a single piece.
  * Returns 0 also for invalid sizes or dtype, on overflow, or (num_splits == 0) when the
  * current device cannot be queried. */
-size_t attn_kvcache_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int num_splits, int dtype);
+size_t attn_kvcache_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int num_splits,
+                                    int dtype);
 
 /*
  * attn_fwd_materialized — the same result by the materialised path of attention.cu
@@ -235,7 +239,7 @@ int attn_device_status(void* stream, int clear);
 const char* attn_status_string(int status);
 
 /* ABI version of this header: (major << 16) | minor (1.1 added attn_fwd_lse, 1.2 attn_bwd,
- * 1.3 attn_fwd_kvcache). */
+ * 1.3 attn_fwd_kvcache, 1.4 head width 128 for the forward entry points). */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

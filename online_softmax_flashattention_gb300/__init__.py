@@ -73,7 +73,7 @@ def raw():
             lib.attn_bwd.restype = ci
             lib.attn_fwd_kvcache.argtypes = [vp, vp, vp, vp, vp, vp, sz, i64, i64, i64, i64, i64, ci, ci, ci, vp]
             lib.attn_fwd_kvcache.restype = ci
-            lib.attn_kvcache_workspace_bytes.argtypes = [i64, i64, i64, i64, ci, ci]
+            lib.attn_kvcache_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, ci, ci]
             lib.attn_kvcache_workspace_bytes.restype = sz
             lib.attn_fwd_materialized.argtypes = [vp, vp, vp, vp, vp, sz, i64, i64, i64, i64, ci, ci, vp]
             lib.attn_fwd_materialized.restype = ci
@@ -187,15 +187,16 @@ ATTN_KV_MAX_SPLITS = 1024  # include/attn.h: most shares the key range may be cu
 
 
 def attn_kvcache_workspace_bytes(B: int, H: int, Nq: int, Nk: int, num_splits: int = 0,
-                                 dtype: torch.dtype = torch.bfloat16, device: torch.device | int | None = None) -> int:
+                                 dtype: torch.dtype = torch.bfloat16, device: torch.device | int | None = None,
+                                 d: int = 64) -> int:
     """Workspace bytes :func:`attn_fwd_kvcache` needs; for ``num_splits == 0`` (balanced) the plan
     depends on the device, which is queried with ``device`` current."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index or 0) \
         if num_splits == 0 else None
     if dev is None:
-        return int(raw().attn_kvcache_workspace_bytes(B, H, Nq, Nk, num_splits, _DTYPES[dtype]))
+        return int(raw().attn_kvcache_workspace_bytes(B, H, Nq, Nk, d, num_splits, _DTYPES[dtype]))
     with torch.cuda.device(dev):
-        return int(raw().attn_kvcache_workspace_bytes(B, H, Nq, Nk, num_splits, _DTYPES[dtype]))
+        return int(raw().attn_kvcache_workspace_bytes(B, H, Nq, Nk, d, num_splits, _DTYPES[dtype]))
 
 
 def attn_fwd_kvcache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = True,
@@ -234,7 +235,7 @@ def attn_fwd_kvcache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: 
     lib = raw()
     with torch.cuda.device(q.device):
         if workspace is None:
-            need = int(lib.attn_kvcache_workspace_bytes(B, H, Nq, Nk, int(num_splits), _DTYPES[q.dtype]))
+            need = int(lib.attn_kvcache_workspace_bytes(B, H, Nq, Nk, d, int(num_splits), _DTYPES[q.dtype]))
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
         st = lib.attn_fwd_kvcache(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                   lse.data_ptr() if want_lse else None, workspace.data_ptr(),

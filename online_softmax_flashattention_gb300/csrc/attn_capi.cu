@@ -136,12 +136,14 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
     return attn::launch_bwd_tc(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal != 0, dtype == ATTN_BF16, s);
 }
 
-size_t attn_kvcache_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int num_splits, int dtype) {
+size_t attn_kvcache_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int num_splits,
+                                    int dtype) {
     if (B < 0 || H < 0 || Nq < 0 || Nk < Nq || B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return 0;
     if (dtype != ATTN_F32 && dtype != ATTN_BF16 && dtype != ATTN_F16) return 0;
+    if (d != kHeadDim && d != 2 * kHeadDim) return 0;
     int num_sms = 0;
     if (num_splits == 0 && check_device(&num_sms) != ATTN_OK) return 0;
-    return attn::decode_workspace_bytes(B * H, Nq, Nk, num_splits, dtype, num_sms);
+    return attn::decode_workspace_bytes(B * H, Nq, Nk, d, num_splits, dtype, num_sms);
 }
 
 int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
@@ -151,7 +153,7 @@ int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
     if (Nq > Nk || num_splits < 0) return ATTN_ERR_INVALID_ARG;
     if (dtype != ATTN_F32 && dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_UNSUPPORTED;
-    if (d != kHeadDim) return ATTN_ERR_UNSUPPORTED;
+    if (d != kHeadDim && d != 2 * kHeadDim) return ATTN_ERR_UNSUPPORTED;
     if (Nk > ATTN_MAX_N || Nq > 8 * 65535ll || num_splits > ATTN_KV_MAX_SPLITS) return ATTN_ERR_UNSUPPORTED;
     if (B > 0x7FFFFFFFll || H > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     const int64_t BH = B * H;
@@ -160,8 +162,8 @@ int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float
     if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return ATTN_ERR_ALIGN;
     const size_t esz = elem_size(dtype);
-    const size_t qbytes = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * kHeadDim * esz;
-    const size_t kbytes = static_cast<size_t>(BH) * static_cast<size_t>(Nk) * kHeadDim * esz;
+    const size_t qbytes = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * static_cast<size_t>(d) * esz;
+    const size_t kbytes = static_cast<size_t>(BH) * static_cast<size_t>(Nk) * static_cast<size_t>(d) * esz;
     if (overlap(o, qbytes, q, qbytes) || overlap(o, qbytes, k, kbytes) || overlap(o, qbytes, v, kbytes))
         return ATTN_ERR_ALIAS;
     const size_t lbytes = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * sizeof(float);
@@ -176,7 +178,7 @@ int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float
     int num_sms = 0;
     int st = ATTN_OK;
     if (num_splits == 0 && (st = check_device(&num_sms)) != ATTN_OK) return st;
-    const size_t need = attn::decode_workspace_bytes(BH, Nq, Nk, num_splits, dtype, num_sms);
+    const size_t need = attn::decode_workspace_bytes(BH, Nq, Nk, d, num_splits, dtype, num_sms);
     // (A balanced plan of one piece per segment needs none; the launch re-checks the size.)
     const bool needs_ws = num_splits > 1 || (num_splits == 0 && need > 0);
     if (needs_ws) {
@@ -190,7 +192,7 @@ int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float
     }
     if (num_splits != 0 && (st = check_device(&num_sms)) != ATTN_OK) return st;
     if (inject_launch_fault()) return ATTN_ERR_LAUNCH;
-    return attn::launch_decode(q, k, v, o, lse, workspace, workspace_bytes, BH, Nq, Nk, causal != 0, dtype,
+    return attn::launch_decode(q, k, v, o, lse, workspace, workspace_bytes, BH, Nq, Nk, d, causal != 0, dtype,
                                num_splits, num_sms, static_cast<cudaStream_t>(stream));
 }
 

@@ -43,6 +43,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
@@ -50,11 +51,6 @@
 namespace attn {
 namespace {
 
-constexpr int kD = 64;
-constexpr int kCW = 4;                  // consumer warps
-constexpr int kThreads = 32 * (kCW + 1);
-constexpr int kRows = 32 * kCW;         // keys per tile
-constexpr int kProducerWarp = kCW;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr uint64_t kDrainTimeoutNs = 100000000ull;
 
@@ -66,35 +62,64 @@ __device__ __forceinline__ float ex2f(float x) {
     return y;
 }
 
-template <typename T>
-struct Elem;
-template <>
-struct Elem<float> {
+// Per element type and head width D (64 or 128): consumer warps (32 keys each, so a tile holds
+// 32 * kCW keys), ring depth, and how many 128-byte boxes make one row. Every configuration
+// keeps about 192 KB of loads in flight per SM (two CTAs of 96 KB, or one of 192 KB).
+template <typename T, int D>
+struct Cfg {
+    static constexpr int kEsz = static_cast<int>(sizeof(T));
+    static constexpr int kCW = (kEsz == 4 && D == 128) ? 2 : 4;
     static constexpr int kStages = 3;
-    static constexpr int kHalves = 2;  // a 64-value fp32 row is two 128-byte boxes
-};
-template <>
-struct Elem<__nv_bfloat16> {
-    static constexpr int kStages = 3;
-    static constexpr int kHalves = 1;
-};
-template <>
-struct Elem<__half> {
-    static constexpr int kStages = 3;
-    static constexpr int kHalves = 1;
+    static constexpr int kRows = 32 * kCW;
+    static constexpr int kThreads = 32 * (kCW + 1);
+    static constexpr int kBoxes = D * kEsz / 128;   // boxes per row (128 bytes each)
+    static constexpr int kBoxElems = 128 / kEsz;    // elements in a box row
+    static constexpr int kChunkElems = 16 / kEsz;   // elements in a 16-byte chunk
+    static constexpr int kDL = D / 32;              // output dims per lane
+    static constexpr int kBoxBytes = kRows * 128;   // one box of a tile
+    static constexpr int kTileBytes = kRows * D * kEsz;  // one of K, V
+    static constexpr int kStageBytes = 2 * kTileBytes;
 };
 
-template <typename T>
-__device__ __forceinline__ float2 to_f2(uint32_t u);
-template <>
-__device__ __forceinline__ float2 to_f2<__nv_bfloat16>(uint32_t u) {
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
-}
-template <>
-__device__ __forceinline__ float2 to_f2<__half>(uint32_t u) {
-    return __half22float2(*reinterpret_cast<const __half2*>(&u));
+// N consecutive values (N * sizeof(T) bytes: 4, 8 or 16, naturally aligned) as fp32.
+template <typename T, int N>
+__device__ __forceinline__ void to_f32(const uint8_t* p, float (&f)[N]) {
+    if constexpr (sizeof(T) == 4) {
+        if constexpr (N == 2) {
+            const float2 x = *reinterpret_cast<const float2*>(p);
+            f[0] = x.x; f[1] = x.y;
+        } else {
+            static_assert(N == 4, "2 or 4 fp32 values");
+            const float4 x = *reinterpret_cast<const float4*>(p);
+            f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+        }
+    } else {
+        uint32_t w[N / 2];
+        if constexpr (N == 2) {
+            w[0] = *reinterpret_cast<const uint32_t*>(p);
+        } else if constexpr (N == 4) {
+            const uint2 x = *reinterpret_cast<const uint2*>(p);
+            w[0] = x.x; w[1] = x.y;
+        } else {
+            static_assert(N == 8, "2, 4 or 8 16-bit values");
+            const uint4 x = *reinterpret_cast<const uint4*>(p);
+            w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+        }
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                f[2 * i] = __uint_as_float(w[i] << 16);
+                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            } else {
+                const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+                f[2 * i] = h.x;
+                f[2 * i + 1] = h.y;
+            }
+        }
+    }
 }
 
+// Two consecutive values from global memory as fp32, and two fp32 stored as T.
 template <typename T>
 __device__ __forceinline__ float2 load2(const T* p);
 template <>
@@ -127,18 +152,18 @@ struct DecodeParams {
     const void* q;
     void* o;
     float* lse;       // null, or [BH, Nq]
-    float* part_o;    // [BH * Nq][P][64]
+    float* part_o;    // [BH * Nq][P][D]
     float* part_lse;  // [BH * Nq][P]
     int Nq, Nk, BH;
     int groups;           // query groups per head
-    int Tn;               // tiles of kRows keys per segment
+    int Tn;               // tiles per segment
     int causal;
     int explicit_splits;  // S >= 1: every segment in S shares; 0: balanced
     int tps;              // explicit: tiles per share
     int P;                // slot stride of the partials (S, or most pieces a segment can have)
     int C;                // CTAs in the grid
     int64_t G;            // balanced: segments * Tn
-    float c;              // log2(e) / sqrt(d)
+    float c;              // log2(e) / sqrt(D)
 };
 
 struct Piece {
@@ -153,8 +178,8 @@ __device__ __host__ __forceinline__ int64_t owner_of(int64_t t, int64_t C, int64
     return ((t + 1) * C - 1) / G;
 }
 
-// The k-th piece of CTA `cta`; false once the CTA has no more.
-template <int QG>
+// The k-th piece of CTA `cta` (tiles of ROWS keys); false once the CTA has no more.
+template <int QG, int ROWS>
 __device__ __forceinline__ bool get_piece(const DecodeParams& p, int cta, int k, Piece& pc) {
     int64_t seg;
     int t0, t1;
@@ -186,26 +211,24 @@ __device__ __forceinline__ bool get_piece(const DecodeParams& p, int cta, int k,
     pc.g0 = static_cast<int>(seg % p.groups) * QG;
     pc.ng = min(QG, p.Nq - pc.g0);
     pc.ke = p.causal ? min(p.Nk, p.Nk - p.Nq + pc.g0 + pc.ng) : p.Nk;
-    const int tv = (pc.ke + kRows - 1) / kRows;  // tiles holding a visible key
+    const int tv = (pc.ke + ROWS - 1) / ROWS;  // tiles holding a visible key
     pc.t0 = min(t0, tv);
     pc.t1 = min(t1, tv);
     return true;
 }
 
-template <typename T, int QG>
+template <typename T, int QG, int D>
 struct Smem {
-    static constexpr int kHalves = Elem<T>::kHalves;
-    static constexpr int kStages = Elem<T>::kStages;
-    static constexpr int kTileBytes = kRows * kD * static_cast<int>(sizeof(T));  // one of K, V
-    static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kRing = kStages * kStageBytes;
-    static constexpr int kQs = kRing;                    // [kCW][QG][64] f32
-    static constexpr int kPs = kQs + kCW * QG * kD * 4;  // [kCW][QG][32] f32
-    static constexpr int kMl = kPs + kCW * QG * 32 * 4;  // [kCW][QG] m, then [kCW][QG] l
-    static constexpr int kBars = kMl + 2 * kCW * QG * 4; // full[S], empty[S], mFull, mFree
-    static constexpr int kAbort = kBars + (2 * kStages + 2) * 8;
+    using C = Cfg<T, D>;
+    static constexpr int kRing = C::kStages * C::kStageBytes;
+    static constexpr int kQs = kRing;                      // [kCW][QG][D] f32
+    static constexpr int kPs = kQs + C::kCW * QG * D * 4;  // [kCW][QG][32] f32
+    static constexpr int kMl = kPs + C::kCW * QG * 32 * 4; // [kCW][QG] m, then [kCW][QG] l
+    static constexpr int kBars = kMl + 2 * C::kCW * QG * 4;  // full[S], empty[S], mFull, mFree
+    static constexpr int kAbort = kBars + (2 * C::kStages + 2) * 8;
     static constexpr int kBytes = kAbort + 16;
     static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
+    static_assert(kAlloc <= 227 * 1024, "shared memory budget of one CTA");
 };
 
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag) {
@@ -218,18 +241,22 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-// Byte offset of the 16-byte chunk `ch` of row r in a tile of 128-byte rows written with the
+// Byte offset of the 16-byte chunk `ch` of row r in a box of 128-byte rows written with the
 // 128-byte swizzle (the chunks of a row are permuted by row % 8).
 __device__ __forceinline__ uint32_t sw_chunk(int r, int ch) {
     return static_cast<uint32_t>(r * 128 + ((ch ^ (r & 7)) << 4));
 }
 
-template <typename T, int QG>
-__global__ void __launch_bounds__(kThreads)
+template <typename T, int QG, int D>
+__global__ void __launch_bounds__(Cfg<T, D>::kThreads)
     attn_decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                        const DecodeParams p) {
-    using L = Smem<T, QG>;
-    constexpr int S = L::kStages;
+    using C = Cfg<T, D>;
+    using L = Smem<T, QG, D>;
+    constexpr int S = C::kStages;
+    constexpr int kCW = C::kCW;
+    constexpr int kRows = C::kRows;
+    constexpr int DL = C::kDL;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t base = smem_u32(smem);
@@ -249,7 +276,7 @@ __global__ void __launch_bounds__(kThreads)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (threadIdx.x == 32 * kProducerWarp) {
+    if (threadIdx.x == 32 * kCW) {
         prefetch_tmap(&mk);
         prefetch_tmap(&mv);
     }
@@ -259,22 +286,23 @@ __global__ void __launch_bounds__(kThreads)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int cta = blockIdx.x;
 
-    if (warp == kProducerWarp) {
+    if (warp == kCW) {
+        // ------------------------------------ producer ------------------------------------
         if (lane != 0) return;
         int nt = 0;  // tiles issued by this CTA
         bool ok = true;
         Piece pc;
-        for (int k = 0; ok && get_piece<QG>(p, cta, k, pc); ++k) {
+        for (int k = 0; ok && get_piece<QG, kRows>(p, cta, k, pc); ++k) {
             for (int t = pc.t0; t < pc.t1; ++t, ++nt) {
                 const int s = nt % S;
                 if (!(ok = mbar_wait(empty(s), ((nt / S) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
-                const uint32_t dst = base + s * L::kStageBytes;
-                mbar_arrive_expect_tx(full(s), L::kStageBytes);
+                const uint32_t dst = base + s * C::kStageBytes;
+                mbar_arrive_expect_tx(full(s), C::kStageBytes);
 #pragma unroll
-                for (int h = 0; h < L::kHalves; ++h) {
-                    const uint32_t hoff = h * (L::kTileBytes / L::kHalves);
-                    tma_load_3d(dst + hoff, &mk, h * 32, t * kRows, pc.bh, full(s));
-                    tma_load_3d(dst + L::kTileBytes + hoff, &mv, h * 32, t * kRows, pc.bh, full(s));
+                for (int h = 0; h < C::kBoxes; ++h) {
+                    tma_load_3d(dst + h * C::kBoxBytes, &mk, h * C::kBoxElems, t * kRows, pc.bh, full(s));
+                    tma_load_3d(dst + C::kTileBytes + h * C::kBoxBytes, &mv, h * C::kBoxElems, t * kRows, pc.bh,
+                                full(s));
                 }
             }
         }
@@ -286,39 +314,47 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     // ------------------------------------ consumers ------------------------------------
-    float* qs = reinterpret_cast<float*>(smem + L::kQs) + warp * QG * kD;  // this warp's queries, scaled
+    float* qs = reinterpret_cast<float*>(smem + L::kQs) + warp * QG * D;  // this warp's queries, scaled
     float* ps = reinterpret_cast<float*>(smem + L::kPs) + warp * QG * 32;  // this warp's probabilities
     float* ml = reinterpret_cast<float*>(smem + L::kMl);                    // m [kCW][QG], l [kCW][QG]
     const int tid = threadIdx.x;  // 0 .. 32*kCW - 1
+    // Lane L owns output dims e0 .. e0 + DL - 1, inside box vb at element ve of its row.
+    const int e0 = DL * lane;
+    const int vb = e0 / C::kBoxElems, ve = e0 % C::kBoxElems;
+    const int vch = ve / C::kChunkElems, vbyte = (ve % C::kChunkElems) * C::kEsz;
     int nt = 0;  // tiles consumed by this CTA
     bool ok = true;
     Piece pc;
-    for (int k = 0; get_piece<QG>(p, cta, k, pc); ++k) {
+    for (int k = 0; get_piece<QG, kRows>(p, cta, k, pc); ++k) {
         // The previous piece's merge read every warp's qs; wait until all are done with it.
         if (k > 0 && !(ok = warp_wait(mFree, (k - 1) & 1, abort_flag))) break;
         {
-            const T* qh = static_cast<const T*>(p.q) + (static_cast<int64_t>(pc.bh) * p.Nq + pc.g0) * kD;
+            const T* qh = static_cast<const T*>(p.q) + (static_cast<int64_t>(pc.bh) * p.Nq + pc.g0) * D;
 #pragma unroll
             for (int i = 0; i < QG; ++i) {
-                float2 x = make_float2(0.f, 0.f);
-                if (i < pc.ng) x = load2<T>(qh + i * kD + 2 * lane);
-                *reinterpret_cast<float2*>(qs + i * kD + 2 * lane) = make_float2(x.x * p.c, x.y * p.c);
+#pragma unroll
+                for (int h = 0; h < DL; h += 2) {
+                    float2 x = make_float2(0.f, 0.f);
+                    if (i < pc.ng) x = load2<T>(qh + i * D + e0 + h);
+                    *reinterpret_cast<float2*>(qs + i * D + e0 + h) = make_float2(x.x * p.c, x.y * p.c);
+                }
             }
             __syncwarp();
         }
-        float m[QG], l[QG], acc[QG][2];
+        float m[QG], l[QG], acc[QG][DL];
 #pragma unroll
         for (int i = 0; i < QG; ++i) {
             m[i] = -INFINITY;
             l[i] = 0.f;
-            acc[i][0] = acc[i][1] = 0.f;
+#pragma unroll
+            for (int h = 0; h < DL; ++h) acc[i][h] = 0.f;
         }
         const int qpos0 = p.Nk - p.Nq + pc.g0;  // position of the group's first query
         for (int t = pc.t0; t < pc.t1; ++t, ++nt) {
             const int s = nt % S;
             if (!(ok = warp_wait(full(s), (nt / S) & 1, abort_flag))) break;
-            const uint8_t* kt = smem + s * L::kStageBytes;
-            const uint8_t* vt = kt + L::kTileBytes;
+            const uint8_t* kt = smem + s * C::kStageBytes;
+            const uint8_t* vt = kt + C::kTileBytes;
             const int r = 32 * warp + lane;
             const int j = t * kRows + r;
             // ---- scores of key j against the group's queries ----
@@ -328,34 +364,21 @@ __global__ void __launch_bounds__(kThreads)
             for (int i = 0; i < QG; ++i)
 #pragma unroll
                 for (int a = 0; a < NA; ++a) sa[i][a] = 0.f;
-            if constexpr (L::kHalves == 1) {
+#pragma unroll
+            for (int h = 0; h < C::kBoxes; ++h) {
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
-                    const uint4 u = *reinterpret_cast<const uint4*>(kt + sw_chunk(r, ch));
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float2 kf = to_f2<T>(w[h]);
-#pragma unroll
-                        for (int i = 0; i < QG; ++i) {
-                            const float2 qv = *reinterpret_cast<const float2*>(qs + i * kD + ch * 8 + 2 * h);
-                            sa[i][(2 * h) % NA] = fmaf(qv.x, kf.x, sa[i][(2 * h) % NA]);
-                            sa[i][(2 * h + 1) % NA] = fmaf(qv.y, kf.y, sa[i][(2 * h + 1) % NA]);
-                        }
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int ch = 0; ch < 16; ++ch) {
-                    const float4 kf =
-                        *reinterpret_cast<const float4*>(kt + (ch >> 3) * (L::kTileBytes / 2) + sw_chunk(r, ch & 7));
+                    float kf[C::kChunkElems];
+                    to_f32<T, C::kChunkElems>(kt + h * C::kBoxBytes + sw_chunk(r, ch), kf);
+                    const int e = h * C::kBoxElems + ch * C::kChunkElems;  // first dim of the chunk
 #pragma unroll
                     for (int i = 0; i < QG; ++i) {
-                        const float4 qv = *reinterpret_cast<const float4*>(qs + i * kD + ch * 4);
-                        sa[i][0 % NA] = fmaf(qv.x, kf.x, sa[i][0 % NA]);
-                        sa[i][1 % NA] = fmaf(qv.y, kf.y, sa[i][1 % NA]);
-                        sa[i][2 % NA] = fmaf(qv.z, kf.z, sa[i][2 % NA]);
-                        sa[i][3 % NA] = fmaf(qv.w, kf.w, sa[i][3 % NA]);
+#pragma unroll
+                        for (int u = 0; u < C::kChunkElems; u += 2) {
+                            const float2 qv = *reinterpret_cast<const float2*>(qs + i * D + e + u);
+                            sa[i][u % NA] = fmaf(qv.x, kf[u], sa[i][u % NA]);
+                            sa[i][(u + 1) % NA] = fmaf(qv.y, kf[u + 1], sa[i][(u + 1) % NA]);
+                        }
                     }
                 }
             }
@@ -375,13 +398,13 @@ __global__ void __launch_bounds__(kThreads)
                 const float alpha = ex2f(m[i] - m_use);
                 const float pr = ex2f(sc - m_use);
                 l[i] = fmaf(l[i], alpha, pr);  // this lane's share of the row total
-                acc[i][0] *= alpha;
-                acc[i][1] *= alpha;
+#pragma unroll
+                for (int h = 0; h < DL; ++h) acc[i][h] *= alpha;
                 m[i] = m_new;
                 ps[i * 32 + lane] = pr;
             }
             __syncwarp();
-            // ---- weighted values: lane L owns dims 2L, 2L+1 ----
+            // ---- weighted values: lane L owns dims e0 .. e0 + DL - 1 ----
             const int nk = min(32, pc.ke - (t * kRows + 32 * warp));  // rows of this warp with a visible key
 #pragma unroll
             for (int k4 = 0; k4 < 32; k4 += 4) {
@@ -392,20 +415,13 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int rr = 32 * warp + k4 + u;
-                    float2 vv;
-                    if constexpr (L::kHalves == 1) {
-                        const uint32_t w =
-                            *reinterpret_cast<const uint32_t*>(vt + sw_chunk(rr, lane >> 2) + ((lane & 3) << 2));
-                        vv = to_f2<T>(w);
-                    } else {
-                        vv = *reinterpret_cast<const float2*>(vt + (lane >> 4) * (L::kTileBytes / 2) +
-                                                              sw_chunk(rr, (lane & 15) >> 1) + ((lane & 1) << 3));
-                    }
+                    float vv[DL];
+                    to_f32<T, DL>(vt + vb * C::kBoxBytes + sw_chunk(rr, vch) + vbyte, vv);
 #pragma unroll
                     for (int i = 0; i < QG; ++i) {
                         const float w = u == 0 ? pp[i].x : u == 1 ? pp[i].y : u == 2 ? pp[i].z : pp[i].w;
-                        acc[i][0] = fmaf(w, vv.x, acc[i][0]);
-                        acc[i][1] = fmaf(w, vv.y, acc[i][1]);
+#pragma unroll
+                        for (int h = 0; h < DL; ++h) acc[i][h] = fmaf(w, vv[h], acc[i][h]);
                     }
                 }
             }
@@ -413,13 +429,15 @@ __global__ void __launch_bounds__(kThreads)
             mbar_arrive_elect(empty(s));
         }
         if (!ok) break;
-        // ---- merge the four warps' states: this warp's O into its qs, m and l beside ----
+        // ---- merge the warps' states: this warp's O into its qs, m and l beside ----
 #pragma unroll
         for (int i = 0; i < QG; ++i) {
             float tl = l[i];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) tl += __shfl_xor_sync(0xffffffffu, tl, off);
-            *reinterpret_cast<float2*>(qs + i * kD + 2 * lane) = make_float2(acc[i][0], acc[i][1]);
+#pragma unroll
+            for (int h = 0; h < DL; h += 2)
+                *reinterpret_cast<float2*>(qs + i * D + e0 + h) = make_float2(acc[i][h], acc[i][h + 1]);
             if (lane == 0) {
                 ml[warp * QG + i] = m[i];
                 ml[kCW * QG + warp * QG + i] = tl;
@@ -429,8 +447,8 @@ __global__ void __launch_bounds__(kThreads)
         mbar_arrive_elect(mFull);
         if (!(ok = warp_wait(mFull, k & 1, abort_flag))) break;
         const float* qall = reinterpret_cast<const float*>(smem + L::kQs);
-        for (int it = tid; it < QG * 32; it += 32 * kCW) {
-            const int i = it >> 5, d2 = 2 * (it & 31);
+        for (int it = tid; it < QG * (D / 2); it += 32 * kCW) {
+            const int i = it / (D / 2), d2 = 2 * (it % (D / 2));
             if (i >= pc.ng) continue;
             float mm = -INFINITY;
 #pragma unroll
@@ -440,7 +458,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int w = 0; w < kCW; ++w) {
                 const float f = ex2f(ml[w * QG + i] - m_use);
-                const float2 ow = *reinterpret_cast<const float2*>(qall + (w * QG + i) * kD + d2);
+                const float2 ow = *reinterpret_cast<const float2*>(qall + (w * QG + i) * D + d2);
                 lt = fmaf(ml[kCW * QG + w * QG + i], f, lt);
                 o0 = fmaf(ow.x, f, o0);
                 o1 = fmaf(ow.y, f, o1);
@@ -449,10 +467,10 @@ __global__ void __launch_bounds__(kThreads)
             const float lse2 = lt > 0.f ? mm + log2f(lt) : -INFINITY;  // -inf: no visible key here
             const int64_t row = static_cast<int64_t>(pc.bh) * p.Nq + pc.g0 + i;
             if (pc.nslots == 1) {
-                store2<T>(static_cast<T*>(p.o) + row * kD + d2, o0 * inv, o1 * inv);
+                store2<T>(static_cast<T*>(p.o) + row * D + d2, o0 * inv, o1 * inv);
                 if (p.lse != nullptr && d2 == 0) p.lse[row] = lse2;
             } else {
-                float* po = p.part_o + (row * p.P + pc.slot) * kD;
+                float* po = p.part_o + (row * p.P + pc.slot) * D;
                 *reinterpret_cast<float2*>(po + d2) = make_float2(o0 * inv, o1 * inv);
                 if (d2 == 0) p.part_lse[row * p.P + pc.slot] = lse2;
             }
@@ -465,8 +483,9 @@ __global__ void __launch_bounds__(kThreads)
 
 // One warp per query row: merge the row's pieces by their log-sum-exps. Rows whose segment is
 // a single piece were written by the main kernel and are skipped. Lane s holds piece s's
-// log-sum-exp and weight (pieces in rounds of 32), so the loads of a round are independent.
-template <typename T, int QG>
+// log-sum-exp and weight (pieces in rounds of 32), so the loads of a round are independent;
+// lane L owns output dims 2L, 2L+1 (+ 64 for D = 128).
+template <typename T, int QG, int D>
 __global__ void __launch_bounds__(128) attn_decode_merge_kernel(const DecodeParams p, int64_t rows) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the main kernel's writes are visible
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
@@ -481,13 +500,16 @@ __global__ void __launch_bounds__(128) attn_decode_merge_kernel(const DecodePara
         n = static_cast<int>(owner_of(s0 + p.Tn - 1, p.C, p.G) - owner_of(s0, p.C, p.G) + 1);
     }
     if (n == 1) return;
+    constexpr int G = D / 64;
     const float* pl = p.part_lse + row * p.P;
-    const float* po = p.part_o + row * p.P * kD + 2 * lane;
+    const float* po = p.part_o + row * p.P * D + 2 * lane;
     float mx = -INFINITY;
     for (int s0 = 0; s0 < n; s0 += 32) mx = fmaxf(mx, s0 + lane < n ? pl[s0 + lane] : -INFINITY);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float w_tot = 0.f, o0 = 0.f, o1 = 0.f;
+    float w_tot = 0.f, o[G][2];
+#pragma unroll
+    for (int g = 0; g < G; ++g) o[g][0] = o[g][1] = 0.f;
     for (int s0 = 0; s0 < n; s0 += 32) {
         const float ls = s0 + lane < n ? pl[s0 + lane] : -INFINITY;
         const float w = ls == -INFINITY ? 0.f : ex2f(ls - mx);  // a piece with no visible key weighs 0
@@ -496,20 +518,51 @@ __global__ void __launch_bounds__(128) attn_decode_merge_kernel(const DecodePara
 #pragma unroll 8
         for (int u = 0; u < m; ++u) {
             const float wu = __shfl_sync(0xffffffffu, w, u);
-            const float2 ov = *reinterpret_cast<const float2*>(po + (s0 + u) * kD);
-            o0 = fmaf(wu, ov.x, o0);
-            o1 = fmaf(wu, ov.y, o1);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float2 ov = *reinterpret_cast<const float2*>(po + (s0 + u) * D + 64 * g);
+                o[g][0] = fmaf(wu, ov.x, o[g][0]);
+                o[g][1] = fmaf(wu, ov.y, o[g][1]);
+            }
         }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) w_tot += __shfl_xor_sync(0xffffffffu, w_tot, off);
     const float inv = 1.f / w_tot;  // every row sees at least one key, so w_tot >= 1
-    store2<T>(static_cast<T*>(p.o) + row * kD + 2 * lane, o0 * inv, o1 * inv);
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+        store2<T>(static_cast<T*>(p.o) + row * D + 64 * g + 2 * lane, o[g][0] * inv, o[g][1] * inv);
     if (p.lse != nullptr && lane == 0) p.lse[row] = mx + log2f(w_tot);
 }
 
 // ------------------------------------------ host side ------------------------------------------
 int queries_per_group(int64_t Nq) { return Nq <= 1 ? 1 : Nq <= 2 ? 2 : Nq <= 4 ? 4 : 8; }
+
+template <typename X>
+struct Tag {
+    using type = X;
+};
+template <int V>
+using IC = std::integral_constant<int, V>;
+
+// Calls f(Tag<T>, IC<QG>, IC<D>) for the element type, query group and head width of a call.
+template <typename F>
+int visit_cfg(int dtype, int64_t d, int qg, F&& f) {
+    auto by_qg = [&](auto t, auto dd) -> int {
+        switch (qg) {
+            case 1: return f(t, IC<1>{}, dd);
+            case 2: return f(t, IC<2>{}, dd);
+            case 4: return f(t, IC<4>{}, dd);
+            default: return f(t, IC<8>{}, dd);
+        }
+    };
+    auto by_d = [&](auto t) -> int { return d == 128 ? by_qg(t, IC<128>{}) : by_qg(t, IC<64>{}); };
+    switch (dtype) {
+        case ATTN_F32: return by_d(Tag<float>{});
+        case ATTN_BF16: return by_d(Tag<__nv_bfloat16>{});
+        default: return by_d(Tag<__half>{});
+    }
+}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -528,16 +581,16 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [BH][Nk][64] tensor; boxes of kRows rows x 128 bytes (64 16-bit values, or 32 fp32 values
-// — an fp32 row takes two boxes), 128-byte swizzle; rows past Nk of a head are out of bounds
+// [BH][Nk][D] tensor; boxes of `rows` rows x 128 bytes (64 16-bit values or 32 fp32 values, so
+// a row takes D * esz / 128 boxes), 128-byte swizzle; rows past Nk of a head are out of bounds
 // (zero-filled), never the next head's.
-bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t Nk, int dtype) {
+bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t Nk, int64_t D, int dtype, int rows) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t esz = dtype == ATTN_F32 ? 4 : 2;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(Nk), static_cast<cuuint64_t>(BH)};
-    const cuuint64_t strides[2] = {kD * esz, static_cast<cuuint64_t>(Nk) * kD * esz};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(kRows), 1};
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Nk), static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * esz, static_cast<cuuint64_t>(Nk) * D * esz};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(rows), 1};
     const cuuint32_t estride[3] = {1, 1, 1};
     const CUtensorMapDataType dt = dtype == ATTN_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -547,47 +600,35 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t Nk, int dty
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int QG>
+// CTAs of the main kernel that fit on one SM (0 if the query fails; only success is cached).
+template <typename T, int QG, int D>
 int ctas_per_sm() {
-    static int n = [] {
-        int v = 0;
-        if (cudaFuncSetAttribute(attn_decode_kernel<T, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Smem<T, QG>::kAlloc) != cudaSuccess)
-            return 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, attn_decode_kernel<T, QG>, kThreads,
-                                                          Smem<T, QG>::kAlloc) != cudaSuccess)
-            return 0;
-        return v;
-    }();
-    return n;
-}
-
-int ctas_per_sm_for(int dtype, int qg) {
-    switch (dtype) {
-        case ATTN_F32:
-            return qg == 1 ? ctas_per_sm<float, 1>() : qg == 2 ? ctas_per_sm<float, 2>()
-                   : qg == 4 ? ctas_per_sm<float, 4>() : ctas_per_sm<float, 8>();
-        case ATTN_BF16:
-            return qg == 1 ? ctas_per_sm<__nv_bfloat16, 1>() : qg == 2 ? ctas_per_sm<__nv_bfloat16, 2>()
-                   : qg == 4 ? ctas_per_sm<__nv_bfloat16, 4>() : ctas_per_sm<__nv_bfloat16, 8>();
-        default:
-            return qg == 1 ? ctas_per_sm<__half, 1>() : qg == 2 ? ctas_per_sm<__half, 2>()
-                   : qg == 4 ? ctas_per_sm<__half, 4>() : ctas_per_sm<__half, 8>();
-    }
+    static int cached = 0;
+    if (cached > 0) return cached;
+    int v = 0;
+    if (cudaFuncSetAttribute(attn_decode_kernel<T, QG, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Smem<T, QG, D>::kAlloc) != cudaSuccess)
+        return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, attn_decode_kernel<T, QG, D>, Cfg<T, D>::kThreads,
+                                                      Smem<T, QG, D>::kAlloc) != cudaSuccess)
+        return 0;
+    cached = v;
+    return v;
 }
 
 // The grid and slot layout of one call. The workspace query and the launch both build it, so
 // they agree on P.
 struct Plan {
-    int qg, groups, Tn, C, P, tps;
+    int qg, groups, rows, Tn, C, P, tps;
     int64_t G;
     bool merge;  // some segment has more than one piece
 };
 
-bool make_plan(int64_t BH, int64_t Nq, int64_t Nk, int splits, int num_sms, int per_sm, Plan* pl) {
+bool make_plan(int64_t BH, int64_t Nq, int64_t Nk, int rows, int splits, int num_sms, int per_sm, Plan* pl) {
     pl->qg = queries_per_group(Nq);
     pl->groups = static_cast<int>((Nq + pl->qg - 1) / pl->qg);
-    pl->Tn = static_cast<int>((Nk + kRows - 1) / kRows);
+    pl->rows = rows;
+    pl->Tn = static_cast<int>((Nk + rows - 1) / rows);
     const int64_t segs = BH * pl->groups;
     const int64_t slots = static_cast<int64_t>(std::max(1, num_sms)) * std::max(1, per_sm);
     if (splits > 0) {
@@ -609,60 +650,37 @@ bool make_plan(int64_t BH, int64_t Nq, int64_t Nk, int splits, int num_sms, int 
     return pl->C >= 1;
 }
 
-template <typename T, int QG>
-int launch_t(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& prm, bool merge, cudaStream_t stream) {
-    attn_decode_kernel<T, QG><<<static_cast<unsigned>(prm.C), kThreads, Smem<T, QG>::kAlloc, stream>>>(mk, mv, prm);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
-    if (merge) {
-        const int64_t rows = static_cast<int64_t>(prm.BH) * prm.Nq;
-        // Programmatic stream serialisation: the merge grid may start while the main grid runs
-        // (it is released by the main kernel's launch_dependents) and waits in griddepcontrol.wait
-        // until that grid has completed and its memory is visible.
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
-        cfg.blockDim = dim3(128);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, attn_decode_merge_kernel<T, QG>, prm, rows) != cudaSuccess) return ATTN_ERR_LAUNCH;
-    }
-    return ATTN_OK;
-}
-
-template <typename T>
-int launch_qg(int qg, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& prm, bool merge,
-              cudaStream_t stream) {
-    switch (qg) {
-        case 1: return launch_t<T, 1>(mk, mv, prm, merge, stream);
-        case 2: return launch_t<T, 2>(mk, mv, prm, merge, stream);
-        case 4: return launch_t<T, 4>(mk, mv, prm, merge, stream);
-        default: return launch_t<T, 8>(mk, mv, prm, merge, stream);
-    }
-}
-
-size_t partial_bytes(int64_t BH, int64_t Nq, int64_t P) {
-    const double need = static_cast<double>(BH) * static_cast<double>(Nq) * static_cast<double>(P) * (kD + 1) * 4.0;
+size_t partial_bytes(int64_t BH, int64_t Nq, int64_t D, int64_t P) {
+    const double need = static_cast<double>(BH) * static_cast<double>(Nq) * static_cast<double>(P) * (D + 1) * 4.0;
     if (need > 9.0e18) return 0;
     const size_t r = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * static_cast<size_t>(P);
-    return (r * kD * sizeof(float) + 255) / 256 * 256 + (r * sizeof(float) + 255) / 256 * 256;
+    return (r * static_cast<size_t>(D) * sizeof(float) + 255) / 256 * 256 + (r * sizeof(float) + 255) / 256 * 256;
+}
+
+// Builds the plan of a call: the kernel's tile rows and occupancy come from its configuration.
+bool plan_for(int64_t BH, int64_t Nq, int64_t Nk, int64_t D, int splits, int dtype, int num_sms, Plan* pl) {
+    int rows = 0, per_sm = 0;
+    visit_cfg(dtype, D, queries_per_group(Nq), [&](auto t, auto qg, auto dd) -> int {
+        using T = typename decltype(t)::type;
+        rows = Cfg<T, decltype(dd)::value>::kRows;
+        // The explicit plan does not depend on occupancy; skip the device query for it.
+        per_sm = splits > 0 ? 1 : ctas_per_sm<T, decltype(qg)::value, decltype(dd)::value>();
+        return 0;
+    });
+    if (per_sm <= 0) return false;
+    return make_plan(BH, Nq, Nk, rows, splits, num_sms, per_sm, pl);
 }
 
 }  // namespace
 
-size_t decode_workspace_bytes(int64_t BH, int64_t Nq, int64_t Nk, int splits, int dtype, int num_sms) {
+size_t decode_workspace_bytes(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int splits, int dtype, int num_sms) {
     if (BH <= 0 || Nq <= 0 || Nk <= 0 || splits < 0 || splits > ATTN_KV_MAX_SPLITS) return 0;
-    if (BH > 0x7FFFFFFFll || Nq > ATTN_MAX_N || Nk > ATTN_MAX_N) return 0;
+    if (BH > 0x7FFFFFFFll || Nq > ATTN_MAX_N || Nk > ATTN_MAX_N || (d != 64 && d != 128)) return 0;
     if (splits == 1) return 0;
-    if (splits > 1) return partial_bytes(BH, Nq, splits);
-    const int per_sm = ctas_per_sm_for(dtype, queries_per_group(Nq));
-    if (per_sm <= 0) return 0;
+    if (splits > 1) return partial_bytes(BH, Nq, d, splits);
     Plan pl;
-    if (!make_plan(BH, Nq, Nk, 0, num_sms, per_sm, &pl)) return 0;
-    return pl.merge ? partial_bytes(BH, Nq, pl.P) : 0;
+    if (!plan_for(BH, Nq, Nk, d, 0, dtype, num_sms, &pl)) return 0;
+    return pl.merge ? partial_bytes(BH, Nq, d, pl.P) : 0;
 }
 
 int decode_device_error(bool clear, unsigned* err) {
@@ -677,14 +695,12 @@ int decode_device_error(bool clear, unsigned* err) {
 }
 
 int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
-                  size_t workspace_bytes, int64_t BH, int64_t Nq, int64_t Nk, bool causal, int dtype, int splits,
-                  int num_sms, cudaStream_t stream) {
+                  size_t workspace_bytes, int64_t BH, int64_t Nq, int64_t Nk, int64_t d, bool causal, int dtype,
+                  int splits, int num_sms, cudaStream_t stream) {
     if (Nk > ATTN_MAX_N || BH > 0x7FFFFFFFll || splits < 0 || splits > ATTN_KV_MAX_SPLITS) return ATTN_ERR_UNSUPPORTED;
-    const int qg = queries_per_group(Nq);
-    const int per_sm = ctas_per_sm_for(dtype, qg);
-    if (per_sm <= 0) return ATTN_ERR_LAUNCH;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     Plan pl;
-    if (!make_plan(BH, Nq, Nk, splits, num_sms, per_sm, &pl)) return ATTN_ERR_UNSUPPORTED;
+    if (!plan_for(BH, Nq, Nk, d, splits, dtype, num_sms, &pl)) return ATTN_ERR_LAUNCH;
     if (BH * pl.groups > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     DecodeParams prm;
     prm.q = q;
@@ -701,25 +717,51 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
     prm.P = pl.P;
     prm.C = pl.C;
     prm.G = pl.G;
-    prm.c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
+    prm.c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     prm.part_o = nullptr;
     prm.part_lse = nullptr;
     if (pl.merge) {
-        const size_t need = partial_bytes(BH, Nq, pl.P);
+        const size_t need = partial_bytes(BH, Nq, d, pl.P);
         if (need == 0) return ATTN_ERR_UNSUPPORTED;
         if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
         const size_t r = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * static_cast<size_t>(pl.P);
         prm.part_o = static_cast<float*>(workspace);
-        prm.part_lse =
-            reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + (r * kD * sizeof(float) + 255) / 256 * 256);
+        prm.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                (r * static_cast<size_t>(d) * sizeof(float) + 255) / 256 * 256);
     }
     CUtensorMap mk, mv;
-    if (!make_map(&mk, k, BH, Nk, dtype) || !make_map(&mv, v, BH, Nk, dtype)) return ATTN_ERR_DEVICE;
-    switch (dtype) {
-        case ATTN_F32: return launch_qg<float>(qg, mk, mv, prm, pl.merge, stream);
-        case ATTN_BF16: return launch_qg<__nv_bfloat16>(qg, mk, mv, prm, pl.merge, stream);
-        default: return launch_qg<__half>(qg, mk, mv, prm, pl.merge, stream);
-    }
+    if (!make_map(&mk, k, BH, Nk, d, dtype, pl.rows) || !make_map(&mv, v, BH, Nk, d, dtype, pl.rows))
+        return ATTN_ERR_DEVICE;
+    return visit_cfg(dtype, d, pl.qg, [&](auto t, auto qg, auto dd) -> int {
+        using T = typename decltype(t)::type;
+        constexpr int QG = decltype(qg)::value, D = decltype(dd)::value;
+        // ctas_per_sm (called by the plan of a balanced call) has set the shared-memory limit;
+        // an explicit plan sets it here.
+        if (cudaFuncSetAttribute(attn_decode_kernel<T, QG, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Smem<T, QG, D>::kAlloc) != cudaSuccess)
+            return ATTN_ERR_LAUNCH;
+        attn_decode_kernel<T, QG, D><<<static_cast<unsigned>(prm.C), Cfg<T, D>::kThreads, Smem<T, QG, D>::kAlloc,
+                                       stream>>>(mk, mv, prm);
+        if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+        if (!pl.merge) return ATTN_OK;
+        // Programmatic stream serialisation: the merge grid may start while the main grid runs
+        // (it is released by the main kernel's launch_dependents) and waits in griddepcontrol.wait
+        // until that grid has completed and its memory is visible.
+        const int64_t rows = static_cast<int64_t>(prm.BH) * prm.Nq;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, attn_decode_merge_kernel<T, QG, D>, prm, rows) != cudaSuccess)
+            return ATTN_ERR_LAUNCH;
+        return ATTN_OK;
+    });
 }
 
 }  // namespace attn

@@ -47,18 +47,19 @@ int launch_materialized(const void* q, const void* k, const void* v, void* o, vo
 // each region rounded up to 256 bytes. Returns 0 on overflow.
 size_t materialized_head_bytes(int64_t N);
 
-// Key-value cache attention (attn_decode.cu): Nq queries [BH, Nq, 64] against Nk keys and
-// values [BH, Nk, 64]. splits == 0 balances the tiles over a persistent grid; splits >= 1 cuts
-// every (head, query group) into that many shares. Pieces of a segment are merged by a second
-// kernel through the workspace; ATTN_ERR_WORKSPACE if it is smaller than the plan needs.
+// Key-value cache attention (attn_decode.cu): Nq queries [BH, Nq, d] against Nk keys and
+// values [BH, Nk, d], d = 64 or 128. splits == 0 balances the tiles over a persistent grid;
+// splits >= 1 cuts every (head, query group) into that many shares. Pieces of a segment are
+// merged by a second kernel through the workspace; ATTN_ERR_WORKSPACE if it is smaller than
+// the plan needs.
 int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
-                  size_t workspace_bytes, int64_t BH, int64_t Nq, int64_t Nk, bool causal, int dtype, int splits,
-                  int num_sms, cudaStream_t stream);
+                  size_t workspace_bytes, int64_t BH, int64_t Nq, int64_t Nk, int64_t d, bool causal, int dtype,
+                  int splits, int num_sms, cudaStream_t stream);
 
 // Workspace bytes launch_decode needs (0 when no segment has more than one piece, or on
 // overflow). For splits == 0 the plan depends on the device: num_sms and the kernel's
 // occupancy, which this queries on the current device.
-size_t decode_workspace_bytes(int64_t BH, int64_t Nq, int64_t Nk, int splits, int dtype, int num_sms);
+size_t decode_workspace_bytes(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int splits, int dtype, int num_sms);
 
 // Reads (and optionally clears) the decode kernel's device error word.
 int decode_device_error(bool clear, unsigned* err);

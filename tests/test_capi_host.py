@@ -130,7 +130,7 @@ def test_valid_call_without_gpu_reports_device_error(lib):
     ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 101, 100, 64, 1, 1, 1), 1),  # Nq > Nk
     ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 2, 1, 1), 1),    # causal not 0/1
     ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 1, -1), 1),   # negative split count
-    ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 128, 1, 1, 1), 2),   # d != 64
+    ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 96, 1, 1, 1), 2),    # d neither 64 nor 128
     ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 5, 1), 2),    # unknown dtype
     ((P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 1, 1025), 2),  # too many shares
     ((None, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 1, 1), 1),  # null q
@@ -152,12 +152,14 @@ def test_kvcache_argument_checks(lib, args, want):
 def test_kvcache_workspace_bytes(lib):
     r = 2 * 3 * 5 * 7  # B * H * Nq * splits
     want = (r * 64 * 4 + 255) // 256 * 256 + (r * 4 + 255) // 256 * 256
-    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 7, 1) == want
-    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 1, 1) == 0   # one share writes o directly
-    assert lib.attn_kvcache_workspace_bytes(-1, 3, 5, 100, 7, 1) == 0
-    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 4, 7, 1) == 0     # Nq > Nk
-    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 1025, 1) == 0
-    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 7, 9) == 0   # unknown dtype
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 64, 7, 1) == want
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 64, 1, 1) == 0   # one share writes o directly
+    assert lib.attn_kvcache_workspace_bytes(-1, 3, 5, 100, 64, 7, 1) == 0
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 4, 64, 7, 1) == 0     # Nq > Nk
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 64, 1025, 1) == 0
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 64, 7, 9) == 0   # unknown dtype
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 128, 7, 1) == (r * 128 * 4 + 255) // 256 * 256 + (r * 4 + 255) // 256 * 256
+    assert lib.attn_kvcache_workspace_bytes(2, 3, 5, 100, 96, 7, 1) == 0   # head width
 
 
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="needs a machine without a GPU")
@@ -165,4 +167,4 @@ def test_kvcache_valid_call_without_gpu_reports_device_error(lib):
     ws = P * 64
     assert lib.attn_fwd_kvcache(P, P * 3, P * 5, P * 9, None, ws, 1 << 20, 1, 2, 4, 100, 64, 1, 1, 4, None) == 5
     assert lib.attn_fwd_kvcache(P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 1, 0, None) == 5
-    assert lib.attn_kvcache_workspace_bytes(1, 2, 4, 100, 0, 1) == 0  # balanced plan needs the device
+    assert lib.attn_kvcache_workspace_bytes(1, 2, 4, 100, 64, 0, 1) == 0  # balanced plan needs the device

@@ -25,14 +25,14 @@ def _lse_bound(ref):
     return 2e-5 * (1.0 + float(np.max(np.abs(ref)))) + 1e-4
 
 
-def _inputs(seed, B, H, Nq, Nk, dtype, qk_scale=1.0):
-    q = si.qkv(seed, B, H, Nq, 64, dtype, qk_scale=qk_scale)[0]
-    _, k, v = si.qkv(seed + 1, B, H, Nk, 64, dtype, qk_scale=qk_scale)
+def _inputs(seed, B, H, Nq, Nk, dtype, qk_scale=1.0, d=64):
+    q = si.qkv(seed, B, H, Nq, d, dtype, qk_scale=qk_scale)[0]
+    _, k, v = si.qkv(seed + 1, B, H, Nk, d, dtype, qk_scale=qk_scale)
     return q, k, v
 
 
-def _run(seed, B, H, Nq, Nk, dtype, causal, splits, qk_scale=1.0):
-    q, k, v = _inputs(seed, B, H, Nq, Nk, dtype, qk_scale)
+def _run(seed, B, H, Nq, Nk, dtype, causal, splits, qk_scale=1.0, d=64):
+    q, k, v = _inputs(seed, B, H, Nq, Nk, dtype, qk_scale, d)
     qd, kd, vd = (to_dev(x, dtype) for x in (q, k, v))
     o, lse = fa.attn_fwd_kvcache(qd, kd, vd, causal=causal, num_splits=splits, lse=True)
     torch.cuda.synchronize()
@@ -144,3 +144,23 @@ def test_kvcache_explicit_workspace_and_outputs_are_used():
     assert float(np.max(np.abs(lse.cpu().numpy() - ref_lse))) <= _lse_bound(ref_lse)
     with pytest.raises(fa.AttnError):  # one byte short
         fa.attn_fwd_kvcache(qd, kd, vd, num_splits=S, workspace=ws[:-1])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (1, 300), (3, 1000), (8, 129), (20, 700)])
+@pytest.mark.parametrize("splits", [0, 1, 5])
+def test_kvcache_head_width_128(dtype, causal, Nq, Nk, splits):
+    _run(0xCAC39000 + Nq * 7919 + Nk, 2, 3, Nq, Nk, dtype, causal, splits, d=128)
+
+
+def test_kvcache_head_width_128_decode_shape():
+    B, H, Nq, Nk = 8, 8, 1, 8192
+    q, k, v = _inputs(0xCAC3A000, B, H, Nq, Nk, "bf16", d=128)
+    qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+    o, lse = fa.attn_fwd_kvcache(qd, kd, vd, causal=True, lse=True)
+    torch.cuda.synchronize()
+    assert fa.attn_device_status(clear=True) == 0
+    ref_o, ref_lse = oracle.attn_fwd_kv(q, k, v, True)
+    check(o.float().cpu().numpy().astype(np.float64), ref_o, "bf16", Nk, "decode d128 B8H8 Nk8192")
+    assert float(np.max(np.abs(lse.cpu().numpy() - ref_lse))) <= _lse_bound(ref_lse)
