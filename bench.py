@@ -24,6 +24,9 @@ Beside the headline line's keys, ``decode`` reports the key-value cache path
 bf16: GB/s of algorithmic bytes (K and V read once, q read, o written) against the measured
 HBM copy bandwidth, 50 calls back to back (K and V, 403 MB, exceed L2, so nothing is flushed).
 
+``d128`` reports the same causal forward at head width 128 (B1 H12 N8192 d128 bf16), timed
+like the headline (30 launches, L2 flushed between them), with its oracle sample.
+
 ``--impl reference`` times the CPU oracle (double precision, all host cores) on the same
 workload instead, each step a bounded sample of query rows, and prints the same line.
 """
@@ -61,6 +64,10 @@ TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_tc_bf16_causal_B1H12N
 DECODE = {"workload": "key-value cache decode, bf16, B16 H12 Nq1 Nk8192 d64 (one new token per sequence)",
           "B": 16, "H": 12, "Nq": 1, "Nk": 8192, "d": 64, "causal": True, "dtype": "bf16"}
 DECODE_SOURCE = os.path.join(ROOT, "online_softmax_flashattention_gb300", "csrc", "attn_decode.cu")
+# Head width 128, reported beside the headline: the same causal forward at B1 H12 N8192 d128 bf16.
+WIDE = {"workload": "causal attention forward, bf16 in/out, fp32 accumulate, B1 H12 N8192 d128",
+        "B": 1, "H": 12, "N": 8192, "d": 128, "causal": True, "dtype": "bf16"}
+WIDE_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_tc_bf16_causal_B1H12N8192d128.md")
 DECODE_PROFILE = os.path.join(ROOT, "profiles", "attn_decode_bf16_B16H12Nq1Nk8192.md")
 
 
@@ -349,6 +356,69 @@ def decode_leg(dev, stream, steps, warmup, with_cpu, cpu_seconds):
     return out
 
 
+def wide_leg(dev, stream, steps, warmup, flush, with_cpu, cpu_seconds):
+    """The forward at head width 128 (attn_fwd, tcgen05 kernel): per-launch CUDA events with the
+    L2 flushed between launches, as for the headline; the oracle on sampled rows beside it."""
+    import torch
+
+    import online_softmax_flashattention_gb300 as fa
+    import seeded_inputs as si
+
+    w = WIDE
+    q, k, v = si.qkv(SEED + 21, w["B"], w["H"], w["N"], w["d"], w["dtype"])
+    qd, kd, vd = (torch.from_numpy(x).to(dev).to(torch.bfloat16) for x in (q, k, v))
+    od = torch.empty_like(qd)
+    fa.attn_fwd(qd, kd, vd, causal=True, out=od)
+    torch.cuda.synchronize(dev)
+    if fa.attn_device_status(clear=True, device=dev) != 0:
+        raise RuntimeError("device-side timeout in the first d = 128 run")
+    for _ in range(warmup):
+        flush.zero_()
+        fa.attn_fwd(qd, kd, vd, causal=True, out=od)
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fa.attn_fwd(qd, kd, vd, causal=True, out=od)
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
+    flop = workload_flops(w["B"], w["H"], w["N"], w["d"], w["causal"])
+    peaks, peak_src = load_peaks()
+    tf = flop / (ms * 1e-3) / 1e12
+    traffic, traffic_src = recorded_traffic(WIDE_PROFILE, TC_SOURCE)
+    out = {"config": dict(WIDE), "steps": steps, "ms_per_step": ms, "value": tf, "unit": UNIT,
+           "l2": "flushed between steps (256 MiB write outside the timed events)",
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": UNIT,
+                        "frac": tf / peaks["bf16_tflops"], "traffic": traffic, "traffic_source": traffic_src,
+                        "peak_source": f"{peak_src} bf16 dense (burst)", "algorithmic_flop_per_launch": flop}}
+    if with_cpu:
+        import oracle
+
+        threads = oracle.default_threads()
+        rows = si.sample_rows(SEED + 22, w["N"], 8)
+        flat = np.concatenate([h * w["N"] + rows for h in range(w["B"] * w["H"])])
+        t0 = time.perf_counter()
+        ref = oracle.attn_fwd(q, k, v, True, rows=flat, threads=threads)
+        cal = max(time.perf_counter() - t0, 1e-3)
+        per_head = int(max(8, min(w["N"], 8 * cpu_seconds / cal)))
+        rows = si.sample_rows(SEED + 23, w["N"], per_head)
+        flat = np.concatenate([h * w["N"] + rows for h in range(w["B"] * w["H"])])
+        t0 = time.perf_counter()
+        ref = oracle.attn_fwd(q, k, v, True, rows=flat, threads=threads)
+        secs = time.perf_counter() - t0
+        fl = row_flops(np.tile(rows, w["B"] * w["H"]), w["d"], w["N"], True)
+        got = od.reshape(-1, w["d"]).float().cpu().numpy().astype(np.float64)[flat]
+        err = float(np.max(np.abs(got - ref)))
+        out["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+                               "sample": f"{len(rows)} seeded query rows per head x {w['B'] * w['H']} heads, {secs:.1f} s"}
+        out["parity"] = {"rows_checked": int(len(flat)), "max_abs_err": err, "tolerance": 2e-2, "pass": bool(err <= 2e-2)}
+    del qd, kd, vd, od
+    return out
+
+
 # ----------------------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local):
     import torch
@@ -471,9 +541,10 @@ def run_ours(args, rank, world, local):
                                  "peak_source": "measured bf16 dense (burst)"}}
         del dout, ob, lse
 
-    decode = None
+    decode = wide = None
     if rank == 0 and not args.no_ablation:
         decode = decode_leg(dev, stream, 50, args.warmup, not args.no_cpu_baseline, min(args.cpu_seconds, 10.0))
+        wide = wide_leg(dev, stream, 30, args.warmup, flush, not args.no_cpu_baseline, min(args.cpu_seconds, 8.0))
 
     cpu = parity = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -506,6 +577,7 @@ def run_ours(args, rank, world, local):
         "ablation": ablation,
         "backward": backward,
         "decode": decode,
+        "d128": wide,
         "launch_ms": {"min": min(launch_ms), "median": statistics.median(launch_ms), "max": max(launch_ms)},
     }
     print(json.dumps(line), flush=True)
@@ -572,6 +644,20 @@ def run_profile(args):
             raise RuntimeError("device-side timeout")
         print(f"profile: {args.profile_launches} calls of attn_fwd_kvcache on {w['workload']}")
         return
+    if args.profile_kernel == "d128":
+        import seeded_inputs as si
+
+        w = WIDE
+        q, k, v = si.qkv(SEED + 21, w["B"], w["H"], w["N"], w["d"], w["dtype"])
+        qd, kd, vd = (torch.from_numpy(x).to("cuda").to(torch.bfloat16) for x in (q, k, v))
+        od = torch.empty_like(qd)
+        for _ in range(args.profile_launches):
+            fa.attn_fwd(qd, kd, vd, causal=True, out=od)
+        torch.cuda.synchronize()
+        if fa.attn_device_status(clear=True) != 0:
+            raise RuntimeError("device-side timeout")
+        print(f"profile: {args.profile_launches} launches of attn_fwd on {w['workload']}")
+        return
     q, k, v = make_inputs()
     qd, kd, vd = (torch.from_numpy(x).to("cuda").to(torch.bfloat16) for x in (q, k, v))
     od = torch.empty_like(qd)
@@ -595,7 +681,7 @@ def main(argv=None):
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--profile", action="store_true", help="only launch the timed kernel (for ncu)")
     ap.add_argument("--profile-launches", type=int, default=4)
-    ap.add_argument("--profile-kernel", choices=["forward", "decode"], default="forward",
+    ap.add_argument("--profile-kernel", choices=["forward", "decode", "d128"], default="forward",
                     help="which path --profile launches")
     args = ap.parse_args(argv)
     if args.warmup < 3:
