@@ -235,11 +235,22 @@ int attn_fwd_materialized_noalloc(const void* q, const void* k, const void* v, v
  */
 int attn_device_status(void* stream, int clear);
 
+/*
+ * attn_selftest_wait_timeout — exercises the device-side timeout path without any fault: one
+ * warp waits on an mbarrier that nothing arrives on, with a limit of timeout_ns (1 us .. 2 s);
+ * when it runs out the warp records ATTN_ERR_TIMEOUT the way every kernel of this library does
+ * and returns, leaving the context usable. attn_device_status then reports the timeout (and
+ * clears it when asked). Returns ATTN_OK once launched, ATTN_ERR_INVALID_ARG for a limit out of
+ * range, ATTN_ERR_DEVICE off sm_103.
+ */
+int attn_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* attn_status_string(int status);
 
 /* ABI version of this header: (major << 16) | minor (1.1 added attn_fwd_lse, 1.2 attn_bwd,
- * 1.3 attn_fwd_kvcache, 1.4 head width 128 for the forward entry points). */
+ * 1.3 attn_fwd_kvcache, 1.4 head width 128 for the forward entry points, 1.5
+ * attn_selftest_wait_timeout). */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

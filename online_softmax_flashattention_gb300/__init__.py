@@ -26,7 +26,7 @@ __all__ = [
     "attn_fwd", "attn_fwd_materialized", "attn_materialized_workspace_bytes", "attn_device_status",
     "attn_status_string", "attn_abi_version", "raw", "attn_fwd_materialized_noalloc",
     "ATTN_NOALLOC_MAX_N", "attn_fwd_lse", "attn_bwd", "attn_fwd_kvcache", "attn_kvcache_workspace_bytes",
-    "ATTN_KV_MAX_SPLITS",
+    "ATTN_KV_MAX_SPLITS", "attn_selftest_wait_timeout",
 ]
 
 ATTN_F32, ATTN_BF16, ATTN_F16 = 0, 1, 2
@@ -79,6 +79,8 @@ def raw():
             lib.attn_fwd_materialized.restype = ci
             lib.attn_materialized_workspace_bytes.argtypes = [i64, i64, i64]
             lib.attn_materialized_workspace_bytes.restype = sz
+            lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+            lib.attn_selftest_wait_timeout.restype = ci
             lib.attn_device_status.argtypes = [vp, ci]
             lib.attn_device_status.restype = ci
             lib.attn_status_string.argtypes = [ci]
@@ -271,6 +273,17 @@ def attn_fwd_materialized(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cau
     if st != 0:
         raise AttnError(st, "attn_fwd_materialized")
     return out
+
+
+def attn_selftest_wait_timeout(timeout_ns: int = 1_000_000, stream: torch.cuda.Stream | None = None,
+                               device: torch.device | int | None = None) -> None:
+    """Launches the library's timeout self-test: one warp whose only wait runs out after
+    ``timeout_ns``; afterwards :func:`attn_device_status` reports ATTN_ERR_TIMEOUT (7)."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index or 0)
+    with torch.cuda.device(dev):
+        st = raw().attn_selftest_wait_timeout(int(timeout_ns), _stream(dev, stream))
+    if st != 0:
+        raise AttnError(st, "attn_selftest_wait_timeout")
 
 
 def attn_device_status(clear: bool = True, stream: torch.cuda.Stream | None = None,

@@ -241,6 +241,14 @@ int attn_fwd_materialized(const void* q, const void* k, const void* v, void* o, 
     return ATTN_OK;
 }
 
+int attn_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
+    if (timeout_ns < 1000 || timeout_ns > 2000000000ull) return ATTN_ERR_INVALID_ARG;
+    int num_sms = 0;
+    int st = check_device(&num_sms);
+    if (st != ATTN_OK) return st;
+    return attn::launch_wait_selftest(timeout_ns, static_cast<cudaStream_t>(stream));
+}
+
 int attn_device_status(void* stream, int clear) {
     unsigned err = 0, berr = 0, derr = 0;
     int st = attn::tc_device_error(static_cast<cudaStream_t>(stream), clear != 0, &err);
@@ -265,6 +273,6 @@ const char* attn_status_string(int status) {
     }
 }
 
-int attn_abi_version(void) { return (1 << 16) | 4; }
+int attn_abi_version(void) { return (1 << 16) | 5; }
 
 }  // extern "C"

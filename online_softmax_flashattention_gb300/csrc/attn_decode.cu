@@ -535,6 +535,22 @@ __global__ void __launch_bounds__(128) attn_decode_merge_kernel(const DecodePara
     if (p.lse != nullptr && lane == 0) p.lse[row] = mx + log2f(w_tot);
 }
 
+// A kernel whose one wait can never complete: a warp waits on the first phase of an mbarrier
+// nobody arrives on, with the caller's limit. When the limit runs out the warp takes the same
+// path as any kernel of this library (abort flag, device error word) and returns.
+__global__ void __launch_bounds__(32) attn_wait_selftest_kernel(uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_word;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_word = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const bool ok = mbar_wait(smem_u32(&bar), 0, nullptr, timeout_ns);
+    if (!__all_sync(0xffffffffu, ok) && threadIdx.x == 0) raise_abort(&abort_word);
+}
+
 // ------------------------------------------ host side ------------------------------------------
 int queries_per_group(int64_t Nq) { return Nq <= 1 ? 1 : Nq <= 2 ? 2 : Nq <= 4 ? 4 : 8; }
 
@@ -681,6 +697,11 @@ size_t decode_workspace_bytes(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int
     Plan pl;
     if (!plan_for(BH, Nq, Nk, d, 0, dtype, num_sms, &pl)) return 0;
     return pl.merge ? partial_bytes(BH, Nq, d, pl.P) : 0;
+}
+
+int launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream) {
+    attn_wait_selftest_kernel<<<1, 32, 0, stream>>>(timeout_ns);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 int decode_device_error(bool clear, unsigned* err) {

@@ -61,6 +61,10 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
 // occupancy, which this queries on the current device.
 size_t decode_workspace_bytes(int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int splits, int dtype, int num_sms);
 
+// Launches one warp whose only wait (on an mbarrier nobody arrives on) runs out after
+// timeout_ns; it then records a timeout in the decode kernel's device error word.
+int launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream);
+
 // Reads (and optionally clears) the decode kernel's device error word.
 int decode_device_error(bool clear, unsigned* err);
 

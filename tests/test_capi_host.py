@@ -168,3 +168,10 @@ def test_kvcache_valid_call_without_gpu_reports_device_error(lib):
     assert lib.attn_fwd_kvcache(P, P * 3, P * 5, P * 9, None, ws, 1 << 20, 1, 2, 4, 100, 64, 1, 1, 4, None) == 5
     assert lib.attn_fwd_kvcache(P, P * 3, P * 5, P * 9, None, None, 0, 1, 2, 4, 100, 64, 1, 1, 0, None) == 5
     assert lib.attn_kvcache_workspace_bytes(1, 2, 4, 100, 64, 0, 1) == 0  # balanced plan needs the device
+
+
+def test_selftest_limit_is_checked_before_the_device(lib):
+    assert lib.attn_selftest_wait_timeout(10, None) == 1           # below 1 us
+    assert lib.attn_selftest_wait_timeout(3_000_000_000, None) == 1  # above 2 s
+    if not __import__("torch").cuda.is_available():
+        assert lib.attn_selftest_wait_timeout(1_000_000, None) == 5

@@ -137,3 +137,18 @@ def test_injected_launch_fault_is_reported(monkeypatch):
     monkeypatch.delenv("ATTN_FAULT")
     fa.attn_fwd(x, x, x)
     torch.cuda.synchronize()
+
+
+def test_device_wait_timeout_is_reported_and_the_context_stays_usable():
+    # A wait that nothing completes runs out after 2 ms; the status reports it once, clearing
+    # works, and the next real call runs normally.
+    assert fa.attn_device_status(clear=True) == 0
+    fa.attn_selftest_wait_timeout(2_000_000)
+    assert fa.attn_device_status(clear=False) == 7
+    assert fa.attn_device_status(clear=True) == 7
+    assert fa.attn_device_status(clear=True) == 0
+    x = torch.randn(1, 2, 100, 64, device="cuda", dtype=torch.bfloat16)
+    o = fa.attn_fwd(x, x, x, causal=True)
+    torch.cuda.synchronize()
+    assert fa.attn_device_status(clear=True) == 0
+    assert torch.isfinite(o.float()).all()
