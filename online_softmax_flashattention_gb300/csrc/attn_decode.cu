@@ -679,8 +679,7 @@ bool plan_for(int64_t BH, int64_t Nq, int64_t Nk, int64_t D, int splits, int dty
     visit_cfg(dtype, D, queries_per_group(Nq), [&](auto t, auto qg, auto dd) -> int {
         using T = typename decltype(t)::type;
         rows = Cfg<T, decltype(dd)::value>::kRows;
-        // The explicit plan does not depend on occupancy; skip the device query for it.
-        per_sm = splits > 0 ? 1 : ctas_per_sm<T, decltype(qg)::value, decltype(dd)::value>();
+        per_sm = ctas_per_sm<T, decltype(qg)::value, decltype(dd)::value>();
         return 0;
     });
     if (per_sm <= 0) return false;

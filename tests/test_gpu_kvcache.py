@@ -164,3 +164,19 @@ def test_kvcache_head_width_128_decode_shape():
     ref_o, ref_lse = oracle.attn_fwd_kv(q, k, v, True)
     check(o.float().cpu().numpy().astype(np.float64), ref_o, "bf16", Nk, "decode d128 B8H8 Nk8192")
     assert float(np.max(np.abs(lse.cpu().numpy() - ref_lse))) <= _lse_bound(ref_lse)
+
+
+def test_kvcache_workspace_reused_across_calls_and_shapes():
+    # One workspace serves a sequence of calls with different shapes and share counts, with
+    # whatever the previous call left in it.
+    ws = torch.full((1 << 22,), 0xFF, dtype=torch.uint8, device="cuda")
+    for seed, (B, H, Nq, Nk, S) in enumerate([(1, 3, 2, 500, 6), (2, 2, 1, 3000, 0), (1, 3, 2, 500, 6),
+                                              (3, 1, 9, 700, 4), (2, 2, 1, 3000, 0)]):
+        q, k, v = _inputs(0xCAC3B000 + seed, B, H, Nq, Nk, "bf16")
+        qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+        assert fa.attn_kvcache_workspace_bytes(B, H, Nq, Nk, S, torch.bfloat16) <= ws.numel()
+        o, lse = fa.attn_fwd_kvcache(qd, kd, vd, causal=True, num_splits=S, workspace=ws, lse=True)
+        torch.cuda.synchronize()
+        ref_o, ref_lse = oracle.attn_fwd_kv(q, k, v, True)
+        check(o.float().cpu().numpy().astype(np.float64), ref_o, "bf16", Nk, f"reuse call {seed}")
+        assert float(np.max(np.abs(lse.cpu().numpy() - ref_lse))) <= _lse_bound(ref_lse)
