@@ -15,7 +15,8 @@
 // swizzle) and TS (A from tensor memory, B an MN-major tile).
 //   dK/dV kernel, per query block, with the keys in the 128 TMEM lanes:
 //     S^T = K Q^T (SS), dP^T = V dO^T (SS)               -> TMEM, 128 columns each
-//     the four "softmax" warps (thread = key) make P^T and dS^T = P^T (dP^T - delta) in
+//     the eight elementwise warps (thread = key; two warpgroups on the same TMEM lanes, each
+//     on half of the block's query columns) make P^T and dS^T = P^T (dP^T - delta) in
 //     registers and store them to TMEM as 16-bit pairs
 //     dV += P^T dO (TS, B = dO tile MN-major), dK += dS^T Q (TS, B = Q tile MN-major)
 //   dQ kernel, per key block, with the queries in the lanes:
@@ -26,8 +27,8 @@
 // delta is computed from the dO and O tiles in shared memory (the dK/dV kernel loads O for
 // that) and lse is read per block, so the call allocates nothing.
 //
-// Roles: warps 0-3 elementwise (thread = TMEM lane), warp 4 TMA producer, warp 5 MMA issuer
-// and tensor-memory owner. Every mbarrier wait is bounded; on expiry the kernel sets the
+// Roles: warps 0-7 elementwise (thread = TMEM lane; warps w and w + 4 share lanes and split the
+// columns), warp 8 TMA producer, warp 9 MMA issuer and tensor-memory owner. Every mbarrier wait is bounded; on expiry the kernel sets the
 // shared device error word (reported by attn_device_status), drains and returns.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -47,9 +48,10 @@ namespace {
 constexpr int kD = 64;
 constexpr int kBlk = 128;                   // queries or keys per block = TMEM lanes
 constexpr int kTile = kBlk * kD * 2;        // 16 KiB: one 128 x 64 tile of 16-bit values
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;
+constexpr int kElemWarps = 8;  // two warpgroups on the same TMEM lanes, each on half the columns
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr uint64_t kDrainTimeoutNs = 100000000ull;
@@ -122,6 +124,26 @@ __device__ __forceinline__ float row_dot(const uint8_t* a, const uint8_t* b, int
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
         const uint32_t off = sw128_offset(r, ch * 8);
+        const uint4 x = *reinterpret_cast<const uint4*>(a + off);
+        const uint4 y = *reinterpret_cast<const uint4*>(b + off);
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 u = unpack2<BF16>(xs[i]), v = unpack2<BF16>(ys[i]);
+            acc = fmaf(u.x, v.x, acc);
+            acc = fmaf(u.y, v.y, acc);
+        }
+    }
+    return acc;
+}
+
+// Half of sum_e a[r,e] b[r,e]: the 32 values of 16-byte chunks 4*half .. 4*half + 3.
+template <bool BF16>
+__device__ __forceinline__ float row_dot_half(const uint8_t* a, const uint8_t* b, int r, int half) {
+    float acc = 0.f;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+        const uint32_t off = sw128_offset(r, (4 * half + c4) * 8);
         const uint4 x = *reinterpret_cast<const uint4*>(a + off);
         const uint4 y = *reinterpret_cast<const uint4*>(b + off);
         const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
@@ -240,11 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(kvSFull), 1);
         mbar_init(bar(kvDPFull), 1);
-        mbar_init(bar(kvSdPFree), 4);
-        mbar_init(bar(kvPdSFull), 4);
+        mbar_init(bar(kvSdPFree), kElemWarps);
+        mbar_init(bar(kvPdSFull), kElemWarps);
         mbar_init(bar(kvDone), 1);
         mbar_init(bar(kvDrain), 1);
-        mbar_init(bar(kvRows), 4);
+        mbar_init(bar(kvRows), kElemWarps);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -257,20 +279,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 4) {
+    if (warp < kElemWarps) {
         // ===================== elementwise warps: thread = key (TMEM lane) =====================
-        const int r = threadIdx.x;  // key row within the block, = TMEM lane
+        const int g = warp >> 2;  // warpgroup: query columns 64g .. 64g + 63
+        const int r = ((warp & 3) << 5) + lane;  // key row within the block, = TMEM lane
         const int key = k0 + r;
-        const uint32_t t = tmem + (static_cast<uint32_t>(warp << 5) << 16);
+        const uint32_t t = tmem + (static_cast<uint32_t>((warp & 3) << 5) << 16);
         bool ok = true;
         for (int i = 0; ok && i < nq; ++i) {
             const int st = i & 1, q0 = (qb0 + i) * kBlk;
             // This block's lse and delta (thread r handles query q0 + r).
             if (!(ok = warp_wait(bar(kvQFull + st), (i >> 1) & 1, abort_flag))) break;
             const uint8_t* stage = gbase + kvOffStage + st * kvStageBytes;
-            const bool qin = q0 + r < N;
-            lse_s[st * kBlk + r] = qin ? p.lse[static_cast<int64_t>(bh) * N + q0 + r] : 0.f;
-            delta_s[st * kBlk + r] = qin ? row_dot<BF16>(stage + kTile, stage + 2 * kTile, r) : 0.f;
+            // Warpgroup g fills queries 64g .. 64g + 63, two threads per query (half a row each).
+            const int qi = 64 * g + (r >> 1), half = r & 1;
+            const bool qin = q0 + qi < N;
+            float dpart = qin ? row_dot_half<BF16>(stage + kTile, stage + 2 * kTile, qi, half) : 0.f;
+            dpart += __shfl_xor_sync(0xffffffffu, dpart, 1);
+            if (half == 0) {
+                lse_s[st * kBlk + qi] = qin ? p.lse[static_cast<int64_t>(bh) * N + q0 + qi] : 0.f;
+                delta_s[st * kBlk + qi] = dpart;
+            }
             // All four warps' rows written (a bounded wait, unlike a named barrier, so a warp that
             // gave up cannot leave the others waiting forever).
             __syncwarp();
@@ -287,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Only the causal diagonal block and ragged edges need a mask.
             const bool masked = (p.causal && qb0 + i == kblk) || q0 + kBlk > N || k0 + kBlk > N;
 #pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {  // 32 queries at a time
+            for (int ch = 2 * g; ch < 2 * g + 2; ++ch) {  // 32 queries at a time
                 if (masked)
                     kv_chunk<BF16, true>(t, ch, ls, dl, p.c, key, q0, N, p.causal);
                 else
@@ -306,27 +335,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && nq > 0) {
             if ((ok = warp_wait(bar(kvDone), (nq - 1) & 1, abort_flag))) {
                 tc_fence_after();
-                uint16_t* const dk = reinterpret_cast<uint16_t*>(p.grad0) + (static_cast<int64_t>(bh) * N + key) * kD;
-                uint16_t* const dv = reinterpret_cast<uint16_t*>(p.grad1) + (static_cast<int64_t>(bh) * N + key) * kD;
+                // Warpgroup 0 stores dK (scaled), warpgroup 1 dV.
+                uint16_t* const dst = reinterpret_cast<uint16_t*>(g == 0 ? p.grad0 : p.grad1) +
+                                      (static_cast<int64_t>(bh) * N + key) * kD;
+                const float sc = g == 0 ? p.scale : 1.f;
+                const uint32_t col = g == 0 ? kvColDK : kvColDV;
 #pragma unroll 1
                 for (int h = 0; h < 4; ++h) {
-                    uint32_t a[16], b[16];
-                    tmem_ld_x16(t + kvColDK + 16 * h, a);
-                    tmem_ld_x16(t + kvColDV + 16 * h, b);
+                    uint32_t a[16];
+                    tmem_ld_x16(t + col + 16 * h, a);
                     tmem_ld_wait();
-                    uint32_t pa[8], pb[8];
+                    uint32_t pa[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        pa[i] = pack2<BF16>(__uint_as_float(a[2 * i]) * p.scale, __uint_as_float(a[2 * i + 1]) * p.scale);
-                        pb[i] = pack2<BF16>(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        pa[i] = pack2<BF16>(__uint_as_float(a[2 * i]) * sc, __uint_as_float(a[2 * i + 1]) * sc);
                     if (key < N) {
-                        uint4* x = reinterpret_cast<uint4*>(dk + 16 * h);
+                        uint4* x = reinterpret_cast<uint4*>(dst + 16 * h);
                         x[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
                         x[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
-                        uint4* y = reinterpret_cast<uint4*>(dv + 16 * h);
-                        y[0] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
-                        y[1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
                     }
                 }
             }
@@ -474,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(qSFull), 1);
         mbar_init(bar(qDPFull), 1);
-        mbar_init(bar(qSdPFree), 4);
-        mbar_init(bar(qDSFull), 4);
+        mbar_init(bar(qSdPFree), kElemWarps);
+        mbar_init(bar(qDSFull), kElemWarps);
         mbar_init(bar(qDone), 1);
         mbar_init(bar(qDrain), 1);
         *abort_flag = 0;
@@ -490,12 +516,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 4) {
+    if (warp < kElemWarps) {
         // ==================== elementwise warps: thread = query (TMEM lane) ====================
-        const int r = threadIdx.x;
+        const int g = warp >> 2;  // warpgroup: key columns 64g .. 64g + 63
+        const int r = ((warp & 3) << 5) + lane;
         const int query = q0 + r;
         const bool qin = query < N;
-        const uint32_t t = tmem + (static_cast<uint32_t>(warp << 5) << 16);
+        const uint32_t t = tmem + (static_cast<uint32_t>((warp & 3) << 5) << 16);
         bool ok = warp_wait(bar(qQ), 0, abort_flag);
         // delta = dO . O for this row (O read from global), and the row's lse.
         float delta = 0.f, l2 = 0.f;
@@ -526,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool masked = (p.causal && j == qblk) || q0 + kBlk > N || k0 + kBlk > N;
 #pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {  // 32 keys at a time
+            for (int ch = 2 * g; ch < 2 * g + 2; ++ch) {  // 32 keys at a time
                 if (masked)
                     q_chunk<BF16, true>(t, ch, l2, delta, p.c, query, k0, N, p.causal);
                 else
@@ -546,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 uint16_t* const dq = reinterpret_cast<uint16_t*>(p.grad0) + (static_cast<int64_t>(bh) * N + query) * kD;
 #pragma unroll 1
-                for (int h = 0; h < 4; ++h) {
+                for (int h = 2 * g; h < 2 * g + 2; ++h) {  // warpgroup g: dims 32g .. 32g + 31
                     uint32_t a[16];
                     tmem_ld_x16(t + qColDQ + 16 * h, a);
                     tmem_ld_wait();
