@@ -339,11 +339,32 @@ def decode_leg(dev, stream, steps, warmup, with_cpu, cpu_seconds):
     if fa.attn_device_status(clear=True, device=dev) != 0:
         raise RuntimeError("device-side timeout in the timed decode runs")
     us = e0.elapsed_time(e1) / steps * 1e3
+    # The same calls captured once into a CUDA graph and replayed (how a serving loop would run
+    # them): reported beside, not as the value.
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cs):
+        fa.attn_fwd_kvcache(q, k, v, causal=True, workspace=ws, out=o, lse=lse)
+    torch.cuda.current_stream(dev).wait_stream(cs)
+    with torch.cuda.graph(g):
+        for _ in range(10):
+            fa.attn_fwd_kvcache(q, k, v, causal=True, workspace=ws, out=o, lse=lse)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    reps = max(1, steps // 10)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    graph_us = e0.elapsed_time(e1) / (10 * reps) * 1e3
     nbytes = decode_bytes(w["B"], w["H"], w["Nq"], w["Nk"], w["d"])
     peaks, peak_src = load_peaks()
     gbs = nbytes / (us * 1e-6) / 1e9
     traffic, traffic_src = recorded_traffic(DECODE_PROFILE, DECODE_SOURCE)
     out = {"config": dict(DECODE), "steps": steps, "us_per_step": us, "value": gbs, "unit": "GB/s",
+           "graph_replay": {"us_per_step": graph_us, "value": nbytes / (graph_us * 1e-6) / 1e9, "unit": "GB/s"},
            "l2": "not flushed: K and V (403 MB) exceed L2; steps run back to back",
            "launches_per_step": 2 if ws_bytes > 0 else 1,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",

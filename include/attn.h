@@ -68,8 +68,8 @@ typedef enum {
  *   B, H, N : sizes >= 0, N <= ATTN_MAX_N, B*H < 2^31. B*H == 0 or N == 0 is a successful
  *             no-op (pointers may then be NULL)
  *   d       : head width, 64 or 128 (ATTN_ERR_UNSUPPORTED otherwise). The pages fix 64; 128
- *             is the other common width (scale 1/sqrt(128)). attn_fwd, attn_fwd_lse and
- *             attn_fwd_kvcache take both; attn_bwd and the materialised path take 64.
+ *             is the other common width (scale 1/sqrt(128)). attn_fwd, attn_fwd_lse, attn_bwd
+ *             and attn_fwd_kvcache take both; the materialised path takes 64.
  *   causal  : 0 (every key visible) or 1 (key j visible to query i iff j <= i)
  *   dtype   : attn_dtype_t. bf16/f16 inputs are multiplied on tcgen05 tensor cores with
  *             fp32 accumulation; the probabilities are rounded to the input type before
@@ -250,7 +250,7 @@ const char* attn_status_string(int status);
 
 /* ABI version of this header: (major << 16) | minor (1.1 added attn_fwd_lse, 1.2 attn_bwd,
  * 1.3 attn_fwd_kvcache, 1.4 head width 128 for the forward entry points, 1.5
- * attn_selftest_wait_timeout). */
+ * attn_selftest_wait_timeout, 1.6 head width 128 for attn_bwd). */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

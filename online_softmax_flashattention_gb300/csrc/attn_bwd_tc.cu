@@ -45,9 +45,8 @@
 namespace attn {
 namespace {
 
-constexpr int kD = 64;
 constexpr int kBlk = 128;                   // queries or keys per block = TMEM lanes
-constexpr int kTile = kBlk * kD * 2;        // 16 KiB: one 128 x 64 tile of 16-bit values
+constexpr int kBlockBytes = kBlk * 64 * 2;  // 16 KiB: 128 rows x 128 bytes (64 values), one TMA box
 constexpr int kThreads = 320;
 constexpr int kElemWarps = 8;  // two warpgroups on the same TMEM lanes, each on half the columns
 constexpr int kProducerWarp = 8;
@@ -157,53 +156,105 @@ __device__ __forceinline__ float row_dot_half(const uint8_t* a, const uint8_t* b
     return acc;
 }
 
-// 128 x 128 product over K = 64 (four K=16 steps) of two K-major tiles into TMEM columns `d`.
+// sum_e a[e] b[e] over one 64-value row of a swizzled tile (a: row r of the tile at `tile`) and
+// 64 contiguous values in global memory (b).
 template <bool BF16>
+__device__ __forceinline__ float row_dot_global(const uint8_t* tile, int r, const uint16_t* b) {
+    float acc = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        const uint4 x = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, ch * 8));
+        const uint4 y = *reinterpret_cast<const uint4*>(b + ch * 8);
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 u = unpack2<BF16>(xs[i]), v = unpack2<BF16>(ys[i]);
+            acc = fmaf(u.x, v.x, acc);
+            acc = fmaf(u.y, v.y, acc);
+        }
+    }
+    return acc;
+}
+
+// 128 x 128 product over K = D of two K-major tiles (each D/64 column blocks of 128-byte rows)
+// into TMEM columns `d`: D/16 steps of K = 16, the ones past 64 in the second column block.
+template <bool BF16, int D>
 __device__ __forceinline__ void mma_ss_128x128(uint32_t d, uint32_t sA, uint32_t sB) {
     constexpr uint32_t kIdesc = idesc_f16(BF16, kBlk, kBlk, false, false);
 #pragma unroll
-    for (int kk = 0; kk < kD / 16; ++kk)
-        umma_ss(d, smem_desc_sw128(sA + 32 * kk, 16, 1024), smem_desc_sw128(sB + 32 * kk, 16, 1024), kIdesc,
-                kk > 0 ? 1u : 0u);
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = static_cast<uint32_t>((kk >> 2) * kBlockBytes + 32 * (kk & 3));
+        umma_ss(d, smem_desc_sw128(sA + off, 16, 1024), smem_desc_sw128(sB + off, 16, 1024), kIdesc, kk > 0 ? 1u : 0u);
+    }
 }
 
-// 128 x 64 product over K = 128 with A (128 lanes x 128 16-bit values) in TMEM columns `a`
-// and B an MN-major 128 x 64 tile (rows = K), accumulated into TMEM columns `d`.
-template <bool BF16>
-__device__ __forceinline__ void mma_ts_128x64(uint32_t d, uint32_t a, uint32_t sB, bool accumulate) {
-    constexpr uint32_t kIdesc = idesc_f16(BF16, kBlk, kD, false, true);
+// 128 x D product over K = 128 with A (128 lanes x 128 16-bit values) in TMEM and B an MN-major
+// tile (rows = K; D/64 column blocks 16 KiB apart, the descriptor's leading byte offset),
+// accumulated into TMEM columns `d`. A's K-step kk sits at column a + 8 kk, or, with `split`,
+// a + 8 kk + 32 for kk >= 4 (the layout the d = 128 dK/dV kernel writes over S^T and dP^T).
+template <bool BF16, int D>
+__device__ __forceinline__ void mma_ts_128xD(uint32_t d, uint32_t a, uint32_t sB, bool accumulate, bool split) {
+    constexpr uint32_t kIdesc = idesc_f16(BF16, kBlk, D, false, true);
+    constexpr uint32_t kLbo = D == 64 ? 16u : static_cast<uint32_t>(kBlockBytes);
 #pragma unroll
     for (int kk = 0; kk < kBlk / 16; ++kk)
-        umma_ts(d, a + 8u * kk, smem_desc_sw128(sB + 2048 * kk, 16, 1024), kIdesc, (accumulate || kk > 0) ? 1u : 0u);
+        umma_ts(d, a + 8u * kk + ((split && kk >= 4) ? 32u : 0u), smem_desc_sw128(sB + 2048 * kk, kLbo, 1024), kIdesc,
+                (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// TMA copy of one 128-row tile of a [BH][N][D] tensor: D/64 boxes of 128 rows x 64 values.
+template <int D>
+__device__ __forceinline__ void tma_tile(uint32_t dst, const void* map, int row, int bh, uint32_t bar) {
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * kBlockBytes, map, 64 * c, row, bh, bar);
 }
 
 // ================================ dK, dV: one CTA per key block ================================
-// Shared memory: K, V tiles, then two stages of (Q, dO, O) tiles, then per-block lse and
-// delta (double-buffered by block parity), then mbarriers.
-constexpr int kvOffK = 0;
-constexpr int kvOffV = kTile;
-constexpr int kvOffStage = 2 * kTile;          // stage s: Q at +0, dO at +kTile, O at +2 kTile
-constexpr int kvStageBytes = 3 * kTile;
-constexpr int kvOffRow = kvOffStage + 2 * kvStageBytes;  // lse[2][128], delta[2][128] floats
-constexpr int kvOffBar = kvOffRow + 4 * kBlk * 4;
+// Shared memory: K, V tiles, then two stages of (Q, dO[, O]) tiles, then per-block lse and delta
+// (double-buffered by block parity), then mbarriers. At d = 64 the O tile comes with each stage
+// and delta is a row product of two tiles; at d = 128 the stage holds Q and dO only (two stages of
+// three 32 KiB tiles would not fit) and delta reads O's rows from global memory.
+// Tensor memory: S^T 0, dP^T 128; d = 64: P^T 256, dS^T 320, dV 384, dK 448; d = 128 (dV and dK
+// take 128 columns each): dV 256, dK 384, and P^T and dS^T are written over the S^T and dP^T
+// columns the elementwise warps have already read (chunk ch at 16 ch, + 32 for ch >= 2, so each
+// warpgroup writes only over its own columns), which makes the next block's S^T, dP^T wait for
+// this block's dV, dK products.
 enum { kvKV = 0, kvQFull = 1, kvQEmpty = 3, kvSFull = 5, kvDPFull, kvSdPFree, kvPdSFull, kvDone, kvDrain,
-       kvRows, kvNumBars };  // kvRows: the four elementwise warps wrote this block's lse and delta
-constexpr int kvOffSlot = kvOffBar + 8 * kvNumBars;
-constexpr int kvOffAbort = kvOffSlot + 4;
-constexpr int kvSmem = kvOffAbort + 4 + 1024;
-static_assert(kvSmem <= 227 * 1024, "shared memory budget");
-constexpr uint32_t kvColS = 0, kvColDP = 128, kvColP = 256, kvColDS = 320, kvColDV = 384, kvColDK = 448;
+       kvRows, kvNumBars };  // kvRows: the elementwise warps wrote this block's lse and delta
 
+template <int D>
+struct KvLay {
+    static constexpr int kTile = kBlk * D * 2;
+    static constexpr bool kOInStage = D == 64;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kTile;
+    static constexpr int kOffStage = 2 * kTile;  // stage s: Q at +0, dO at +kTile, (O at +2 kTile)
+    static constexpr int kStageBytes = (kOInStage ? 3 : 2) * kTile;
+    static constexpr int kOffRow = kOffStage + 2 * kStageBytes;  // lse[2][128], delta[2][128] floats
+    static constexpr int kOffBar = kOffRow + 4 * kBlk * 4;
+    static constexpr int kOffSlot = kOffBar + 8 * kvNumBars;
+    static constexpr int kOffAbort = kOffSlot + 4;
+    static constexpr int kSmem = kOffAbort + 4 + 1024;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    static constexpr bool kAlias = D > 64;
+    static constexpr uint32_t kColS = 0, kColDP = 128;
+    static constexpr uint32_t kColP = kAlias ? 0 : 256, kColDS = kAlias ? 128 : 320;
+    static constexpr uint32_t kColDV = kAlias ? 256 : 384, kColDK = kAlias ? 384 : 448;
+    __host__ __device__ static constexpr uint32_t chunk_col(int ch) {
+        return static_cast<uint32_t>(16 * ch + ((kAlias && ch >= 2) ? 32 : 0));
+    }
+};
 
 // One 32-query chunk of the dK/dV kernel's elementwise step for this thread's key: P^T and
 // dS^T = P^T (dP^T - delta) from S^T and dP^T in TMEM, stored back as 16-bit pairs. The
 // queries' lse and delta come from shared memory four at a time.
-template <bool BF16, bool kMasked>
+template <bool BF16, bool kMasked, int D>
 __device__ __forceinline__ void kv_chunk(uint32_t t, int ch, const float* ls, const float* dl, float c, int key,
                                          int q0, int N, int causal) {
+    using L = KvLay<D>;
     uint32_t s[32], dp[32];
-    ATTN_TMEM_LD_X32(t + kvColS + 32 * ch, s);
-    ATTN_TMEM_LD_X32(t + kvColDP + 32 * ch, dp);
+    ATTN_TMEM_LD_X32(t + L::kColS + 32 * ch, s);
+    ATTN_TMEM_LD_X32(t + L::kColDP + 32 * ch, dp);
     tmem_ld_wait();
     uint32_t pp[16], ds[16];
 #pragma unroll
@@ -227,23 +278,25 @@ __device__ __forceinline__ void kv_chunk(uint32_t t, int ch, const float* ls, co
         ds[2 * u4] = pack2<BF16>(dv[0], dv[1]);
         ds[2 * u4 + 1] = pack2<BF16>(dv[2], dv[3]);
     }
-    tmem_st_x16(t + kvColP + 16 * ch, pp);
-    tmem_st_x16(t + kvColDS + 16 * ch, ds);
+    tmem_st_x16(t + L::kColP + L::chunk_col(ch), pp);
+    tmem_st_x16(t + L::kColDS + L::chunk_col(ch), ds);
 }
 
-template <bool BF16>
+template <bool BF16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                             const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+    using L = KvLay<D>;
+    constexpr int kTile = L::kTile;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const gbase = smem_raw + (base - raw);
-    auto bar = [&](int i) -> uint32_t { return base + kvOffBar + 8u * static_cast<uint32_t>(i); };
-    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + kvOffSlot);
-    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + kvOffAbort);
-    float* const lse_s = reinterpret_cast<float*>(gbase + kvOffRow);     // [2][128]
+    auto bar = [&](int i) -> uint32_t { return base + L::kOffBar + 8u * static_cast<uint32_t>(i); };
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kOffSlot);
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + L::kOffAbort);
+    float* const lse_s = reinterpret_cast<float*>(gbase + L::kOffRow);  // [2][128]
     float* const delta_s = lse_s + 2 * kBlk;                              // [2][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -288,19 +341,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int i = 0; ok && i < nq; ++i) {
             const int st = i & 1, q0 = (qb0 + i) * kBlk;
-            // This block's lse and delta (thread r handles query q0 + r).
+            // This block's lse and delta: warpgroup g fills queries 64g .. 64g + 63, two threads
+            // per query (one half of the row's dot product each).
             if (!(ok = warp_wait(bar(kvQFull + st), (i >> 1) & 1, abort_flag))) break;
-            const uint8_t* stage = gbase + kvOffStage + st * kvStageBytes;
-            // Warpgroup g fills queries 64g .. 64g + 63, two threads per query (half a row each).
+            const uint8_t* stage = gbase + L::kOffStage + st * L::kStageBytes;
             const int qi = 64 * g + (r >> 1), half = r & 1;
             const bool qin = q0 + qi < N;
-            float dpart = qin ? row_dot_half<BF16>(stage + kTile, stage + 2 * kTile, qi, half) : 0.f;
+            float dpart = 0.f;
+            if (qin) {
+                if constexpr (L::kOInStage) {
+                    dpart = row_dot_half<BF16>(stage + kTile, stage + 2 * kTile, qi, half);
+                } else {
+                    const uint16_t* orow = reinterpret_cast<const uint16_t*>(p.o) +
+                                           (static_cast<int64_t>(bh) * N + q0 + qi) * D + 64 * half;
+                    dpart = row_dot_global<BF16>(stage + kTile + half * kBlockBytes, qi, orow);
+                }
+            }
             dpart += __shfl_xor_sync(0xffffffffu, dpart, 1);
             if (half == 0) {
                 lse_s[st * kBlk + qi] = qin ? p.lse[static_cast<int64_t>(bh) * N + q0 + qi] : 0.f;
                 delta_s[st * kBlk + qi] = dpart;
             }
-            // All four warps' rows written (a bounded wait, unlike a named barrier, so a warp that
+            // All warps' rows written (a bounded wait, unlike a named barrier, so a warp that
             // gave up cannot leave the others waiting forever).
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kvRows));
@@ -318,9 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int ch = 2 * g; ch < 2 * g + 2; ++ch) {  // 32 queries at a time
                 if (masked)
-                    kv_chunk<BF16, true>(t, ch, ls, dl, p.c, key, q0, N, p.causal);
+                    kv_chunk<BF16, true, D>(t, ch, ls, dl, p.c, key, q0, N, p.causal);
                 else
-                    kv_chunk<BF16, false>(t, ch, ls, dl, p.c, key, q0, N, p.causal);
+                    kv_chunk<BF16, false, D>(t, ch, ls, dl, p.c, key, q0, N, p.causal);
             }
             // S^T and dP^T are copied out: the next block's products may overwrite them.
             tc_fence_before();
@@ -331,24 +393,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kvPdSFull));
         }
-        // ---- epilogue: dK * scale and dV, rounded to the output type; keys >= N not stored ----
+        // ---- epilogue: dK * scale (warpgroup 0) and dV (warpgroup 1), rounded; keys >= N not stored ----
         if (ok && nq > 0) {
             if ((ok = warp_wait(bar(kvDone), (nq - 1) & 1, abort_flag))) {
                 tc_fence_after();
-                // Warpgroup 0 stores dK (scaled), warpgroup 1 dV.
                 uint16_t* const dst = reinterpret_cast<uint16_t*>(g == 0 ? p.grad0 : p.grad1) +
-                                      (static_cast<int64_t>(bh) * N + key) * kD;
+                                      (static_cast<int64_t>(bh) * N + key) * D;
                 const float sc = g == 0 ? p.scale : 1.f;
-                const uint32_t col = g == 0 ? kvColDK : kvColDV;
+                const uint32_t col = g == 0 ? L::kColDK : L::kColDV;
 #pragma unroll 1
-                for (int h = 0; h < 4; ++h) {
+                for (int h = 0; h < D / 16; ++h) {
                     uint32_t a[16];
                     tmem_ld_x16(t + col + 16 * h, a);
                     tmem_ld_wait();
                     uint32_t pa[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        pa[i] = pack2<BF16>(__uint_as_float(a[2 * i]) * sc, __uint_as_float(a[2 * i + 1]) * sc);
+                    for (int j = 0; j < 8; ++j)
+                        pa[j] = pack2<BF16>(__uint_as_float(a[2 * j]) * sc, __uint_as_float(a[2 * j + 1]) * sc);
                     if (key < N) {
                         uint4* x = reinterpret_cast<uint4*>(dst + 16 * h);
                         x[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
@@ -363,21 +424,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
-        prefetch_tmap(&tm_o);
         prefetch_tmap(&tm_do);
+        if constexpr (L::kOInStage) prefetch_tmap(&tm_o);
         mbar_arrive_expect_tx(bar(kvKV), 2 * kTile);
-        tma_load_3d(base + kvOffK, &tm_k, 0, k0, bh, bar(kvKV));
-        tma_load_3d(base + kvOffV, &tm_v, 0, k0, bh, bar(kvKV));
+        tma_tile<D>(base + L::kOffK, &tm_k, k0, bh, bar(kvKV));
+        tma_tile<D>(base + L::kOffV, &tm_v, k0, bh, bar(kvKV));
         bool ok = true;
         int issued = 0;
         for (int i = 0; i < nq; ++i) {
             const int st = i & 1, q0 = (qb0 + i) * kBlk;
             if (!(ok = mbar_wait(bar(kvQEmpty + st), ((i >> 1) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
-            const uint32_t stage = base + kvOffStage + st * kvStageBytes;
-            mbar_arrive_expect_tx(bar(kvQFull + st), 3 * kTile);
-            tma_load_3d(stage, &tm_q, 0, q0, bh, bar(kvQFull + st));
-            tma_load_3d(stage + kTile, &tm_do, 0, q0, bh, bar(kvQFull + st));
-            tma_load_3d(stage + 2 * kTile, &tm_o, 0, q0, bh, bar(kvQFull + st));
+            const uint32_t stage = base + L::kOffStage + st * L::kStageBytes;
+            mbar_arrive_expect_tx(bar(kvQFull + st), L::kStageBytes);
+            tma_tile<D>(stage, &tm_q, q0, bh, bar(kvQFull + st));
+            tma_tile<D>(stage + kTile, &tm_do, q0, bh, bar(kvQFull + st));
+            if constexpr (L::kOInStage) tma_tile<D>(stage + 2 * kTile, &tm_o, q0, bh, bar(kvQFull + st));
             issued = i + 1;
         }
         if (!ok) raise_abort(abort_flag);
@@ -387,32 +448,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(bar(kvQFull + (i & 1)), (i >> 1) & 1, nullptr, kDrainTimeoutNs);
     } else if (warp == kMmaWarp && lane == 0) {
         // ================================ MMA issuer ================================
-        // S^T(0), dP^T(0); then per block i: S^T(i+1), dP^T(i+1) once block i's were copied
-        // out, and dV, dK += block i's P^T dO, dS^T Q once P^T and dS^T are in TMEM.
+        // S^T(0), dP^T(0); then per block i: S^T(i+1), dP^T(i+1) once block i's were copied out
+        // (d = 128: once block i's dV, dK products are done, as P^T and dS^T sit over S^T and
+        // dP^T), and dV, dK += block i's P^T dO, dS^T Q once P^T and dS^T are in TMEM.
         bool ok = mbar_wait(bar(kvKV), 0, abort_flag, kWaitTimeoutNs);
         auto issue_sdp = [&](int i) {
-            const uint32_t stage = base + kvOffStage + (i & 1) * kvStageBytes;
+            const uint32_t stage = base + L::kOffStage + (i & 1) * L::kStageBytes;
             if (!mbar_wait(bar(kvQFull + (i & 1)), (i >> 1) & 1, abort_flag, kWaitTimeoutNs)) return false;
             tc_fence_after();
-            mma_ss_128x128<BF16>(tmem + kvColS, base + kvOffK, stage);           // S^T = K Q^T
+            mma_ss_128x128<BF16, D>(tmem + L::kColS, base + L::kOffK, stage);           // S^T = K Q^T
             umma_commit(bar(kvSFull));
-            mma_ss_128x128<BF16>(tmem + kvColDP, base + kvOffV, stage + kTile);  // dP^T = V dO^T
+            mma_ss_128x128<BF16, D>(tmem + L::kColDP, base + L::kOffV, stage + kTile);  // dP^T = V dO^T
             umma_commit(bar(kvDPFull));
             return true;
         };
         if (ok && nq > 0) ok = issue_sdp(0);
         for (int i = 0; ok && i < nq; ++i) {
-            if (i + 1 < nq) {
+            if (!L::kAlias && i + 1 < nq) {
                 if (!(ok = mbar_wait(bar(kvSdPFree), i & 1, abort_flag, kWaitTimeoutNs))) break;
                 if (!(ok = issue_sdp(i + 1))) break;
             }
             if (!(ok = mbar_wait(bar(kvPdSFull), i & 1, abort_flag, kWaitTimeoutNs))) break;
             tc_fence_after();
-            const uint32_t stage = base + kvOffStage + (i & 1) * kvStageBytes;
-            mma_ts_128x64<BF16>(tmem + kvColDV, tmem + kvColP, stage + kTile, i > 0);  // dV += P^T dO
-            mma_ts_128x64<BF16>(tmem + kvColDK, tmem + kvColDS, stage, i > 0);          // dK += dS^T Q
+            const uint32_t stage = base + L::kOffStage + (i & 1) * L::kStageBytes;
+            mma_ts_128xD<BF16, D>(tmem + L::kColDV, tmem + L::kColP, stage + kTile, i > 0, L::kAlias);  // dV += P^T dO
+            mma_ts_128xD<BF16, D>(tmem + L::kColDK, tmem + L::kColDS, stage, i > 0, L::kAlias);          // dK += dS^T Q
             umma_commit(bar(kvDone));
             umma_commit(bar(kvQEmpty + (i & 1)));
+            if (L::kAlias && i + 1 < nq) {
+                if (!(ok = mbar_wait(bar(kvDone), i & 1, abort_flag, kWaitTimeoutNs))) break;
+                tc_fence_after();
+                if (!(ok = issue_sdp(i + 1))) break;
+            }
         }
         if (!ok) raise_abort(abort_flag);
         umma_commit(bar(kvDrain));
@@ -429,29 +496,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ================================== dQ: one CTA per query block ==================================
-constexpr int qOffQ = 0;
-constexpr int qOffDO = kTile;
-constexpr int qOffKV = 2 * kTile;               // stage s: K at +0, V at +kTile
-constexpr int qStageBytes = 2 * kTile;
-constexpr int qStages = 3;
-constexpr int qOffBar = qOffKV + qStages * qStageBytes;
-enum { qQ = 0, qKVFull = 1, qKVEmpty = qKVFull + qStages, qSFull = qKVEmpty + qStages, qDPFull, qSdPFree, qDSFull,
-       qDone, qDrain, qNumBars };
-constexpr int qOffSlot = qOffBar + 8 * qNumBars;
-constexpr int qOffAbort = qOffSlot + 4;
-constexpr int qSmem = qOffAbort + 4 + 1024;
-static_assert(qSmem <= 227 * 1024, "shared memory budget");
-constexpr uint32_t qColS = 0, qColDP = 128, qColDS = 256, qColDQ = 320;
+// Shared memory: Q and dO tiles, then a ring of (K, V) stages (three at d = 64, two at d = 128).
+// Tensor memory: S 0, dP 128, dS 256 (64 columns), dQ 320 (d columns).
+enum { qQ = 0, qKVFull = 1 };
 
+template <int D>
+struct QLay {
+    static constexpr int kTile = kBlk * D * 2;
+    static constexpr int kStages = D == 64 ? 3 : 2;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffDO = kTile;
+    static constexpr int kOffKV = 2 * kTile;  // stage s: K at +0, V at +kTile
+    static constexpr int kStageBytes = 2 * kTile;
+    static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
+    static constexpr int kKVEmpty = qKVFull + kStages;
+    static constexpr int kSFull = kKVEmpty + kStages;
+    static constexpr int kDPFull = kSFull + 1, kSdPFree = kSFull + 2, kDSFull = kSFull + 3, kDone = kSFull + 4,
+                         kDrain = kSFull + 5, kNumBars = kSFull + 6;
+    static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
+    static constexpr int kOffAbort = kOffSlot + 4;
+    static constexpr int kSmem = kOffAbort + 4 + 1024;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 320;
+};
 
 // One 32-key chunk of the dQ kernel's elementwise step for this thread's query: dS = P (dP -
 // delta) from S and dP in TMEM, stored back as 16-bit pairs.
-template <bool BF16, bool kMasked>
+template <bool BF16, bool kMasked, int D>
 __device__ __forceinline__ void q_chunk(uint32_t t, int ch, float l2, float delta, float c, int query, int k0, int N,
                                         int causal) {
+    using L = QLay<D>;
     uint32_t s[32], dp[32];
-    ATTN_TMEM_LD_X32(t + qColS + 32 * ch, s);
-    ATTN_TMEM_LD_X32(t + qColDP + 32 * ch, dp);
+    ATTN_TMEM_LD_X32(t + L::kColS + 32 * ch, s);
+    ATTN_TMEM_LD_X32(t + L::kColDP + 32 * ch, dp);
     tmem_ld_wait();
     uint32_t ds[16];
 #pragma unroll
@@ -468,21 +545,24 @@ __device__ __forceinline__ void q_chunk(uint32_t t, int ch, float l2, float delt
         }
         ds[u] = pack2<BF16>(dv[0], dv[1]);
     }
-    tmem_st_x16(t + qColDS + 16 * ch, ds);
+    tmem_st_x16(t + L::kColDS + 16 * ch, ds);
 }
 
-template <bool BF16>
+template <bool BF16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                           const BwdParams p) {
+    using L = QLay<D>;
+    constexpr int kTile = L::kTile;
+    constexpr int S = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const gbase = smem_raw + (base - raw);
-    auto bar = [&](int i) -> uint32_t { return base + qOffBar + 8u * static_cast<uint32_t>(i); };
-    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + qOffSlot);
-    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + qOffAbort);
+    auto bar = [&](int i) -> uint32_t { return base + L::kOffBar + 8u * static_cast<uint32_t>(i); };
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kOffSlot);
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + L::kOffAbort);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = p.N;
@@ -494,16 +574,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(qQ), 1);
-        for (int s = 0; s < qStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(bar(qKVFull + s), 1);
-            mbar_init(bar(qKVEmpty + s), 1);
+            mbar_init(bar(L::kKVEmpty + s), 1);
         }
-        mbar_init(bar(qSFull), 1);
-        mbar_init(bar(qDPFull), 1);
-        mbar_init(bar(qSdPFree), kElemWarps);
-        mbar_init(bar(qDSFull), kElemWarps);
-        mbar_init(bar(qDone), 1);
-        mbar_init(bar(qDrain), 1);
+        mbar_init(bar(L::kSFull), 1);
+        mbar_init(bar(L::kDPFull), 1);
+        mbar_init(bar(L::kSdPFree), kElemWarps);
+        mbar_init(bar(L::kDSFull), kElemWarps);
+        mbar_init(bar(L::kDone), 1);
+        mbar_init(bar(L::kDrain), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -527,55 +607,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         // delta = dO . O for this row (O read from global), and the row's lse.
         float delta = 0.f, l2 = 0.f;
         if (ok && qin) {
-            const uint8_t* dO = gbase + qOffDO;
-            const uint16_t* orow = reinterpret_cast<const uint16_t*>(p.o) + (static_cast<int64_t>(bh) * N + query) * kD;
+            const uint16_t* orow = reinterpret_cast<const uint16_t*>(p.o) + (static_cast<int64_t>(bh) * N + query) * D;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const uint4 x = *reinterpret_cast<const uint4*>(dO + sw128_offset(r, ch * 8));
-                const uint4 y = *reinterpret_cast<const uint4*>(orow + ch * 8);
-                const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 u = unpack2<BF16>(xs[i]), v = unpack2<BF16>(ys[i]);
-                    delta = fmaf(u.x, v.x, delta);
-                    delta = fmaf(u.y, v.y, delta);
-                }
-            }
+            for (int c = 0; c < D / 64; ++c)
+                delta += row_dot_global<BF16>(gbase + L::kOffDO + c * kBlockBytes, r, orow + 64 * c);
             l2 = p.lse[static_cast<int64_t>(bh) * N + query];
         }
         for (int j = 0; ok && j < nk; ++j) {
             const int k0 = j * kBlk;
-            if (!(ok = warp_wait(bar(qSFull), j & 1, abort_flag))) break;
-            if (!(ok = warp_wait(bar(qDPFull), j & 1, abort_flag))) break;
+            if (!(ok = warp_wait(bar(L::kSFull), j & 1, abort_flag))) break;
+            if (!(ok = warp_wait(bar(L::kDPFull), j & 1, abort_flag))) break;
             tc_fence_after();
             // The previous block's dQ product reads dS: wait before overwriting it.
-            if (j > 0 && !(ok = warp_wait(bar(qDone), (j - 1) & 1, abort_flag))) break;
+            if (j > 0 && !(ok = warp_wait(bar(L::kDone), (j - 1) & 1, abort_flag))) break;
             tc_fence_after();
             const bool masked = (p.causal && j == qblk) || q0 + kBlk > N || k0 + kBlk > N;
 #pragma unroll 1
             for (int ch = 2 * g; ch < 2 * g + 2; ++ch) {  // 32 keys at a time
                 if (masked)
-                    q_chunk<BF16, true>(t, ch, l2, delta, p.c, query, k0, N, p.causal);
+                    q_chunk<BF16, true, D>(t, ch, l2, delta, p.c, query, k0, N, p.causal);
                 else
-                    q_chunk<BF16, false>(t, ch, l2, delta, p.c, query, k0, N, p.causal);
+                    q_chunk<BF16, false, D>(t, ch, l2, delta, p.c, query, k0, N, p.causal);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(qSdPFree));
+            if (lane == 0) mbar_arrive(bar(L::kSdPFree));
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(qDSFull));
+            if (lane == 0) mbar_arrive(bar(L::kDSFull));
         }
-        // ---- epilogue: dQ * scale, rounded to the output type; rows >= N not stored ----
+        // ---- epilogue: dQ * scale (warpgroup g: dims D/2 g .. D/2 (g + 1) - 1), rounded; rows >= N not stored ----
         if (ok && nk > 0) {
-            if ((ok = warp_wait(bar(qDone), (nk - 1) & 1, abort_flag))) {
+            if ((ok = warp_wait(bar(L::kDone), (nk - 1) & 1, abort_flag))) {
                 tc_fence_after();
-                uint16_t* const dq = reinterpret_cast<uint16_t*>(p.grad0) + (static_cast<int64_t>(bh) * N + query) * kD;
+                uint16_t* const dq = reinterpret_cast<uint16_t*>(p.grad0) + (static_cast<int64_t>(bh) * N + query) * D;
 #pragma unroll 1
-                for (int h = 2 * g; h < 2 * g + 2; ++h) {  // warpgroup g: dims 32g .. 32g + 31
+                for (int h = g * (D / 32); h < (g + 1) * (D / 32); ++h) {
                     uint32_t a[16];
-                    tmem_ld_x16(t + qColDQ + 16 * h, a);
+                    tmem_ld_x16(t + L::kColDQ + 16 * h, a);
                     tmem_ld_wait();
                     uint32_t pa[8];
 #pragma unroll
@@ -597,53 +667,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_do);
         mbar_arrive_expect_tx(bar(qQ), 2 * kTile);
-        tma_load_3d(base + qOffQ, &tm_q, 0, q0, bh, bar(qQ));
-        tma_load_3d(base + qOffDO, &tm_do, 0, q0, bh, bar(qQ));
+        tma_tile<D>(base + L::kOffQ, &tm_q, q0, bh, bar(qQ));
+        tma_tile<D>(base + L::kOffDO, &tm_do, q0, bh, bar(qQ));
         bool ok = true;
         int issued = 0;
         for (int j = 0; j < nk; ++j) {
-            const int st = j % qStages;
-            if (!(ok = mbar_wait(bar(qKVEmpty + st), ((j / qStages) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
-            const uint32_t stage = base + qOffKV + st * qStageBytes;
+            const int st = j % S;
+            if (!(ok = mbar_wait(bar(L::kKVEmpty + st), ((j / S) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
+            const uint32_t stage = base + L::kOffKV + st * L::kStageBytes;
             mbar_arrive_expect_tx(bar(qKVFull + st), 2 * kTile);
-            tma_load_3d(stage, &tm_k, 0, j * kBlk, bh, bar(qKVFull + st));
-            tma_load_3d(stage + kTile, &tm_v, 0, j * kBlk, bh, bar(qKVFull + st));
+            tma_tile<D>(stage, &tm_k, j * kBlk, bh, bar(qKVFull + st));
+            tma_tile<D>(stage + kTile, &tm_v, j * kBlk, bh, bar(qKVFull + st));
             issued = j + 1;
         }
         if (!ok) raise_abort(abort_flag);
         mbar_wait(bar(qQ), 0, nullptr, kDrainTimeoutNs);
-        for (int j = (issued > qStages ? issued - qStages : 0); j < issued; ++j)
-            mbar_wait(bar(qKVFull + j % qStages), (j / qStages) & 1, nullptr, kDrainTimeoutNs);
+        for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
+            mbar_wait(bar(qKVFull + j % S), (j / S) & 1, nullptr, kDrainTimeoutNs);
     } else if (warp == kMmaWarp && lane == 0) {
         // ================================ MMA issuer ================================
         bool ok = mbar_wait(bar(qQ), 0, abort_flag, kWaitTimeoutNs);
         auto issue_sdp = [&](int j) {
-            const int st = j % qStages;
-            const uint32_t stage = base + qOffKV + st * qStageBytes;
-            if (!mbar_wait(bar(qKVFull + st), (j / qStages) & 1, abort_flag, kWaitTimeoutNs)) return false;
+            const int st = j % S;
+            const uint32_t stage = base + L::kOffKV + st * L::kStageBytes;
+            if (!mbar_wait(bar(qKVFull + st), (j / S) & 1, abort_flag, kWaitTimeoutNs)) return false;
             tc_fence_after();
-            mma_ss_128x128<BF16>(tmem + qColS, base + qOffQ, stage);             // S = Q K^T
-            umma_commit(bar(qSFull));
-            mma_ss_128x128<BF16>(tmem + qColDP, base + qOffDO, stage + kTile);   // dP = dO V^T
-            umma_commit(bar(qDPFull));
+            mma_ss_128x128<BF16, D>(tmem + L::kColS, base + L::kOffQ, stage);             // S = Q K^T
+            umma_commit(bar(L::kSFull));
+            mma_ss_128x128<BF16, D>(tmem + L::kColDP, base + L::kOffDO, stage + kTile);   // dP = dO V^T
+            umma_commit(bar(L::kDPFull));
             return true;
         };
         if (ok && nk > 0) ok = issue_sdp(0);
         for (int j = 0; ok && j < nk; ++j) {
             if (j + 1 < nk) {
-                if (!(ok = mbar_wait(bar(qSdPFree), j & 1, abort_flag, kWaitTimeoutNs))) break;
+                if (!(ok = mbar_wait(bar(L::kSdPFree), j & 1, abort_flag, kWaitTimeoutNs))) break;
                 if (!(ok = issue_sdp(j + 1))) break;
             }
-            if (!(ok = mbar_wait(bar(qDSFull), j & 1, abort_flag, kWaitTimeoutNs))) break;
+            if (!(ok = mbar_wait(bar(L::kDSFull), j & 1, abort_flag, kWaitTimeoutNs))) break;
             tc_fence_after();
-            const uint32_t stage = base + qOffKV + (j % qStages) * qStageBytes;
-            mma_ts_128x64<BF16>(tmem + qColDQ, tmem + qColDS, stage, j > 0);  // dQ += dS K
-            umma_commit(bar(qDone));
-            umma_commit(bar(qKVEmpty + j % qStages));
+            const uint32_t stage = base + L::kOffKV + (j % S) * L::kStageBytes;
+            mma_ts_128xD<BF16, D>(tmem + L::kColDQ, tmem + L::kColDS, stage, j > 0, false);  // dQ += dS K
+            umma_commit(bar(L::kDone));
+            umma_commit(bar(L::kKVEmpty + j % S));
         }
         if (!ok) raise_abort(abort_flag);
-        umma_commit(bar(qDrain));
-        mbar_wait(bar(qDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+        umma_commit(bar(L::kDrain));
+        mbar_wait(bar(L::kDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
     }
 
     tc_fence_before();
@@ -673,14 +743,15 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [BH][N][64] 16-bit tensor; boxes of 128 rows x 64 values, 128-byte swizzle; rows past N of
-// a head are out of bounds (zero-filled), never the next head's.
-bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, bool bf16) {
+// [BH][N][D] 16-bit tensor; boxes of 128 rows x 64 values (128 bytes, the swizzle span), one per
+// 64-value column block; rows past N of a head are out of bounds (zero-filled), never the next
+// head's.
+bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t D, bool bf16) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(N) * kD * 2};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kBlk), 1};
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(kBlk), 1};
     const cuuint32_t estride[3] = {1, 1, 1};
     return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                const_cast<void*>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -688,17 +759,17 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, bool bf1
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool BF16>
+template <bool BF16, int D>
 int launch_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                 void* dq, void* dk, void* dv, int64_t BH, int64_t N, bool causal, cudaStream_t stream) {
     CUtensorMap mq, mk, mv, mo, mdo;
-    if (!make_map(&mq, q, BH, N, BF16) || !make_map(&mk, k, BH, N, BF16) || !make_map(&mv, v, BH, N, BF16) ||
-        !make_map(&mo, o, BH, N, BF16) || !make_map(&mdo, dout, BH, N, BF16))
+    if (!make_map(&mq, q, BH, N, D, BF16) || !make_map(&mk, k, BH, N, D, BF16) || !make_map(&mv, v, BH, N, D, BF16) ||
+        !make_map(&mo, o, BH, N, D, BF16) || !make_map(&mdo, dout, BH, N, D, BF16))
         return ATTN_ERR_DEVICE;
-    if (cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kvSmem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, qSmem) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<BF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KvLay<D>::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<BF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             QLay<D>::kSmem) != cudaSuccess)
         return ATTN_ERR_LAUNCH;
     BwdParams prm;
     prm.o = o;
@@ -707,27 +778,35 @@ int launch_impl(const void* q, const void* k, const void* v, const void* o, cons
     prm.BH = static_cast<int>(BH);
     prm.nblk = static_cast<int>((N + kBlk - 1) / kBlk);
     prm.causal = causal ? 1 : 0;
-    prm.c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
-    prm.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(kD)));
+    prm.c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    prm.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
     const int64_t blocks = static_cast<int64_t>(prm.nblk) * BH;
     if (blocks > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     prm.grad0 = dk;
     prm.grad1 = dv;
-    attn_bwd_dkdv_tc_kernel<BF16><<<static_cast<unsigned>(blocks), kThreads, kvSmem, stream>>>(mq, mk, mv, mo, mdo, prm);
+    attn_bwd_dkdv_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, KvLay<D>::kSmem, stream>>>(
+        mq, mk, mv, mo, mdo, prm);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     prm.grad0 = dq;
     prm.grad1 = nullptr;
-    attn_bwd_dq_tc_kernel<BF16><<<static_cast<unsigned>(blocks), kThreads, qSmem, stream>>>(mq, mk, mv, mdo, prm);
+    attn_bwd_dq_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, QLay<D>::kSmem, stream>>>(
+        mq, mk, mv, mdo, prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 }  // namespace
 
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                  void* dq, void* dk, void* dv, int64_t BH, int64_t N, bool causal, bool bf16, cudaStream_t stream) {
+                  void* dq, void* dk, void* dv, int64_t BH, int64_t N, int64_t d, bool causal, bool bf16,
+                  cudaStream_t stream) {
     if (N > 0x7FFFFFFFll - kBlk || BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
-    return bf16 ? launch_impl<true>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream)
-                : launch_impl<false>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream);
+    if (d == 64)
+        return bf16 ? launch_impl<true, 64>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream)
+                    : launch_impl<false, 64>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream);
+    if (d == 128)
+        return bf16 ? launch_impl<true, 128>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream)
+                    : launch_impl<false, 128>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream);
+    return ATTN_ERR_UNSUPPORTED;
 }
 
 int bwd_tc_device_error(bool clear, unsigned* err) {

@@ -109,7 +109,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
     bool skip = false;
     // q, k, v and o get the forward's checks (o plays the output's part, so it may not alias
     // q, k or v); then the backward's own tensors.
-    int st = check_common(q, k, v, o, B, H, N, d, causal, dtype, &BH, &bytes, &skip);
+    int st = check_common(q, k, v, o, B, H, N, d, causal, dtype, &BH, &bytes, &skip, true);
     if (st != ATTN_OK || skip) return st;
     if (!dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
     if (!aligned(dout, 16) || !aligned(lse, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
@@ -132,8 +132,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
         return attn::launch_bwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
                                     static_cast<const float*>(v), static_cast<const float*>(o),
                                     static_cast<const float*>(dout), lse, static_cast<float*>(dq),
-                                    static_cast<float*>(dk), static_cast<float*>(dv), BH, N, causal != 0, s);
-    return attn::launch_bwd_tc(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal != 0, dtype == ATTN_BF16, s);
+                                    static_cast<float*>(dk), static_cast<float*>(dv), BH, N, d, causal != 0, s);
+    return attn::launch_bwd_tc(q, k, v, o, dout, lse, dq, dk, dv, BH, N, d, causal != 0, dtype == ATTN_BF16, s);
 }
 
 size_t attn_kvcache_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int num_splits,
@@ -262,7 +262,7 @@ const char* attn_status_string(int status) {
     switch (status) {
         case ATTN_OK: return "ok";
         case ATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or causal not 0/1)";
-        case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim 64, or 128 for the forward; dtype f32/bf16/f16; size limits)";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim 64 or 128, 64 for the ablation; dtype f32/bf16/f16; size limits)";
         case ATTN_ERR_ALIGN: return "pointer not aligned (tensors 16 bytes, workspace 256 bytes)";
         case ATTN_ERR_ALIAS: return "output or workspace overlaps another buffer";
         case ATTN_ERR_DEVICE: return "current device is not sm_103 or a CUDA query failed";
@@ -273,6 +273,6 @@ const char* attn_status_string(int status) {
     }
 }
 
-int attn_abi_version(void) { return (1 << 16) | 5; }
+int attn_abi_version(void) { return (1 << 16) | 6; }
 
 }  // extern "C"

@@ -21,14 +21,16 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
                   int64_t N, int64_t d, bool causal, bool bf16, int num_sms, cudaStream_t stream);
 
 // Backward pass for float32 tensors (two FFMA kernels): dq, dk, dv from q, k, v, the forward's
-// o, the output gradient dout and the forward's base-2 log-sum-exps lse ([BH, N] float32).
+// o, the output gradient dout and the forward's base-2 log-sum-exps lse ([BH, N] float32);
+// head width d = 64 or 128.
 int launch_bwd_f32(const float* q, const float* k, const float* v, const float* o, const float* dout,
-                   const float* lse, float* dq, float* dk, float* dv, int64_t BH, int64_t N, bool causal,
+                   const float* lse, float* dq, float* dk, float* dv, int64_t BH, int64_t N, int64_t d, bool causal,
                    cudaStream_t stream);
 
 // The same for bf16 (bf16 = true) or fp16 tensors on tcgen05 tensor cores (two kernels).
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                  void* dq, void* dk, void* dv, int64_t BH, int64_t N, bool causal, bool bf16, cudaStream_t stream);
+                  void* dq, void* dk, void* dv, int64_t BH, int64_t N, int64_t d, bool causal, bool bf16,
+                  cudaStream_t stream);
 
 // Reads (and optionally clears) the tensor-core backward kernels' device error word.
 int bwd_tc_device_error(bool clear, unsigned* err);

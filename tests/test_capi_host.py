@@ -81,15 +81,17 @@ def test_lse_argument_checks(lib, lse, want):
     assert lib.attn_fwd_lse(P, P * 3, P * 5, P * 9, lse, 1, 1, 8, 64, 0, 1, None) == want
 
 
-def test_head_width_128_is_a_forward_only_width(lib):
-    # d = 128 passes the forward's checks (and then needs the device), the other entry points
-    # refuse it before touching one.
+def test_head_width_128_is_taken_by_all_but_the_ablation(lib):
+    # d = 128 passes the checks of the forward, backward and key-value cache entry points (and
+    # then needs the device); the materialised ablation refuses it before touching one.
     if not __import__("torch").cuda.is_available():
         assert lib.attn_fwd(P, P * 3, P * 5, P * 9, 1, 1, 8, 128, 0, 1, None) == 5
         assert lib.attn_fwd_lse(P, P * 3, P * 5, P * 9, P * 20, 1, 1, 8, 128, 0, 1, None) == 5
+        assert lib.attn_bwd(P, P * 3, P * 5, P * 7, P * 9, P * 11, P * 13, P * 15, P * 17, 1, 1, 8, 128, 0, 1,
+                            None) == 5
     assert lib.attn_fwd(P, P * 3, P * 5, P * 9, 1, 1, 8, 96, 0, 1, None) == 2
     assert lib.attn_fwd(P, P * 3, P * 5, P * 9, 1, 1, 8, 256, 0, 1, None) == 2
-    assert lib.attn_bwd(P, P * 3, P * 5, P * 7, P * 9, P * 11, P * 13, P * 15, P * 17, 1, 1, 8, 128, 0, 1, None) == 2
+    assert lib.attn_bwd(P, P * 3, P * 5, P * 7, P * 9, P * 11, P * 13, P * 15, P * 17, 1, 1, 8, 96, 0, 1, None) == 2
     assert lib.attn_fwd_materialized(P, P * 3, P * 5, P * 9, P * 40, 1 << 20, 1, 1, 8, 128, 0, 1, None) == 2
 
 

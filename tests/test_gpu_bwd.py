@@ -31,9 +31,9 @@ def _torch_grads(q, k, v, do, dtype, causal):
     return [t.grad.float().cpu().numpy().astype(np.float64) for t in (tq, tk, tv)]
 
 
-def _case(seed, B, H, N, dtype, causal, qk_scale=1.0):
-    q, k, v = si.qkv(seed, B, H, N, 64, dtype, qk_scale=qk_scale)
-    do = si.qkv(seed + 1, B, H, N, 64, dtype)[0]
+def _case(seed, B, H, N, dtype, causal, qk_scale=1.0, d=64):
+    q, k, v = si.qkv(seed, B, H, N, d, dtype, qk_scale=qk_scale)
+    do = si.qkv(seed + 1, B, H, N, d, dtype)[0]
     qd, kd, vd, dod = (to_dev(x, dtype) for x in (q, k, v, do))
     o, lse = fa.attn_fwd_lse(qd, kd, vd, causal=causal)
     dq, dk, dv = fa.attn_bwd(qd, kd, vd, o, dod, lse, causal=causal)
@@ -75,3 +75,17 @@ def test_bwd_single_key_closed_form():
     torch.cuda.synchronize()
     assert torch.equal(dv, do)
     assert float(dq.abs().max()) <= 1e-3 and float(dk.abs().max()) <= 1e-3
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 65, 128, 129, 300, 640])
+def test_bwd_head_width_128(dtype, causal, N):
+    # d = 128: the tensor-core dK/dV kernel writes P^T and dS^T over S^T and dP^T and reads O's
+    # rows from global memory; several key and query blocks exercise the two-stage ring.
+    _case(0xA77E0600 + N, 2, 3, N, dtype, causal, d=128)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_bwd_head_width_128_qk_scaled_x8(dtype):
+    _case(0xA77E0700, 1, 2, 300, dtype, True, qk_scale=8.0, d=128)

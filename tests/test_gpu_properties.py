@@ -152,3 +152,42 @@ def test_device_wait_timeout_is_reported_and_the_context_stays_usable():
     torch.cuda.synchronize()
     assert fa.attn_device_status(clear=True) == 0
     assert torch.isfinite(o.float()).all()
+
+
+def test_calls_capture_into_a_cuda_graph_and_replay_bit_identically():
+    # Every entry point is stream-ordered and allocation-free once its workspace exists, so a
+    # step of forward, log-sum-exps, backward and key-value cache calls can be captured once and
+    # replayed; the replay must reproduce the eager results bit for bit.
+    torch.manual_seed(0)
+    q, k, v, do = (torch.randn(2, 3, 300, 64, device="cuda", dtype=torch.bfloat16) for _ in range(4))
+    kc, vc = (torch.randn(2, 3, 5000, 64, device="cuda", dtype=torch.bfloat16) for _ in range(2))
+    q1 = torch.randn(2, 3, 1, 64, device="cuda", dtype=torch.bfloat16)
+    ws = torch.empty(max(1, fa.attn_kvcache_workspace_bytes(2, 3, 1, 5000, 0, torch.bfloat16)), dtype=torch.uint8,
+                     device="cuda")
+    o, lse = torch.empty_like(q), torch.empty(2, 3, 300, device="cuda")
+    od = torch.empty_like(q1)
+
+    def step():
+        fa.attn_fwd_lse(q, k, v, causal=True, out=o, lse=lse)
+        grads = fa.attn_bwd(q, k, v, o, do, lse, causal=True)
+        fa.attn_fwd_kvcache(q1, kc, vc, causal=True, workspace=ws, out=od)
+        return grads
+
+    eager = [x.clone() for x in (*step(), o, lse, od)]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm the per-function attribute caches outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        grads = step()
+    for x in (o, lse, od, *grads):
+        x.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert fa.attn_device_status(clear=True) == 0
+    for a, b in zip(eager, (*grads, o, lse, od)):
+        assert torch.equal(a, b)
