@@ -22,16 +22,16 @@
 // GB300 mapping (a fresh design; the pages' kernels target sm_75 CUDA cores and a Triton
 // kernel on sm_89):
 //   * One CTA owns two query tiles A and B of 128 rows (rows 256c .. 256c+255 of one head)
-//     and streams K/V tiles of 128 keys past both, so each K/V tile is fetched once for
-//     256 queries.
+//     and streams K/V tiles of BN keys past both (BN = 128 at head width 64, 64 at 128), so
+//     each K/V tile is fetched once for 256 queries.
 //   * Warp 8 issues TMA loads (128-byte swizzle) into a 3-stage K/V ring guarded by
 //     full/empty mbarriers. Warp 9 owns the tensor memory and issues every tcgen05.mma from
 //     one thread, in whatever order their inputs become ready. Warps 0-3 (tile A) and 4-7
 //     (tile B) are the softmax warpgroups: thread t of a group owns query row t, which is
 //     TMEM lane t, so row reductions need no shuffles. The third warpgroup (warps 8-11)
 //     gives up registers so the softmax groups can hold a whole row of scores.
-//   * Tensor memory (512 columns x 128 lanes x 32 bit): S_A, S_B fp32 scores (128 columns
-//     each), O_A, O_B fp32 outputs (64 each), P_A, P_B probabilities as 16-bit pairs (64
+//   * Tensor memory (512 columns x 128 lanes x 32 bit): S_A, S_B fp32 scores (BN columns
+//     each), O_A, O_B fp32 outputs (d each), P_A, P_B probabilities as 16-bit pairs (BN/2
 //     each). S = Q K^T runs with both operands in shared memory; O += P V takes P from
 //     tensor memory and V (dims contiguous, "MN-major") from shared memory.
 //   * S_X(j+1) is issued as soon as softmax X has copied S_X(j) into registers, so the
@@ -58,15 +58,12 @@ namespace attn {
 namespace {
 
 constexpr int kBM = 128;  // query rows per tile = TMEM lanes
-constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kBlockBytes = kBM * 64 * 2;  // one 128-row x 128-byte column block (the swizzle span)
+constexpr int kBlockBytes = kBM * 64 * 2;  // one 128-row x 128-byte column block of a Q tile
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kSIssuerWarp = 9;   // also owns the tensor memory
 constexpr int kPVIssuerWarp = 10;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // + 128 * tile
-constexpr uint32_t kColO = 256;  // + D * tile
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s for any single wait
 constexpr uint64_t kDrainTimeoutNs = 100000000ull;  // 100 ms to drain after an abort
 constexpr unsigned kPollSleepNs = 32;  // MMA issuers' back-off between unproductive polls
@@ -81,28 +78,34 @@ static_assert(2 * 128 * kRegsSoftmax + (kThreads - 2 * 128) * kRegsOther <= kThr
               "register split must fit the launch allocation");
 static_assert(kThreads * kRegsLaunch <= 65536, "launch allocation must fit the register file");
 
-// Everything that depends on the head width D (64 or 128). A tile of 128 rows x D 16-bit
-// values is D/64 column blocks of 128 rows x 128 bytes, each loaded by its own TMA box.
-// Tensor memory: S_X at column 128X, O_X at 256 + D X; P_X (the probabilities as 16-bit
-// pairs, 64 columns) at 384 + 64X for D = 64, and over the first 64 columns of S_X for
-// D = 128, where the S and O of both tiles fill all 512 columns. With P over S, S_X(j+1) may
-// only start once PV_X(j) has read P_X(j).
+// Everything that depends on the head width D (64 or 128) and the key-tile size BN (128 keys at
+// D = 64, 64 at D = 128). A Q tile of 128 rows x D 16-bit values is D/64 column blocks of 128
+// rows x 128 bytes, a K or V tile D/64 blocks of BN rows x 128 bytes, each loaded by its own TMA
+// box. Tensor memory: S_X (BN fp32 columns) at BN X, O_X (D columns) at 2 BN + D X, P_X (the
+// probabilities as 16-bit pairs, BN/2 columns) at 2 BN + 2 D + BN/2 X: 512 columns at D = 64,
+// 448 at D = 128. (With 128-key tiles at D = 128, S and O alone would fill the 512 columns, P
+// would have to sit over S and S_X(j+1) would wait for PV_X(j); 64-key tiles avoid that.)
 template <int D>
 struct Lay {
     static_assert(D == 64 || D == 128, "head width 64 or 128");
+    static constexpr int kBN = D == 64 ? 128 : 64;
     static constexpr int kBlocks = D / 64;
-    static constexpr int kTileBytes = kBlocks * kBlockBytes;  // 16 or 32 KiB
-    static constexpr int kKStages = D == 64 ? 4 : 2;  // K ring depth (QK^T reads K one step ahead)
-    static constexpr int kVStages = D == 64 ? 3 : 2;  // V ring depth
-    static constexpr bool kPOverS = D > 64;
-    __host__ __device__ static constexpr uint32_t colP(int X) {
-        return kPOverS ? kColS + 128u * static_cast<uint32_t>(X) : 384u + 64u * static_cast<uint32_t>(X);
-    }
+    static constexpr int kTileBytes = kBlocks * kBlockBytes;     // Q tile: 16 or 32 KiB
+    static constexpr int kKVBlockBytes = kBN * 128;              // one column block of a K/V tile
+    static constexpr int kKVTileBytes = kBlocks * kKVBlockBytes; // K or V tile: 16 KiB
+    static constexpr int kKStages = 4;  // K ring depth (QK^T reads K one step ahead)
+    static constexpr int kVStages = 3;  // V ring depth
+    static constexpr uint32_t kColS = 0;
+    static constexpr uint32_t kColO = 2 * kBN;
+    static constexpr uint32_t kColP0 = 2 * kBN + 2 * D;
+    __host__ __device__ static constexpr uint32_t colS(int X) { return kColS + kBN * static_cast<uint32_t>(X); }
+    __host__ __device__ static constexpr uint32_t colO(int X) { return kColO + D * static_cast<uint32_t>(X); }
+    __host__ __device__ static constexpr uint32_t colP(int X) { return kColP0 + (kBN / 2) * static_cast<uint32_t>(X); }
     // Shared-memory layout (byte offsets from a 1024-byte aligned base).
-    static constexpr int kOffQ = 0;                                // 2 tiles
-    static constexpr int kOffK = kOffQ + 2 * kTileBytes;           // kKStages tiles
-    static constexpr int kOffV = kOffK + kKStages * kTileBytes;    // kVStages tiles
-    static constexpr int kOffBar = kOffV + kVStages * kTileBytes;  // mbarriers, 8 bytes each
+    static constexpr int kOffQ = 0;                                  // 2 tiles
+    static constexpr int kOffK = kOffQ + 2 * kTileBytes;             // kKStages tiles
+    static constexpr int kOffV = kOffK + kKStages * kKVTileBytes;    // kVStages tiles
+    static constexpr int kOffBar = kOffV + kVStages * kKVTileBytes;  // mbarriers, 8 bytes each
     static constexpr int kBarQFull = 0;
     static constexpr int kBarKFull = 1;
     static constexpr int kBarKEmpty = kBarKFull + kKStages;
@@ -120,7 +123,7 @@ struct Lay {
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget of one CTA");
     static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzle atoms need 1024-byte alignment");
-    static_assert(kColO + 2 * D <= kTmemCols && (kPOverS || 384 + 128 <= kTmemCols), "tensor memory budget");
+    static_assert(kColP0 + kBN <= kTmemCols, "tensor memory budget");
 };
 
 __device__ unsigned int g_tc_error = 0;
@@ -170,30 +173,32 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 
-// Row maximum of 128 scores as eight independent chains of 3-input max, then a tree.
-__device__ __forceinline__ float row_max128(const float (&s)[kBN]) {
+// Row maximum of BN (64 or 128) scores as eight independent chains of 3-input max, then a tree.
+template <int BN>
+__device__ __forceinline__ float row_max(const float (&s)[BN]) {
+    static_assert(BN / 8 % 2 == 0 && BN >= 32, "an even number of 8-wide groups");
     float mx[8];
 #pragma unroll
     for (int g = 0; g < 8; ++g) mx[g] = fmax3(s[g], s[g + 8], s[g + 16]);
 #pragma unroll
-    for (int t = 3; t < 15; t += 2)
+    for (int t = 3; t < BN / 8 - 1; t += 2)
 #pragma unroll
         for (int g = 0; g < 8; ++g) mx[g] = fmax3(mx[g], s[g + 8 * t], s[g + 8 * t + 8]);
 #pragma unroll
-    for (int g = 0; g < 8; ++g) mx[g] = fmaxf(mx[g], s[g + 120]);
+    for (int g = 0; g < 8; ++g) mx[g] = fmaxf(mx[g], s[g + BN - 8]);
     return fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
 }
 
-// p = 2^(s * c - m) for the 128 scores of a row, packed to 16-bit pairs (round to nearest
+// p = 2^(s * c - m) for the BN scores of a row, packed to 16-bit pairs (round to nearest
 // even) in `pk`; returns the fp32 sum of the unrounded p (four independent partial sums).
-template <bool BF16>
-__device__ __forceinline__ float row_exp2_t(const uint32_t (&su)[kBN], float2 c2, float2 negm,
-                                            uint32_t (&pk)[kBN / 2]) {
+template <bool BF16, int BN>
+__device__ __forceinline__ float row_exp2_t(const uint32_t (&su)[BN], float2 c2, float2 negm,
+                                            uint32_t (&pk)[BN / 2]) {
     float2 acc[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < kBN / 2; ++i) {
+    for (int i = 0; i < BN / 2; ++i) {
         const float2 t = ffma2(make_float2(__uint_as_float(su[2 * i]), __uint_as_float(su[2 * i + 1])), c2, negm);
         const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
         acc[i & 3] = fadd2(acc[i & 3], pp);
@@ -213,12 +218,11 @@ struct SoftmaxCtx {
     int lane;
 };
 
-__device__ __forceinline__ void load_s(const SoftmaxCtx& cx, uint32_t (&su)[kBN]) {
+template <int BN>
+__device__ __forceinline__ void load_s(const SoftmaxCtx& cx, uint32_t (&su)[BN]) {
     tc_fence_after();
-    ATTN_TMEM_LD_X32(cx.tS + 0, (su + 0));
-    ATTN_TMEM_LD_X32(cx.tS + 32, (su + 32));
-    ATTN_TMEM_LD_X32(cx.tS + 64, (su + 64));
-    ATTN_TMEM_LD_X32(cx.tS + 96, (su + 96));
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) ATTN_TMEM_LD_X32(cx.tS + 32 * c, (su + 32 * c));
 }
 
 __device__ __forceinline__ void release_s(const SoftmaxCtx& cx) {
@@ -233,8 +237,9 @@ __device__ __forceinline__ void release_s(const SoftmaxCtx& cx) {
 // reference moves, starts loading S(j+1) and signals the MMA issuers. Returns false when a
 // wait timed out or the CTA is aborting (the result is the same in all lanes of a warp).
 template <bool BF16, bool kMasked, int D>
-__device__ __forceinline__ bool softmax_step(const SoftmaxCtx& cx, uint32_t (&su)[kBN], float& m,
+__device__ __forceinline__ bool softmax_step(const SoftmaxCtx& cx, uint32_t (&su)[Lay<D>::kBN], float& m,
                                              float& l, int j, int nX) {
+    constexpr int kBN = Lay<D>::kBN;
     // The scores stay in the registers tcgen05.ld filled (as bit patterns); masked keys get
     // the bit pattern of -inf.
     if constexpr (kMasked) {
@@ -250,13 +255,13 @@ __device__ __forceinline__ bool softmax_step(const SoftmaxCtx& cx, uint32_t (&su
     // otherwise (or on the first tile) the row maximum is computed and p redone if m moves.
     uint32_t pk[kBN / 2];
     float tile_sum = INFINITY;
-    if (m != -INFINITY) tile_sum = row_exp2_t<BF16>(su, c2, make_float2(-m, -m), pk);
+    if (m != -INFINITY) tile_sum = row_exp2_t<BF16, kBN>(su, c2, make_float2(-m, -m), pk);
     float alpha = 1.f;
     if (!(tile_sum <= kLazyBound)) {
         float s[kBN];
 #pragma unroll
         for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(su[i]);
-        const float mt = row_max128(s) * c;
+        const float mt = row_max<kBN>(s) * c;
         if (mt > m + kLazyLog2) {
             alpha = ex2_approx(m - mt);  // 0 on the first tile (m = -inf)
             m = mt;
@@ -265,7 +270,7 @@ __device__ __forceinline__ bool softmax_step(const SoftmaxCtx& cx, uint32_t (&su
         // A row with every key masked so far keeps a zero reference (no inf - inf).
         const float m_use = (m == -INFINITY) ? 0.f : m;
         if (alpha != 1.f || tile_sum == INFINITY || tile_sum != tile_sum)
-            tile_sum = row_exp2_t<BF16>(su, c2, make_float2(-m_use, -m_use), pk);
+            tile_sum = row_exp2_t<BF16, kBN>(su, c2, make_float2(-m_use, -m_use), pk);
     }
     bool rescale = false;
     if (j > 0) {
@@ -273,8 +278,8 @@ __device__ __forceinline__ bool softmax_step(const SoftmaxCtx& cx, uint32_t (&su
         tc_fence_after();
         rescale = __any_sync(0xffffffffu, alpha != 1.f);
     }
-    tmem_st_x32(cx.tP, pk);
-    tmem_st_x32(cx.tP + 32, pk + 32);
+#pragma unroll
+    for (int c = 0; c < kBN / 64; ++c) tmem_st_x32(cx.tP + 32 * c, pk + 32 * c);
     if (rescale) {
         // O <- alpha * O (rare: only when some row of this warp moved its reference); done in
         // 16-column pieces so it adds few registers to the step.
@@ -296,60 +301,47 @@ __device__ __forceinline__ bool softmax_step(const SoftmaxCtx& cx, uint32_t (&su
     l += tile_sum;
     const bool more = j + 1 < nX;
     bool ok = true;
-    if constexpr (Lay<D>::kPOverS) {
-        // P_X(j) sits over S_X's columns, so S_X(j+1) follows PV_X(j): hand P over first.
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (cx.lane == 0) mbar_arrive(cx.bar_p_full);
-        if (more) {
-            ok = warp_wait(cx.bar_s_full, (j + 1) & 1, cx.abort_flag);
-            if (ok) {
-                load_s(cx, su);
-                release_s(cx);
-            }
-        }
-    } else {
-        if (more) {  // the next scores start moving while P drains
-            ok = warp_wait(cx.bar_s_full, (j + 1) & 1, cx.abort_flag);
-            if (ok) load_s(cx, su);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (cx.lane == 0) mbar_arrive(cx.bar_p_full);
-        if (more && ok) release_s(cx);
+    if (more) {  // the next scores start moving while P drains
+        ok = warp_wait(cx.bar_s_full, (j + 1) & 1, cx.abort_flag);
+        if (ok) load_s<kBN>(cx, su);
     }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (cx.lane == 0) mbar_arrive(cx.bar_p_full);
+    if (more && ok) release_s(cx);
     return ok;
 }
 
-// S_X(j) = Q_X K_j^T : M=128, N=128, K=D as D/16 steps of K=16 (32 bytes of a 128-byte row;
-// steps 4..7 of D = 128 read the second column block).
+// S_X(j) = Q_X K_j^T : M=128, N=BN, K=D as D/16 steps of K=16 (32 bytes of a 128-byte row;
+// steps 4..7 of D = 128 read the second column block of each tile).
 template <bool BF16, int D>
 __device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sQx, uint32_t sKs, int X, uint32_t bar_s_full) {
-    constexpr uint32_t kIdescQK = idesc_f16(BF16, kBM, kBN, false, false);
+    using L = Lay<D>;
+    constexpr uint32_t kIdescQK = idesc_f16(BF16, kBM, L::kBN, false, false);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = static_cast<uint32_t>((kk >> 2) * kBlockBytes + 32 * (kk & 3));
-        const uint64_t a = smem_desc_sw128(sQx + off, 16, 1024);
-        const uint64_t b = smem_desc_sw128(sKs + off, 16, 1024);
-        umma_ss(tmem + kColS + 128u * X, a, b, kIdescQK, kk > 0 ? 1u : 0u);
+        const uint32_t a_off = static_cast<uint32_t>((kk >> 2) * kBlockBytes + 32 * (kk & 3));
+        const uint32_t b_off = static_cast<uint32_t>((kk >> 2) * L::kKVBlockBytes + 32 * (kk & 3));
+        const uint64_t a = smem_desc_sw128(sQx + a_off, 16, 1024);
+        const uint64_t b = smem_desc_sw128(sKs + b_off, 16, 1024);
+        umma_ss(tmem + L::colS(X), a, b, kIdescQK, kk > 0 ? 1u : 0u);
     }
     umma_commit(bar_s_full);
 }
 
-// O_X += P_X V_j : M=128, N=D, K=128 as eight K=16 steps (16 keys = 2048 bytes of each V
+// O_X += P_X V_j : M=128, N=D, K=BN as BN/16 steps of K=16 (16 keys = 2048 bytes of each V
 // column block), P from tensor memory. V is the MN-major operand (dims contiguous); for D = 128
-// its two 64-dim column blocks are 16 KiB apart, the descriptor's leading byte offset.
+// its two 64-dim column blocks are one K/V block apart, the descriptor's leading byte offset.
 template <bool BF16, int D>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sVs, int X, bool accumulate, uint32_t bar_o_ready) {
+    using L = Lay<D>;
     constexpr uint32_t kIdescPV = idesc_f16(BF16, kBM, D, false, true);
-    constexpr uint32_t kLbo = D == 64 ? 16u : static_cast<uint32_t>(kBlockBytes);
+    constexpr uint32_t kLbo = D == 64 ? 16u : static_cast<uint32_t>(L::kKVBlockBytes);
 #pragma unroll
-    for (int kk = 0; kk < kBN / 16; ++kk) {
+    for (int kk = 0; kk < L::kBN / 16; ++kk) {
         const uint64_t b = smem_desc_sw128(sVs + 2048 * kk, kLbo, 1024);
-        umma_ts(tmem + kColO + static_cast<uint32_t>(D) * X, tmem + Lay<D>::colP(X) + 8u * kk, b, kIdescPV,
-                (accumulate || kk > 0) ? 1u : 0u);
+        umma_ts(tmem + L::colO(X), tmem + L::colP(X) + 8u * kk, b, kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
     }
     umma_commit(bar_o_ready);
 }
@@ -382,9 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pair = p.causal ? (p.num_pairs - 1 - slot) : slot;
     const int rowA = pair * 2 * kBM;
     const int rowB = rowA + kBM;
+    constexpr int kBN = L::kBN;
     const int nkv = (N + kBN - 1) / kBN;
-    const int nA = p.causal ? min(nkv, rowA / kBN + 1) : nkv;
-    const int nB = (rowB < N) ? (p.causal ? min(nkv, rowB / kBN + 1) : nkv) : 0;
+    const int nA = p.causal ? min(nkv, (rowA + kBM - 1) / kBN + 1) : nkv;
+    const int nB = (rowB < N) ? (p.causal ? min(nkv, (rowB + kBM - 1) / kBN + 1) : nkv) : 0;
     const int nmax = max(nA, nB);
 
     // ---- setup: barriers (thread 0), tensor memory (S-issuer warp) ----
@@ -424,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nX = X ? nB : nA;
         const int row = (X ? rowB : rowA) + ((warp & 3) << 5) + lane;
         const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) << 5) << 16;
-        const SoftmaxCtx cx{tmem + lane_addr + kColS + 128u * X, tmem + lane_addr + kColO + static_cast<uint32_t>(D) * X,
+        const SoftmaxCtx cx{tmem + lane_addr + L::colS(X), tmem + lane_addr + L::colO(X),
                             tmem + lane_addr + L::colP(X), bar(L::kBarSFull + X), bar(L::kBarSFree + X),
                             bar(L::kBarPFull + X), bar(L::kBarOReady + X), abort_flag, p.scale_log2,
                             p.causal ? min(row + 1, N) : N, lane};
@@ -437,14 +430,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nX > 0) {
             ok = warp_wait(cx.bar_s_full, 0, abort_flag);
             if (ok) {
-                load_s(cx, su);
+                load_s<kBN>(cx, su);
                 release_s(cx);
             }
         }
-        // Only a query tile's last key tile can hold masked keys (the causal diagonal or
-        // keys past N), so the loop runs mask-free and the last step is peeled off.
-        for (int j = 0; ok && j + 1 < nX; ++j) ok = softmax_step<BF16, false, D>(cx, su, m, l, j, nX);
-        if (ok && nX > 0) ok = softmax_step<BF16, true, D>(cx, su, m, l, nX - 1, nX);
+        if constexpr (kBN == kBM) {
+            // Only a query tile's last key tile can hold masked keys (the causal diagonal or
+            // keys past N), so the loop runs mask-free and the last step is peeled off.
+            for (int j = 0; ok && j + 1 < nX; ++j) ok = softmax_step<BF16, false, D>(cx, su, m, l, j, nX);
+            if (ok && nX > 0) ok = softmax_step<BF16, true, D>(cx, su, m, l, nX - 1, nX);
+        } else {
+            // Key tiles wholly below the tile's first row (causal) and below N need no mask; the
+            // diagonal tiles (two with 64-key tiles) and a ragged last tile take the masked step.
+            const int rowX = X ? rowB : rowA;
+            const int nfree = min(nX, (p.causal ? min(rowX + 1, N) : N) / kBN);
+            int j = 0;
+            for (; ok && j < nfree; ++j) ok = softmax_step<BF16, false, D>(cx, su, m, l, j, nX);
+            for (; ok && j < nX; ++j) ok = softmax_step<BF16, true, D>(cx, su, m, l, j, nX);
+        }
 
         // ---- epilogue: O / l, rounded to the output type, rows >= N not stored ----
         if (ok && nX > 0) {
@@ -495,10 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int sk = j % L::kKStages;
                 if (!(ok = mbar_wait(bar(L::kBarKEmpty + sk), ((j / L::kKStages) & 1) ^ 1, abort_flag, kWaitTimeoutNs)))
                     break;
-                mbar_arrive_expect_tx(bar(L::kBarKFull + sk), L::kTileBytes);
+                mbar_arrive_expect_tx(bar(L::kBarKFull + sk), L::kKVTileBytes);
 #pragma unroll
                 for (int c = 0; c < L::kBlocks; ++c)
-                    tma_load_3d(sK + sk * L::kTileBytes + c * kBlockBytes, &tmap_k, 64 * c, j * kBN, bh,
+                    tma_load_3d(sK + sk * L::kKVTileBytes + c * L::kKVBlockBytes, &tmap_k, 64 * c, j * kBN, bh,
                                 bar(L::kBarKFull + sk));
                 kissued = j + 1;
                 for (; vissued < j; ++vissued) {  // V_{j-1} after K_j
@@ -506,10 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = mbar_wait(bar(L::kBarVEmpty + sv), ((vissued / L::kVStages) & 1) ^ 1, abort_flag,
                                          kWaitTimeoutNs)))
                         break;
-                    mbar_arrive_expect_tx(bar(L::kBarVFull + sv), L::kTileBytes);
+                    mbar_arrive_expect_tx(bar(L::kBarVFull + sv), L::kKVTileBytes);
 #pragma unroll
                     for (int c = 0; c < L::kBlocks; ++c)
-                        tma_load_3d(sV + sv * L::kTileBytes + c * kBlockBytes, &tmap_v, 64 * c, vissued * kBN, bh,
+                        tma_load_3d(sV + sv * L::kKVTileBytes + c * L::kKVBlockBytes, &tmap_v, 64 * c, vissued * kBN, bh,
                                     bar(L::kBarVFull + sv));
                 }
             }
@@ -518,10 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = mbar_wait(bar(L::kBarVEmpty + sv), ((vissued / L::kVStages) & 1) ^ 1, abort_flag,
                                      kWaitTimeoutNs)))
                     break;
-                mbar_arrive_expect_tx(bar(L::kBarVFull + sv), L::kTileBytes);
+                mbar_arrive_expect_tx(bar(L::kBarVFull + sv), L::kKVTileBytes);
 #pragma unroll
                 for (int c = 0; c < L::kBlocks; ++c)
-                    tma_load_3d(sV + sv * L::kTileBytes + c * kBlockBytes, &tmap_v, 64 * c, vissued * kBN, bh,
+                    tma_load_3d(sV + sv * L::kKVTileBytes + c * L::kKVBlockBytes, &tmap_v, 64 * c, vissued * kBN, bh,
                                 bar(L::kBarVFull + sv));
             }
             if (!ok) raise_abort(abort_flag);
@@ -548,10 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int& j = X ? ns1 : ns0;
                     const int nX = X ? nB : nA, nO = X ? nA : nB;
                     if (j < nX && mbar_test(bar(L::kBarKFull + j % L::kKStages), (j / L::kKStages) & 1) &&
-                        (j == 0 || (mbar_test(bar(L::kBarSFree + X), (j - 1) & 1) &&
-                                    (!L::kPOverS || mbar_test(bar(L::kBarOReady + X), (j - 1) & 1))))) {
+                        (j == 0 || mbar_test(bar(L::kBarSFree + X), (j - 1) & 1))) {
                         tc_fence_after();
-                        issue_s<BF16, D>(tmem, sQ + X * L::kTileBytes, sK + (j % L::kKStages) * L::kTileBytes, X,
+                        issue_s<BF16, D>(tmem, sQ + X * L::kTileBytes, sK + (j % L::kKStages) * L::kKVTileBytes, X,
                                       bar(L::kBarSFull + X));
                         umma_commit(bar(L::kBarKEmpty + j % L::kKStages));
                         if (j >= nO) umma_commit(bar(L::kBarKEmpty + j % L::kKStages));
@@ -591,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (j < nX && mbar_test(bar(L::kBarVFull + j % L::kVStages), (j / L::kVStages) & 1) &&
                         mbar_test(bar(L::kBarPFull + X), j & 1)) {
                         tc_fence_after();
-                        issue_pv<BF16, D>(tmem, sV + (j % L::kVStages) * L::kTileBytes, X, j > 0, bar(L::kBarOReady + X));
+                        issue_pv<BF16, D>(tmem, sV + (j % L::kVStages) * L::kKVTileBytes, X, j > 0, bar(L::kBarOReady + X));
                         umma_commit(bar(L::kBarVEmpty + j % L::kVStages));
                         if (j >= nO) umma_commit(bar(L::kBarVEmpty + j % L::kVStages));
                         ++j;
@@ -649,14 +651,14 @@ EncodeTiledFn get_encode_fn() {
 
 // [BH][N][D] 16-bit tensor; boxes of 128 rows x 64 values (128 bytes, the swizzle span), one
 // per 64-dim column block.
-bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t D, bool bf16) {
+bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t D, int rows, bool bf16) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                                    static_cast<cuuint64_t>(N) * D * 2};
-    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(kBM), 1};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(rows), 1};
     const cuuint32_t estride[3] = {1, 1, 1};
     return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                const_cast<void*>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -679,8 +681,8 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
         return ATTN_ERR_LAUNCH;
     }
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, BH, N, D, BF16) || !make_map(&mk, k, BH, N, D, BF16) ||
-        !make_map(&mv, v, BH, N, D, BF16))
+    if (!make_map(&mq, q, BH, N, D, kBM, BF16) || !make_map(&mk, k, BH, N, D, Lay<D>::kBN, BF16) ||
+        !make_map(&mv, v, BH, N, D, Lay<D>::kBN, BF16))
         return ATTN_ERR_DEVICE;
     // The attribute is per device; setting it on every call is cheap and thread-safe.
     const cudaError_t aerr = cudaFuncSetAttribute(attn_fwd_tc_kernel<BF16, D>,
