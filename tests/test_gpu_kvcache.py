@@ -180,3 +180,35 @@ def test_kvcache_workspace_reused_across_calls_and_shapes():
         ref_o, ref_lse = oracle.attn_fwd_kv(q, k, v, True)
         check(o.float().cpu().numpy().astype(np.float64), ref_o, "bf16", Nk, f"reuse call {seed}")
         assert float(np.max(np.abs(lse.cpu().numpy() - ref_lse))) <= _lse_bound(ref_lse)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 4])
+def test_kvcache_causal_rows_ignore_keys_they_cannot_see(splits):
+    # Causal with Nq = 6 new queries: query i sees keys 0 .. Nk - Nq + i. Rewriting the keys and
+    # values past query 2's position must leave queries 0..2 bit-identical (their weights on
+    # those keys are exactly zero) and change query 5.
+    B, H, Nq, Nk = 1, 2, 6, 700
+    q, k, v = _inputs(0xCAC3C000, B, H, Nq, Nk, "bf16")
+    qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+    o1, l1 = fa.attn_fwd_kvcache(qd, kd, vd, causal=True, num_splits=splits, lse=True)
+    last_seen = Nk - Nq + 2
+    kd2, vd2 = kd.clone(), vd.clone()
+    kd2[:, :, last_seen + 1:] = torch.randn_like(kd2[:, :, last_seen + 1:]) * 3
+    vd2[:, :, last_seen + 1:] = torch.randn_like(vd2[:, :, last_seen + 1:]) * 3
+    o2, l2 = fa.attn_fwd_kvcache(qd, kd2, vd2, causal=True, num_splits=splits, lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1[:, :, :3], o2[:, :, :3]) and torch.equal(l1[:, :, :3], l2[:, :, :3])
+    assert not torch.equal(o1[:, :, 5], o2[:, :, 5])
+
+
+def test_kvcache_noncausal_ignores_key_order():
+    # Without the mask, permuting the cache rows (keys and values together) permutes nothing in
+    # the result: equal within rounding of the summation order.
+    B, H, Nq, Nk = 2, 2, 3, 900
+    q, k, v = _inputs(0xCAC3D000, B, H, Nq, Nk, "f32")
+    qd, kd, vd = (to_dev(x, "f32") for x in (q, k, v))
+    perm = torch.randperm(Nk, generator=torch.Generator().manual_seed(5)).to("cuda")
+    o1 = fa.attn_fwd_kvcache(qd, kd, vd, causal=False)
+    o2 = fa.attn_fwd_kvcache(qd, kd[:, :, perm].contiguous(), vd[:, :, perm].contiguous(), causal=False)
+    torch.cuda.synchronize()
+    assert float((o1 - o2).abs().max()) <= 1e-5
