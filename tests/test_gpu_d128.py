@@ -109,3 +109,21 @@ def test_d128_matches_torch_sdpa_within_the_page_gate():
     ours = float(np.abs(o.float().cpu().numpy() - ref).max())
     torch_err = float(np.abs(theirs.float().cpu().numpy() - ref).max())
     assert ours <= 2.0 * torch_err, (ours, torch_err)
+
+
+def test_d128_long_context_sampled_rows():
+    # B1 H4 N32768 d128 bf16 causal: 128 sampled rows per head (and rows 0, N-1) against the
+    # oracle; row offsets and key-tile counts well past the headline's.
+    B, H, N = 1, 4, 32768
+    q, k, v = si.qkv(0xD1286000, B, H, N, D, "bf16")
+    qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+    o, lse = fa.attn_fwd_lse(qd, kd, vd, causal=True)
+    torch.cuda.synchronize()
+    assert fa.attn_device_status(clear=True) == 0
+    rows = np.concatenate([[0, N - 1], si.sample_rows(0xD1286001, N, 126)])
+    flat = np.concatenate([h * N + rows for h in range(B * H)])
+    ref_o, ref_l = oracle.attn_fwd_lse(q, k, v, True, rows=flat)
+    got_o = o.reshape(-1, D).float().cpu().numpy().astype(np.float64)[flat]
+    got_l = lse.reshape(-1).cpu().numpy().astype(np.float64)[flat]
+    check(got_o, ref_o, "bf16", N, "d128 B1H4N32768 sampled")
+    assert float(np.max(np.abs(got_l - ref_l))) <= _lse_bound(ref_l)
