@@ -23,12 +23,14 @@
 //     S = Q K^T (SS), dP = dO V^T (SS); dS = P (dP - delta) -> TMEM; dQ += dS K (TS, B = K)
 // Tensor memory (512 columns): dK/dV kernel S^T 0, dP^T 128, P^T 256, dS^T 320, dV 384, dK 448;
 // dQ kernel S 0, dP 128, dS 256, dQ 320. The next block's S and dP products go out as soon as
-// the softmax warps have copied the current ones out, so they overlap the elementwise work.
+// the elementwise warps have loaded the current ones into registers, before their arithmetic,
+// so the products overlap it.
 // delta is computed from the dO and O tiles in shared memory (the dK/dV kernel loads O for
 // that) and lse is read per block, so the call allocates nothing.
 //
 // Roles: warps 0-7 elementwise (thread = TMEM lane; warps w and w + 4 share lanes and split the
-// columns), warp 8 TMA producer, warp 9 MMA issuer and tensor-memory owner. Every mbarrier wait is bounded; on expiry the kernel sets the
+// columns), warp 8 TMA producer, warp 9 MMA issuer and tensor-memory owner, warps 10-11 idle
+// (they only give up registers). Every mbarrier wait is bounded; on expiry the kernel sets the
 // shared device error word (reported by attn_device_status), drains and returns.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -47,10 +49,20 @@ namespace {
 
 constexpr int kBlk = 128;                   // queries or keys per block = TMEM lanes
 constexpr int kBlockBytes = kBlk * 64 * 2;  // 16 KiB: 128 rows x 128 bytes (64 values), one TMA box
-constexpr int kThreads = 320;
-constexpr int kElemWarps = 8;  // two warpgroups on the same TMEM lanes, each on half the columns
+// Warps 0-7: elementwise (two warpgroups on the same TMEM lanes, each on half the columns);
+// warpgroup 2: the TMA producer (warp 8), the MMA issuer (warp 9) and two idle warps. Ten warps
+// would already put three on some SM sub-partition and cap every thread at 168 registers; the two
+// idle warps complete warpgroup 2 so that it can hand registers to the elementwise warpgroups
+// (setmaxnreg acts on whole warpgroups): 56 a thread there, 224 in warps 0-7.
+constexpr int kThreads = 384;
+constexpr int kElemWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kRegsLaunch = 168;  // 65536 / 384, rounded down to the allocation granule of 8
+constexpr int kRegsElem = 224;
+constexpr int kRegsOther = 56;
+static_assert(32 * kElemWarps * kRegsElem + (kThreads - 32 * kElemWarps) * kRegsOther <= kThreads * kRegsLaunch,
+              "the register split must fit in the block's launch allocation");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr uint64_t kDrainTimeoutNs = 100000000ull;
@@ -249,13 +261,10 @@ struct KvLay {
 // dS^T = P^T (dP^T - delta) from S^T and dP^T in TMEM, stored back as 16-bit pairs. The
 // queries' lse and delta come from shared memory four at a time.
 template <bool BF16, bool kMasked, int D>
-__device__ __forceinline__ void kv_chunk(uint32_t t, int ch, const float* ls, const float* dl, float c, int key,
-                                         int q0, int N, int causal) {
+__device__ __forceinline__ void kv_chunk(uint32_t t, int ch, const uint32_t (&s)[32], const uint32_t (&dp)[32],
+                                         const float* ls, const float* dl, float c, int key, int q0, int N,
+                                         int causal) {
     using L = KvLay<D>;
-    uint32_t s[32], dp[32];
-    ATTN_TMEM_LD_X32(t + L::kColS + 32 * ch, s);
-    ATTN_TMEM_LD_X32(t + L::kColDP + 32 * ch, dp);
-    tmem_ld_wait();
     uint32_t pp[16], ds[16];
 #pragma unroll
     for (int u4 = 0; u4 < 8; ++u4) {
@@ -334,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < kElemWarps) {
         // ===================== elementwise warps: thread = key (TMEM lane) =====================
+        regs_increase<kRegsElem>();
         const int g = warp >> 2;  // warpgroup: query columns 64g .. 64g + 63
         const int r = ((warp & 3) << 5) + lane;  // key row within the block, = TMEM lane
         const int key = k0 + r;
@@ -372,22 +382,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = warp_wait(bar(kvSFull), i & 1, abort_flag))) break;
             if (!(ok = warp_wait(bar(kvDPFull), i & 1, abort_flag))) break;
             tc_fence_after();
+            // This warpgroup's two chunks of S^T and dP^T into registers, then they are released
+            // so that the next block's products run during the arithmetic below.
+            uint32_t s0[32], dp0[32], s1[32], dp1[32];
+            ATTN_TMEM_LD_X32(t + L::kColS + 64 * g, s0);
+            ATTN_TMEM_LD_X32(t + L::kColDP + 64 * g, dp0);
+            ATTN_TMEM_LD_X32(t + L::kColS + 64 * g + 32, s1);
+            ATTN_TMEM_LD_X32(t + L::kColDP + 64 * g + 32, dp1);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kvSdPFree));
             // The previous block's dV/dK products read P^T and dS^T: wait before overwriting.
             if (i > 0 && !(ok = warp_wait(bar(kvDone), (i - 1) & 1, abort_flag))) break;
             tc_fence_after();
             // Only the causal diagonal block and ragged edges need a mask.
             const bool masked = (p.causal && qb0 + i == kblk) || q0 + kBlk > N || k0 + kBlk > N;
-#pragma unroll 1
-            for (int ch = 2 * g; ch < 2 * g + 2; ++ch) {  // 32 queries at a time
-                if (masked)
-                    kv_chunk<BF16, true, D>(t, ch, ls, dl, p.c, key, q0, N, p.causal);
-                else
-                    kv_chunk<BF16, false, D>(t, ch, ls, dl, p.c, key, q0, N, p.causal);
+            if (masked) {
+                kv_chunk<BF16, true, D>(t, 2 * g, s0, dp0, ls, dl, p.c, key, q0, N, p.causal);
+                kv_chunk<BF16, true, D>(t, 2 * g + 1, s1, dp1, ls, dl, p.c, key, q0, N, p.causal);
+            } else {
+                kv_chunk<BF16, false, D>(t, 2 * g, s0, dp0, ls, dl, p.c, key, q0, N, p.causal);
+                kv_chunk<BF16, false, D>(t, 2 * g + 1, s1, dp1, ls, dl, p.c, key, q0, N, p.causal);
             }
-            // S^T and dP^T are copied out: the next block's products may overwrite them.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kvSdPFree));
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -419,71 +436,74 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (!ok) raise_abort(abort_flag);
-    } else if (warp == kProducerWarp && lane == 0) {
-        // =============================== TMA producer ===============================
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
-        prefetch_tmap(&tm_do);
-        if constexpr (L::kOInStage) prefetch_tmap(&tm_o);
-        mbar_arrive_expect_tx(bar(kvKV), 2 * kTile);
-        tma_tile<D>(base + L::kOffK, &tm_k, k0, bh, bar(kvKV));
-        tma_tile<D>(base + L::kOffV, &tm_v, k0, bh, bar(kvKV));
-        bool ok = true;
-        int issued = 0;
-        for (int i = 0; i < nq; ++i) {
-            const int st = i & 1, q0 = (qb0 + i) * kBlk;
-            if (!(ok = mbar_wait(bar(kvQEmpty + st), ((i >> 1) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
-            const uint32_t stage = base + L::kOffStage + st * L::kStageBytes;
-            mbar_arrive_expect_tx(bar(kvQFull + st), L::kStageBytes);
-            tma_tile<D>(stage, &tm_q, q0, bh, bar(kvQFull + st));
-            tma_tile<D>(stage + kTile, &tm_do, q0, bh, bar(kvQFull + st));
-            if constexpr (L::kOInStage) tma_tile<D>(stage + 2 * kTile, &tm_o, q0, bh, bar(kvQFull + st));
-            issued = i + 1;
-        }
-        if (!ok) raise_abort(abort_flag);
-        // Every copy must land before the CTA exits (normally they were all consumed).
-        mbar_wait(bar(kvKV), 0, nullptr, kDrainTimeoutNs);
-        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
-            mbar_wait(bar(kvQFull + (i & 1)), (i >> 1) & 1, nullptr, kDrainTimeoutNs);
-    } else if (warp == kMmaWarp && lane == 0) {
-        // ================================ MMA issuer ================================
-        // S^T(0), dP^T(0); then per block i: S^T(i+1), dP^T(i+1) once block i's were copied out
-        // (d = 128: once block i's dV, dK products are done, as P^T and dS^T sit over S^T and
-        // dP^T), and dV, dK += block i's P^T dO, dS^T Q once P^T and dS^T are in TMEM.
-        bool ok = mbar_wait(bar(kvKV), 0, abort_flag, kWaitTimeoutNs);
-        auto issue_sdp = [&](int i) {
-            const uint32_t stage = base + L::kOffStage + (i & 1) * L::kStageBytes;
-            if (!mbar_wait(bar(kvQFull + (i & 1)), (i >> 1) & 1, abort_flag, kWaitTimeoutNs)) return false;
-            tc_fence_after();
-            mma_ss_128x128<BF16, D>(tmem + L::kColS, base + L::kOffK, stage);           // S^T = K Q^T
-            umma_commit(bar(kvSFull));
-            mma_ss_128x128<BF16, D>(tmem + L::kColDP, base + L::kOffV, stage + kTile);  // dP^T = V dO^T
-            umma_commit(bar(kvDPFull));
-            return true;
-        };
-        if (ok && nq > 0) ok = issue_sdp(0);
-        for (int i = 0; ok && i < nq; ++i) {
-            if (!L::kAlias && i + 1 < nq) {
-                if (!(ok = mbar_wait(bar(kvSdPFree), i & 1, abort_flag, kWaitTimeoutNs))) break;
-                if (!(ok = issue_sdp(i + 1))) break;
+    } else {
+        regs_decrease<kRegsOther>();
+        if (warp == kProducerWarp && lane == 0) {
+            // =============================== TMA producer ===============================
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            if constexpr (L::kOInStage) prefetch_tmap(&tm_o);
+            mbar_arrive_expect_tx(bar(kvKV), 2 * kTile);
+            tma_tile<D>(base + L::kOffK, &tm_k, k0, bh, bar(kvKV));
+            tma_tile<D>(base + L::kOffV, &tm_v, k0, bh, bar(kvKV));
+            bool ok = true;
+            int issued = 0;
+            for (int i = 0; i < nq; ++i) {
+                const int st = i & 1, q0 = (qb0 + i) * kBlk;
+                if (!(ok = mbar_wait(bar(kvQEmpty + st), ((i >> 1) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
+                const uint32_t stage = base + L::kOffStage + st * L::kStageBytes;
+                mbar_arrive_expect_tx(bar(kvQFull + st), L::kStageBytes);
+                tma_tile<D>(stage, &tm_q, q0, bh, bar(kvQFull + st));
+                tma_tile<D>(stage + kTile, &tm_do, q0, bh, bar(kvQFull + st));
+                if constexpr (L::kOInStage) tma_tile<D>(stage + 2 * kTile, &tm_o, q0, bh, bar(kvQFull + st));
+                issued = i + 1;
             }
-            if (!(ok = mbar_wait(bar(kvPdSFull), i & 1, abort_flag, kWaitTimeoutNs))) break;
-            tc_fence_after();
-            const uint32_t stage = base + L::kOffStage + (i & 1) * L::kStageBytes;
-            mma_ts_128xD<BF16, D>(tmem + L::kColDV, tmem + L::kColP, stage + kTile, i > 0, L::kAlias);  // dV += P^T dO
-            mma_ts_128xD<BF16, D>(tmem + L::kColDK, tmem + L::kColDS, stage, i > 0, L::kAlias);          // dK += dS^T Q
-            umma_commit(bar(kvDone));
-            umma_commit(bar(kvQEmpty + (i & 1)));
-            if (L::kAlias && i + 1 < nq) {
-                if (!(ok = mbar_wait(bar(kvDone), i & 1, abort_flag, kWaitTimeoutNs))) break;
+            if (!ok) raise_abort(abort_flag);
+            // Every copy must land before the CTA exits (normally they were all consumed).
+            mbar_wait(bar(kvKV), 0, nullptr, kDrainTimeoutNs);
+            for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
+                mbar_wait(bar(kvQFull + (i & 1)), (i >> 1) & 1, nullptr, kDrainTimeoutNs);
+        } else if (warp == kMmaWarp && lane == 0) {
+            // ================================ MMA issuer ================================
+            // S^T(0), dP^T(0); then per block i: S^T(i+1), dP^T(i+1) once block i's were copied out
+            // (d = 128: once block i's dV, dK products are done, as P^T and dS^T sit over S^T and
+            // dP^T), and dV, dK += block i's P^T dO, dS^T Q once P^T and dS^T are in TMEM.
+            bool ok = mbar_wait(bar(kvKV), 0, abort_flag, kWaitTimeoutNs);
+            auto issue_sdp = [&](int i) {
+                const uint32_t stage = base + L::kOffStage + (i & 1) * L::kStageBytes;
+                if (!mbar_wait(bar(kvQFull + (i & 1)), (i >> 1) & 1, abort_flag, kWaitTimeoutNs)) return false;
                 tc_fence_after();
-                if (!(ok = issue_sdp(i + 1))) break;
+                mma_ss_128x128<BF16, D>(tmem + L::kColS, base + L::kOffK, stage);           // S^T = K Q^T
+                umma_commit(bar(kvSFull));
+                mma_ss_128x128<BF16, D>(tmem + L::kColDP, base + L::kOffV, stage + kTile);  // dP^T = V dO^T
+                umma_commit(bar(kvDPFull));
+                return true;
+            };
+            if (ok && nq > 0) ok = issue_sdp(0);
+            for (int i = 0; ok && i < nq; ++i) {
+                if (!L::kAlias && i + 1 < nq) {
+                    if (!(ok = mbar_wait(bar(kvSdPFree), i & 1, abort_flag, kWaitTimeoutNs))) break;
+                    if (!(ok = issue_sdp(i + 1))) break;
+                }
+                if (!(ok = mbar_wait(bar(kvPdSFull), i & 1, abort_flag, kWaitTimeoutNs))) break;
+                tc_fence_after();
+                const uint32_t stage = base + L::kOffStage + (i & 1) * L::kStageBytes;
+                mma_ts_128xD<BF16, D>(tmem + L::kColDV, tmem + L::kColP, stage + kTile, i > 0, L::kAlias);  // dV += P^T dO
+                mma_ts_128xD<BF16, D>(tmem + L::kColDK, tmem + L::kColDS, stage, i > 0, L::kAlias);          // dK += dS^T Q
+                umma_commit(bar(kvDone));
+                umma_commit(bar(kvQEmpty + (i & 1)));
+                if (L::kAlias && i + 1 < nq) {
+                    if (!(ok = mbar_wait(bar(kvDone), i & 1, abort_flag, kWaitTimeoutNs))) break;
+                    tc_fence_after();
+                    if (!(ok = issue_sdp(i + 1))) break;
+                }
             }
+            if (!ok) raise_abort(abort_flag);
+            umma_commit(bar(kvDrain));
+            mbar_wait(bar(kvDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         }
-        if (!ok) raise_abort(abort_flag);
-        umma_commit(bar(kvDrain));
-        mbar_wait(bar(kvDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
     }
 
     tc_fence_before();
@@ -523,13 +543,9 @@ struct QLay {
 // One 32-key chunk of the dQ kernel's elementwise step for this thread's query: dS = P (dP -
 // delta) from S and dP in TMEM, stored back as 16-bit pairs.
 template <bool BF16, bool kMasked, int D>
-__device__ __forceinline__ void q_chunk(uint32_t t, int ch, float l2, float delta, float c, int query, int k0, int N,
-                                        int causal) {
+__device__ __forceinline__ void q_chunk(uint32_t t, int ch, const uint32_t (&s)[32], const uint32_t (&dp)[32], float l2,
+                                        float delta, float c, int query, int k0, int N, int causal) {
     using L = QLay<D>;
-    uint32_t s[32], dp[32];
-    ATTN_TMEM_LD_X32(t + L::kColS + 32 * ch, s);
-    ATTN_TMEM_LD_X32(t + L::kColDP + 32 * ch, dp);
-    tmem_ld_wait();
     uint32_t ds[16];
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
@@ -598,6 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < kElemWarps) {
         // ==================== elementwise warps: thread = query (TMEM lane) ====================
+        regs_increase<kRegsElem>();
         const int g = warp >> 2;  // warpgroup: key columns 64g .. 64g + 63
         const int r = ((warp & 3) << 5) + lane;
         const int query = q0 + r;
@@ -618,20 +635,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = warp_wait(bar(L::kSFull), j & 1, abort_flag))) break;
             if (!(ok = warp_wait(bar(L::kDPFull), j & 1, abort_flag))) break;
             tc_fence_after();
+            // This warpgroup's two chunks of S and dP into registers, released before the
+            // arithmetic so the next block's products overlap it.
+            uint32_t s0[32], dp0[32], s1[32], dp1[32];
+            ATTN_TMEM_LD_X32(t + L::kColS + 64 * g, s0);
+            ATTN_TMEM_LD_X32(t + L::kColDP + 64 * g, dp0);
+            ATTN_TMEM_LD_X32(t + L::kColS + 64 * g + 32, s1);
+            ATTN_TMEM_LD_X32(t + L::kColDP + 64 * g + 32, dp1);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kSdPFree));
             // The previous block's dQ product reads dS: wait before overwriting it.
             if (j > 0 && !(ok = warp_wait(bar(L::kDone), (j - 1) & 1, abort_flag))) break;
             tc_fence_after();
             const bool masked = (p.causal && j == qblk) || q0 + kBlk > N || k0 + kBlk > N;
-#pragma unroll 1
-            for (int ch = 2 * g; ch < 2 * g + 2; ++ch) {  // 32 keys at a time
-                if (masked)
-                    q_chunk<BF16, true, D>(t, ch, l2, delta, p.c, query, k0, N, p.causal);
-                else
-                    q_chunk<BF16, false, D>(t, ch, l2, delta, p.c, query, k0, N, p.causal);
+            if (masked) {
+                q_chunk<BF16, true, D>(t, 2 * g, s0, dp0, l2, delta, p.c, query, k0, N, p.causal);
+                q_chunk<BF16, true, D>(t, 2 * g + 1, s1, dp1, l2, delta, p.c, query, k0, N, p.causal);
+            } else {
+                q_chunk<BF16, false, D>(t, 2 * g, s0, dp0, l2, delta, p.c, query, k0, N, p.causal);
+                q_chunk<BF16, false, D>(t, 2 * g + 1, s1, dp1, l2, delta, p.c, query, k0, N, p.causal);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kSdPFree));
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -660,60 +685,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (!ok) raise_abort(abort_flag);
-    } else if (warp == kProducerWarp && lane == 0) {
-        // =============================== TMA producer ===============================
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
-        prefetch_tmap(&tm_do);
-        mbar_arrive_expect_tx(bar(qQ), 2 * kTile);
-        tma_tile<D>(base + L::kOffQ, &tm_q, q0, bh, bar(qQ));
-        tma_tile<D>(base + L::kOffDO, &tm_do, q0, bh, bar(qQ));
-        bool ok = true;
-        int issued = 0;
-        for (int j = 0; j < nk; ++j) {
-            const int st = j % S;
-            if (!(ok = mbar_wait(bar(L::kKVEmpty + st), ((j / S) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
-            const uint32_t stage = base + L::kOffKV + st * L::kStageBytes;
-            mbar_arrive_expect_tx(bar(qKVFull + st), 2 * kTile);
-            tma_tile<D>(stage, &tm_k, j * kBlk, bh, bar(qKVFull + st));
-            tma_tile<D>(stage + kTile, &tm_v, j * kBlk, bh, bar(qKVFull + st));
-            issued = j + 1;
-        }
-        if (!ok) raise_abort(abort_flag);
-        mbar_wait(bar(qQ), 0, nullptr, kDrainTimeoutNs);
-        for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
-            mbar_wait(bar(qKVFull + j % S), (j / S) & 1, nullptr, kDrainTimeoutNs);
-    } else if (warp == kMmaWarp && lane == 0) {
-        // ================================ MMA issuer ================================
-        bool ok = mbar_wait(bar(qQ), 0, abort_flag, kWaitTimeoutNs);
-        auto issue_sdp = [&](int j) {
-            const int st = j % S;
-            const uint32_t stage = base + L::kOffKV + st * L::kStageBytes;
-            if (!mbar_wait(bar(qKVFull + st), (j / S) & 1, abort_flag, kWaitTimeoutNs)) return false;
-            tc_fence_after();
-            mma_ss_128x128<BF16, D>(tmem + L::kColS, base + L::kOffQ, stage);             // S = Q K^T
-            umma_commit(bar(L::kSFull));
-            mma_ss_128x128<BF16, D>(tmem + L::kColDP, base + L::kOffDO, stage + kTile);   // dP = dO V^T
-            umma_commit(bar(L::kDPFull));
-            return true;
-        };
-        if (ok && nk > 0) ok = issue_sdp(0);
-        for (int j = 0; ok && j < nk; ++j) {
-            if (j + 1 < nk) {
-                if (!(ok = mbar_wait(bar(L::kSdPFree), j & 1, abort_flag, kWaitTimeoutNs))) break;
-                if (!(ok = issue_sdp(j + 1))) break;
+    } else {
+        regs_decrease<kRegsOther>();
+        if (warp == kProducerWarp && lane == 0) {
+            // =============================== TMA producer ===============================
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            mbar_arrive_expect_tx(bar(qQ), 2 * kTile);
+            tma_tile<D>(base + L::kOffQ, &tm_q, q0, bh, bar(qQ));
+            tma_tile<D>(base + L::kOffDO, &tm_do, q0, bh, bar(qQ));
+            bool ok = true;
+            int issued = 0;
+            for (int j = 0; j < nk; ++j) {
+                const int st = j % S;
+                if (!(ok = mbar_wait(bar(L::kKVEmpty + st), ((j / S) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
+                const uint32_t stage = base + L::kOffKV + st * L::kStageBytes;
+                mbar_arrive_expect_tx(bar(qKVFull + st), 2 * kTile);
+                tma_tile<D>(stage, &tm_k, j * kBlk, bh, bar(qKVFull + st));
+                tma_tile<D>(stage + kTile, &tm_v, j * kBlk, bh, bar(qKVFull + st));
+                issued = j + 1;
             }
-            if (!(ok = mbar_wait(bar(L::kDSFull), j & 1, abort_flag, kWaitTimeoutNs))) break;
-            tc_fence_after();
-            const uint32_t stage = base + L::kOffKV + (j % S) * L::kStageBytes;
-            mma_ts_128xD<BF16, D>(tmem + L::kColDQ, tmem + L::kColDS, stage, j > 0, false);  // dQ += dS K
-            umma_commit(bar(L::kDone));
-            umma_commit(bar(L::kKVEmpty + j % S));
+            if (!ok) raise_abort(abort_flag);
+            mbar_wait(bar(qQ), 0, nullptr, kDrainTimeoutNs);
+            for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
+                mbar_wait(bar(qKVFull + j % S), (j / S) & 1, nullptr, kDrainTimeoutNs);
+        } else if (warp == kMmaWarp && lane == 0) {
+            // ================================ MMA issuer ================================
+            bool ok = mbar_wait(bar(qQ), 0, abort_flag, kWaitTimeoutNs);
+            auto issue_sdp = [&](int j) {
+                const int st = j % S;
+                const uint32_t stage = base + L::kOffKV + st * L::kStageBytes;
+                if (!mbar_wait(bar(qKVFull + st), (j / S) & 1, abort_flag, kWaitTimeoutNs)) return false;
+                tc_fence_after();
+                mma_ss_128x128<BF16, D>(tmem + L::kColS, base + L::kOffQ, stage);             // S = Q K^T
+                umma_commit(bar(L::kSFull));
+                mma_ss_128x128<BF16, D>(tmem + L::kColDP, base + L::kOffDO, stage + kTile);   // dP = dO V^T
+                umma_commit(bar(L::kDPFull));
+                return true;
+            };
+            if (ok && nk > 0) ok = issue_sdp(0);
+            for (int j = 0; ok && j < nk; ++j) {
+                if (j + 1 < nk) {
+                    if (!(ok = mbar_wait(bar(L::kSdPFree), j & 1, abort_flag, kWaitTimeoutNs))) break;
+                    if (!(ok = issue_sdp(j + 1))) break;
+                }
+                if (!(ok = mbar_wait(bar(L::kDSFull), j & 1, abort_flag, kWaitTimeoutNs))) break;
+                tc_fence_after();
+                const uint32_t stage = base + L::kOffKV + (j % S) * L::kStageBytes;
+                mma_ts_128xD<BF16, D>(tmem + L::kColDQ, tmem + L::kColDS, stage, j > 0, false);  // dQ += dS K
+                umma_commit(bar(L::kDone));
+                umma_commit(bar(L::kKVEmpty + j % S));
+            }
+            if (!ok) raise_abort(abort_flag);
+            umma_commit(bar(L::kDrain));
+            mbar_wait(bar(L::kDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         }
-        if (!ok) raise_abort(abort_flag);
-        umma_commit(bar(L::kDrain));
-        mbar_wait(bar(L::kDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
     }
 
     tc_fence_before();
