@@ -222,8 +222,8 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const void* map, int row,
 }
 
 // ================================ dK, dV: one CTA per key block ================================
-// Shared memory: K, V tiles, then two stages of (Q, dO[, O]) tiles, then per-block lse and delta
-// (double-buffered by block parity), then mbarriers. At d = 64 the O tile comes with each stage
+// Shared memory: K, V tiles, then a ring of (Q, dO[, O]) stages (three at d = 64, two at
+// d = 128), then per-block lse and delta (double-buffered by block parity), then mbarriers. At d = 64 the O tile comes with each stage
 // and delta is a row product of two tiles; at d = 128 the stage holds Q and dO only (two stages of
 // three 32 KiB tiles would not fit) and delta reads O's rows from global memory.
 // Tensor memory: S^T 0, dP^T 128; d = 64: P^T 256, dS^T 320, dV 384, dK 448; d = 128 (dV and dK
@@ -231,8 +231,6 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const void* map, int row,
 // columns the elementwise warps have already read (chunk ch at 16 ch, + 32 for ch >= 2, so each
 // warpgroup writes only over its own columns), which makes the next block's S^T, dP^T wait for
 // this block's dV, dK products.
-enum { kvKV = 0, kvQFull = 1, kvQEmpty = 3, kvSFull = 5, kvDPFull, kvSdPFree, kvPdSFull, kvDone, kvDrain,
-       kvRows, kvNumBars };  // kvRows: the elementwise warps wrote this block's lse and delta
 
 template <int D>
 struct KvLay {
@@ -242,9 +240,16 @@ struct KvLay {
     static constexpr int kOffV = kTile;
     static constexpr int kOffStage = 2 * kTile;  // stage s: Q at +0, dO at +kTile, (O at +2 kTile)
     static constexpr int kStageBytes = (kOInStage ? 3 : 2) * kTile;
-    static constexpr int kOffRow = kOffStage + 2 * kStageBytes;  // lse[2][128], delta[2][128] floats
+    static constexpr int kStages = D == 64 ? 3 : 2;
+    static constexpr int kOffRow = kOffStage + kStages * kStageBytes;  // lse[2][128], delta[2][128] floats
     static constexpr int kOffBar = kOffRow + 4 * kBlk * 4;
-    static constexpr int kOffSlot = kOffBar + 8 * kvNumBars;
+    // Barriers: K and V landed; per stage full / empty; S^T and dP^T written; S^T and dP^T read
+    // out; P^T and dS^T written; dV, dK products done; the final drain; this block's lse and
+    // delta written by the elementwise warps.
+    static constexpr int kKV = 0, kQFull = 1, kQEmpty = kQFull + kStages, kSFull = kQEmpty + kStages,
+                         kDPFull = kSFull + 1, kSdPFree = kSFull + 2, kPdSFull = kSFull + 3, kDone = kSFull + 4,
+                         kDrain = kSFull + 5, kRows = kSFull + 6, kNumBars = kSFull + 7;
+    static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
     static constexpr int kOffAbort = kOffSlot + 4;
     static constexpr int kSmem = kOffAbort + 4 + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -317,18 +322,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nq = p.nblk - qb0;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(kvKV), 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(kvQFull + s), 1);
-            mbar_init(bar(kvQEmpty + s), 1);
+        mbar_init(bar(L::kKV), 1);
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(bar(L::kQFull + s), 1);
+            mbar_init(bar(L::kQEmpty + s), 1);
         }
-        mbar_init(bar(kvSFull), 1);
-        mbar_init(bar(kvDPFull), 1);
-        mbar_init(bar(kvSdPFree), kElemWarps);
-        mbar_init(bar(kvPdSFull), kElemWarps);
-        mbar_init(bar(kvDone), 1);
-        mbar_init(bar(kvDrain), 1);
-        mbar_init(bar(kvRows), kElemWarps);
+        mbar_init(bar(L::kSFull), 1);
+        mbar_init(bar(L::kDPFull), 1);
+        mbar_init(bar(L::kSdPFree), kElemWarps);
+        mbar_init(bar(L::kPdSFull), kElemWarps);
+        mbar_init(bar(L::kDone), 1);
+        mbar_init(bar(L::kDrain), 1);
+        mbar_init(bar(L::kRows), kElemWarps);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -350,10 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t = tmem + (static_cast<uint32_t>((warp & 3) << 5) << 16);
         bool ok = true;
         for (int i = 0; ok && i < nq; ++i) {
-            const int st = i & 1, q0 = (qb0 + i) * kBlk;
+            const int st = i % L::kStages, rb = i & 1, q0 = (qb0 + i) * kBlk;
             // This block's lse and delta: warpgroup g fills queries 64g .. 64g + 63, two threads
             // per query (one half of the row's dot product each).
-            if (!(ok = warp_wait(bar(kvQFull + st), (i >> 1) & 1, abort_flag))) break;
+            if (!(ok = warp_wait(bar(L::kQFull + st), (i / L::kStages) & 1, abort_flag))) break;
             const uint8_t* stage = gbase + L::kOffStage + st * L::kStageBytes;
             const int qi = 64 * g + (r >> 1), half = r & 1;
             const bool qin = q0 + qi < N;
@@ -369,18 +374,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             dpart += __shfl_xor_sync(0xffffffffu, dpart, 1);
             if (half == 0) {
-                lse_s[st * kBlk + qi] = qin ? p.lse[static_cast<int64_t>(bh) * N + q0 + qi] : 0.f;
-                delta_s[st * kBlk + qi] = dpart;
+                lse_s[rb * kBlk + qi] = qin ? p.lse[static_cast<int64_t>(bh) * N + q0 + qi] : 0.f;
+                delta_s[rb * kBlk + qi] = dpart;
             }
             // All warps' rows written (a bounded wait, unlike a named barrier, so a warp that
             // gave up cannot leave the others waiting forever).
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kvRows));
-            if (!(ok = warp_wait(bar(kvRows), i & 1, abort_flag))) break;
-            const float* ls = lse_s + st * kBlk;
-            const float* dl = delta_s + st * kBlk;
-            if (!(ok = warp_wait(bar(kvSFull), i & 1, abort_flag))) break;
-            if (!(ok = warp_wait(bar(kvDPFull), i & 1, abort_flag))) break;
+            if (lane == 0) mbar_arrive(bar(L::kRows));
+            if (!(ok = warp_wait(bar(L::kRows), i & 1, abort_flag))) break;
+            const float* ls = lse_s + rb * kBlk;
+            const float* dl = delta_s + rb * kBlk;
+            if (!(ok = warp_wait(bar(L::kSFull), i & 1, abort_flag))) break;
+            if (!(ok = warp_wait(bar(L::kDPFull), i & 1, abort_flag))) break;
             tc_fence_after();
             // This warpgroup's two chunks of S^T and dP^T into registers, then they are released
             // so that the next block's products run during the arithmetic below.
@@ -392,9 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kvSdPFree));
+            if (lane == 0) mbar_arrive(bar(L::kSdPFree));
             // The previous block's dV/dK products read P^T and dS^T: wait before overwriting.
-            if (i > 0 && !(ok = warp_wait(bar(kvDone), (i - 1) & 1, abort_flag))) break;
+            if (i > 0 && !(ok = warp_wait(bar(L::kDone), (i - 1) & 1, abort_flag))) break;
             tc_fence_after();
             // Only the causal diagonal block and ragged edges need a mask.
             const bool masked = (p.causal && qb0 + i == kblk) || q0 + kBlk > N || k0 + kBlk > N;
@@ -408,11 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kvPdSFull));
+            if (lane == 0) mbar_arrive(bar(L::kPdSFull));
         }
         // ---- epilogue: dK * scale (warpgroup 0) and dV (warpgroup 1), rounded; keys >= N not stored ----
         if (ok && nq > 0) {
-            if ((ok = warp_wait(bar(kvDone), (nq - 1) & 1, abort_flag))) {
+            if ((ok = warp_wait(bar(L::kDone), (nq - 1) & 1, abort_flag))) {
                 tc_fence_after();
                 uint16_t* const dst = reinterpret_cast<uint16_t*>(g == 0 ? p.grad0 : p.grad1) +
                                       (static_cast<int64_t>(bh) * N + key) * D;
@@ -445,64 +450,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
             if constexpr (L::kOInStage) prefetch_tmap(&tm_o);
-            mbar_arrive_expect_tx(bar(kvKV), 2 * kTile);
-            tma_tile<D>(base + L::kOffK, &tm_k, k0, bh, bar(kvKV));
-            tma_tile<D>(base + L::kOffV, &tm_v, k0, bh, bar(kvKV));
+            mbar_arrive_expect_tx(bar(L::kKV), 2 * kTile);
+            tma_tile<D>(base + L::kOffK, &tm_k, k0, bh, bar(L::kKV));
+            tma_tile<D>(base + L::kOffV, &tm_v, k0, bh, bar(L::kKV));
             bool ok = true;
             int issued = 0;
             for (int i = 0; i < nq; ++i) {
-                const int st = i & 1, q0 = (qb0 + i) * kBlk;
-                if (!(ok = mbar_wait(bar(kvQEmpty + st), ((i >> 1) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
+                const int st = i % L::kStages, q0 = (qb0 + i) * kBlk;
+                if (!(ok = mbar_wait(bar(L::kQEmpty + st), ((i / L::kStages) & 1) ^ 1, abort_flag, kWaitTimeoutNs)))
+                    break;
                 const uint32_t stage = base + L::kOffStage + st * L::kStageBytes;
-                mbar_arrive_expect_tx(bar(kvQFull + st), L::kStageBytes);
-                tma_tile<D>(stage, &tm_q, q0, bh, bar(kvQFull + st));
-                tma_tile<D>(stage + kTile, &tm_do, q0, bh, bar(kvQFull + st));
-                if constexpr (L::kOInStage) tma_tile<D>(stage + 2 * kTile, &tm_o, q0, bh, bar(kvQFull + st));
+                mbar_arrive_expect_tx(bar(L::kQFull + st), L::kStageBytes);
+                tma_tile<D>(stage, &tm_q, q0, bh, bar(L::kQFull + st));
+                tma_tile<D>(stage + kTile, &tm_do, q0, bh, bar(L::kQFull + st));
+                if constexpr (L::kOInStage) tma_tile<D>(stage + 2 * kTile, &tm_o, q0, bh, bar(L::kQFull + st));
                 issued = i + 1;
             }
             if (!ok) raise_abort(abort_flag);
             // Every copy must land before the CTA exits (normally they were all consumed).
-            mbar_wait(bar(kvKV), 0, nullptr, kDrainTimeoutNs);
-            for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
-                mbar_wait(bar(kvQFull + (i & 1)), (i >> 1) & 1, nullptr, kDrainTimeoutNs);
+            mbar_wait(bar(L::kKV), 0, nullptr, kDrainTimeoutNs);
+            for (int i = (issued > L::kStages ? issued - L::kStages : 0); i < issued; ++i)
+                mbar_wait(bar(L::kQFull + i % L::kStages), (i / L::kStages) & 1, nullptr, kDrainTimeoutNs);
         } else if (warp == kMmaWarp && lane == 0) {
             // ================================ MMA issuer ================================
             // S^T(0), dP^T(0); then per block i: S^T(i+1), dP^T(i+1) once block i's were copied out
             // (d = 128: once block i's dV, dK products are done, as P^T and dS^T sit over S^T and
             // dP^T), and dV, dK += block i's P^T dO, dS^T Q once P^T and dS^T are in TMEM.
-            bool ok = mbar_wait(bar(kvKV), 0, abort_flag, kWaitTimeoutNs);
+            bool ok = mbar_wait(bar(L::kKV), 0, abort_flag, kWaitTimeoutNs);
             auto issue_sdp = [&](int i) {
-                const uint32_t stage = base + L::kOffStage + (i & 1) * L::kStageBytes;
-                if (!mbar_wait(bar(kvQFull + (i & 1)), (i >> 1) & 1, abort_flag, kWaitTimeoutNs)) return false;
+                const uint32_t stage = base + L::kOffStage + (i % L::kStages) * L::kStageBytes;
+                if (!mbar_wait(bar(L::kQFull + i % L::kStages), (i / L::kStages) & 1, abort_flag, kWaitTimeoutNs))
+                    return false;
                 tc_fence_after();
                 mma_ss_128x128<BF16, D>(tmem + L::kColS, base + L::kOffK, stage);           // S^T = K Q^T
-                umma_commit(bar(kvSFull));
+                umma_commit(bar(L::kSFull));
                 mma_ss_128x128<BF16, D>(tmem + L::kColDP, base + L::kOffV, stage + kTile);  // dP^T = V dO^T
-                umma_commit(bar(kvDPFull));
+                umma_commit(bar(L::kDPFull));
                 return true;
             };
             if (ok && nq > 0) ok = issue_sdp(0);
             for (int i = 0; ok && i < nq; ++i) {
                 if (!L::kAlias && i + 1 < nq) {
-                    if (!(ok = mbar_wait(bar(kvSdPFree), i & 1, abort_flag, kWaitTimeoutNs))) break;
+                    if (!(ok = mbar_wait(bar(L::kSdPFree), i & 1, abort_flag, kWaitTimeoutNs))) break;
                     if (!(ok = issue_sdp(i + 1))) break;
                 }
-                if (!(ok = mbar_wait(bar(kvPdSFull), i & 1, abort_flag, kWaitTimeoutNs))) break;
+                if (!(ok = mbar_wait(bar(L::kPdSFull), i & 1, abort_flag, kWaitTimeoutNs))) break;
                 tc_fence_after();
-                const uint32_t stage = base + L::kOffStage + (i & 1) * L::kStageBytes;
+                const uint32_t stage = base + L::kOffStage + (i % L::kStages) * L::kStageBytes;
                 mma_ts_128xD<BF16, D>(tmem + L::kColDV, tmem + L::kColP, stage + kTile, i > 0, L::kAlias);  // dV += P^T dO
                 mma_ts_128xD<BF16, D>(tmem + L::kColDK, tmem + L::kColDS, stage, i > 0, L::kAlias);          // dK += dS^T Q
-                umma_commit(bar(kvDone));
-                umma_commit(bar(kvQEmpty + (i & 1)));
+                umma_commit(bar(L::kDone));
+                umma_commit(bar(L::kQEmpty + i % L::kStages));
                 if (L::kAlias && i + 1 < nq) {
-                    if (!(ok = mbar_wait(bar(kvDone), i & 1, abort_flag, kWaitTimeoutNs))) break;
+                    if (!(ok = mbar_wait(bar(L::kDone), i & 1, abort_flag, kWaitTimeoutNs))) break;
                     tc_fence_after();
                     if (!(ok = issue_sdp(i + 1))) break;
                 }
             }
             if (!ok) raise_abort(abort_flag);
-            umma_commit(bar(kvDrain));
-            mbar_wait(bar(kvDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+            umma_commit(bar(L::kDrain));
+            mbar_wait(bar(L::kDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         }
     }
 
