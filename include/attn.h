@@ -118,7 +118,9 @@ int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* ls
  *   lse              : const device pointer, float32 [B, H, N], 16-byte aligned: the base-2
  *                      log-sum-exps attn_fwd_lse stored for the same q, k
  *   dq, dk, dv       : device pointers, [B, H, N, d] of dtype, 16-byte aligned; they must not
- *                      overlap each other or any input; every element is written
+ *                      overlap each other or any input; every element is written (bf16/fp16:
+ *                      dq's rows hold intermediate values until the last kernel of the call
+ *                      overwrites them, so dq must not be read before the call completes)
  *   other arguments  : as attn_fwd (same checks and status codes)
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,

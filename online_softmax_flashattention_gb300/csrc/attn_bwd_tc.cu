@@ -25,17 +25,20 @@
 // dQ kernel S 0, dP 128, dS 256, dQ 320. The next block's S and dP products go out as soon as
 // the elementwise warps have loaded the current ones into registers, before their arithmetic,
 // so the products overlap it.
-// delta is computed from the dO and O tiles in shared memory (the dK/dV kernel loads O for
-// that) and lse is read per block, so the call allocates nothing.
+// delta is made once per query row by a small pre-pass (one 16-byte piece of dO and O per
+// lane) and parked in the first four bytes of that row of dq, an output that the dQ kernel
+// overwrites last, so the call allocates nothing; the dK/dV kernel's warps 10-11 copy each
+// query block's lse and delta into shared memory a block ahead of their use.
 //
 // Roles: warps 0-7 elementwise (thread = TMEM lane; warps w and w + 4 share lanes and split the
-// columns), warp 8 TMA producer, warp 9 MMA issuer and tensor-memory owner, warps 10-11 idle
-// (they only give up registers). Every mbarrier wait is bounded; on expiry the kernel sets the
+// columns), warp 8 TMA producer, warp 9 MMA issuer and tensor-memory owner, warps 10-11 the
+// dK/dV kernel's lse/delta loader (idle in the dQ kernel). Every mbarrier wait is bounded; on expiry the kernel sets the
 // shared device error word (reported by attn_device_status), drains and returns.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -53,14 +56,14 @@ constexpr int kBlockBytes = kBlk * 64 * 2;  // 16 KiB: 128 rows x 128 bytes (64 
 // warpgroup 2: the TMA producer (warp 8), the MMA issuer (warp 9) and two idle warps. Ten warps
 // would already put three on some SM sub-partition and cap every thread at 168 registers; the two
 // idle warps complete warpgroup 2 so that it can hand registers to the elementwise warpgroups
-// (setmaxnreg acts on whole warpgroups): 56 a thread there, 224 in warps 0-7.
+// (setmaxnreg acts on whole warpgroups): 72 a thread there, 216 in warps 0-7.
 constexpr int kThreads = 384;
 constexpr int kElemWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kRegsLaunch = 168;  // 65536 / 384, rounded down to the allocation granule of 8
-constexpr int kRegsElem = 224;
-constexpr int kRegsOther = 56;
+constexpr int kRegsElem = 216;
+constexpr int kRegsOther = 72;
 static_assert(32 * kElemWarps * kRegsElem + (kThreads - 32 * kElemWarps) * kRegsOther <= kThreads * kRegsLaunch,
               "the register split must fit in the block's launch allocation");
 constexpr uint32_t kTmemCols = 512;
@@ -72,7 +75,7 @@ __device__ unsigned int g_bwd_error = 0;
 struct BwdParams {
     void* grad0;  // dk (kv kernel) or dq (q kernel)
     void* grad1;  // dv (kv kernel)
-    const void* o;
+    const uint8_t* delta_rows;  // dq: delta of query row n in the first four bytes of row n
     const float* lse;
     int N;
     int BH;
@@ -112,12 +115,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 
-// Element (row r, column e) of a 128-row x 64 tile written by TMA with the 128-byte swizzle:
-// 16-byte chunks of a row are permuted by row % 8.
-__device__ __forceinline__ uint32_t sw128_offset(int r, int e) {
-    return static_cast<uint32_t>(r * 128 + ((((e >> 3) ^ (r & 7)) << 4)) + ((e & 7) << 1));
-}
-
 template <bool BF16>
 __device__ __forceinline__ float2 unpack2(uint32_t u) {
     if constexpr (BF16) {
@@ -128,64 +125,36 @@ __device__ __forceinline__ float2 unpack2(uint32_t u) {
     }
 }
 
-// sum_e a[r,e] b[r,e] over one row of two swizzled tiles (fp32 accumulation).
-template <bool BF16>
-__device__ __forceinline__ float row_dot(const uint8_t* a, const uint8_t* b, int r) {
-    float acc = 0.f;
+// delta_n = sum_e dO[n,e] O[n,e] (fp32) for every query row n of all heads, stored as the first
+// four bytes of dq's row n: dq is an output the call may use as scratch, and the dQ kernel
+// reads each row's delta in the CTA that later overwrites that row. D/8 lanes share a row, one
+// 16-byte piece of dO and of O each; a warp covers 32 / (D/8) whole rows per step.
+template <bool BF16, int D>
+__global__ void __launch_bounds__(256)
+    attn_bwd_delta_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout, uint8_t* __restrict__ dq,
+                          int64_t rows) {
+    constexpr int kLanes = D / 8;
+    const int64_t total = rows * kLanes;
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t g0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31u); g0 < total;
+         g0 += stride) {
+        const int64_t gi = g0 + lane;  // 16-byte piece gi % kLanes of row gi / kLanes
+        float acc = 0.f;
+        if (gi < total) {
+            const uint4 x = o[gi], y = dout[gi];
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        const uint32_t off = sw128_offset(r, ch * 8);
-        const uint4 x = *reinterpret_cast<const uint4*>(a + off);
-        const uint4 y = *reinterpret_cast<const uint4*>(b + off);
-        const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 u = unpack2<BF16>(xs[i]), v = unpack2<BF16>(ys[i]);
-            acc = fmaf(u.x, v.x, acc);
-            acc = fmaf(u.y, v.y, acc);
+            for (int i = 0; i < 4; ++i) {
+                const float2 u = unpack2<BF16>(xs[i]), v = unpack2<BF16>(ys[i]);
+                acc = fmaf(u.x, v.x, acc);
+                acc = fmaf(u.y, v.y, acc);
+            }
         }
+#pragma unroll
+        for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (gi < total && gi % kLanes == 0) *reinterpret_cast<float*>(dq + (gi / kLanes) * (2 * D)) = acc;
     }
-    return acc;
-}
-
-// Half of sum_e a[r,e] b[r,e]: the 32 values of 16-byte chunks 4*half .. 4*half + 3.
-template <bool BF16>
-__device__ __forceinline__ float row_dot_half(const uint8_t* a, const uint8_t* b, int r, int half) {
-    float acc = 0.f;
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-        const uint32_t off = sw128_offset(r, (4 * half + c4) * 8);
-        const uint4 x = *reinterpret_cast<const uint4*>(a + off);
-        const uint4 y = *reinterpret_cast<const uint4*>(b + off);
-        const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 u = unpack2<BF16>(xs[i]), v = unpack2<BF16>(ys[i]);
-            acc = fmaf(u.x, v.x, acc);
-            acc = fmaf(u.y, v.y, acc);
-        }
-    }
-    return acc;
-}
-
-// sum_e a[e] b[e] over one 64-value row of a swizzled tile (a: row r of the tile at `tile`) and
-// 64 contiguous values in global memory (b).
-template <bool BF16>
-__device__ __forceinline__ float row_dot_global(const uint8_t* tile, int r, const uint16_t* b) {
-    float acc = 0.f;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        const uint4 x = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, ch * 8));
-        const uint4 y = *reinterpret_cast<const uint4*>(b + ch * 8);
-        const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 u = unpack2<BF16>(xs[i]), v = unpack2<BF16>(ys[i]);
-            acc = fmaf(u.x, v.x, acc);
-            acc = fmaf(u.y, v.y, acc);
-        }
-    }
-    return acc;
 }
 
 // 128 x 128 product over K = D of two K-major tiles (each D/64 column blocks of 128-byte rows)
@@ -222,10 +191,9 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const void* map, int row,
 }
 
 // ================================ dK, dV: one CTA per key block ================================
-// Shared memory: K, V tiles, then a ring of (Q, dO[, O]) stages (three at d = 64, two at
-// d = 128), then per-block lse and delta (double-buffered by block parity), then mbarriers. At d = 64 the O tile comes with each stage
-// and delta is a row product of two tiles; at d = 128 the stage holds Q and dO only (two stages of
-// three 32 KiB tiles would not fit) and delta reads O's rows from global memory.
+// Shared memory: K, V tiles, then a ring of (Q, dO) stages (four at d = 64, two at d = 128),
+// then per-block lse and delta (double-buffered by block parity, filled by warps 10-11 from lse
+// and from the delta pre-pass), then mbarriers.
 // Tensor memory: S^T 0, dP^T 128; d = 64: P^T 256, dS^T 320, dV 384, dK 448; d = 128 (dV and dK
 // take 128 columns each): dV 256, dK 384, and P^T and dS^T are written over the S^T and dP^T
 // columns the elementwise warps have already read (chunk ch at 16 ch, + 32 for ch >= 2, so each
@@ -235,20 +203,20 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const void* map, int row,
 template <int D>
 struct KvLay {
     static constexpr int kTile = kBlk * D * 2;
-    static constexpr bool kOInStage = D == 64;
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kTile;
-    static constexpr int kOffStage = 2 * kTile;  // stage s: Q at +0, dO at +kTile, (O at +2 kTile)
-    static constexpr int kStageBytes = (kOInStage ? 3 : 2) * kTile;
-    static constexpr int kStages = D == 64 ? 3 : 2;
+    static constexpr int kOffStage = 2 * kTile;  // stage s: Q at +0, dO at +kTile
+    static constexpr int kStageBytes = 2 * kTile;
+    static constexpr int kStages = D == 64 ? 4 : 2;
     static constexpr int kOffRow = kOffStage + kStages * kStageBytes;  // lse[2][128], delta[2][128] floats
     static constexpr int kOffBar = kOffRow + 4 * kBlk * 4;
     // Barriers: K and V landed; per stage full / empty; S^T and dP^T written; S^T and dP^T read
-    // out; P^T and dS^T written; dV, dK products done; the final drain; this block's lse and
-    // delta written by the elementwise warps.
+    // out; P^T and dS^T written; dV, dK products done; the final drain; per row buffer: lse and
+    // delta written / read.
     static constexpr int kKV = 0, kQFull = 1, kQEmpty = kQFull + kStages, kSFull = kQEmpty + kStages,
                          kDPFull = kSFull + 1, kSdPFree = kSFull + 2, kPdSFull = kSFull + 3, kDone = kSFull + 4,
-                         kDrain = kSFull + 5, kRows = kSFull + 6, kNumBars = kSFull + 7;
+                         kDrain = kSFull + 5, kRowsFull = kSFull + 6, kRowsEmpty = kRowsFull + 2,
+                         kNumBars = kRowsEmpty + 2;
     static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
     static constexpr int kOffAbort = kOffSlot + 4;
     static constexpr int kSmem = kOffAbort + 4 + 1024;
@@ -299,8 +267,8 @@ __device__ __forceinline__ void kv_chunk(uint32_t t, int ch, const uint32_t (&s)
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                            const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                            const BwdParams p) {
     using L = KvLay<D>;
     constexpr int kTile = L::kTile;
     extern __shared__ uint8_t smem_raw[];
@@ -333,7 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(L::kPdSFull), kElemWarps);
         mbar_init(bar(L::kDone), 1);
         mbar_init(bar(L::kDrain), 1);
-        mbar_init(bar(L::kRows), kElemWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::kRowsFull + b), 2);
+            mbar_init(bar(L::kRowsEmpty + b), kElemWarps);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -355,33 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t = tmem + (static_cast<uint32_t>((warp & 3) << 5) << 16);
         bool ok = true;
         for (int i = 0; ok && i < nq; ++i) {
-            const int st = i % L::kStages, rb = i & 1, q0 = (qb0 + i) * kBlk;
-            // This block's lse and delta: warpgroup g fills queries 64g .. 64g + 63, two threads
-            // per query (one half of the row's dot product each).
-            if (!(ok = warp_wait(bar(L::kQFull + st), (i / L::kStages) & 1, abort_flag))) break;
-            const uint8_t* stage = gbase + L::kOffStage + st * L::kStageBytes;
-            const int qi = 64 * g + (r >> 1), half = r & 1;
-            const bool qin = q0 + qi < N;
-            float dpart = 0.f;
-            if (qin) {
-                if constexpr (L::kOInStage) {
-                    dpart = row_dot_half<BF16>(stage + kTile, stage + 2 * kTile, qi, half);
-                } else {
-                    const uint16_t* orow = reinterpret_cast<const uint16_t*>(p.o) +
-                                           (static_cast<int64_t>(bh) * N + q0 + qi) * D + 64 * half;
-                    dpart = row_dot_global<BF16>(stage + kTile + half * kBlockBytes, qi, orow);
-                }
-            }
-            dpart += __shfl_xor_sync(0xffffffffu, dpart, 1);
-            if (half == 0) {
-                lse_s[rb * kBlk + qi] = qin ? p.lse[static_cast<int64_t>(bh) * N + q0 + qi] : 0.f;
-                delta_s[rb * kBlk + qi] = dpart;
-            }
-            // All warps' rows written (a bounded wait, unlike a named barrier, so a warp that
-            // gave up cannot leave the others waiting forever).
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kRows));
-            if (!(ok = warp_wait(bar(L::kRows), i & 1, abort_flag))) break;
+            const int rb = i & 1, q0 = (qb0 + i) * kBlk;
+            if (!(ok = warp_wait(bar(L::kRowsFull + rb), (i >> 1) & 1, abort_flag))) break;
             const float* ls = lse_s + rb * kBlk;
             const float* dl = delta_s + rb * kBlk;
             if (!(ok = warp_wait(bar(L::kSFull), i & 1, abort_flag))) break;
@@ -410,6 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kv_chunk<BF16, false, D>(t, 2 * g, s0, dp0, ls, dl, p.c, key, q0, N, p.causal);
                 kv_chunk<BF16, false, D>(t, 2 * g + 1, s1, dp1, ls, dl, p.c, key, q0, N, p.causal);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kRowsEmpty + rb));
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -449,7 +397,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
-            if constexpr (L::kOInStage) prefetch_tmap(&tm_o);
             mbar_arrive_expect_tx(bar(L::kKV), 2 * kTile);
             tma_tile<D>(base + L::kOffK, &tm_k, k0, bh, bar(L::kKV));
             tma_tile<D>(base + L::kOffV, &tm_v, k0, bh, bar(L::kKV));
@@ -463,7 +410,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(bar(L::kQFull + st), L::kStageBytes);
                 tma_tile<D>(stage, &tm_q, q0, bh, bar(L::kQFull + st));
                 tma_tile<D>(stage + kTile, &tm_do, q0, bh, bar(L::kQFull + st));
-                if constexpr (L::kOInStage) tma_tile<D>(stage + 2 * kTile, &tm_o, q0, bh, bar(L::kQFull + st));
                 issued = i + 1;
             }
             if (!ok) raise_abort(abort_flag);
@@ -510,6 +456,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) raise_abort(abort_flag);
             umma_commit(bar(L::kDrain));
             mbar_wait(bar(L::kDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+        } else if (warp > kMmaWarp) {
+            // ================= warps 10-11: each query block's lse and delta =================
+            // into the row buffer the elementwise warps released two blocks ago, so the global
+            // loads run a block ahead of their use.
+            const int lt = static_cast<int>(threadIdx.x) - 32 * (kMmaWarp + 1);  // 0 .. 63
+            bool ok = true;
+            for (int i = 0; i < nq; ++i) {
+                const int rb = i & 1, q0 = (qb0 + i) * kBlk;
+                if (!(ok = warp_wait(bar(L::kRowsEmpty + rb), ((i >> 1) & 1) ^ 1, abort_flag))) break;
+#pragma unroll
+                for (int u = lt; u < kBlk; u += 64) {
+                    const int q = q0 + u;
+                    float l2 = 0.f, dl = 0.f;
+                    if (q < N) {
+                        const int64_t row = static_cast<int64_t>(bh) * N + q;
+                        l2 = p.lse[row];
+                        dl = *reinterpret_cast<const float*>(p.delta_rows + row * (2 * D));
+                    }
+                    lse_s[rb * kBlk + u] = l2;
+                    delta_s[rb * kBlk + u] = dl;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::kRowsFull + rb));
+            }
+            if (!ok) raise_abort(abort_flag);
         }
     }
 
@@ -627,15 +598,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int query = q0 + r;
         const bool qin = query < N;
         const uint32_t t = tmem + (static_cast<uint32_t>((warp & 3) << 5) << 16);
-        bool ok = warp_wait(bar(qQ), 0, abort_flag);
-        // delta = dO . O for this row (O read from global), and the row's lse.
+        bool ok = true;
+        // This row's delta (from the pre-pass, in the row's own dq bytes, which only this CTA's
+        // epilogue overwrites, after every elementwise warp has passed this point) and lse.
         float delta = 0.f, l2 = 0.f;
-        if (ok && qin) {
-            const uint16_t* orow = reinterpret_cast<const uint16_t*>(p.o) + (static_cast<int64_t>(bh) * N + query) * D;
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                delta += row_dot_global<BF16>(gbase + L::kOffDO + c * kBlockBytes, r, orow + 64 * c);
-            l2 = p.lse[static_cast<int64_t>(bh) * N + query];
+        if (qin) {
+            const int64_t row = static_cast<int64_t>(bh) * N + query;
+            delta = *reinterpret_cast<const float*>(p.delta_rows + row * (2 * D));
+            l2 = p.lse[row];
         }
         for (int j = 0; ok && j < nk; ++j) {
             const int k0 = j * kBlk;
@@ -797,9 +767,9 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t 
 template <bool BF16, int D>
 int launch_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                 void* dq, void* dk, void* dv, int64_t BH, int64_t N, bool causal, cudaStream_t stream) {
-    CUtensorMap mq, mk, mv, mo, mdo;
+    CUtensorMap mq, mk, mv, mdo;
     if (!make_map(&mq, q, BH, N, D, BF16) || !make_map(&mk, k, BH, N, D, BF16) || !make_map(&mv, v, BH, N, D, BF16) ||
-        !make_map(&mo, o, BH, N, D, BF16) || !make_map(&mdo, dout, BH, N, D, BF16))
+        !make_map(&mdo, dout, BH, N, D, BF16))
         return ATTN_ERR_DEVICE;
     if (cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<BF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              KvLay<D>::kSmem) != cudaSuccess ||
@@ -807,7 +777,7 @@ int launch_impl(const void* q, const void* k, const void* v, const void* o, cons
                              QLay<D>::kSmem) != cudaSuccess)
         return ATTN_ERR_LAUNCH;
     BwdParams prm;
-    prm.o = o;
+    prm.delta_rows = static_cast<const uint8_t*>(dq);
     prm.lse = lse;
     prm.N = static_cast<int>(N);
     prm.BH = static_cast<int>(BH);
@@ -817,10 +787,17 @@ int launch_impl(const void* q, const void* k, const void* v, const void* o, cons
     prm.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
     const int64_t blocks = static_cast<int64_t>(prm.nblk) * BH;
     if (blocks > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+    // delta of every query row into dq's rows, then dK/dV, then dQ (which overwrites them).
+    const int64_t rows = BH * N;
+    const int64_t pieces = rows * (D / 8);
+    const unsigned dblocks = static_cast<unsigned>(std::min<int64_t>((pieces + 255) / 256, 4096));
+    attn_bwd_delta_kernel<BF16, D><<<dblocks, 256, 0, stream>>>(
+        static_cast<const uint4*>(o), static_cast<const uint4*>(dout), static_cast<uint8_t*>(dq), rows);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     prm.grad0 = dk;
     prm.grad1 = dv;
     attn_bwd_dkdv_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, KvLay<D>::kSmem, stream>>>(
-        mq, mk, mv, mo, mdo, prm);
+        mq, mk, mv, mdo, prm);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     prm.grad0 = dq;
     prm.grad1 = nullptr;
