@@ -536,7 +536,8 @@ def run_ours(args, rank, world, local):
     # Backward pass on the same workload (attn_fwd_lse, then attn_bwd with a seeded output
     # gradient), once, outside the timed region. Algorithmic work: five products against the
     # forward's two (section "Backwards, and training with it"), i.e. 2.5x the forward's flop;
-    # the two tensor-core kernels recompute S and dP, so they execute seven (3.5x).
+    # the two tensor-core kernels (after the delta pre-pass) recompute S and dP, so they
+    # execute seven (3.5x).
     backward = None
     if rank == 0 and not args.no_ablation:
         dout = torch.randn(qd.shape, generator=torch.Generator(device=dev).manual_seed(SEED + 7),
@@ -665,6 +666,19 @@ def run_profile(args):
             raise RuntimeError("device-side timeout")
         print(f"profile: {args.profile_launches} calls of attn_fwd_kvcache on {w['workload']}")
         return
+    if args.profile_kernel == "backward":
+        q, k, v = make_inputs()
+        qd, kd, vd = (torch.from_numpy(x).to("cuda").to(torch.bfloat16) for x in (q, k, v))
+        dout = torch.randn(qd.shape, generator=torch.Generator(device="cuda").manual_seed(SEED + 7),
+                           device="cuda", dtype=torch.float32).to(qd.dtype)
+        ob, lse = fa.attn_fwd_lse(qd, kd, vd, causal=True)
+        for _ in range(args.profile_launches):
+            fa.attn_bwd(qd, kd, vd, ob, dout, lse, causal=True)
+        torch.cuda.synchronize()
+        if fa.attn_device_status(clear=True) != 0:
+            raise RuntimeError("device-side timeout")
+        print(f"profile: {args.profile_launches} calls of attn_bwd on {WORKLOAD['workload']}")
+        return
     if args.profile_kernel == "d128":
         import seeded_inputs as si
 
@@ -702,7 +716,7 @@ def main(argv=None):
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--profile", action="store_true", help="only launch the timed kernel (for ncu)")
     ap.add_argument("--profile-launches", type=int, default=4)
-    ap.add_argument("--profile-kernel", choices=["forward", "decode", "d128"], default="forward",
+    ap.add_argument("--profile-kernel", choices=["forward", "decode", "d128", "backward"], default="forward",
                     help="which path --profile launches")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -27,13 +27,14 @@
 // so the products overlap it.
 // delta is made once per query row by a small pre-pass (one 16-byte piece of dO and O per
 // lane) and parked in the first four bytes of that row of dq, an output that the dQ kernel
-// overwrites last, so the call allocates nothing; the dK/dV kernel's warps 10-11 copy each
+// overwrites last, so the call allocates nothing; the dK/dV kernel's warp 11 copies each
 // query block's lse and delta into shared memory a block ahead of their use.
 //
 // Roles: warps 0-7 elementwise (thread = TMEM lane; warps w and w + 4 share lanes and split the
-// columns), warp 8 TMA producer, warp 9 MMA issuer and tensor-memory owner, warps 10-11 the
-// dK/dV kernel's lse/delta loader (idle in the dQ kernel). Every mbarrier wait is bounded; on expiry the kernel sets the
-// shared device error word (reported by attn_device_status), drains and returns.
+// columns), warp 8 TMA producer, warp 9 issuer of the S and dP products and tensor-memory
+// owner, warp 10 issuer of the products that take P and dS, warp 11 the dK/dV kernel's lse/delta
+// loader (idle in the dQ kernel). Every mbarrier wait is bounded; on expiry the kernel sets
+// the shared device error word (reported by attn_device_status), drains and returns.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -53,14 +54,16 @@ namespace {
 constexpr int kBlk = 128;                   // queries or keys per block = TMEM lanes
 constexpr int kBlockBytes = kBlk * 64 * 2;  // 16 KiB: 128 rows x 128 bytes (64 values), one TMA box
 // Warps 0-7: elementwise (two warpgroups on the same TMEM lanes, each on half the columns);
-// warpgroup 2: the TMA producer (warp 8), the MMA issuer (warp 9) and two idle warps. Ten warps
-// would already put three on some SM sub-partition and cap every thread at 168 registers; the two
-// idle warps complete warpgroup 2 so that it can hand registers to the elementwise warpgroups
-// (setmaxnreg acts on whole warpgroups): 72 a thread there, 216 in warps 0-7.
+// warpgroup 2: the TMA producer (warp 8), the two MMA issuers (warps 9, 10) and the lse/delta
+// loader (warp 11). A whole warpgroup there also lets registers move: setmaxnreg acts on whole
+// warpgroups, and twelve warps at launch get 168 a thread, so warpgroup 2 gives up to 72 and
+// warps 0-7 take 216.
 constexpr int kThreads = 384;
 constexpr int kElemWarps = 8;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;    // S and dP products; tensor-memory owner
+constexpr int kMma2Warp = 10;  // the products that take P and dS (dV and dK, or dQ)
+constexpr int kLoaderWarp = 11;
 constexpr int kRegsLaunch = 168;  // 65536 / 384, rounded down to the allocation granule of 8
 constexpr int kRegsElem = 216;
 constexpr int kRegsOther = 72;
@@ -192,7 +195,7 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const void* map, int row,
 
 // ================================ dK, dV: one CTA per key block ================================
 // Shared memory: K, V tiles, then a ring of (Q, dO) stages (four at d = 64, two at d = 128),
-// then per-block lse and delta (double-buffered by block parity, filled by warps 10-11 from lse
+// then per-block lse and delta (double-buffered by block parity, filled by warp 11 from lse
 // and from the delta pre-pass), then mbarriers.
 // Tensor memory: S^T 0, dP^T 128; d = 64: P^T 256, dS^T 320, dV 384, dK 448; d = 128 (dV and dK
 // take 128 columns each): dV 256, dK 384, and P^T and dS^T are written over the S^T and dP^T
@@ -216,7 +219,7 @@ struct KvLay {
     static constexpr int kKV = 0, kQFull = 1, kQEmpty = kQFull + kStages, kSFull = kQEmpty + kStages,
                          kDPFull = kSFull + 1, kSdPFree = kSFull + 2, kPdSFull = kSFull + 3, kDone = kSFull + 4,
                          kDrain = kSFull + 5, kRowsFull = kSFull + 6, kRowsEmpty = kRowsFull + 2,
-                         kNumBars = kRowsEmpty + 2;
+                         kDrain2 = kRowsEmpty + 2, kNumBars = kDrain2 + 1;
     static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
     static constexpr int kOffAbort = kOffSlot + 4;
     static constexpr int kSmem = kOffAbort + 4 + 1024;
@@ -232,33 +235,36 @@ struct KvLay {
 
 // One 32-query chunk of the dK/dV kernel's elementwise step for this thread's key: P^T and
 // dS^T = P^T (dP^T - delta) from S^T and dP^T in TMEM, stored back as 16-bit pairs. The
-// queries' lse and delta come from shared memory four at a time.
+// queries' lse and delta come from shared memory, negated, four at a time; the arithmetic runs
+// on query pairs with the f32x2 forms (each lane rounds as the scalar operation would).
 template <bool BF16, bool kMasked, int D>
 __device__ __forceinline__ void kv_chunk(uint32_t t, int ch, const uint32_t (&s)[32], const uint32_t (&dp)[32],
-                                         const float* ls, const float* dl, float c, int key, int q0, int N,
+                                         const float* nls, const float* ndl, float c, int key, int q0, int N,
                                          int causal) {
     using L = KvLay<D>;
     uint32_t pp[16], ds[16];
+    const float2 c2 = make_float2(c, c);
 #pragma unroll
     for (int u4 = 0; u4 < 8; ++u4) {
-        const float4 lv = *reinterpret_cast<const float4*>(ls + ch * 32 + 4 * u4);
-        const float4 dv4 = *reinterpret_cast<const float4*>(dl + ch * 32 + 4 * u4);
-        const float lq[4] = {lv.x, lv.y, lv.z, lv.w}, dq[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
-        float pv[4], dv[4];
+        const float4 lv = *reinterpret_cast<const float4*>(nls + ch * 32 + 4 * u4);
+        const float4 dv4 = *reinterpret_cast<const float4*>(ndl + ch * 32 + 4 * u4);
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            float pr = ex2_approx(fmaf(__uint_as_float(s[4 * u4 + h]), c, -lq[h]));
+        for (int h = 0; h < 2; ++h) {
+            const int e = 4 * u4 + 2 * h;
+            const float2 x = ffma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), c2,
+                                   h == 0 ? make_float2(lv.x, lv.y) : make_float2(lv.z, lv.w));
+            float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
             if constexpr (kMasked) {
-                const int query = q0 + ch * 32 + 4 * u4 + h;
-                if (!(query < N && key < N && (!causal || key <= query))) pr = 0.f;
+                const int query = q0 + ch * 32 + e;
+                if (!(query < N && key < N && (!causal || key <= query))) pr.x = 0.f;
+                if (!(query + 1 < N && key < N && (!causal || key <= query + 1))) pr.y = 0.f;
             }
-            pv[h] = pr;
-            dv[h] = pr * (__uint_as_float(dp[4 * u4 + h]) - dq[h]);
+            const float2 dd = fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                    h == 0 ? make_float2(dv4.x, dv4.y) : make_float2(dv4.z, dv4.w));
+            const float2 dsv = fmul2(pr, dd);
+            pp[2 * u4 + h] = pack2<BF16>(pr.x, pr.y);
+            ds[2 * u4 + h] = pack2<BF16>(dsv.x, dsv.y);
         }
-        pp[2 * u4] = pack2<BF16>(pv[0], pv[1]);
-        pp[2 * u4 + 1] = pack2<BF16>(pv[2], pv[3]);
-        ds[2 * u4] = pack2<BF16>(dv[0], dv[1]);
-        ds[2 * u4 + 1] = pack2<BF16>(dv[2], dv[3]);
     }
     tmem_st_x16(t + L::kColP + L::chunk_col(ch), pp);
     tmem_st_x16(t + L::kColDS + L::chunk_col(ch), ds);
@@ -278,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return base + L::kOffBar + 8u * static_cast<uint32_t>(i); };
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kOffSlot);
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + L::kOffAbort);
-    float* const lse_s = reinterpret_cast<float*>(gbase + L::kOffRow);  // [2][128]
-    float* const delta_s = lse_s + 2 * kBlk;                              // [2][128]
+    float* const lse_s = reinterpret_cast<float*>(gbase + L::kOffRow);  // [2][128], negated
+    float* const delta_s = lse_s + 2 * kBlk;                              // [2][128], negated
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = p.N;
@@ -301,8 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(L::kPdSFull), kElemWarps);
         mbar_init(bar(L::kDone), 1);
         mbar_init(bar(L::kDrain), 1);
+        mbar_init(bar(L::kDrain2), 1);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(L::kRowsFull + b), 2);
+            mbar_init(bar(L::kRowsFull + b), 1);
             mbar_init(bar(L::kRowsEmpty + b), kElemWarps);
         }
         *abort_flag = 0;
@@ -418,10 +425,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = (issued > L::kStages ? issued - L::kStages : 0); i < issued; ++i)
                 mbar_wait(bar(L::kQFull + i % L::kStages), (i / L::kStages) & 1, nullptr, kDrainTimeoutNs);
         } else if (warp == kMmaWarp && lane == 0) {
-            // ================================ MMA issuer ================================
-            // S^T(0), dP^T(0); then per block i: S^T(i+1), dP^T(i+1) once block i's were copied out
-            // (d = 128: once block i's dV, dK products are done, as P^T and dS^T sit over S^T and
-            // dP^T), and dV, dK += block i's P^T dO, dS^T Q once P^T and dS^T are in TMEM.
+            // ============================ MMA issuer: S^T, dP^T ============================
+            // S^T(0), dP^T(0); then block i+1's once block i's were copied out (d = 128: once
+            // block i's dV, dK products are done, as P^T and dS^T sit over S^T and dP^T). The
+            // products that take P^T and dS^T come from another warp: a thread's barrier waits
+            // queue behind the tensor-core instructions it issued before, so one issuer would
+            // let the pipe drain at every hand-off.
             bool ok = mbar_wait(bar(L::kKV), 0, abort_flag, kWaitTimeoutNs);
             auto issue_sdp = [&](int i) {
                 const uint32_t stage = base + L::kOffStage + (i % L::kStages) * L::kStageBytes;
@@ -435,11 +444,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             if (ok && nq > 0) ok = issue_sdp(0);
+            for (int i = 0; ok && i + 1 < nq; ++i) {
+                if (!(ok = mbar_wait(bar(L::kAlias ? L::kDone : L::kSdPFree), i & 1, abort_flag, kWaitTimeoutNs)))
+                    break;
+                tc_fence_after();
+                if (!(ok = issue_sdp(i + 1))) break;
+            }
+            if (!ok) raise_abort(abort_flag);
+            umma_commit(bar(L::kDrain));
+            mbar_wait(bar(L::kDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+        } else if (warp == kMma2Warp && lane == 0) {
+            // ============================ MMA issuer: dV, dK ============================
+            // dV, dK += block i's P^T dO, dS^T Q once P^T and dS^T are in TMEM (block i's
+            // S^T, dP^T products are then done, so the stage's tiles have landed).
+            bool ok = true;
             for (int i = 0; ok && i < nq; ++i) {
-                if (!L::kAlias && i + 1 < nq) {
-                    if (!(ok = mbar_wait(bar(L::kSdPFree), i & 1, abort_flag, kWaitTimeoutNs))) break;
-                    if (!(ok = issue_sdp(i + 1))) break;
-                }
                 if (!(ok = mbar_wait(bar(L::kPdSFull), i & 1, abort_flag, kWaitTimeoutNs))) break;
                 tc_fence_after();
                 const uint32_t stage = base + L::kOffStage + (i % L::kStages) * L::kStageBytes;
@@ -447,26 +466,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_ts_128xD<BF16, D>(tmem + L::kColDK, tmem + L::kColDS, stage, i > 0, L::kAlias);          // dK += dS^T Q
                 umma_commit(bar(L::kDone));
                 umma_commit(bar(L::kQEmpty + i % L::kStages));
-                if (L::kAlias && i + 1 < nq) {
-                    if (!(ok = mbar_wait(bar(L::kDone), i & 1, abort_flag, kWaitTimeoutNs))) break;
-                    tc_fence_after();
-                    if (!(ok = issue_sdp(i + 1))) break;
-                }
             }
             if (!ok) raise_abort(abort_flag);
-            umma_commit(bar(L::kDrain));
-            mbar_wait(bar(L::kDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
-        } else if (warp > kMmaWarp) {
-            // ================= warps 10-11: each query block's lse and delta =================
+            umma_commit(bar(L::kDrain2));
+            mbar_wait(bar(L::kDrain2), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+        } else if (warp == kLoaderWarp) {
+            // ==================== warp 11: each query block's lse and delta ====================
             // into the row buffer the elementwise warps released two blocks ago, so the global
             // loads run a block ahead of their use.
-            const int lt = static_cast<int>(threadIdx.x) - 32 * (kMmaWarp + 1);  // 0 .. 63
             bool ok = true;
             for (int i = 0; i < nq; ++i) {
                 const int rb = i & 1, q0 = (qb0 + i) * kBlk;
                 if (!(ok = warp_wait(bar(L::kRowsEmpty + rb), ((i >> 1) & 1) ^ 1, abort_flag))) break;
 #pragma unroll
-                for (int u = lt; u < kBlk; u += 64) {
+                for (int u = lane; u < kBlk; u += 32) {
                     const int q = q0 + u;
                     float l2 = 0.f, dl = 0.f;
                     if (q < N) {
@@ -474,8 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         l2 = p.lse[row];
                         dl = *reinterpret_cast<const float*>(p.delta_rows + row * (2 * D));
                     }
-                    lse_s[rb * kBlk + u] = l2;
-                    delta_s[rb * kBlk + u] = dl;
+                    lse_s[rb * kBlk + u] = -l2;
+                    delta_s[rb * kBlk + u] = -dl;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(L::kRowsFull + rb));
@@ -510,7 +523,7 @@ struct QLay {
     static constexpr int kKVEmpty = qKVFull + kStages;
     static constexpr int kSFull = kKVEmpty + kStages;
     static constexpr int kDPFull = kSFull + 1, kSdPFree = kSFull + 2, kDSFull = kSFull + 3, kDone = kSFull + 4,
-                         kDrain = kSFull + 5, kNumBars = kSFull + 6;
+                         kDrain = kSFull + 5, kDrain2 = kSFull + 6, kNumBars = kSFull + 7;
     static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
     static constexpr int kOffAbort = kOffSlot + 4;
     static constexpr int kSmem = kOffAbort + 4 + 1024;
@@ -525,19 +538,19 @@ __device__ __forceinline__ void q_chunk(uint32_t t, int ch, const uint32_t (&s)[
                                         float delta, float c, int query, int k0, int N, int causal) {
     using L = QLay<D>;
     uint32_t ds[16];
+    const float2 c2 = make_float2(c, c), nl2 = make_float2(-l2, -l2), nd2 = make_float2(-delta, -delta);
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
-        float dv[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float pr = ex2_approx(fmaf(__uint_as_float(s[2 * u + h]), c, -l2));
-            if constexpr (kMasked) {
-                const int key = k0 + ch * 32 + 2 * u + h;
-                if (!(query < N && key < N && (!causal || key <= query))) pr = 0.f;
-            }
-            dv[h] = pr * (__uint_as_float(dp[2 * u + h]) - delta);
+        const float2 x = ffma2(make_float2(__uint_as_float(s[2 * u]), __uint_as_float(s[2 * u + 1])), c2, nl2);
+        float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if constexpr (kMasked) {
+            const int key = k0 + ch * 32 + 2 * u;
+            if (!(query < N && key < N && (!causal || key <= query))) pr.x = 0.f;
+            if (!(query < N && key + 1 < N && (!causal || key + 1 <= query))) pr.y = 0.f;
         }
-        ds[u] = pack2<BF16>(dv[0], dv[1]);
+        const float2 dsv =
+            fmul2(pr, fadd2(make_float2(__uint_as_float(dp[2 * u]), __uint_as_float(dp[2 * u + 1])), nd2));
+        ds[u] = pack2<BF16>(dsv.x, dsv.y);
     }
     tmem_st_x16(t + L::kColDS + 16 * ch, ds);
 }
@@ -578,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(L::kDSFull), kElemWarps);
         mbar_init(bar(L::kDone), 1);
         mbar_init(bar(L::kDrain), 1);
+        mbar_init(bar(L::kDrain2), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -689,7 +703,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
                 mbar_wait(bar(qKVFull + j % S), (j / S) & 1, nullptr, kDrainTimeoutNs);
         } else if (warp == kMmaWarp && lane == 0) {
-            // ================================ MMA issuer ================================
+            // ============================= MMA issuer: S, dP =============================
+            // S(0), dP(0); then key block j+1's once block j's were copied out. dQ comes from
+            // another warp (see the dK/dV kernel).
             bool ok = mbar_wait(bar(qQ), 0, abort_flag, kWaitTimeoutNs);
             auto issue_sdp = [&](int j) {
                 const int st = j % S;
@@ -703,11 +719,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             if (ok && nk > 0) ok = issue_sdp(0);
+            for (int j = 0; ok && j + 1 < nk; ++j) {
+                if (!(ok = mbar_wait(bar(L::kSdPFree), j & 1, abort_flag, kWaitTimeoutNs))) break;
+                tc_fence_after();
+                if (!(ok = issue_sdp(j + 1))) break;
+            }
+            if (!ok) raise_abort(abort_flag);
+            umma_commit(bar(L::kDrain));
+            mbar_wait(bar(L::kDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+        } else if (warp == kMma2Warp && lane == 0) {
+            // ============================== MMA issuer: dQ ==============================
+            // dQ += dS K once block j's dS is in TMEM (its S, dP products are then done).
+            bool ok = true;
             for (int j = 0; ok && j < nk; ++j) {
-                if (j + 1 < nk) {
-                    if (!(ok = mbar_wait(bar(L::kSdPFree), j & 1, abort_flag, kWaitTimeoutNs))) break;
-                    if (!(ok = issue_sdp(j + 1))) break;
-                }
                 if (!(ok = mbar_wait(bar(L::kDSFull), j & 1, abort_flag, kWaitTimeoutNs))) break;
                 tc_fence_after();
                 const uint32_t stage = base + L::kOffKV + (j % S) * L::kStageBytes;
@@ -716,8 +740,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(bar(L::kKVEmpty + j % S));
             }
             if (!ok) raise_abort(abort_flag);
-            umma_commit(bar(L::kDrain));
-            mbar_wait(bar(L::kDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+            umma_commit(bar(L::kDrain2));
+            mbar_wait(bar(L::kDrain2), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         }
     }
 
