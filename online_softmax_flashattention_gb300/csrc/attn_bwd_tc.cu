@@ -131,7 +131,9 @@ __device__ __forceinline__ float2 unpack2(uint32_t u) {
 // delta_n = sum_e dO[n,e] O[n,e] (fp32) for every query row n of all heads, stored as the first
 // four bytes of dq's row n: dq is an output the call may use as scratch, and the dQ kernel
 // reads each row's delta in the CTA that later overwrites that row. D/8 lanes share a row, one
-// 16-byte piece of dO and of O each; a warp covers 32 / (D/8) whole rows per step.
+// 16-byte piece of dO and of O each; a warp takes kDeltaUnroll groups of 32 pieces (whole
+// rows) per step, all loads issued before the arithmetic.
+constexpr int kDeltaUnroll = 4;
 template <bool BF16, int D>
 __global__ void __launch_bounds__(256)
     attn_bwd_delta_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout, uint8_t* __restrict__ dq,
@@ -139,24 +141,31 @@ __global__ void __launch_bounds__(256)
     constexpr int kLanes = D / 8;
     const int64_t total = rows * kLanes;
     const int lane = static_cast<int>(threadIdx.x & 31);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t g0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31u); g0 < total;
-         g0 += stride) {
-        const int64_t gi = g0 + lane;  // 16-byte piece gi % kLanes of row gi / kLanes
-        float acc = 0.f;
-        if (gi < total) {
-            const uint4 x = o[gi], y = dout[gi];
-            const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+    const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t g0 = warp_id * 32 * kDeltaUnroll; g0 < total; g0 += nwarps * 32 * kDeltaUnroll) {
+        uint4 x[kDeltaUnroll], y[kDeltaUnroll];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 u = unpack2<BF16>(xs[i]), v = unpack2<BF16>(ys[i]);
-                acc = fmaf(u.x, v.x, acc);
-                acc = fmaf(u.y, v.y, acc);
-            }
+        for (int u = 0; u < kDeltaUnroll; ++u) {
+            const int64_t gi = g0 + 32 * u + lane;  // 16-byte piece gi % kLanes of row gi / kLanes
+            x[u] = gi < total ? o[gi] : make_uint4(0, 0, 0, 0);
+            y[u] = gi < total ? dout[gi] : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (gi < total && gi % kLanes == 0) *reinterpret_cast<float*>(dq + (gi / kLanes) * (2 * D)) = acc;
+        for (int u = 0; u < kDeltaUnroll; ++u) {
+            const int64_t gi = g0 + 32 * u + lane;
+            const uint32_t xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w}, ys[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 a = unpack2<BF16>(xs[i]), b = unpack2<BF16>(ys[i]);
+                acc = fmaf(a.x, b.x, acc);
+                acc = fmaf(a.y, b.y, acc);
+            }
+#pragma unroll
+            for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (gi < total && gi % kLanes == 0) *reinterpret_cast<float*>(dq + (gi / kLanes) * (2 * D)) = acc;
+        }
     }
 }
 
@@ -814,7 +823,8 @@ int launch_impl(const void* q, const void* k, const void* v, const void* o, cons
     // delta of every query row into dq's rows, then dK/dV, then dQ (which overwrites them).
     const int64_t rows = BH * N;
     const int64_t pieces = rows * (D / 8);
-    const unsigned dblocks = static_cast<unsigned>(std::min<int64_t>((pieces + 255) / 256, 4096));
+    const unsigned dblocks =
+        static_cast<unsigned>(std::min<int64_t>((pieces + 256 * kDeltaUnroll - 1) / (256 * kDeltaUnroll), 2048));
     attn_bwd_delta_kernel<BF16, D><<<dblocks, 256, 0, stream>>>(
         static_cast<const uint4*>(o), static_cast<const uint4*>(dout), static_cast<uint8_t*>(dq), rows);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
