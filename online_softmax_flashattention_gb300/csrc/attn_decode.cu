@@ -358,12 +358,14 @@ __global__ void __launch_bounds__(Cfg<T, D>::kThreads)
             const int r = 32 * warp + lane;
             const int j = t * kRows + r;
             // ---- scores of key j against the group's queries ----
-            constexpr int NA = QG >= 4 ? 1 : 4 / QG;  // independent partial sums per query
-            float sa[QG][NA];
+            // Pairs of dims on the f32x2 FMA, q read four dims at a time; NA2 pairs of
+            // independent partial sums per query.
+            constexpr int NA2 = QG == 1 ? 2 : 1;
+            float2 sa[QG][NA2];
 #pragma unroll
             for (int i = 0; i < QG; ++i)
 #pragma unroll
-                for (int a = 0; a < NA; ++a) sa[i][a] = 0.f;
+                for (int a = 0; a < NA2; ++a) sa[i][a] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int h = 0; h < C::kBoxes; ++h) {
 #pragma unroll
@@ -374,10 +376,11 @@ __global__ void __launch_bounds__(Cfg<T, D>::kThreads)
 #pragma unroll
                     for (int i = 0; i < QG; ++i) {
 #pragma unroll
-                        for (int u = 0; u < C::kChunkElems; u += 2) {
-                            const float2 qv = *reinterpret_cast<const float2*>(qs + i * D + e + u);
-                            sa[i][u % NA] = fmaf(qv.x, kf[u], sa[i][u % NA]);
-                            sa[i][(u + 1) % NA] = fmaf(qv.y, kf[u + 1], sa[i][(u + 1) % NA]);
+                        for (int u = 0; u < C::kChunkElems; u += 4) {
+                            const float4 qv = *reinterpret_cast<const float4*>(qs + i * D + e + u);
+                            float2& a0 = sa[i][(u / 4) % NA2];
+                            a0 = ffma2(make_float2(qv.x, qv.y), make_float2(kf[u], kf[u + 1]), a0);
+                            a0 = ffma2(make_float2(qv.z, qv.w), make_float2(kf[u + 2], kf[u + 3]), a0);
                         }
                     }
                 }
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(Cfg<T, D>::kThreads)
             for (int i = 0; i < QG; ++i) {
                 float sc = 0.f;
 #pragma unroll
-                for (int a = 0; a < NA; ++a) sc += sa[i][a];
+                for (int a = 0; a < NA2; ++a) sc += sa[i][a].x + sa[i][a].y;
                 const bool vis = j < pc.ke && i < pc.ng && (!p.causal || j <= qpos0 + i);
                 sc = vis ? sc : -INFINITY;
                 float mx = sc;
@@ -399,7 +402,11 @@ __global__ void __launch_bounds__(Cfg<T, D>::kThreads)
                 const float pr = ex2f(sc - m_use);
                 l[i] = fmaf(l[i], alpha, pr);  // this lane's share of the row total
 #pragma unroll
-                for (int h = 0; h < DL; ++h) acc[i][h] *= alpha;
+                for (int h = 0; h < DL; h += 2) {
+                    const float2 v = fmul2(make_float2(acc[i][h], acc[i][h + 1]), make_float2(alpha, alpha));
+                    acc[i][h] = v.x;
+                    acc[i][h + 1] = v.y;
+                }
                 m[i] = m_new;
                 ps[i * 32 + lane] = pr;
             }
@@ -421,7 +428,12 @@ __global__ void __launch_bounds__(Cfg<T, D>::kThreads)
                     for (int i = 0; i < QG; ++i) {
                         const float w = u == 0 ? pp[i].x : u == 1 ? pp[i].y : u == 2 ? pp[i].z : pp[i].w;
 #pragma unroll
-                        for (int h = 0; h < DL; ++h) acc[i][h] = fmaf(w, vv[h], acc[i][h]);
+                        for (int h = 0; h < DL; h += 2) {
+                            const float2 v = ffma2(make_float2(w, w), make_float2(vv[h], vv[h + 1]),
+                                                   make_float2(acc[i][h], acc[i][h + 1]));
+                            acc[i][h] = v.x;
+                            acc[i][h + 1] = v.y;
+                        }
                     }
                 }
             }
