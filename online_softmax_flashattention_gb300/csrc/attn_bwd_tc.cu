@@ -243,15 +243,13 @@ struct KvLay {
 };
 
 // One 32-query chunk of the dK/dV kernel's elementwise step for this thread's key: P^T and
-// dS^T = P^T (dP^T - delta) from S^T and dP^T in TMEM, stored back as 16-bit pairs. The
+// dS^T = P^T (dP^T - delta) from this thread's row of S^T and dP^T, as 16-bit pairs. The
 // queries' lse and delta come from shared memory, negated, four at a time; the arithmetic runs
 // on query pairs with the f32x2 forms (each lane rounds as the scalar operation would).
-template <bool BF16, bool kMasked, int D>
-__device__ __forceinline__ void kv_chunk(uint32_t t, int ch, const uint32_t (&s)[32], const uint32_t (&dp)[32],
-                                         const float* nls, const float* ndl, float c, int key, int q0, int N,
-                                         int causal) {
-    using L = KvLay<D>;
-    uint32_t pp[16], ds[16];
+template <bool BF16, bool kMasked>
+__device__ __forceinline__ void kv_chunk(int ch, const uint32_t (&s)[32], const uint32_t (&dp)[32], const float* nls,
+                                         const float* ndl, float c, int key, int q0, int N, int causal,
+                                         uint32_t (&pp)[16], uint32_t (&ds)[16]) {
     const float2 c2 = make_float2(c, c);
 #pragma unroll
     for (int u4 = 0; u4 < 8; ++u4) {
@@ -275,8 +273,6 @@ __device__ __forceinline__ void kv_chunk(uint32_t t, int ch, const uint32_t (&s)
             ds[2 * u4 + h] = pack2<BF16>(dsv.x, dsv.y);
         }
     }
-    tmem_st_x16(t + L::kColP + L::chunk_col(ch), pp);
-    tmem_st_x16(t + L::kColDS + L::chunk_col(ch), ds);
 }
 
 template <bool BF16, int D>
@@ -360,20 +356,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kSdPFree));
-            // The previous block's dV/dK products read P^T and dS^T: wait before overwriting.
-            if (i > 0 && !(ok = warp_wait(bar(L::kDone), (i - 1) & 1, abort_flag))) break;
-            tc_fence_after();
             // Only the causal diagonal block and ragged edges need a mask.
             const bool masked = (p.causal && qb0 + i == kblk) || q0 + kBlk > N || k0 + kBlk > N;
+            uint32_t pp0[16], ds0[16], pp1[16], ds1[16];
             if (masked) {
-                kv_chunk<BF16, true, D>(t, 2 * g, s0, dp0, ls, dl, p.c, key, q0, N, p.causal);
-                kv_chunk<BF16, true, D>(t, 2 * g + 1, s1, dp1, ls, dl, p.c, key, q0, N, p.causal);
+                kv_chunk<BF16, true>(2 * g, s0, dp0, ls, dl, p.c, key, q0, N, p.causal, pp0, ds0);
+                kv_chunk<BF16, true>(2 * g + 1, s1, dp1, ls, dl, p.c, key, q0, N, p.causal, pp1, ds1);
             } else {
-                kv_chunk<BF16, false, D>(t, 2 * g, s0, dp0, ls, dl, p.c, key, q0, N, p.causal);
-                kv_chunk<BF16, false, D>(t, 2 * g + 1, s1, dp1, ls, dl, p.c, key, q0, N, p.causal);
+                kv_chunk<BF16, false>(2 * g, s0, dp0, ls, dl, p.c, key, q0, N, p.causal, pp0, ds0);
+                kv_chunk<BF16, false>(2 * g + 1, s1, dp1, ls, dl, p.c, key, q0, N, p.causal, pp1, ds1);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kRowsEmpty + rb));
+            // The previous block's dV/dK products read P^T and dS^T: wait only now, before
+            // overwriting them, so that those products run under the arithmetic above.
+            if (i > 0 && !(ok = warp_wait(bar(L::kDone), (i - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            tmem_st_x16(t + L::kColP + L::chunk_col(2 * g), pp0);
+            tmem_st_x16(t + L::kColDS + L::chunk_col(2 * g), ds0);
+            tmem_st_x16(t + L::kColP + L::chunk_col(2 * g + 1), pp1);
+            tmem_st_x16(t + L::kColDS + L::chunk_col(2 * g + 1), ds1);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -541,12 +543,10 @@ struct QLay {
 };
 
 // One 32-key chunk of the dQ kernel's elementwise step for this thread's query: dS = P (dP -
-// delta) from S and dP in TMEM, stored back as 16-bit pairs.
-template <bool BF16, bool kMasked, int D>
-__device__ __forceinline__ void q_chunk(uint32_t t, int ch, const uint32_t (&s)[32], const uint32_t (&dp)[32], float l2,
-                                        float delta, float c, int query, int k0, int N, int causal) {
-    using L = QLay<D>;
-    uint32_t ds[16];
+// delta) from this thread's row of S and dP, as 16-bit pairs.
+template <bool BF16, bool kMasked>
+__device__ __forceinline__ void q_chunk(int ch, const uint32_t (&s)[32], const uint32_t (&dp)[32], float l2, float delta,
+                                        float c, int query, int k0, int N, int causal, uint32_t (&ds)[16]) {
     const float2 c2 = make_float2(c, c), nl2 = make_float2(-l2, -l2), nd2 = make_float2(-delta, -delta);
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
@@ -561,7 +561,6 @@ __device__ __forceinline__ void q_chunk(uint32_t t, int ch, const uint32_t (&s)[
             fmul2(pr, fadd2(make_float2(__uint_as_float(dp[2 * u]), __uint_as_float(dp[2 * u + 1])), nd2));
         ds[u] = pack2<BF16>(dsv.x, dsv.y);
     }
-    tmem_st_x16(t + L::kColDS + 16 * ch, ds);
 }
 
 template <bool BF16, int D>
@@ -646,17 +645,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kSdPFree));
-            // The previous block's dQ product reads dS: wait before overwriting it.
+            const bool masked = (p.causal && j == qblk) || q0 + kBlk > N || k0 + kBlk > N;
+            uint32_t ds0[16], ds1[16];
+            if (masked) {
+                q_chunk<BF16, true>(2 * g, s0, dp0, l2, delta, p.c, query, k0, N, p.causal, ds0);
+                q_chunk<BF16, true>(2 * g + 1, s1, dp1, l2, delta, p.c, query, k0, N, p.causal, ds1);
+            } else {
+                q_chunk<BF16, false>(2 * g, s0, dp0, l2, delta, p.c, query, k0, N, p.causal, ds0);
+                q_chunk<BF16, false>(2 * g + 1, s1, dp1, l2, delta, p.c, query, k0, N, p.causal, ds1);
+            }
+            // The previous block's dQ product reads dS: wait only now, before overwriting it.
             if (j > 0 && !(ok = warp_wait(bar(L::kDone), (j - 1) & 1, abort_flag))) break;
             tc_fence_after();
-            const bool masked = (p.causal && j == qblk) || q0 + kBlk > N || k0 + kBlk > N;
-            if (masked) {
-                q_chunk<BF16, true, D>(t, 2 * g, s0, dp0, l2, delta, p.c, query, k0, N, p.causal);
-                q_chunk<BF16, true, D>(t, 2 * g + 1, s1, dp1, l2, delta, p.c, query, k0, N, p.causal);
-            } else {
-                q_chunk<BF16, false, D>(t, 2 * g, s0, dp0, l2, delta, p.c, query, k0, N, p.causal);
-                q_chunk<BF16, false, D>(t, 2 * g + 1, s1, dp1, l2, delta, p.c, query, k0, N, p.causal);
-            }
+            tmem_st_x16(t + L::kColDS + 32 * g, ds0);
+            tmem_st_x16(t + L::kColDS + 32 * g + 16, ds1);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
