@@ -13,16 +13,17 @@
 // GB300 mapping. Every product is a tcgen05.mma (bf16/fp16 operands, fp32 accumulate) with
 // the forward kernel's two shapes: SS (both operands K-major tiles as TMA writes them, 128-byte
 // swizzle) and TS (A from tensor memory, B an MN-major tile).
-//   dK/dV kernel, per query block, with the keys in the 128 TMEM lanes:
-//     S^T = K Q^T (SS), dP^T = V dO^T (SS)               -> TMEM, 128 columns each
+//   dK/dV kernel, per query block of BQ queries (128 at d = 64, 64 at d = 128), with the keys
+//   in the 128 TMEM lanes:
+//     S^T = K Q^T (SS), dP^T = V dO^T (SS)               -> TMEM, BQ columns each
 //     the eight elementwise warps (thread = key; two warpgroups on the same TMEM lanes, each
 //     on half of the block's query columns) make P^T and dS^T = P^T (dP^T - delta) in
 //     registers and store them to TMEM as 16-bit pairs
 //     dV += P^T dO (TS, B = dO tile MN-major), dK += dS^T Q (TS, B = Q tile MN-major)
 //   dQ kernel, per key block, with the queries in the lanes:
 //     S = Q K^T (SS), dP = dO V^T (SS); dS = P (dP - delta) -> TMEM; dQ += dS K (TS, B = K)
-// Tensor memory (512 columns): dK/dV kernel S^T 0, dP^T 128, P^T 256, dS^T 320, dV 384, dK 448;
-// dQ kernel S 0, dP 128, dS 256, dQ 320. The next block's S and dP products go out as soon as
+// Tensor memory (512 columns): dK/dV kernel S^T 0, dP^T BQ, P^T 2 BQ, dS^T 2.5 BQ, dV 3 BQ,
+// dK 3 BQ + d (512 columns at d = 64, 448 at d = 128); dQ kernel S 0, dP 128, dS 256, dQ 320. The next block's S and dP products go out as soon as
 // the elementwise warps have loaded the current ones into registers, before their arithmetic,
 // so the products overlap it.
 // delta is made once per query row by a small pre-pass (one 16-byte piece of dO and O per
@@ -169,59 +170,64 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// 128 x 128 product over K = D of two K-major tiles (each D/64 column blocks of 128-byte rows)
-// into TMEM columns `d`: D/16 steps of K = 16, the ones past 64 in the second column block.
-template <bool BF16, int D>
-__device__ __forceinline__ void mma_ss_128x128(uint32_t d, uint32_t sA, uint32_t sB) {
-    constexpr uint32_t kIdesc = idesc_f16(BF16, kBlk, kBlk, false, false);
+// 128 x NB product over K = D of two K-major tiles (D/64 column blocks of 128-byte rows each,
+// kABlk and kBBlk bytes apart in A and B) into TMEM columns `d`: D/16 steps of K = 16, the ones
+// past 64 in the second column block.
+template <bool BF16, int D, int NB, int kABlk, int kBBlk>
+__device__ __forceinline__ void mma_ss_kmajor(uint32_t d, uint32_t sA, uint32_t sB) {
+    constexpr uint32_t kIdesc = idesc_f16(BF16, kBlk, NB, false, false);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = static_cast<uint32_t>((kk >> 2) * kBlockBytes + 32 * (kk & 3));
-        umma_ss(d, smem_desc_sw128(sA + off, 16, 1024), smem_desc_sw128(sB + off, 16, 1024), kIdesc, kk > 0 ? 1u : 0u);
+        const uint32_t a_off = static_cast<uint32_t>((kk >> 2) * kABlk + 32 * (kk & 3));
+        const uint32_t b_off = static_cast<uint32_t>((kk >> 2) * kBBlk + 32 * (kk & 3));
+        umma_ss(d, smem_desc_sw128(sA + a_off, 16, 1024), smem_desc_sw128(sB + b_off, 16, 1024), kIdesc,
+                kk > 0 ? 1u : 0u);
     }
 }
 
-// 128 x D product over K = 128 with A (128 lanes x 128 16-bit values) in TMEM and B an MN-major
-// tile (rows = K; D/64 column blocks 16 KiB apart, the descriptor's leading byte offset),
-// accumulated into TMEM columns `d`. A's K-step kk sits at column a + 8 kk, or, with `split`,
-// a + 8 kk + 32 for kk >= 4 (the layout the d = 128 dK/dV kernel writes over S^T and dP^T).
-template <bool BF16, int D>
-__device__ __forceinline__ void mma_ts_128xD(uint32_t d, uint32_t a, uint32_t sB, bool accumulate, bool split) {
+// 128 x D product over K = 16 KSTEPS with A (128 lanes, K-step kk at column a + 8 kk) in TMEM
+// and B an MN-major tile (rows = K, 16 rows = 2048 bytes a step; D/64 column blocks kBBlk bytes
+// apart, the descriptor's leading byte offset), accumulated into TMEM columns `d`.
+template <bool BF16, int D, int KSTEPS, int kBBlk>
+__device__ __forceinline__ void mma_ts_mn(uint32_t d, uint32_t a, uint32_t sB, bool accumulate) {
     constexpr uint32_t kIdesc = idesc_f16(BF16, kBlk, D, false, true);
-    constexpr uint32_t kLbo = D == 64 ? 16u : static_cast<uint32_t>(kBlockBytes);
+    constexpr uint32_t kLbo = D == 64 ? 16u : static_cast<uint32_t>(kBBlk);
 #pragma unroll
-    for (int kk = 0; kk < kBlk / 16; ++kk)
-        umma_ts(d, a + 8u * kk + ((split && kk >= 4) ? 32u : 0u), smem_desc_sw128(sB + 2048 * kk, kLbo, 1024), kIdesc,
-                (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < KSTEPS; ++kk)
+        umma_ts(d, a + 8u * kk, smem_desc_sw128(sB + 2048 * kk, kLbo, 1024), kIdesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// TMA copy of one 128-row tile of a [BH][N][D] tensor: D/64 boxes of 128 rows x 64 values.
-template <int D>
+// TMA copy of one tile of a [BH][N][D] tensor: D/64 boxes of 64 values (the map's box rows),
+// landing kColBlk bytes apart.
+template <int D, int kColBlk>
 __device__ __forceinline__ void tma_tile(uint32_t dst, const void* map, int row, int bh, uint32_t bar) {
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * kBlockBytes, map, 64 * c, row, bh, bar);
+    for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * kColBlk, map, 64 * c, row, bh, bar);
 }
 
 // ================================ dK, dV: one CTA per key block ================================
-// Shared memory: K, V tiles, then a ring of (Q, dO) stages (four at d = 64, two at d = 128),
-// then per-block lse and delta (double-buffered by block parity, filled by warp 11 from lse
-// and from the delta pre-pass), then mbarriers.
-// Tensor memory: S^T 0, dP^T 128; d = 64: P^T 256, dS^T 320, dV 384, dK 448; d = 128 (dV and dK
-// take 128 columns each): dV 256, dK 384, and P^T and dS^T are written over the S^T and dP^T
-// columns the elementwise warps have already read (chunk ch at 16 ch, + 32 for ch >= 2, so each
-// warpgroup writes only over its own columns), which makes the next block's S^T, dP^T wait for
-// this block's dV, dK products.
+// The query blocks that go past the CTA's 128 keys hold BQ queries: 128 at d = 64, 64 at
+// d = 128, so that S^T, dP^T (BQ columns each), P^T, dS^T (BQ/2 each), dV and dK (d each) fit
+// the 512 tensor-memory columns side by side (512 and 448) and the next block's S^T, dP^T never
+// wait for this block's dV, dK products.
+// Shared memory: K, V tiles, then a 4-stage ring of (Q, dO) tiles, then per-block lse and delta
+// (double-buffered by block parity, filled by warp 11 from lse and from the delta pre-pass),
+// then mbarriers.
 
 template <int D>
 struct KvLay {
-    static constexpr int kTile = kBlk * D * 2;
+    static constexpr int kBQ = D == 64 ? 128 : 64;     // queries per query block
+    static constexpr int kChunks = kBQ / 64;           // 32-query chunks per elementwise warpgroup
+    static constexpr int kTile = kBlk * D * 2;          // K or V tile
+    static constexpr int kTileQ = kBQ * D * 2;          // Q or dO tile
+    static constexpr int kQBlockBytes = kBQ * 128;      // one 64-value column block of a Q or dO tile
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kTile;
-    static constexpr int kOffStage = 2 * kTile;  // stage s: Q at +0, dO at +kTile
-    static constexpr int kStageBytes = 2 * kTile;
-    static constexpr int kStages = D == 64 ? 4 : 2;
-    static constexpr int kOffRow = kOffStage + kStages * kStageBytes;  // lse[2][128], delta[2][128] floats
-    static constexpr int kOffBar = kOffRow + 4 * kBlk * 4;
+    static constexpr int kOffStage = 2 * kTile;  // stage s: Q at +0, dO at +kTileQ
+    static constexpr int kStageBytes = 2 * kTileQ;
+    static constexpr int kStages = 4;
+    static constexpr int kOffRow = kOffStage + kStages * kStageBytes;  // lse[2][BQ], delta[2][BQ] floats
+    static constexpr int kOffBar = kOffRow + 4 * kBQ * 4;
     // Barriers: K and V landed; per stage full / empty; S^T and dP^T written; S^T and dP^T read
     // out; P^T and dS^T written; dV, dK products done; the final drain; per row buffer: lse and
     // delta written / read.
@@ -233,13 +239,9 @@ struct KvLay {
     static constexpr int kOffAbort = kOffSlot + 4;
     static constexpr int kSmem = kOffAbort + 4 + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
-    static constexpr bool kAlias = D > 64;
-    static constexpr uint32_t kColS = 0, kColDP = 128;
-    static constexpr uint32_t kColP = kAlias ? 0 : 256, kColDS = kAlias ? 128 : 320;
-    static constexpr uint32_t kColDV = kAlias ? 256 : 384, kColDK = kAlias ? 384 : 448;
-    __host__ __device__ static constexpr uint32_t chunk_col(int ch) {
-        return static_cast<uint32_t>(16 * ch + ((kAlias && ch >= 2) ? 32 : 0));
-    }
+    static constexpr uint32_t kColS = 0, kColDP = kBQ, kColP = 2 * kBQ, kColDS = 2 * kBQ + kBQ / 2;
+    static constexpr uint32_t kColDV = 3 * kBQ, kColDK = 3 * kBQ + D;
+    static_assert(kColDK + D <= kTmemCols, "tensor-memory budget");
 };
 
 // One 32-query chunk of the dK/dV kernel's elementwise step for this thread's key: P^T and
@@ -289,16 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return base + L::kOffBar + 8u * static_cast<uint32_t>(i); };
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kOffSlot);
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + L::kOffAbort);
-    float* const lse_s = reinterpret_cast<float*>(gbase + L::kOffRow);  // [2][128], negated
-    float* const delta_s = lse_s + 2 * kBlk;                              // [2][128], negated
+    constexpr int BQ = L::kBQ;
+    float* const lse_s = reinterpret_cast<float*>(gbase + L::kOffRow);  // [2][BQ], negated
+    float* const delta_s = lse_s + 2 * BQ;                                // [2][BQ], negated
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = p.N;
     const int bh = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.BH));
     const int kblk = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.BH));  // block 0 sees most queries
     const int k0 = kblk * kBlk;
-    const int qb0 = p.causal ? kblk : 0;  // the first query block that sees these keys
-    const int nq = p.nblk - qb0;
+    const int qb0 = p.causal ? k0 / BQ : 0;  // the first query block that sees these keys
+    const int nq = (N + BQ - 1) / BQ - qb0;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::kKV), 1);
@@ -332,39 +335,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < kElemWarps) {
         // ===================== elementwise warps: thread = key (TMEM lane) =====================
         regs_increase<kRegsElem>();
-        const int g = warp >> 2;  // warpgroup: query columns 64g .. 64g + 63
+        const int g = warp >> 2;  // warpgroup: query chunks g kChunks .. (g + 1) kChunks - 1
         const int r = ((warp & 3) << 5) + lane;  // key row within the block, = TMEM lane
         const int key = k0 + r;
         const uint32_t t = tmem + (static_cast<uint32_t>((warp & 3) << 5) << 16);
         bool ok = true;
         for (int i = 0; ok && i < nq; ++i) {
-            const int rb = i & 1, q0 = (qb0 + i) * kBlk;
+            const int rb = i & 1, q0 = (qb0 + i) * BQ;
             if (!(ok = warp_wait(bar(L::kRowsFull + rb), (i >> 1) & 1, abort_flag))) break;
-            const float* ls = lse_s + rb * kBlk;
-            const float* dl = delta_s + rb * kBlk;
+            const float* ls = lse_s + rb * BQ;
+            const float* dl = delta_s + rb * BQ;
             if (!(ok = warp_wait(bar(L::kSFull), i & 1, abort_flag))) break;
             if (!(ok = warp_wait(bar(L::kDPFull), i & 1, abort_flag))) break;
             tc_fence_after();
-            // This warpgroup's two chunks of S^T and dP^T into registers, then they are released
-            // so that the next block's products run during the arithmetic below.
-            uint32_t s0[32], dp0[32], s1[32], dp1[32];
-            ATTN_TMEM_LD_X32(t + L::kColS + 64 * g, s0);
-            ATTN_TMEM_LD_X32(t + L::kColDP + 64 * g, dp0);
-            ATTN_TMEM_LD_X32(t + L::kColS + 64 * g + 32, s1);
-            ATTN_TMEM_LD_X32(t + L::kColDP + 64 * g + 32, dp1);
+            // This warpgroup's chunks of S^T and dP^T into registers, then they are released so
+            // that the next block's products run during the arithmetic below.
+            constexpr int NC = L::kChunks;
+            uint32_t sv[NC][32], dpv[NC][32];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                ATTN_TMEM_LD_X32(t + L::kColS + 32 * (g * NC + c), sv[c]);
+                ATTN_TMEM_LD_X32(t + L::kColDP + 32 * (g * NC + c), dpv[c]);
+            }
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kSdPFree));
-            // Only the causal diagonal block and ragged edges need a mask.
-            const bool masked = (p.causal && qb0 + i == kblk) || q0 + kBlk > N || k0 + kBlk > N;
-            uint32_t pp0[16], ds0[16], pp1[16], ds1[16];
-            if (masked) {
-                kv_chunk<BF16, true>(2 * g, s0, dp0, ls, dl, p.c, key, q0, N, p.causal, pp0, ds0);
-                kv_chunk<BF16, true>(2 * g + 1, s1, dp1, ls, dl, p.c, key, q0, N, p.causal, pp1, ds1);
-            } else {
-                kv_chunk<BF16, false>(2 * g, s0, dp0, ls, dl, p.c, key, q0, N, p.causal, pp0, ds0);
-                kv_chunk<BF16, false>(2 * g + 1, s1, dp1, ls, dl, p.c, key, q0, N, p.causal, pp1, ds1);
+            // Only query blocks that reach below the keys' last row (causal) and ragged edges
+            // need a mask.
+            const bool masked = (p.causal && q0 < k0 + kBlk) || q0 + BQ > N || k0 + kBlk > N;
+            uint32_t ppv[NC][16], dsv[NC][16];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                if (masked)
+                    kv_chunk<BF16, true>(g * NC + c, sv[c], dpv[c], ls, dl, p.c, key, q0, N, p.causal, ppv[c], dsv[c]);
+                else
+                    kv_chunk<BF16, false>(g * NC + c, sv[c], dpv[c], ls, dl, p.c, key, q0, N, p.causal, ppv[c], dsv[c]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kRowsEmpty + rb));
@@ -372,10 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // overwriting them, so that those products run under the arithmetic above.
             if (i > 0 && !(ok = warp_wait(bar(L::kDone), (i - 1) & 1, abort_flag))) break;
             tc_fence_after();
-            tmem_st_x16(t + L::kColP + L::chunk_col(2 * g), pp0);
-            tmem_st_x16(t + L::kColDS + L::chunk_col(2 * g), ds0);
-            tmem_st_x16(t + L::kColP + L::chunk_col(2 * g + 1), pp1);
-            tmem_st_x16(t + L::kColDS + L::chunk_col(2 * g + 1), ds1);
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                tmem_st_x16(t + L::kColP + 16 * (g * NC + c), ppv[c]);
+                tmem_st_x16(t + L::kColDS + 16 * (g * NC + c), dsv[c]);
+            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -416,18 +423,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
             mbar_arrive_expect_tx(bar(L::kKV), 2 * kTile);
-            tma_tile<D>(base + L::kOffK, &tm_k, k0, bh, bar(L::kKV));
-            tma_tile<D>(base + L::kOffV, &tm_v, k0, bh, bar(L::kKV));
+            tma_tile<D, kBlockBytes>(base + L::kOffK, &tm_k, k0, bh, bar(L::kKV));
+            tma_tile<D, kBlockBytes>(base + L::kOffV, &tm_v, k0, bh, bar(L::kKV));
             bool ok = true;
             int issued = 0;
             for (int i = 0; i < nq; ++i) {
-                const int st = i % L::kStages, q0 = (qb0 + i) * kBlk;
+                const int st = i % L::kStages, q0 = (qb0 + i) * BQ;
                 if (!(ok = mbar_wait(bar(L::kQEmpty + st), ((i / L::kStages) & 1) ^ 1, abort_flag, kWaitTimeoutNs)))
                     break;
                 const uint32_t stage = base + L::kOffStage + st * L::kStageBytes;
                 mbar_arrive_expect_tx(bar(L::kQFull + st), L::kStageBytes);
-                tma_tile<D>(stage, &tm_q, q0, bh, bar(L::kQFull + st));
-                tma_tile<D>(stage + kTile, &tm_do, q0, bh, bar(L::kQFull + st));
+                tma_tile<D, L::kQBlockBytes>(stage, &tm_q, q0, bh, bar(L::kQFull + st));
+                tma_tile<D, L::kQBlockBytes>(stage + L::kTileQ, &tm_do, q0, bh, bar(L::kQFull + st));
                 issued = i + 1;
             }
             if (!ok) raise_abort(abort_flag);
@@ -448,16 +455,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(bar(L::kQFull + i % L::kStages), (i / L::kStages) & 1, abort_flag, kWaitTimeoutNs))
                     return false;
                 tc_fence_after();
-                mma_ss_128x128<BF16, D>(tmem + L::kColS, base + L::kOffK, stage);           // S^T = K Q^T
+                mma_ss_kmajor<BF16, D, BQ, kBlockBytes, L::kQBlockBytes>(tmem + L::kColS, base + L::kOffK,
+                                                                         stage);  // S^T = K Q^T
                 umma_commit(bar(L::kSFull));
-                mma_ss_128x128<BF16, D>(tmem + L::kColDP, base + L::kOffV, stage + kTile);  // dP^T = V dO^T
+                mma_ss_kmajor<BF16, D, BQ, kBlockBytes, L::kQBlockBytes>(tmem + L::kColDP, base + L::kOffV,
+                                                                         stage + L::kTileQ);  // dP^T = V dO^T
                 umma_commit(bar(L::kDPFull));
                 return true;
             };
             if (ok && nq > 0) ok = issue_sdp(0);
             for (int i = 0; ok && i + 1 < nq; ++i) {
-                if (!(ok = mbar_wait(bar(L::kAlias ? L::kDone : L::kSdPFree), i & 1, abort_flag, kWaitTimeoutNs)))
-                    break;
+                if (!(ok = mbar_wait(bar(L::kSdPFree), i & 1, abort_flag, kWaitTimeoutNs))) break;
                 tc_fence_after();
                 if (!(ok = issue_sdp(i + 1))) break;
             }
@@ -473,8 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = mbar_wait(bar(L::kPdSFull), i & 1, abort_flag, kWaitTimeoutNs))) break;
                 tc_fence_after();
                 const uint32_t stage = base + L::kOffStage + (i % L::kStages) * L::kStageBytes;
-                mma_ts_128xD<BF16, D>(tmem + L::kColDV, tmem + L::kColP, stage + kTile, i > 0, L::kAlias);  // dV += P^T dO
-                mma_ts_128xD<BF16, D>(tmem + L::kColDK, tmem + L::kColDS, stage, i > 0, L::kAlias);          // dK += dS^T Q
+                mma_ts_mn<BF16, D, BQ / 16, L::kQBlockBytes>(tmem + L::kColDV, tmem + L::kColP, stage + L::kTileQ,
+                                                             i > 0);  // dV += P^T dO
+                mma_ts_mn<BF16, D, BQ / 16, L::kQBlockBytes>(tmem + L::kColDK, tmem + L::kColDS, stage,
+                                                             i > 0);  // dK += dS^T Q
                 umma_commit(bar(L::kDone));
                 umma_commit(bar(L::kQEmpty + i % L::kStages));
             }
@@ -487,10 +497,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // loads run a block ahead of their use.
             bool ok = true;
             for (int i = 0; i < nq; ++i) {
-                const int rb = i & 1, q0 = (qb0 + i) * kBlk;
+                const int rb = i & 1, q0 = (qb0 + i) * BQ;
                 if (!(ok = warp_wait(bar(L::kRowsEmpty + rb), ((i >> 1) & 1) ^ 1, abort_flag))) break;
 #pragma unroll
-                for (int u = lane; u < kBlk; u += 32) {
+                for (int u = lane; u < BQ; u += 32) {
                     const int q = q0 + u;
                     float l2 = 0.f, dl = 0.f;
                     if (q < N) {
@@ -498,8 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         l2 = p.lse[row];
                         dl = *reinterpret_cast<const float*>(p.delta_rows + row * (2 * D));
                     }
-                    lse_s[rb * kBlk + u] = -l2;
-                    delta_s[rb * kBlk + u] = -dl;
+                    lse_s[rb * BQ + u] = -l2;
+                    delta_s[rb * BQ + u] = -dl;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(L::kRowsFull + rb));
@@ -696,8 +706,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
             mbar_arrive_expect_tx(bar(qQ), 2 * kTile);
-            tma_tile<D>(base + L::kOffQ, &tm_q, q0, bh, bar(qQ));
-            tma_tile<D>(base + L::kOffDO, &tm_do, q0, bh, bar(qQ));
+            tma_tile<D, kBlockBytes>(base + L::kOffQ, &tm_q, q0, bh, bar(qQ));
+            tma_tile<D, kBlockBytes>(base + L::kOffDO, &tm_do, q0, bh, bar(qQ));
             bool ok = true;
             int issued = 0;
             for (int j = 0; j < nk; ++j) {
@@ -705,8 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = mbar_wait(bar(L::kKVEmpty + st), ((j / S) & 1) ^ 1, abort_flag, kWaitTimeoutNs))) break;
                 const uint32_t stage = base + L::kOffKV + st * L::kStageBytes;
                 mbar_arrive_expect_tx(bar(qKVFull + st), 2 * kTile);
-                tma_tile<D>(stage, &tm_k, j * kBlk, bh, bar(qKVFull + st));
-                tma_tile<D>(stage + kTile, &tm_v, j * kBlk, bh, bar(qKVFull + st));
+                tma_tile<D, kBlockBytes>(stage, &tm_k, j * kBlk, bh, bar(qKVFull + st));
+                tma_tile<D, kBlockBytes>(stage + kTile, &tm_v, j * kBlk, bh, bar(qKVFull + st));
                 issued = j + 1;
             }
             if (!ok) raise_abort(abort_flag);
@@ -723,9 +733,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t stage = base + L::kOffKV + st * L::kStageBytes;
                 if (!mbar_wait(bar(qKVFull + st), (j / S) & 1, abort_flag, kWaitTimeoutNs)) return false;
                 tc_fence_after();
-                mma_ss_128x128<BF16, D>(tmem + L::kColS, base + L::kOffQ, stage);             // S = Q K^T
+                mma_ss_kmajor<BF16, D, kBlk, kBlockBytes, kBlockBytes>(tmem + L::kColS, base + L::kOffQ,
+                                                                       stage);  // S = Q K^T
                 umma_commit(bar(L::kSFull));
-                mma_ss_128x128<BF16, D>(tmem + L::kColDP, base + L::kOffDO, stage + kTile);   // dP = dO V^T
+                mma_ss_kmajor<BF16, D, kBlk, kBlockBytes, kBlockBytes>(tmem + L::kColDP, base + L::kOffDO,
+                                                                       stage + kTile);  // dP = dO V^T
                 umma_commit(bar(L::kDPFull));
                 return true;
             };
@@ -746,7 +758,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = mbar_wait(bar(L::kDSFull), j & 1, abort_flag, kWaitTimeoutNs))) break;
                 tc_fence_after();
                 const uint32_t stage = base + L::kOffKV + (j % S) * L::kStageBytes;
-                mma_ts_128xD<BF16, D>(tmem + L::kColDQ, tmem + L::kColDS, stage, j > 0, false);  // dQ += dS K
+                mma_ts_mn<BF16, D, kBlk / 16, kBlockBytes>(tmem + L::kColDQ, tmem + L::kColDS, stage,
+                                                           j > 0);  // dQ += dS K
                 umma_commit(bar(L::kDone));
                 umma_commit(bar(L::kKVEmpty + j % S));
             }
@@ -786,12 +799,12 @@ EncodeTiledFn encode_fn() {
 // [BH][N][D] 16-bit tensor; boxes of 128 rows x 64 values (128 bytes, the swizzle span), one per
 // 64-value column block; rows past N of a head are out of bounds (zero-filled), never the next
 // head's.
-bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t D, bool bf16) {
+bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t D, bool bf16, int rows = kBlk) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
-    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(kBlk), 1};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(rows), 1};
     const cuuint32_t estride[3] = {1, 1, 1};
     return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                const_cast<void*>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -802,9 +815,13 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t 
 template <bool BF16, int D>
 int launch_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                 void* dq, void* dk, void* dv, int64_t BH, int64_t N, bool causal, cudaStream_t stream) {
-    CUtensorMap mq, mk, mv, mdo;
+    // The dQ kernel takes 128-row tiles of everything; the dK/dV kernel takes its Q and dO tiles
+    // in query blocks of KvLay<D>::kBQ rows.
+    constexpr int kBQ = KvLay<D>::kBQ;
+    CUtensorMap mq, mk, mv, mdo, mqb, mdob;
     if (!make_map(&mq, q, BH, N, D, BF16) || !make_map(&mk, k, BH, N, D, BF16) || !make_map(&mv, v, BH, N, D, BF16) ||
-        !make_map(&mdo, dout, BH, N, D, BF16))
+        !make_map(&mdo, dout, BH, N, D, BF16) || !make_map(&mqb, q, BH, N, D, BF16, kBQ) ||
+        !make_map(&mdob, dout, BH, N, D, BF16, kBQ))
         return ATTN_ERR_DEVICE;
     if (cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<BF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              KvLay<D>::kSmem) != cudaSuccess ||
@@ -833,7 +850,7 @@ int launch_impl(const void* q, const void* k, const void* v, const void* o, cons
     prm.grad0 = dk;
     prm.grad1 = dv;
     attn_bwd_dkdv_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, KvLay<D>::kSmem, stream>>>(
-        mq, mk, mv, mdo, prm);
+        mqb, mk, mv, mdob, prm);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     prm.grad0 = dq;
     prm.grad1 = nullptr;
