@@ -737,15 +737,23 @@ std::vector<uint16_t> plan_order(int N, int BH, int num_pairs, int BN, int num_s
     return std::vector<uint16_t>(idx.begin(), idx.end());
 }
 
-// Plans are cached per shape (the first causal call of a shape pays well under a millisecond).
-const std::vector<uint16_t>& cached_order(int N, int BH, int num_pairs, int BN, int num_sms) {
+// Plans are cached per shape (the first causal call of a shape pays well under a millisecond);
+// the cache holds at most kPlanCacheMax shapes (it starts over when full) and is copied out
+// under its lock.
+constexpr size_t kPlanCacheMax = 256;
+
+int cached_order(int N, int BH, int num_pairs, int BN, int num_sms, uint16_t* out) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, int>, std::vector<uint16_t>> cache;
     std::lock_guard<std::mutex> lock(mu);
     const auto key = std::make_tuple(N, BH, BN, num_sms);
     auto it = cache.find(key);
-    if (it == cache.end()) it = cache.emplace(key, plan_order(N, BH, num_pairs, BN, num_sms)).first;
-    return it->second;
+    if (it == cache.end()) {
+        if (cache.size() >= kPlanCacheMax) cache.clear();
+        it = cache.emplace(key, plan_order(N, BH, num_pairs, BN, num_sms)).first;
+    }
+    std::copy(it->second.begin(), it->second.end(), out);
+    return static_cast<int>(it->second.size());
 }
 
 template <bool BF16, int D>
@@ -787,10 +795,7 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     if (blocks > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     prm.order_len = 0;
     if (causal && blocks <= kOrderMax && num_sms > 0) {
-        const std::vector<uint16_t>& ord =
-            cached_order(prm.N, prm.BH, prm.num_pairs, Lay<D>::kBN, num_sms);
-        std::copy(ord.begin(), ord.end(), prm.order);
-        prm.order_len = static_cast<int>(ord.size());
+        prm.order_len = cached_order(prm.N, prm.BH, prm.num_pairs, Lay<D>::kBN, num_sms, prm.order);
     }
     attn_fwd_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, kSmemBytes, stream>>>(
         mq, mk, mv, prm);
