@@ -45,6 +45,8 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <string>
+#include <vector>
 
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
@@ -76,6 +78,12 @@ constexpr uint64_t kDrainTimeoutNs = 100000000ull;
 
 __device__ unsigned int g_bwd_error = 0;
 
+// Causal calls with at most kOrderMax blocks carry a launch order (block -> item = block
+// index * BH + head, planned on the host by plan_launch_order); otherwise the grid runs the
+// heaviest blocks first.
+constexpr int kOrderMax = 2048;
+constexpr int kFixedSteps = 3;  // per-CTA fill and drain, in block steps, for the plan
+
 struct BwdParams {
     void* grad0;  // dk (kv kernel) or dq (q kernel)
     void* grad1;  // dv (kv kernel)
@@ -87,6 +95,8 @@ struct BwdParams {
     int causal;
     float c;      // log2(e) / sqrt(d)
     float scale;  // 1 / sqrt(d)
+    int order_len;  // 0: no table
+    uint16_t order[kOrderMax];
 };
 
 __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -297,8 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = p.N;
-    const int bh = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.BH));
-    const int kblk = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.BH));  // block 0 sees most queries
+    const int item = p.order_len > 0 ? p.order[blockIdx.x] : static_cast<int>(blockIdx.x);
+    const int bh = item % p.BH;
+    const int kblk = item / p.BH;  // without a table, block 0 (which sees most queries) goes first
     const int k0 = kblk * kBlk;
     const int qb0 = p.causal ? k0 / BQ : 0;  // the first query block that sees these keys
     const int nq = (N + BQ - 1) / BQ - qb0;
@@ -591,9 +602,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = p.N;
-    const int bh = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.BH));
-    const int slot = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.BH));
-    const int qblk = p.causal ? (p.nblk - 1 - slot) : slot;  // heaviest causal blocks first
+    const int item = p.order_len > 0 ? p.order[blockIdx.x] : static_cast<int>(blockIdx.x);
+    const int bh = item % p.BH;
+    const int slot = item / p.BH;
+    const int qblk = p.causal ? (p.nblk - 1 - slot) : slot;  // without a table, heaviest causal blocks first
     const int q0 = qblk * kBlk;
     const int nk = p.causal ? qblk + 1 : p.nblk;  // keys up to the block's last query
 
@@ -814,7 +826,7 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t 
 
 template <bool BF16, int D>
 int launch_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                void* dq, void* dk, void* dv, int64_t BH, int64_t N, bool causal, cudaStream_t stream) {
+                void* dq, void* dk, void* dv, int64_t BH, int64_t N, bool causal, int num_sms, cudaStream_t stream) {
     // The dQ kernel takes 128-row tiles of everything; the dK/dV kernel takes its Q and dO tiles
     // in query blocks of KvLay<D>::kBQ rows.
     constexpr int kBQ = KvLay<D>::kBQ;
@@ -847,6 +859,21 @@ int launch_impl(const void* q, const void* k, const void* v, const void* o, cons
     attn_bwd_delta_kernel<BF16, D><<<dblocks, 256, 0, stream>>>(
         static_cast<const uint4*>(o), static_cast<const uint4*>(dout), static_cast<uint8_t*>(dq), rows);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+    // Launch orders (causal calls up to kOrderMax blocks): dK/dV item kblk * BH + head weighs its
+    // query blocks, dQ item slot * BH + head its key blocks.
+    const bool plan = causal && blocks <= kOrderMax && num_sms > 0;
+    std::vector<int> w;
+    prm.order_len = 0;
+    if (plan) {
+        const int nqb = static_cast<int>((N + kBQ - 1) / kBQ);
+        w.resize(static_cast<size_t>(blocks));
+        for (int kb = 0; kb < prm.nblk; ++kb)
+            for (int h = 0; h < prm.BH; ++h) w[static_cast<size_t>(kb) * prm.BH + h] = nqb - kb * kBlk / kBQ;
+        prm.order_len = plan_launch_order(w, kFixedSteps, num_sms,
+                                          "bwd kv " + std::to_string(N) + " " + std::to_string(BH) + " " +
+                                              std::to_string(D),
+                                          prm.order);
+    }
     prm.grad0 = dk;
     prm.grad1 = dv;
     attn_bwd_dkdv_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, KvLay<D>::kSmem, stream>>>(
@@ -854,6 +881,14 @@ int launch_impl(const void* q, const void* k, const void* v, const void* o, cons
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
     prm.grad0 = dq;
     prm.grad1 = nullptr;
+    if (plan) {
+        for (int sl = 0; sl < prm.nblk; ++sl)
+            for (int h = 0; h < prm.BH; ++h) w[static_cast<size_t>(sl) * prm.BH + h] = prm.nblk - sl;
+        prm.order_len = plan_launch_order(w, kFixedSteps, num_sms,
+                                          "bwd q " + std::to_string(N) + " " + std::to_string(BH) + " " +
+                                              std::to_string(D),
+                                          prm.order);
+    }
     attn_bwd_dq_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, QLay<D>::kSmem, stream>>>(
         mq, mk, mv, mdo, prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
@@ -863,14 +898,14 @@ int launch_impl(const void* q, const void* k, const void* v, const void* o, cons
 
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                   void* dq, void* dk, void* dv, int64_t BH, int64_t N, int64_t d, bool causal, bool bf16,
-                  cudaStream_t stream) {
+                  int num_sms, cudaStream_t stream) {
     if (N > 0x7FFFFFFFll - kBlk || BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     if (d == 64)
-        return bf16 ? launch_impl<true, 64>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream)
-                    : launch_impl<false, 64>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream);
+        return bf16 ? launch_impl<true, 64>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, num_sms, stream)
+                    : launch_impl<false, 64>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, num_sms, stream);
     if (d == 128)
-        return bf16 ? launch_impl<true, 128>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream)
-                    : launch_impl<false, 128>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, stream);
+        return bf16 ? launch_impl<true, 128>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, num_sms, stream)
+                    : launch_impl<false, 128>(q, k, v, o, dout, lse, dq, dk, dv, BH, N, causal, num_sms, stream);
     return ATTN_ERR_UNSUPPORTED;
 }
 

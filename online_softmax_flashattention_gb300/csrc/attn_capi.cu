@@ -133,7 +133,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
                                     static_cast<const float*>(v), static_cast<const float*>(o),
                                     static_cast<const float*>(dout), lse, static_cast<float*>(dq),
                                     static_cast<float*>(dk), static_cast<float*>(dv), BH, N, d, causal != 0, s);
-    return attn::launch_bwd_tc(q, k, v, o, dout, lse, dq, dk, dv, BH, N, d, causal != 0, dtype == ATTN_BF16, s);
+    return attn::launch_bwd_tc(q, k, v, o, dout, lse, dq, dk, dv, BH, N, d, causal != 0, dtype == ATTN_BF16, num_sms,
+                               s);
 }
 
 size_t attn_kvcache_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int num_splits,

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <string>
+#include <vector>
 
 #include "attn.h"
 
@@ -30,7 +32,15 @@ int launch_bwd_f32(const float* q, const float* k, const float* v, const float* 
 // The same for bf16 (bf16 = true) or fp16 tensors on tcgen05 tensor cores (two kernels).
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                   void* dq, void* dk, void* dv, int64_t BH, int64_t N, int64_t d, bool causal, bool bf16,
-                  cudaStream_t stream);
+                  int num_sms, cudaStream_t stream);
+
+// Launch order for a grid of work items of unequal length, one CTA resident per SM at a time
+// (the hardware gives the next block to the first SM that frees up): a best-fit-decreasing
+// packing of the items, weight[i] + fixed each, into num_sms bins at the smallest capacity that
+// packs, then the items in order of their start time in that packing. Writes the permutation
+// (block -> item) to out and returns its length. Plans are cached by `key` (at most 256 keys,
+// thread-safe); weights.size() must not exceed 65536.
+int plan_launch_order(const std::vector<int>& weights, int fixed, int num_sms, const std::string& key, uint16_t* out);
 
 // Reads (and optionally clears) the tensor-core backward kernels' device error word.
 int bwd_tc_device_error(bool clear, unsigned* err);

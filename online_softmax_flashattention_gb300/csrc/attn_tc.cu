@@ -51,6 +51,7 @@
 #include <cstdlib>
 #include <algorithm>
 #include <map>
+#include <string>
 #include <mutex>
 #include <tuple>
 #include <vector>
@@ -133,7 +134,7 @@ struct Lay {
 __device__ unsigned int g_tc_error = 0;
 
 // Launch order of the work items (item = pair * BH + head) for causal calls with at most
-// kOrderMax items: block b runs item order[b] (see plan_order on the host). Longer calls, and
+// kOrderMax items: block b runs item order[b] (see plan_launch_order). Longer calls, and
 // non-causal ones, run heaviest pairs first without a table.
 constexpr int kOrderMax = 2048;
 
@@ -695,67 +696,6 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t 
 // at B1 H12 N8192 it finishes about 107 steps in, the packing about 98.)
 constexpr int kFixedSteps = 5;
 
-std::vector<uint16_t> plan_order(int N, int BH, int num_pairs, int BN, int num_sms) {
-    const int nkv = (N + BN - 1) / BN;
-    const int items = num_pairs * BH;
-    std::vector<int> w(static_cast<size_t>(items));
-    int64_t total = 0;
-    int wmax = 0;
-    for (int pr = 0; pr < num_pairs; ++pr) {
-        const int rowB = pr * 2 * kBM + kBM;
-        const int nA = std::min(nkv, (pr * 2 * kBM + kBM - 1) / BN + 1);
-        const int nB = rowB < N ? std::min(nkv, (rowB + kBM - 1) / BN + 1) : 0;
-        const int steps = std::max(nA, nB) + kFixedSteps;
-        for (int h = 0; h < BH; ++h) w[static_cast<size_t>(pr) * BH + h] = steps;
-        total += static_cast<int64_t>(steps) * BH;
-        wmax = std::max(wmax, steps);
-    }
-    std::vector<int> idx(static_cast<size_t>(items));
-    for (int i = 0; i < items; ++i) idx[static_cast<size_t>(i)] = i;
-    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return w[a] > w[b]; });
-    const int bins = std::max(1, num_sms);
-    std::vector<int> load(static_cast<size_t>(bins)), start(static_cast<size_t>(items));
-    for (int64_t cap = std::max<int64_t>(wmax, (total + bins - 1) / bins);; ++cap) {
-        std::fill(load.begin(), load.end(), 0);
-        bool fits = true;
-        for (int i : idx) {
-            int best = -1;
-            for (int b = 0; b < bins; ++b)
-                if (load[b] + w[i] <= cap && (best < 0 || load[b] > load[best])) best = b;
-            if (best < 0) {
-                fits = false;
-                break;
-            }
-            start[static_cast<size_t>(i)] = load[best];
-            load[best] += w[i];
-        }
-        if (fits) break;
-    }
-    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) {
-        return start[a] != start[b] ? start[a] < start[b] : w[a] > w[b];
-    });
-    return std::vector<uint16_t>(idx.begin(), idx.end());
-}
-
-// Plans are cached per shape (the first causal call of a shape pays well under a millisecond);
-// the cache holds at most kPlanCacheMax shapes (it starts over when full) and is copied out
-// under its lock.
-constexpr size_t kPlanCacheMax = 256;
-
-int cached_order(int N, int BH, int num_pairs, int BN, int num_sms, uint16_t* out) {
-    static std::mutex mu;
-    static std::map<std::tuple<int, int, int, int>, std::vector<uint16_t>> cache;
-    std::lock_guard<std::mutex> lock(mu);
-    const auto key = std::make_tuple(N, BH, BN, num_sms);
-    auto it = cache.find(key);
-    if (it == cache.end()) {
-        if (cache.size() >= kPlanCacheMax) cache.clear();
-        it = cache.emplace(key, plan_order(N, BH, num_pairs, BN, num_sms)).first;
-    }
-    std::copy(it->second.begin(), it->second.end(), out);
-    return static_cast<int>(it->second.size());
-}
-
 template <bool BF16, int D>
 int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
                 int64_t N, bool causal, int num_sms, cudaStream_t stream) {
@@ -795,7 +735,18 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     if (blocks > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     prm.order_len = 0;
     if (causal && blocks <= kOrderMax && num_sms > 0) {
-        prm.order_len = cached_order(prm.N, prm.BH, prm.num_pairs, Lay<D>::kBN, num_sms, prm.order);
+        // Item pair * BH + head weighs its key-tile steps, max(nA, nB) as the kernel counts them.
+        constexpr int BN = Lay<D>::kBN;
+        const int nkv = static_cast<int>((N + BN - 1) / BN);
+        std::vector<int> w(static_cast<size_t>(blocks));
+        for (int pr = 0; pr < prm.num_pairs; ++pr) {
+            const int rowA = pr * 2 * kBM, rowB = rowA + kBM;
+            const int nA = std::min(nkv, (rowA + kBM - 1) / BN + 1);
+            const int nB = rowB < N ? std::min(nkv, (rowB + kBM - 1) / BN + 1) : 0;
+            for (int h = 0; h < prm.BH; ++h) w[static_cast<size_t>(pr) * prm.BH + h] = std::max(nA, nB);
+        }
+        const std::string key = "fwd " + std::to_string(N) + " " + std::to_string(BH) + " " + std::to_string(BN);
+        prm.order_len = plan_launch_order(w, kFixedSteps, num_sms, key, prm.order);
     }
     attn_fwd_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, kSmemBytes, stream>>>(
         mq, mk, mv, prm);
@@ -806,6 +757,55 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
 }
 
 }  // namespace
+
+int plan_launch_order(const std::vector<int>& weights, int fixed, int num_sms, const std::string& key,
+                      uint16_t* out) {
+    static std::mutex mu;
+    static std::map<std::string, std::vector<uint16_t>> cache;
+    const std::string full = key + " @" + std::to_string(num_sms) + "/" + std::to_string(fixed);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(full);
+    if (it == cache.end()) {
+        const int items = static_cast<int>(weights.size());
+        std::vector<int> w(weights);
+        int64_t total = 0;
+        int wmax = 0;
+        for (int& x : w) {
+            x += fixed;
+            total += x;
+            wmax = std::max(wmax, x);
+        }
+        std::vector<int> idx(static_cast<size_t>(items));
+        for (int i = 0; i < items; ++i) idx[static_cast<size_t>(i)] = i;
+        std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return w[a] > w[b]; });
+        const int bins = std::max(1, num_sms);
+        std::vector<int64_t> load(static_cast<size_t>(bins));
+        std::vector<int64_t> start(static_cast<size_t>(items));
+        for (int64_t cap = std::max<int64_t>(wmax, (total + bins - 1) / bins);; ++cap) {
+            std::fill(load.begin(), load.end(), 0);
+            bool fits = true;
+            for (int i : idx) {
+                int best = -1;
+                for (int b = 0; b < bins; ++b)
+                    if (load[b] + w[i] <= cap && (best < 0 || load[b] > load[best])) best = b;
+                if (best < 0) {
+                    fits = false;
+                    break;
+                }
+                start[static_cast<size_t>(i)] = load[best];
+                load[best] += w[i];
+            }
+            if (fits) break;
+        }
+        std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) {
+            return start[a] != start[b] ? start[a] < start[b] : w[a] > w[b];
+        });
+        if (cache.size() >= 256) cache.clear();
+        it = cache.emplace(full, std::vector<uint16_t>(idx.begin(), idx.end())).first;
+    }
+    std::copy(it->second.begin(), it->second.end(), out);
+    return static_cast<int>(it->second.size());
+}
 
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
                   int64_t N, int64_t d, bool causal, bool bf16, int num_sms, cudaStream_t stream) {
