@@ -405,11 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(L::kBarQFull), 1);
         for (int s = 0; s < L::kKStages; ++s) {
             mbar_init(bar(L::kBarKFull + s), 1);
-            mbar_init(bar(L::kBarKEmpty + s), 2);  // one release per query tile
+            mbar_init(bar(L::kBarKEmpty + s), 1);  // released by the last query tile that reads it
         }
         for (int s = 0; s < L::kVStages; ++s) {
             mbar_init(bar(L::kBarVFull + s), 1);
-            mbar_init(bar(L::kBarVEmpty + s), 2);
+            mbar_init(bar(L::kBarVEmpty + s), 1);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(L::kBarSFull + x), 1);
@@ -558,8 +558,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == kSIssuerWarp && lane == 0) {
             // ============================ S issuer: QK^T ============================
             // S_X(j) goes out as soon as K_j has landed and (j > 0) softmax X has copied
-            // S_X(j-1) out of tensor memory; the two tiles progress independently. Each tile
-            // releases K_j once (twice when the other tile does not read K_j).
+            // S_X(j-1) out of tensor memory; the two tiles progress independently. K_j's stage
+            // is released by the later of the two tiles' products (the only one when the other
+            // tile does not read K_j).
             bool ok = mbar_wait(bar(L::kBarQFull), 0, abort_flag, kWaitTimeoutNs);
             int ns0 = 0, ns1 = 0;
             uint64_t idle_since = 0;
@@ -569,14 +570,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int X = 0; X < 2; ++X) {
                     int& j = X ? ns1 : ns0;
-                    const int nX = X ? nB : nA, nO = X ? nA : nB;
-                    if (j < nX && mbar_test(bar(L::kBarKFull + j % L::kKStages), (j / L::kKStages) & 1) &&
-                        (j == 0 || mbar_test(bar(L::kBarSFree + X), (j - 1) & 1))) {
+                    const int nX = X ? nB : nA, nO = X ? nA : nB, other = X ? ns0 : ns1;
+                    // The usually-late condition first: barrier tests are slow while products
+                    // stream their operands out of shared memory.
+                    if (j < nX && (j == 0 || mbar_test(bar(L::kBarSFree + X), (j - 1) & 1)) &&
+                        mbar_test(bar(L::kBarKFull + j % L::kKStages), (j / L::kKStages) & 1)) {
                         tc_fence_after();
                         issue_s<BF16, D>(tmem, sQ + X * L::kTileBytes, sK + (j % L::kKStages) * L::kKVTileBytes, X,
                                       bar(L::kBarSFull + X));
-                        umma_commit(bar(L::kBarKEmpty + j % L::kKStages));
-                        if (j >= nO) umma_commit(bar(L::kBarKEmpty + j % L::kKStages));
+                        // K_j is released once, after the last product that reads it (a commit
+                        // covers every earlier product of this thread).
+                        if (other > j || j >= nO) umma_commit(bar(L::kBarKEmpty + j % L::kKStages));
                         ++j;
                         progressed = true;
                     }
@@ -599,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == kPVIssuerWarp && lane == 0) {
             // ============================== PV issuer ==============================
             // PV_X(j) goes out as soon as V_j has landed and softmax X has written P_X(j); the
-            // two tiles progress independently and each releases V_j as above.
+            // two tiles progress independently and V_j's stage is released as K_j's is.
             bool ok = true;
             int np0 = 0, np1 = 0;
             uint64_t idle_since = 0;
@@ -609,13 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int X = 0; X < 2; ++X) {
                     int& j = X ? np1 : np0;
-                    const int nX = X ? nB : nA, nO = X ? nA : nB;
-                    if (j < nX && mbar_test(bar(L::kBarVFull + j % L::kVStages), (j / L::kVStages) & 1) &&
-                        mbar_test(bar(L::kBarPFull + X), j & 1)) {
+                    const int nX = X ? nB : nA, nO = X ? nA : nB, other = X ? np0 : np1;
+                    if (j < nX && mbar_test(bar(L::kBarPFull + X), j & 1) &&
+                        mbar_test(bar(L::kBarVFull + j % L::kVStages), (j / L::kVStages) & 1)) {
                         tc_fence_after();
                         issue_pv<BF16, D>(tmem, sV + (j % L::kVStages) * L::kKVTileBytes, X, j > 0, bar(L::kBarOReady + X));
-                        umma_commit(bar(L::kBarVEmpty + j % L::kVStages));
-                        if (j >= nO) umma_commit(bar(L::kBarVEmpty + j % L::kVStages));
+                        if (other > j || j >= nO) umma_commit(bar(L::kBarVEmpty + j % L::kVStages));
                         ++j;
                         progressed = true;
                     }
