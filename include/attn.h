@@ -18,8 +18,10 @@
  * Ownership and synchronisation. The caller owns every buffer and the stream. Calls are
  * stream-ordered and asynchronous: they validate, enqueue on `stream` (a cudaStream_t;
  * NULL is the legacy default stream) and return. The library keeps no state between calls
- * apart from per-device caches of device properties and driver entry points, and is safe
- * to call from several host threads. attn_fwd allocates no device memory.
+ * apart from per-device caches of device properties and driver entry points and a host-side
+ * cache of causal launch orders per problem shape (at most 256 entries per kind of kernel,
+ * a few KiB each), and is safe to call from several host threads (the caches are guarded by
+ * mutexes). attn_fwd allocates no device memory.
  *
  * Errors. Every entry point returns an attn_status_t and never exits the process.
  * Argument checks happen before any launch; a non-OK status means nothing was enqueued.
