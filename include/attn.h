@@ -19,7 +19,7 @@
  * stream-ordered and asynchronous: they validate, enqueue on `stream` (a cudaStream_t;
  * NULL is the legacy default stream) and return. The library keeps no state between calls
  * apart from per-device caches of device properties and driver entry points and a host-side
- * cache of causal launch orders per problem shape (at most 256 entries per kind of kernel,
+ * cache of causal launch orders per problem shape and kernel (at most 256 entries,
  * a few KiB each), and is safe to call from several host threads (the caches are guarded by
  * mutexes). attn_fwd allocates no device memory.
  *
