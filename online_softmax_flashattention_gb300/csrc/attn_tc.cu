@@ -567,8 +567,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t polls = 0;
             while (ok && (ns0 < nA || ns1 < nB)) {
                 bool progressed = false;
+                // Tile B is tested first here and tile A first in the PV issuer: a fixed order
+                // keeps the two tiles' steps interleaved (alternating it each pass cost 16 %),
+                // and this one measured best of the four fixed ones.
 #pragma unroll
-                for (int X = 0; X < 2; ++X) {
+                for (int XX = 0; XX < 2; ++XX) {
+                    const int X = XX ^ 1;
                     int& j = X ? ns1 : ns0;
                     const int nX = X ? nB : nA, nO = X ? nA : nB, other = X ? ns0 : ns1;
                     // The usually-late condition first: barrier tests are slow while products
