@@ -238,12 +238,12 @@ struct KvLay {
     static constexpr int kStages = 4;
     static constexpr int kOffRow = kOffStage + kStages * kStageBytes;  // lse[2][BQ], delta[2][BQ] floats
     static constexpr int kOffBar = kOffRow + 4 * kBQ * 4;
-    // Barriers: K and V landed; per stage full / empty; S^T and dP^T written; S^T and dP^T read
-    // out; P^T and dS^T written; dV, dK products done; the final drain; per row buffer: lse and
+    // Barriers: K and V landed; per stage full / empty; S^T and dP^T written (one commit after
+    // both products); S^T and dP^T read out; P^T and dS^T written; dV, dK products done; the final drain; per row buffer: lse and
     // delta written / read.
-    static constexpr int kKV = 0, kQFull = 1, kQEmpty = kQFull + kStages, kSFull = kQEmpty + kStages,
-                         kDPFull = kSFull + 1, kSdPFree = kSFull + 2, kPdSFull = kSFull + 3, kDone = kSFull + 4,
-                         kDrain = kSFull + 5, kRowsFull = kSFull + 6, kRowsEmpty = kRowsFull + 2,
+    static constexpr int kKV = 0, kQFull = 1, kQEmpty = kQFull + kStages, kDPFull = kQEmpty + kStages,
+                         kSdPFree = kDPFull + 1, kPdSFull = kDPFull + 2, kDone = kDPFull + 3,
+                         kDrain = kDPFull + 4, kRowsFull = kDPFull + 5, kRowsEmpty = kRowsFull + 2,
                          kDrain2 = kRowsEmpty + 2, kNumBars = kDrain2 + 1;
     static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
     static constexpr int kOffAbort = kOffSlot + 4;
@@ -320,7 +320,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::kQFull + s), 1);
             mbar_init(bar(L::kQEmpty + s), 1);
         }
-        mbar_init(bar(L::kSFull), 1);
         mbar_init(bar(L::kDPFull), 1);
         mbar_init(bar(L::kSdPFree), kElemWarps);
         mbar_init(bar(L::kPdSFull), kElemWarps);
@@ -356,7 +355,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = warp_wait(bar(L::kRowsFull + rb), (i >> 1) & 1, abort_flag))) break;
             const float* ls = lse_s + rb * BQ;
             const float* dl = delta_s + rb * BQ;
-            if (!(ok = warp_wait(bar(L::kSFull), i & 1, abort_flag))) break;
             if (!(ok = warp_wait(bar(L::kDPFull), i & 1, abort_flag))) break;
             tc_fence_after();
             // This warpgroup's chunks of S^T and dP^T into registers, then they are released so
@@ -468,7 +466,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 mma_ss_kmajor<BF16, D, BQ, kBlockBytes, L::kQBlockBytes>(tmem + L::kColS, base + L::kOffK,
                                                                          stage);  // S^T = K Q^T
-                umma_commit(bar(L::kSFull));
                 mma_ss_kmajor<BF16, D, BQ, kBlockBytes, L::kQBlockBytes>(tmem + L::kColDP, base + L::kOffV,
                                                                          stage + L::kTileQ);  // dP^T = V dO^T
                 umma_commit(bar(L::kDPFull));
@@ -553,9 +550,10 @@ struct QLay {
     static constexpr int kStageBytes = 2 * kTile;
     static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
     static constexpr int kKVEmpty = qKVFull + kStages;
-    static constexpr int kSFull = kKVEmpty + kStages;
-    static constexpr int kDPFull = kSFull + 1, kSdPFree = kSFull + 2, kDSFull = kSFull + 3, kDone = kSFull + 4,
-                         kDrain = kSFull + 5, kDrain2 = kSFull + 6, kNumBars = kSFull + 7;
+    // kDPFull: S and dP written (one commit after both products).
+    static constexpr int kDPFull = kKVEmpty + kStages;
+    static constexpr int kSdPFree = kDPFull + 1, kDSFull = kDPFull + 2, kDone = kDPFull + 3, kDrain = kDPFull + 4,
+                         kDrain2 = kDPFull + 5, kNumBars = kDPFull + 6;
     static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
     static constexpr int kOffAbort = kOffSlot + 4;
     static constexpr int kSmem = kOffAbort + 4 + 1024;
@@ -615,7 +613,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(qKVFull + s), 1);
             mbar_init(bar(L::kKVEmpty + s), 1);
         }
-        mbar_init(bar(L::kSFull), 1);
         mbar_init(bar(L::kDPFull), 1);
         mbar_init(bar(L::kSdPFree), kElemWarps);
         mbar_init(bar(L::kDSFull), kElemWarps);
@@ -653,7 +650,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 0; ok && j < nk; ++j) {
             const int k0 = j * kBlk;
-            if (!(ok = warp_wait(bar(L::kSFull), j & 1, abort_flag))) break;
             if (!(ok = warp_wait(bar(L::kDPFull), j & 1, abort_flag))) break;
             tc_fence_after();
             // This warpgroup's two chunks of S and dP into registers, released before the
@@ -747,7 +743,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 mma_ss_kmajor<BF16, D, kBlk, kBlockBytes, kBlockBytes>(tmem + L::kColS, base + L::kOffQ,
                                                                        stage);  // S = Q K^T
-                umma_commit(bar(L::kSFull));
                 mma_ss_kmajor<BF16, D, kBlk, kBlockBytes, kBlockBytes>(tmem + L::kColDP, base + L::kOffDO,
                                                                        stage + kTile);  // dP = dO V^T
                 umma_commit(bar(L::kDPFull));
