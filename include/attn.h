@@ -249,12 +249,30 @@ int attn_device_status(void* stream, int clear);
  */
 int attn_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
 
+/*
+ * attn_plan_launch_order — the block order the causal kernels use (host only, no device): items
+ * of unequal length, one CTA resident per SM at a time, and the hardware giving the next block
+ * to the first SM that frees up. The items, weights[i] + fixed each, are packed best-fit
+ * decreasing into num_sms bins at the smallest capacity that packs (capacities tried upward
+ * from the even split in unit steps; after 64 tries the step doubles, which bounds the host
+ * time for very large weights), and returned in order of their start time in that packing
+ * (ties: heavier first), so that list scheduling in this order follows the packing. attn_fwd, attn_fwd_lse and attn_bwd plan their causal grids this
+ * way (weights = key or query tiles of each work item) when a call has at most 2048 items.
+ *   weights : host array of n weights, each 0 .. 2^24
+ *   n       : 1 .. 65536
+ *   fixed   : per-item cost added to every weight, 0 .. 2^24
+ *   num_sms : bins, 1 .. 4096
+ *   order   : host array of n entries; receives the permutation (position -> item index)
+ * Returns ATTN_OK, or ATTN_ERR_INVALID_ARG for a null pointer or a value out of range.
+ */
+int attn_plan_launch_order(const int32_t* weights, int64_t n, int32_t fixed, int32_t num_sms, uint16_t* order);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* attn_status_string(int status);
 
 /* ABI version of this header: (major << 16) | minor (1.1 added attn_fwd_lse, 1.2 attn_bwd,
  * 1.3 attn_fwd_kvcache, 1.4 head width 128 for the forward entry points, 1.5
- * attn_selftest_wait_timeout, 1.6 head width 128 for attn_bwd). */
+ * attn_selftest_wait_timeout, 1.6 head width 128 for attn_bwd, 1.7 attn_plan_launch_order). */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

@@ -26,7 +26,7 @@ __all__ = [
     "attn_fwd", "attn_fwd_materialized", "attn_materialized_workspace_bytes", "attn_device_status",
     "attn_status_string", "attn_abi_version", "raw", "attn_fwd_materialized_noalloc",
     "ATTN_NOALLOC_MAX_N", "attn_fwd_lse", "attn_bwd", "attn_fwd_kvcache", "attn_kvcache_workspace_bytes",
-    "ATTN_KV_MAX_SPLITS", "attn_selftest_wait_timeout",
+    "ATTN_KV_MAX_SPLITS", "attn_selftest_wait_timeout", "attn_plan_launch_order",
 ]
 
 ATTN_F32, ATTN_BF16, ATTN_F16 = 0, 1, 2
@@ -87,6 +87,8 @@ def raw():
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_abi_version.argtypes = []
             lib.attn_abi_version.restype = ci
+            lib.attn_plan_launch_order.argtypes = [vp, i64, ctypes.c_int32, ctypes.c_int32, vp]
+            lib.attn_plan_launch_order.restype = ci
             _lib = lib
     return _lib
 
@@ -97,6 +99,18 @@ def attn_status_string(status: int) -> str:
 
 def attn_abi_version() -> int:
     return int(raw().attn_abi_version())
+
+
+def attn_plan_launch_order(weights, fixed: int, num_sms: int) -> list[int]:
+    """The launch order the causal kernels use for items of these weights (host only): a list
+    of item indices, position -> item. See attn_plan_launch_order in include/attn.h."""
+    w = (ctypes.c_int32 * len(weights))(*[int(x) for x in weights])
+    out = (ctypes.c_uint16 * max(1, len(weights)))()
+    st = raw().attn_plan_launch_order(ctypes.cast(w, ctypes.c_void_p), len(weights), int(fixed), int(num_sms),
+                                      ctypes.cast(out, ctypes.c_void_p))
+    if st != 0:
+        raise AttnError(st, "attn_plan_launch_order")
+    return list(out[:len(weights)])
 
 
 def _check(q, k, v):

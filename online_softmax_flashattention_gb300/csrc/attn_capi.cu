@@ -8,6 +8,9 @@
 #include <cstring>
 
 #include "attn.h"
+#include <algorithm>
+#include <vector>
+
 #include "attn_internal.h"
 
 namespace {
@@ -274,6 +277,20 @@ const char* attn_status_string(int status) {
     }
 }
 
-int attn_abi_version(void) { return (1 << 16) | 6; }
+int attn_plan_launch_order(const int32_t* weights, int64_t n, int32_t fixed, int32_t num_sms, uint16_t* order) {
+    if (!weights || !order || n < 1 || n > 65536 || fixed < 0 || fixed > (1 << 24) || num_sms < 1 ||
+        num_sms > 4096)
+        return ATTN_ERR_INVALID_ARG;
+    std::vector<int> w(static_cast<size_t>(n));
+    for (int64_t i = 0; i < n; ++i) {
+        if (weights[i] < 0 || weights[i] > (1 << 24)) return ATTN_ERR_INVALID_ARG;
+        w[static_cast<size_t>(i)] = weights[i];
+    }
+    const std::vector<uint16_t> ord = attn::plan_order_compute(w, fixed, num_sms);
+    std::copy(ord.begin(), ord.end(), order);
+    return ATTN_OK;
+}
+
+int attn_abi_version(void) { return (1 << 16) | 7; }
 
 }  // extern "C"

@@ -41,6 +41,8 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, co
 // (block -> item) to out and returns its length. Plans are cached by `key` (at most 256 keys,
 // thread-safe); weights.size() must not exceed 65536.
 int plan_launch_order(const std::vector<int>& weights, int fixed, int num_sms, const std::string& key, uint16_t* out);
+// The same plan without the cache (for the attn_plan_launch_order entry point).
+std::vector<uint16_t> plan_order_compute(const std::vector<int>& weights, int fixed, int num_sms);
 
 // Reads (and optionally clears) the tensor-core backward kernels' device error word.
 int bwd_tc_device_error(bool clear, unsigned* err);

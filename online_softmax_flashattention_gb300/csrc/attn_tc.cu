@@ -765,55 +765,6 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
 
 }  // namespace
 
-int plan_launch_order(const std::vector<int>& weights, int fixed, int num_sms, const std::string& key,
-                      uint16_t* out) {
-    static std::mutex mu;
-    static std::map<std::string, std::vector<uint16_t>> cache;
-    const std::string full = key + " @" + std::to_string(num_sms) + "/" + std::to_string(fixed);
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(full);
-    if (it == cache.end()) {
-        const int items = static_cast<int>(weights.size());
-        std::vector<int> w(weights);
-        int64_t total = 0;
-        int wmax = 0;
-        for (int& x : w) {
-            x += fixed;
-            total += x;
-            wmax = std::max(wmax, x);
-        }
-        std::vector<int> idx(static_cast<size_t>(items));
-        for (int i = 0; i < items; ++i) idx[static_cast<size_t>(i)] = i;
-        std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return w[a] > w[b]; });
-        const int bins = std::max(1, num_sms);
-        std::vector<int64_t> load(static_cast<size_t>(bins));
-        std::vector<int64_t> start(static_cast<size_t>(items));
-        for (int64_t cap = std::max<int64_t>(wmax, (total + bins - 1) / bins);; ++cap) {
-            std::fill(load.begin(), load.end(), 0);
-            bool fits = true;
-            for (int i : idx) {
-                int best = -1;
-                for (int b = 0; b < bins; ++b)
-                    if (load[b] + w[i] <= cap && (best < 0 || load[b] > load[best])) best = b;
-                if (best < 0) {
-                    fits = false;
-                    break;
-                }
-                start[static_cast<size_t>(i)] = load[best];
-                load[best] += w[i];
-            }
-            if (fits) break;
-        }
-        std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) {
-            return start[a] != start[b] ? start[a] < start[b] : w[a] > w[b];
-        });
-        if (cache.size() >= 256) cache.clear();
-        it = cache.emplace(full, std::vector<uint16_t>(idx.begin(), idx.end())).first;
-    }
-    std::copy(it->second.begin(), it->second.end(), out);
-    return static_cast<int>(it->second.size());
-}
-
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
                   int64_t N, int64_t d, bool causal, bool bf16, int num_sms, cudaStream_t stream) {
     if (N > 0x7FFFFFFFll - 2 * kBM || BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
