@@ -27,15 +27,28 @@ def causal_pairs(n_pairs, heads):
     return [2 * p + 2 for p in range(n_pairs) for _ in range(heads)]
 
 
+def causal_pairs_wide(n_pairs, heads):
+    # head width 128: 64-key tiles, so pair p of 128-row query tiles sees 4p + 4 of them
+    return [4 * p + 4 for p in range(n_pairs) for _ in range(heads)]
+
+
 def causal_blocks(n_blocks, heads):
     # backward dK/dV items: key block kb sees n_blocks - kb query blocks
     return [n_blocks - kb for kb in range(n_blocks) for _ in range(heads)]
 
 
+def kv_blocks_wide(n, heads):
+    # backward dK/dV at head width 128: key block kb (128 keys) sees the 64-query blocks from
+    # its own on, n / 64 - 2 kb of them
+    return [n // 64 - 2 * kb for kb in range(n // 128) for _ in range(heads)]
+
+
 @pytest.mark.parametrize("weights,fixed,bins", [
     (causal_pairs(32, 12), 5, 152),   # forward, B1 H12 N8192
     (causal_pairs(16, 24), 5, 152),   # forward, B2 H12 N4096
+    (causal_pairs_wide(32, 12), 5, 152),  # forward, B1 H12 N8192 d128
     (causal_blocks(64, 12), 3, 152),  # backward kernels, B1 H12 N8192
+    (kv_blocks_wide(4096, 24), 3, 152),  # backward dK/dV at d128, B2 H12 N4096
     (causal_blocks(32, 12), 3, 148),
 ])
 def test_planned_order_beats_heaviest_first(weights, fixed, bins):
