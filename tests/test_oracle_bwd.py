@@ -5,7 +5,8 @@ then in Triton" page, section "Backwards, and training with it": dV = P^T dO, dP
 delta = rowsum(dO * O), dS = P (dP - delta), dQ = dS K scale, dK = dS^T Q scale. The pins:
 central finite differences of a float64 forward written here (a different method: no
 gradient formula), PyTorch's float64 autograd through its own attention, closed forms (one
-key; equal scores), and planted mistakes in the C source that these must catch.
+key; equal scores), two exact sum identities (dK's rows sum to zero, dV's rows to dO's rows),
+and planted mistakes in the C source that these must catch.
 """
 
 import ctypes
@@ -110,9 +111,8 @@ MUTANTS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_planted_backward_mistakes_are_caught(tmp_path, name):
-    torch = pytest.importorskip("torch")
+def _mutant_bwd(tmp_path, name, q, k, v, do, causal):
+    """dq, dk, dv from the oracle's C source with mutant `name` planted."""
     old, new = MUTANTS[name]
     assert SRC.count(old) == 1, name
     c = tmp_path / f"{name}.c"
@@ -122,14 +122,52 @@ def test_planted_backward_mistakes_are_caught(tmp_path, name):
     lib = ctypes.CDLL(str(so))
     i64, fp, dp = ctypes.c_int64, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double)
     lib.oracle_attn_bwd.argtypes = [fp, fp, fp, fp, i64, i64, i64, i64, ctypes.c_int, dp, dp, dp, ctypes.c_int]
+    outs = [np.empty(q.shape) for _ in range(3)]
+    assert lib.oracle_attn_bwd(q.ctypes.data_as(fp), k.ctypes.data_as(fp), v.ctypes.data_as(fp), do.ctypes.data_as(fp),
+                               *q.shape, int(causal), *(x.ctypes.data_as(dp) for x in outs), 2) == 0
+    return outs
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_backward_mistakes_are_caught(tmp_path, name):
+    torch = pytest.importorskip("torch")
     shape = (1, 2, 17, 64)
     q, k, v = si.qkv(241, *shape)
     do = si.qkv(242, *shape)[0]
-    outs = [np.empty(shape) for _ in range(3)]
-    assert lib.oracle_attn_bwd(q.ctypes.data_as(fp), k.ctypes.data_as(fp), v.ctypes.data_as(fp), do.ctypes.data_as(fp),
-                               *shape, 1, *(x.ctypes.data_as(dp) for x in outs), 2) == 0
+    outs = _mutant_bwd(tmp_path, name, q, k, v, do, 1)
     tq, tk, tv = (torch.from_numpy(x).double().requires_grad_() for x in (q, k, v))
     o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True)
     o.backward(torch.from_numpy(do).double())
     ok = all(np.allclose(g, t.grad.numpy(), rtol=1e-9, atol=1e-10) for g, t in zip(outs, (tq, tk, tv)))
     assert not ok, f"mutant {name} not caught"
+
+
+def _sum_identities_hold(dk, dv, do):
+    # Each row of dS = P (dP - delta) sums to zero (delta is the row's P-weighted dP), so the
+    # rows of dK = scale dS^T Q sum to zero in every head; each row of P sums to one, so the
+    # rows of dV = P^T dO sum to the rows of dO.
+    dk_ok = np.abs(dk.sum(axis=2)).max() <= 1e-12 * np.abs(dk).sum(axis=2).max()
+    dv_ok = np.abs(dv.sum(axis=2) - do.astype(np.float64).sum(axis=2)).max() <= 1e-12 * np.abs(do).sum(axis=2).max()
+    return dk_ok, dv_ok
+
+
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("d", [64, 128])
+def test_gradient_sum_identities(causal, d):
+    shape = (2, 3, 37, d)
+    q, k, v = si.qkv(251, *shape)
+    do = si.qkv(252, *shape)[0]
+    _, dk, dv = oracle.attn_bwd(q, k, v, do, causal)
+    assert _sum_identities_hold(dk, dv, do) == (True, True)
+
+
+@pytest.mark.parametrize("name,broken", [("delta_sign", 0), ("delta_dropped", 0), ("dv_not_transposed", 1)])
+def test_sum_identities_catch_mutants(tmp_path, name, broken):
+    # Without PyTorch: the identities alone reject a wrong or missing delta and an
+    # untransposed P in dV.
+    shape = (1, 2, 17, 64)
+    q, k, v = si.qkv(243, *shape)
+    do = si.qkv(244, *shape)[0]
+    _, dk, dv = _mutant_bwd(tmp_path, name, q, k, v, do, 1)
+    assert not _sum_identities_hold(dk, dv, do)[broken], name
+
