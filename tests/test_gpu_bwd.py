@@ -89,3 +89,33 @@ def test_bwd_head_width_128(dtype, causal, N):
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_bwd_head_width_128_qk_scaled_x8(dtype):
     _case(0xA77E0700, 1, 2, 300, dtype, True, qk_scale=8.0, d=128)
+
+
+def test_bwd_full_size_sum_identities():
+    # The bf16 causal B1 H12 N8192 d64 backward as the bench times it (a planned launch order),
+    # checked through properties that hold at any size. Each row of dS = P (dP - delta) sums to
+    # zero and each row of P to one, so in exact arithmetic dK's rows sum to zero in every head
+    # and dV's rows sum to dO's rows. What the kernels round breaks this only slightly: delta
+    # comes from the bf16 output o, P and dS are rounded to bf16 before their products, and
+    # dk, dv are rounded once. Each of these is unit roundoff (2^-9) times terms of random sign,
+    # about 1e-4 of sum_j |dk_j| (or |dv_j|) at this size; the bound is 2e-3 of that sum, per
+    # head and column.
+    B, H, N, d = 1, 12, 8192, 64
+    q, k, v = si.qkv(0xA77E0600, B, H, N, d, "bf16")
+    do = si.qkv(0xA77E0601, B, H, N, d, "bf16")[0]
+    qd, kd, vd, dod = (to_dev(x, "bf16") for x in (q, k, v, do))
+    o, lse = fa.attn_fwd_lse(qd, kd, vd, causal=True)
+    dq, dk, dv = fa.attn_bwd(qd, kd, vd, o, dod, lse, causal=True)
+    torch.cuda.synchronize()
+    assert fa.attn_device_status(clear=True) == 0
+    for t in (dq, dk, dv):
+        assert bool(torch.isfinite(t).all())
+    dk64, dv64, do64 = dk.double(), dv.double(), dod.double()
+    dk_dev = dk64.sum(dim=2).abs()
+    dk_bound = 2e-3 * dk64.abs().sum(dim=2)
+    assert bool((dk_dev <= dk_bound).all()), f"max |sum dk| {float(dk_dev.max()):.3e}, bound {float(dk_bound.min()):.3e}"
+    dv_dev = (dv64.sum(dim=2) - do64.sum(dim=2)).abs()
+    dv_bound = 2e-3 * dv64.abs().sum(dim=2)
+    assert bool((dv_dev <= dv_bound).all()), f"max |sum dv - sum do| {float(dv_dev.max()):.3e}, bound {float(dv_bound.min()):.3e}"
+    print(f"max |sum dk| {float(dk_dev.max()):.3e} (sum |dk| >= {float(dk64.abs().sum(dim=2).min()):.1f}); "
+          f"max |sum dv - sum do| {float(dv_dev.max()):.3e} (sum |dv| >= {float(dv64.abs().sum(dim=2).min()):.1f})")
