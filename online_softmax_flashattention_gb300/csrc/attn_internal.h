@@ -35,9 +35,10 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, co
                   int num_sms, cudaStream_t stream);
 
 // Launch order for a grid of work items of unequal length, one CTA resident per SM at a time
-// (the hardware gives the next block to the first SM that frees up): a best-fit-decreasing
-// packing of the items, weight[i] + fixed each, into num_sms bins at the smallest capacity that
-// packs, then the items in order of their start time in that packing. Writes the permutation
+// (the hardware gives the next block to the first SM that frees up; attn_plan.cu): a
+// best-fit-decreasing packing of the items, weight[i] + fixed each, into num_sms bins at the
+// smallest capacity that packs (tried upward from the even split, the step doubling after 64
+// tries), then the items in order of their start time in that packing. Writes the permutation
 // (block -> item) to out and returns its length. Plans are cached by `key` (at most 256 keys,
 // thread-safe); weights.size() must not exceed 65536.
 int plan_launch_order(const std::vector<int>& weights, int fixed, int num_sms, const std::string& key, uint16_t* out);
