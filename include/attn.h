@@ -18,10 +18,11 @@
  * Ownership and synchronisation. The caller owns every buffer and the stream. Calls are
  * stream-ordered and asynchronous: they validate, enqueue on `stream` (a cudaStream_t;
  * NULL is the legacy default stream) and return. The library keeps no state between calls
- * apart from per-device caches of device properties and driver entry points and a host-side
- * cache of causal launch orders per problem shape and kernel (at most 256 entries,
- * a few KiB each), and is safe to call from several host threads (the caches are guarded by
- * mutexes). attn_fwd allocates no device memory.
+ * apart from host-side caches: per device, its properties, driver entry points and kernel
+ * attributes (set once); the forward's tensor maps of the last 8 (pointer, shape) combinations;
+ * and causal launch orders per problem shape and kernel (at most 256 entries, a few KiB each).
+ * It is safe to call from several host threads (the caches are guarded by mutexes). attn_fwd
+ * allocates no device memory.
  *
  * Errors. Every entry point returns an attn_status_t and never exits the process.
  * Argument checks happen before any launch; a non-OK status means nothing was enqueued.
@@ -212,14 +213,16 @@ size_t attn_materialized_workspace_bytes(int64_t B, int64_t H, int64_t N);
  * it does not own, or on a path that must not call cudaMalloc/cudaFree because those can
  * synchronise the device.
  *
- *   Scratch: a fixed array of ATTN_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU
- *            that loads the library holds it until the process exits. Heads run in groups of
- *            as many as fit.
+ *   Scratch: a fixed array of ATTN_NOALLOC_SCRATCH_BYTES compiled into the library, in a
+ *            module of its own: a GPU holds it from the first call of this entry point on that
+ *            device until the process exits (callers of the other entry points never load it).
+ *            Heads run in groups of as many as fit.
  *   Limit:   N <= ATTN_NOALLOC_MAX_N (one head's scores and probabilities must fit the
  *            array); larger N returns ATTN_ERR_UNSUPPORTED and launches nothing.
- *   Set-up:  the first call on a device looks up the array's device address
- *            (cudaGetSymbolAddress) with that device current; make that first call before
- *            capturing a stream into a graph.
+ *   Set-up:  every call looks up the array's device address (cudaGetSymbolAddress) on the
+ *            current device, so a device reset cannot leave a stale address; the first call on
+ *            a device also loads the array's module, so make it before capturing a stream
+ *            into a graph.
  *   Sharing: all calls use the same array, which keeps the previous call's contents (no call
  *            depends on them: everything is written before it is read). Calls whose kernels
  *            overlap on the GPU — unordered streams, several host threads — race on it.
@@ -259,9 +262,10 @@ int attn_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
  * (ties: heavier first), so that list scheduling in this order follows the packing. attn_fwd, attn_fwd_lse and attn_bwd plan their causal grids this
  * way (weights = key or query tiles of each work item) when a call has at most 2048 items.
  *   weights : host array of n weights, each 0 .. 2^24
- *   n       : 1 .. 65536
+ *   n       : 1 .. 8192
  *   fixed   : per-item cost added to every weight, 0 .. 2^24
- *   num_sms : bins, 1 .. 4096
+ *   num_sms : bins, 1 .. 1024, with n * num_sms <= 2^20 (each capacity tried costs n * num_sms
+ *             steps; the bound keeps a call well under a second)
  *   order   : host array of n entries; receives the permutation (position -> item index)
  * Returns ATTN_OK, or ATTN_ERR_INVALID_ARG for a null pointer or a value out of range.
  */

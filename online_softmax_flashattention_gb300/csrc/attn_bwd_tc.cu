@@ -830,10 +830,15 @@ int launch_impl(const void* q, const void* k, const void* v, const void* o, cons
         !make_map(&mdo, dout, BH, N, D, BF16) || !make_map(&mqb, q, BH, N, D, BF16, kBQ) ||
         !make_map(&mdob, dout, BH, N, D, BF16, kBQ))
         return ATTN_ERR_DEVICE;
-    if (cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<BF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KvLay<D>::kSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<BF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             QLay<D>::kSmem) != cudaSuccess)
+    static uint64_t ready = 0;  // shared-memory grants, once per device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
+    if (!once_per_device(&ready, dev, [] {
+            return cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<BF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        KvLay<D>::kSmem) == cudaSuccess &&
+                   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<BF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        QLay<D>::kSmem) == cudaSuccess;
+        }))
         return ATTN_ERR_LAUNCH;
     BwdParams prm;
     prm.delta_rows = static_cast<const uint8_t*>(dq);
@@ -857,17 +862,16 @@ int launch_impl(const void* q, const void* k, const void* v, const void* o, cons
     // Launch orders (causal calls up to kOrderMax blocks): dK/dV item kblk * BH + head weighs its
     // query blocks, dQ item slot * BH + head its key blocks.
     const bool plan = causal && blocks <= kOrderMax && num_sms > 0;
-    std::vector<int> w;
     prm.order_len = 0;
+    const int nblk = prm.nblk;
     if (plan) {
-        const int nqb = static_cast<int>((N + kBQ - 1) / kBQ);
-        w.resize(static_cast<size_t>(blocks));
-        for (int kb = 0; kb < prm.nblk; ++kb)
-            for (int h = 0; h < prm.BH; ++h) w[static_cast<size_t>(kb) * prm.BH + h] = nqb - kb * kBlk / kBQ;
-        prm.order_len = plan_launch_order(w, kFixedSteps, num_sms,
-                                          "bwd kv " + std::to_string(N) + " " + std::to_string(BH) + " " +
-                                              std::to_string(D),
-                                          prm.order);
+        prm.order_len = plan_launch_order(PlanKey{1, N, BH, D, 0}, kFixedSteps, num_sms, [&] {
+            const int nqb = static_cast<int>((N + kBQ - 1) / kBQ);
+            std::vector<int> w(static_cast<size_t>(blocks));
+            for (int kb = 0; kb < nblk; ++kb)
+                for (int64_t h = 0; h < BH; ++h) w[static_cast<size_t>(kb) * BH + h] = nqb - kb * kBlk / kBQ;
+            return w;
+        }, prm.order);
     }
     prm.grad0 = dk;
     prm.grad1 = dv;
@@ -877,12 +881,12 @@ int launch_impl(const void* q, const void* k, const void* v, const void* o, cons
     prm.grad0 = dq;
     prm.grad1 = nullptr;
     if (plan) {
-        for (int sl = 0; sl < prm.nblk; ++sl)
-            for (int h = 0; h < prm.BH; ++h) w[static_cast<size_t>(sl) * prm.BH + h] = prm.nblk - sl;
-        prm.order_len = plan_launch_order(w, kFixedSteps, num_sms,
-                                          "bwd q " + std::to_string(N) + " " + std::to_string(BH) + " " +
-                                              std::to_string(D),
-                                          prm.order);
+        prm.order_len = plan_launch_order(PlanKey{2, N, BH, D, 0}, kFixedSteps, num_sms, [&] {
+            std::vector<int> w(static_cast<size_t>(blocks));
+            for (int sl = 0; sl < nblk; ++sl)
+                for (int64_t h = 0; h < BH; ++h) w[static_cast<size_t>(sl) * BH + h] = nblk - sl;
+            return w;
+        }, prm.order);
     }
     attn_bwd_dq_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, QLay<D>::kSmem, stream>>>(
         mq, mk, mv, mdo, prm);

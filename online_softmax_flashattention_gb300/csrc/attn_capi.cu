@@ -58,15 +58,25 @@ int check_common(const void* q, const void* k, const void* v, const void* o, int
     return ATTN_OK;
 }
 
-// The kernels are built for sm_103a only; any other device is refused up front.
+// The kernels are built for sm_103a only; any other device is refused up front. The compute
+// capability and SM count of each device ordinal are read once and kept.
 int check_device(int* num_sms) {
-    int dev = 0, major = 0, minor = 0;
+    constexpr int kMaxDev = 64;
+    static int sms_of[kMaxDev];  // 0: not read yet, -1: not an sm_103 device, else the SM count
+    int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return ATTN_ERR_DEVICE;
-    if (major != 10 || minor != 3) return ATTN_ERR_DEVICE;
+    int known = (dev >= 0 && dev < kMaxDev) ? __atomic_load_n(&sms_of[dev], __ATOMIC_ACQUIRE) : 0;
+    if (known == 0) {
+        int major = 0, minor = 0, n = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_DEVICE;
+        known = (major == 10 && minor == 3 && n > 0) ? n : -1;
+        if (dev >= 0 && dev < kMaxDev) __atomic_store_n(&sms_of[dev], known, __ATOMIC_RELEASE);
+    }
+    if (known < 0) return ATTN_ERR_DEVICE;
+    *num_sms = known;
     return ATTN_OK;
 }
 
@@ -278,8 +288,10 @@ const char* attn_status_string(int status) {
 }
 
 int attn_plan_launch_order(const int32_t* weights, int64_t n, int32_t fixed, int32_t num_sms, uint16_t* order) {
-    if (!weights || !order || n < 1 || n > 65536 || fixed < 0 || fixed > (1 << 24) || num_sms < 1 ||
-        num_sms > 4096)
+    // Each capacity try costs n * num_sms steps; the bounds keep the whole search well under a
+    // second (the kernels plan at most 2048 items over the device's SMs).
+    if (!weights || !order || n < 1 || n > 8192 || fixed < 0 || fixed > (1 << 24) || num_sms < 1 ||
+        num_sms > 1024 || n * num_sms > (int64_t{1} << 20))
         return ATTN_ERR_INVALID_ARG;
     std::vector<int> w(static_cast<size_t>(n));
     for (int64_t i = 0; i < n; ++i) {

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <functional>
 #include <string>
 #include <vector>
 
@@ -34,16 +35,45 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, co
                   void* dq, void* dk, void* dv, int64_t BH, int64_t N, int64_t d, bool causal, bool bf16,
                   int num_sms, cudaStream_t stream);
 
+// Identifies one launch-order plan: the kernel (kind), its shape and any tile sizes that change
+// the item weights. Plans are cached per key, SM count and fixed cost.
+struct PlanKey {
+    int kind;
+    int64_t n;
+    int64_t bh;
+    int a;
+    int b;
+    bool operator<(const PlanKey& o) const {
+        if (kind != o.kind) return kind < o.kind;
+        if (n != o.n) return n < o.n;
+        if (bh != o.bh) return bh < o.bh;
+        if (a != o.a) return a < o.a;
+        return b < o.b;
+    }
+};
+
 // Launch order for a grid of work items of unequal length, one CTA resident per SM at a time
 // (the hardware gives the next block to the first SM that frees up; attn_plan.cu): a
 // best-fit-decreasing packing of the items, weight[i] + fixed each, into num_sms bins at the
 // smallest capacity that packs (tried upward from the even split, the step doubling after 64
 // tries), then the items in order of their start time in that packing. Writes the permutation
-// (block -> item) to out and returns its length. Plans are cached by `key` (at most 256 keys,
-// thread-safe); weights.size() must not exceed 65536.
-int plan_launch_order(const std::vector<int>& weights, int fixed, int num_sms, const std::string& key, uint16_t* out);
+// (block -> item) to out and returns its length. Plans are cached by key (at most 256 plans,
+// thread-safe); `weights` is called only on a cache miss and must return at most 65536 weights.
+int plan_launch_order(const PlanKey& key, int fixed, int num_sms, const std::function<std::vector<int>()>& weights,
+                      uint16_t* out);
 // The same plan without the cache (for the attn_plan_launch_order entry point).
 std::vector<uint16_t> plan_order_compute(const std::vector<int>& weights, int fixed, int num_sms);
+
+// The same packing for persistent grids: the items of bin b (one bin per persistent CTA or
+// cluster) are order[bin_start[b] .. bin_start[b+1]), in order of their start in the packing.
+// The item count must not exceed 65536 and bins must be at least 1.
+void plan_bins_compute(const std::vector<int>& weights, int fixed, int bins, std::vector<uint16_t>& order,
+                       std::vector<uint16_t>& bin_start);
+
+// Runs `setup` once per device ordinal (0..63) for the calling site's `done` mask: the first call on
+// a device runs it under a lock and records success; later calls return at once. Returns false if
+// setup failed (it is then tried again on the next call).
+bool once_per_device(uint64_t* done, int dev, const std::function<bool()>& setup);
 
 // Reads (and optionally clears) the tensor-core backward kernels' device error word.
 int bwd_tc_device_error(bool clear, unsigned* err);

@@ -703,33 +703,75 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t N, int64_t 
 // at B1 H12 N8192 it finishes about 107 steps in, the packing about 98.)
 constexpr int kFixedSteps = 5;
 
+// The three tensor maps of a call depend only on the pointers and the shape, so the last few
+// calls' maps are kept (a small cache shared by all threads, behind a lock).
+struct FwdMaps {
+    const void* q;
+    const void* k;
+    const void* v;
+    int64_t BH, N;
+    int D;
+    bool bf16;
+    CUtensorMap mq, mk, mv;
+};
+
+bool fwd_maps(const void* q, const void* k, const void* v, int64_t BH, int64_t N, int D, int kv_rows, bool bf16,
+              CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv) {
+    constexpr int kSlots = 8;
+    static std::mutex mu;
+    static FwdMaps slots[kSlots];
+    static int used = 0, next = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i) {
+        const FwdMaps& e = slots[i];
+        if (e.q == q && e.k == k && e.v == v && e.BH == BH && e.N == N && e.D == D && e.bf16 == bf16) {
+            *mq = e.mq;
+            *mk = e.mk;
+            *mv = e.mv;
+            return true;
+        }
+    }
+    FwdMaps e{q, k, v, BH, N, D, bf16, {}, {}, {}};
+    if (!make_map(&e.mq, q, BH, N, D, kBM, bf16) || !make_map(&e.mk, k, BH, N, D, kv_rows, bf16) ||
+        !make_map(&e.mv, v, BH, N, D, kv_rows, bf16))
+        return false;
+    slots[next] = e;
+    next = (next + 1) % kSlots;
+    used = used < kSlots ? used + 1 : kSlots;
+    *mq = e.mq;
+    *mk = e.mk;
+    *mv = e.mv;
+    return true;
+}
+
 template <bool BF16, int D>
 int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t BH,
                 int64_t N, bool causal, int num_sms, cudaStream_t stream) {
     constexpr int kSmemBytes = Lay<D>::kSmemBytes;
-    // The register split assumes the launch allocation; a smaller one could leave the
-    // softmax groups waiting for registers forever, so it is refused instead.
-    cudaFuncAttributes fattr;
-    if (cudaFuncGetAttributes(&fattr, attn_fwd_tc_kernel<BF16, D>) != cudaSuccess ||
-        fattr.numRegs < kRegsLaunch) {
-        if (std::getenv("ATTN_DEBUG"))
-            std::fprintf(stderr, "attn: kernel has %d registers per thread, the register split needs %d\n",
-                         fattr.numRegs, kRegsLaunch);
-        return ATTN_ERR_LAUNCH;
-    }
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, BH, N, D, kBM, BF16) || !make_map(&mk, k, BH, N, D, Lay<D>::kBN, BF16) ||
-        !make_map(&mv, v, BH, N, D, Lay<D>::kBN, BF16))
-        return ATTN_ERR_DEVICE;
-    // The attribute is per device; setting it on every call is cheap and thread-safe.
-    const cudaError_t aerr = cudaFuncSetAttribute(attn_fwd_tc_kernel<BF16, D>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (aerr != cudaSuccess) {
-        if (std::getenv("ATTN_DEBUG"))
+    // Once per device: the register split assumes the launch allocation (a smaller one could
+    // leave the softmax groups waiting for registers forever, so it is refused instead), and the
+    // shared-memory grant.
+    static uint64_t ready = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
+    const bool ok = once_per_device(&ready, dev, [] {
+        cudaFuncAttributes fattr;
+        if (cudaFuncGetAttributes(&fattr, attn_fwd_tc_kernel<BF16, D>) != cudaSuccess || fattr.numRegs < kRegsLaunch) {
+            if (std::getenv("ATTN_DEBUG"))
+                std::fprintf(stderr, "attn: kernel has %d registers per thread, the register split needs %d\n",
+                             fattr.numRegs, kRegsLaunch);
+            return false;
+        }
+        const cudaError_t aerr = cudaFuncSetAttribute(attn_fwd_tc_kernel<BF16, D>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (aerr != cudaSuccess && std::getenv("ATTN_DEBUG"))
             std::fprintf(stderr, "attn: cannot grant %d bytes of shared memory: %s\n", kSmemBytes,
                          cudaGetErrorString(aerr));
-        return ATTN_ERR_LAUNCH;
-    }
+        return aerr == cudaSuccess;
+    });
+    if (!ok) return ATTN_ERR_LAUNCH;
+    CUtensorMap mq, mk, mv;
+    if (!fwd_maps(q, k, v, BH, N, D, Lay<D>::kBN, BF16, &mq, &mk, &mv)) return ATTN_ERR_DEVICE;
     TcParams prm;
     prm.o = o;
     prm.lse = lse;
@@ -744,16 +786,19 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
     if (causal && blocks <= kOrderMax && num_sms > 0) {
         // Item pair * BH + head weighs its key-tile steps, max(nA, nB) as the kernel counts them.
         constexpr int BN = Lay<D>::kBN;
-        const int nkv = static_cast<int>((N + BN - 1) / BN);
-        std::vector<int> w(static_cast<size_t>(blocks));
-        for (int pr = 0; pr < prm.num_pairs; ++pr) {
-            const int rowA = pr * 2 * kBM, rowB = rowA + kBM;
-            const int nA = std::min(nkv, (rowA + kBM - 1) / BN + 1);
-            const int nB = rowB < N ? std::min(nkv, (rowB + kBM - 1) / BN + 1) : 0;
-            for (int h = 0; h < prm.BH; ++h) w[static_cast<size_t>(pr) * prm.BH + h] = std::max(nA, nB);
-        }
-        const std::string key = "fwd " + std::to_string(N) + " " + std::to_string(BH) + " " + std::to_string(BN);
-        prm.order_len = plan_launch_order(w, kFixedSteps, num_sms, key, prm.order);
+        const PlanKey key{0, N, BH, BN, 0};
+        const int num_pairs = prm.num_pairs;
+        prm.order_len = plan_launch_order(key, kFixedSteps, num_sms, [&] {
+            const int nkv = static_cast<int>((N + BN - 1) / BN);
+            std::vector<int> w(static_cast<size_t>(blocks));
+            for (int pr = 0; pr < num_pairs; ++pr) {
+                const int rowA = pr * 2 * kBM, rowB = rowA + kBM;
+                const int nA = std::min(nkv, (rowA + kBM - 1) / BN + 1);
+                const int nB = rowB < N ? std::min(nkv, (rowB + kBM - 1) / BN + 1) : 0;
+                for (int64_t h = 0; h < BH; ++h) w[static_cast<size_t>(pr) * BH + h] = std::max(nA, nB);
+            }
+            return w;
+        }, prm.order);
     }
     attn_fwd_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, kSmemBytes, stream>>>(
         mq, mk, mv, prm);

@@ -97,6 +97,20 @@ def test_large_weights_end_quickly():
     assert list_schedule(w, order, 1 << 24, 152) <= even + 2 * (2 << 24)
 
 
+@pytest.mark.parametrize("n,bins", [(8192, 128), (2048, 512)])
+def test_largest_accepted_input_is_cheap(n, bins):
+    # the largest inputs the bounds accept, with the largest weights, plan in well under a second
+    import random
+    import time
+
+    rng = random.Random(n + bins)
+    w = [rng.randrange(1 << 24) for _ in range(n)]
+    t0 = time.perf_counter()
+    order = fa.attn_plan_launch_order(w, 1 << 24, bins)
+    assert time.perf_counter() - t0 < 3.0
+    assert sorted(order) == list(range(n))
+
+
 def test_invalid_arguments():
     import ctypes
 
@@ -108,10 +122,15 @@ def test_invalid_arguments():
     assert lib.attn_plan_launch_order(None, 3, 0, 4, op) == 1
     assert lib.attn_plan_launch_order(wp, 3, 0, 4, None) == 1
     assert lib.attn_plan_launch_order(wp, 0, 0, 4, op) == 1
-    assert lib.attn_plan_launch_order(wp, 65537, 0, 4, op) == 1
+    assert lib.attn_plan_launch_order(wp, 8193, 0, 4, op) == 1
     assert lib.attn_plan_launch_order(wp, 3, -1, 4, op) == 1
     assert lib.attn_plan_launch_order(wp, 3, 0, 0, op) == 1
-    assert lib.attn_plan_launch_order(wp, 3, 0, 4097, op) == 1
+    assert lib.attn_plan_launch_order(wp, 3, 0, 1025, op) == 1
+    big = (ctypes.c_int32 * 2049)()
+    bigo = (ctypes.c_uint16 * 2049)()
+    # 2049 items over 512 bins exceeds the n * num_sms bound of 2^20
+    assert lib.attn_plan_launch_order(ctypes.cast(big, ctypes.c_void_p), 2049, 0, 512,
+                                      ctypes.cast(bigo, ctypes.c_void_p)) == 1
     assert lib.attn_plan_launch_order(wp, 3, (1 << 24) + 1, 4, op) == 1
     bad = (ctypes.c_int32 * 3)(1, -2, 3)
     assert lib.attn_plan_launch_order(ctypes.cast(bad, ctypes.c_void_p), 3, 0, 4, op) == 1
