@@ -271,12 +271,27 @@ int attn_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
  */
 int attn_plan_launch_order(const int32_t* weights, int64_t n, int32_t fixed, int32_t num_sms, uint16_t* order);
 
+/*
+ * attn_probe_fp32_fma — the fp32 roofline that the FFMA (float32) kernels are measured against,
+ * taken on the device itself (the pages give no fp32 peak for it; their own kernels ran on
+ * CUDA cores). Enqueues one kernel of one 1024-thread block per SM in which every thread runs 8
+ * independent chains of `iters` fused multiply-adds, and writes that launch's flop count
+ * (2 per multiply-add) to *flop on the host; the caller times the launch with CUDA events on
+ * `stream` and divides. Not a step of the attention path.
+ *   sink        : device buffer of sink_floats float32, at least SMs x 1024 (each thread writes
+ *                 one value so the chains are not optimised away); ATTN_ERR_WORKSPACE if smaller
+ *   iters       : 1 .. 2^24
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_DEVICE off sm_103, ATTN_ERR_LAUNCH.
+ */
+int attn_probe_fp32_fma(float* sink, int64_t sink_floats, int64_t iters, double* flop, void* stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* attn_status_string(int status);
 
 /* ABI version of this header: (major << 16) | minor (1.1 added attn_fwd_lse, 1.2 attn_bwd,
  * 1.3 attn_fwd_kvcache, 1.4 head width 128 for the forward entry points, 1.5
- * attn_selftest_wait_timeout, 1.6 head width 128 for attn_bwd, 1.7 attn_plan_launch_order). */
+ * attn_selftest_wait_timeout, 1.6 head width 128 for attn_bwd, 1.7 attn_plan_launch_order, 1.8
+ * attn_probe_fp32_fma). */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

@@ -177,3 +177,14 @@ def test_selftest_limit_is_checked_before_the_device(lib):
     assert lib.attn_selftest_wait_timeout(3_000_000_000, None) == 1  # above 2 s
     if not __import__("torch").cuda.is_available():
         assert lib.attn_selftest_wait_timeout(1_000_000, None) == 5
+
+
+def test_fma_probe_checks_before_the_device(lib):
+    import ctypes
+
+    flop = ctypes.c_double(0.0)
+    fp = ctypes.byref(flop)
+    assert lib.attn_probe_fp32_fma(None, 1 << 20, 16, fp, None) == 1      # no sink
+    assert lib.attn_probe_fp32_fma(P, 1 << 20, 0, fp, None) == 1          # iters < 1
+    assert lib.attn_probe_fp32_fma(P, 1 << 20, (1 << 24) + 1, fp, None) == 1
+    assert lib.attn_probe_fp32_fma(P, 1 << 20, 16, None, None) == 1       # no flop out
