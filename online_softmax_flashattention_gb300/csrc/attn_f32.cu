@@ -18,6 +18,13 @@
 // With an `lse` pointer each row's log-sum-exp is stored too, in base 2 as the page's
 // forward kernel keeps it for the backward pass (m + log2 l, "Backwards, and training with
 // it").
+//
+// Small grids (fewer blocks than the GPU has SMs to fill, e.g. one head of 4096 queries) split
+// the keys inside the CTA: G groups of BM*4 threads share the Q tile and each takes the key tiles
+// t = g, g + G, ... with a running max, total and output of its own (the online softmax over a
+// subset of the keys), synchronising on a named barrier of its own; at the end the groups'
+// partial results merge as the online softmax merges tiles: M = max m_g, o = sum 2^(m_g - M)
+// O_g / sum 2^(m_g - M) l_g.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -40,22 +47,33 @@ __device__ __forceinline__ float ex2f(float x) {
     return y;
 }
 
-template <int BM, int D>
-__global__ void __launch_bounds__(BM * 4)
+// Group-local barrier (G > 1) or the whole CTA (G = 1).
+template <int G, int kThreads>
+__device__ __forceinline__ void group_sync(int grp) {
+    if constexpr (G == 1) {
+        __syncthreads();
+    } else {
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kThreads) : "memory");
+    }
+}
+
+template <int BM, int D, int G>
+__global__ void __launch_bounds__(BM * 4 * G)
     attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                         const float* __restrict__ v, float* __restrict__ o, float* __restrict__ lse,
                         int N, int BH, int nblk, int causal, float c) {
-    constexpr int kThreads = BM * 4;
+    constexpr int kThreads = BM * 4;  // one group
     constexpr int kLd = ld_of<D>();
     constexpr int kD4 = D / 4;   // float4 per row
     constexpr int kG = D / 64;   // 64-dim groups of this thread's output columns
     extern __shared__ float4 smem4[];
+    const int grp = static_cast<int>(threadIdx.x) / kThreads;
     float* const Qs = reinterpret_cast<float*>(smem4);
-    float* const Ks = Qs + BM * kLd;
+    float* const Ks = Qs + BM * kLd + grp * (2 * kBN + BM) * kLd;
     float* const Vs = Ks + kBN * kLd;
     float* const Ps = Vs + kBN * kLd;
 
-    const int tid = threadIdx.x;
+    const int tid = static_cast<int>(threadIdx.x) % kThreads;
     const int tx = tid & 15;
     const int ty = tid >> 4;
     const int bh = static_cast<int>(blockIdx.x % static_cast<unsigned>(BH));
@@ -67,8 +85,8 @@ __global__ void __launch_bounds__(BM * 4)
     const float* kh = k + head;
     const float* vh = v + head;
 
-    // Q tile, rows >= N read as zero.
-    for (int idx = tid; idx < BM * kD4; idx += kThreads) {
+    // Q tile, rows >= N read as zero (all groups load it together).
+    for (int idx = static_cast<int>(threadIdx.x); idx < BM * kD4; idx += kThreads * G) {
         const int r = idx / kD4, e4 = idx % kD4;
         float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
         if (row0 + r < N) val = *reinterpret_cast<const float4*>(qh + static_cast<int64_t>(row0 + r) * D + 4 * e4);
@@ -84,11 +102,12 @@ __global__ void __launch_bounds__(BM * 4)
         for (int j = 0; j < 4 * kG; ++j) acc[i][j] = 0.f;
     }
 
+    if constexpr (G > 1) __syncthreads();  // Q is in
     const int kend = causal ? min(N, row0 + BM) : N;
     const int ntiles = (kend + kBN - 1) / kBN;
-    for (int t = 0; t < ntiles; ++t) {
+    for (int t = grp; t < ntiles; t += G) {
         const int kbase = t * kBN;
-        __syncthreads();  // the previous tile's products are done with Ks, Vs and Ps
+        group_sync<G, kThreads>(grp);  // the previous tile's products are done with Ks, Vs and Ps
         for (int idx = tid; idx < kBN * kD4; idx += kThreads) {
             const int r = idx / kD4, e4 = idx % kD4;
             float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
@@ -100,7 +119,7 @@ __global__ void __launch_bounds__(BM * 4)
             *reinterpret_cast<float4*>(Ks + r * kLd + 4 * e4) = kv;
             *reinterpret_cast<float4*>(Vs + r * kLd + 4 * e4) = vv;
         }
-        __syncthreads();
+        group_sync<G, kThreads>(grp);
 
         // S micro-tile: rows ty*4+i, keys tx+16j.
         float s[4][4];
@@ -159,7 +178,7 @@ __global__ void __launch_bounds__(BM * 4)
 #pragma unroll
             for (int j = 0; j < 4 * kG; ++j) acc[i][j] *= alpha;
         }
-        __syncthreads();
+        group_sync<G, kThreads>(grp);
 
         // O micro-tile += P V: rows ty*4+i, dims 64g + tx*4+j.
 #pragma unroll 4
@@ -188,37 +207,91 @@ __global__ void __launch_bounds__(BM * 4)
         }
     }
 
-    // Row totals across the 16 threads of the row, then O / l.
+    // Row totals across the 16 threads of the row.
+    float tot[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        float tot = l[i];
+        tot[i] = l[i];
 #pragma unroll
-        for (int off = 8; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        for (int off = 8; off > 0; off >>= 1) tot[i] += __shfl_xor_sync(0xffffffffu, tot[i], off);
+    }
+    if constexpr (G > 1) {
+        // Merge the groups' partial results into group 0 through shared memory (the K/V/P tiles
+        // are free once every group is past its last tile). A group with no key tile, or whose
+        // rows saw no key yet, has m = -inf and l = 0 and contributes nothing.
+        __syncthreads();
+        float* const X = reinterpret_cast<float*>(smem4) + BM * kLd;  // [G][kThreads][4 * (4 kG + 2)]
+        constexpr int kRec = 4 * (4 * kG + 2);
+        float* const mine = X + (grp * kThreads + tid) * kRec;
+        if (grp > 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                mine[i * (4 * kG + 2)] = m[i];
+                mine[i * (4 * kG + 2) + 1] = tot[i];
+#pragma unroll
+                for (int j = 0; j < 4 * kG; ++j) mine[i * (4 * kG + 2) + 2 + j] = acc[i][j];
+            }
+        }
+        __syncthreads();
+        if (grp > 0) return;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float M = m[i];
+#pragma unroll
+            for (int h = 1; h < G; ++h) M = fmaxf(M, X[(h * kThreads + tid) * kRec + i * (4 * kG + 2)]);
+            const float a0 = (m[i] == -INFINITY) ? 0.f : ex2f(m[i] - M);
+            tot[i] *= a0;
+#pragma unroll
+            for (int j = 0; j < 4 * kG; ++j) acc[i][j] *= a0;
+#pragma unroll
+            for (int h = 1; h < G; ++h) {
+                const float* r = X + (h * kThreads + tid) * kRec + i * (4 * kG + 2);
+                const float a = (r[0] == -INFINITY) ? 0.f : ex2f(r[0] - M);
+                tot[i] = fmaf(r[1], a, tot[i]);
+#pragma unroll
+                for (int j = 0; j < 4 * kG; ++j) acc[i][j] = fmaf(r[2 + j], a, acc[i][j]);
+            }
+            m[i] = M;
+        }
+    }
+    // O / l.
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
         const int row = row0 + ty * 4 + i;
         if (row < N) {
-            const float inv = 1.f / tot;
+            const float inv = 1.f / tot[i];
 #pragma unroll
             for (int g = 0; g < kG; ++g)
                 *reinterpret_cast<float4*>(o + head + static_cast<int64_t>(row) * D + 64 * g + 4 * tx) =
                     make_float4(acc[i][4 * g] * inv, acc[i][4 * g + 1] * inv, acc[i][4 * g + 2] * inv,
                                 acc[i][4 * g + 3] * inv);
-            if (lse != nullptr && tx == 0) lse[static_cast<int64_t>(bh) * N + row] = m[i] + log2f(tot);
+            if (lse != nullptr && tx == 0) lse[static_cast<int64_t>(bh) * N + row] = m[i] + log2f(tot[i]);
         }
     }
 }
 
-template <int BM, int D>
+template <int BM, int D, int G>
 int launch_bm(const float* q, const float* k, const float* v, float* o, float* lse, int64_t BH,
               int64_t N, bool causal, cudaStream_t stream) {
-    const int smem = (2 * BM + 2 * kBN) * ld_of<D>() * static_cast<int>(sizeof(float));
-    if (cudaFuncSetAttribute(attn_fwd_f32_kernel<BM, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
+    // Q, then per group K, V and P tiles; the groups' merge records reuse the K/V/P space.
+    constexpr int kLd = ld_of<D>();
+    constexpr int kTiles = (BM + G * (2 * kBN + BM)) * kLd * static_cast<int>(sizeof(float));
+    constexpr int kMerge = (BM * kLd + G * BM * 4 * 4 * (4 * (D / 64) + 2)) * static_cast<int>(sizeof(float));
+    constexpr int smem = kTiles > kMerge ? kTiles : kMerge;
+    static_assert(smem <= 227 * 1024, "shared memory of one CTA");
+    static uint64_t ready = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
+    if (!once_per_device(&ready, dev, [] {
+            return cudaFuncSetAttribute(attn_fwd_f32_kernel<BM, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem) == cudaSuccess;
+        }))
         return ATTN_ERR_LAUNCH;
     const int64_t nblk = (N + BM - 1) / BM;
     const int64_t blocks = nblk * BH;
     if (blocks > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     const float c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-    attn_fwd_f32_kernel<BM, D><<<static_cast<unsigned>(blocks), BM * 4, smem, stream>>>(
+    attn_fwd_f32_kernel<BM, D, G><<<static_cast<unsigned>(blocks), BM * 4 * G, smem, stream>>>(
         q, k, v, o, lse, static_cast<int>(N), static_cast<int>(BH), static_cast<int>(nblk), causal ? 1 : 0, c);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
@@ -228,15 +301,20 @@ int launch_bm(const float* q, const float* k, const float* v, float* o, float* l
 int launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int64_t BH,
                    int64_t N, int64_t d, bool causal, int num_sms, cudaStream_t stream) {
     if (N > 0x7FFFFFFFll - 64 || BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
-    // Small problems use 32-row blocks so that more SMs get work.
+    // Grids that fill the GPU run 64-row blocks; smaller ones 32-row blocks, and when even those
+    // leave most SMs with a single block, the keys are split over G groups inside each block.
     const int64_t blocks64 = ((N + 63) / 64) * BH;
+    const int64_t blocks32 = ((N + 31) / 32) * BH;
     const bool small = blocks64 < 2 * static_cast<int64_t>(num_sms);
+    const bool split = blocks32 < 2 * static_cast<int64_t>(num_sms) && N > 2 * kBN;
     if (d == 64)
-        return small ? launch_bm<32, 64>(q, k, v, o, lse, BH, N, causal, stream)
-                     : launch_bm<64, 64>(q, k, v, o, lse, BH, N, causal, stream);
+        return split ? launch_bm<32, 64, 4>(q, k, v, o, lse, BH, N, causal, stream)
+               : small ? launch_bm<32, 64, 1>(q, k, v, o, lse, BH, N, causal, stream)
+                       : launch_bm<64, 64, 1>(q, k, v, o, lse, BH, N, causal, stream);
     if (d == 128)
-        return small ? launch_bm<32, 128>(q, k, v, o, lse, BH, N, causal, stream)
-                     : launch_bm<64, 128>(q, k, v, o, lse, BH, N, causal, stream);
+        return split ? launch_bm<32, 128, 2>(q, k, v, o, lse, BH, N, causal, stream)
+               : small ? launch_bm<32, 128, 1>(q, k, v, o, lse, BH, N, causal, stream)
+                       : launch_bm<64, 128, 1>(q, k, v, o, lse, BH, N, causal, stream);
     return ATTN_ERR_UNSUPPORTED;
 }
 
