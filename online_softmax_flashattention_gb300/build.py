@@ -22,7 +22,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libattn.so")
 SOURCES = ["attn_capi.cu", "attn_f32.cu", "attn_tc.cu", "attn_plan.cu", "attn_materialized.cu", "attn_materialized_noalloc.cu",
-           "attn_bwd.cu", "attn_bwd_tc.cu", "attn_decode.cu", "attn_probe.cu"]
+           "attn_bwd.cu", "attn_bwd_tc.cu", "attn_decode.cu", "attn_decode_tc.cu", "attn_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-strict-aliasing",
               "--expt-relaxed-constexpr"]

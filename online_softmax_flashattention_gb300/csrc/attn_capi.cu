@@ -264,12 +264,13 @@ int attn_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
 }
 
 int attn_device_status(void* stream, int clear) {
-    unsigned err = 0, berr = 0, derr = 0;
+    unsigned err = 0, berr = 0, derr = 0, dterr = 0;
     int st = attn::tc_device_error(static_cast<cudaStream_t>(stream), clear != 0, &err);
     if (st != ATTN_OK) return st;
     if ((st = attn::bwd_tc_device_error(clear != 0, &berr)) != ATTN_OK) return st;
     if ((st = attn::decode_device_error(clear != 0, &derr)) != ATTN_OK) return st;
-    return (err || berr || derr) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    if ((st = attn::decode_tc_device_error(clear != 0, &dterr)) != ATTN_OK) return st;
+    return (err || berr || derr || dterr) ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 const char* attn_status_string(int status) {

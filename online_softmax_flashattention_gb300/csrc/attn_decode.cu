@@ -45,6 +45,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "attn_decode_common.cuh"
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -146,75 +147,6 @@ __device__ __forceinline__ void store2<__nv_bfloat16>(__nv_bfloat16* p, float a,
 template <>
 __device__ __forceinline__ void store2<__half>(__half* p, float a, float b) {
     *reinterpret_cast<__half2*>(p) = __floats2half2_rn(a, b);
-}
-
-struct DecodeParams {
-    const void* q;
-    void* o;
-    float* lse;       // null, or [BH, Nq]
-    float* part_o;    // [BH * Nq][P][D]
-    float* part_lse;  // [BH * Nq][P]
-    int Nq, Nk, BH;
-    int groups;           // query groups per head
-    int Tn;               // tiles per segment
-    int causal;
-    int explicit_splits;  // S >= 1: every segment in S shares; 0: balanced
-    int tps;              // explicit: tiles per share
-    int P;                // slot stride of the partials (S, or most pieces a segment can have)
-    int C;                // CTAs in the grid
-    int64_t G;            // balanced: segments * Tn
-    float c;              // log2(e) / sqrt(D)
-};
-
-struct Piece {
-    int bh, g0, ng;  // head, first query of the group, queries in the group
-    int t0, t1;      // tiles [t0, t1) of the segment, already clipped to the visible keys
-    int ke;          // the segment's visible keys end before ke
-    int slot, nslots;
-};
-
-// Balanced mode: the CTA whose run holds global tile t.
-__device__ __host__ __forceinline__ int64_t owner_of(int64_t t, int64_t C, int64_t G) {
-    return ((t + 1) * C - 1) / G;
-}
-
-// The k-th piece of CTA `cta` (tiles of ROWS keys); false once the CTA has no more.
-template <int QG, int ROWS>
-__device__ __forceinline__ bool get_piece(const DecodeParams& p, int cta, int k, Piece& pc) {
-    int64_t seg;
-    int t0, t1;
-    if (p.explicit_splits > 0) {
-        const int64_t idx = static_cast<int64_t>(cta) + static_cast<int64_t>(k) * p.C;
-        const int64_t nseg = static_cast<int64_t>(p.BH) * p.groups;
-        if (idx >= nseg * p.explicit_splits) return false;
-        seg = idx / p.explicit_splits;
-        const int share = static_cast<int>(idx % p.explicit_splits);
-        t0 = min(p.Tn, share * p.tps);
-        t1 = min(p.Tn, t0 + p.tps);
-        pc.slot = share;
-        pc.nslots = p.explicit_splits;
-    } else {
-        const int64_t A = static_cast<int64_t>(cta) * p.G / p.C;
-        const int64_t Bend = (static_cast<int64_t>(cta) + 1) * p.G / p.C;
-        if (A >= Bend) return false;
-        seg = A / p.Tn + k;
-        const int64_t s0 = seg * p.Tn;
-        if (s0 >= Bend) return false;
-        const int64_t a = max(A, s0), b = min(Bend, s0 + p.Tn);
-        t0 = static_cast<int>(a - s0);
-        t1 = static_cast<int>(b - s0);
-        const int64_t first = owner_of(s0, p.C, p.G), last = owner_of(s0 + p.Tn - 1, p.C, p.G);
-        pc.slot = static_cast<int>(cta - first);
-        pc.nslots = static_cast<int>(last - first + 1);
-    }
-    pc.bh = static_cast<int>(seg / p.groups);
-    pc.g0 = static_cast<int>(seg % p.groups) * QG;
-    pc.ng = min(QG, p.Nq - pc.g0);
-    pc.ke = p.causal ? min(p.Nk, p.Nk - p.Nq + pc.g0 + pc.ng) : p.Nk;
-    const int tv = (pc.ke + ROWS - 1) / ROWS;  // tiles holding a visible key
-    pc.t0 = min(t0, tv);
-    pc.t1 = min(t1, tv);
-    return true;
 }
 
 template <typename T, int QG, int D>
@@ -652,8 +584,8 @@ struct Plan {
     bool merge;  // some segment has more than one piece
 };
 
-bool make_plan(int64_t BH, int64_t Nq, int64_t Nk, int rows, int splits, int num_sms, int per_sm, Plan* pl) {
-    pl->qg = queries_per_group(Nq);
+bool make_plan(int64_t BH, int64_t Nq, int64_t Nk, int rows, int splits, int num_sms, int per_sm, int qg, Plan* pl) {
+    pl->qg = qg;
     pl->groups = static_cast<int>((Nq + pl->qg - 1) / pl->qg);
     pl->rows = rows;
     pl->Tn = static_cast<int>((Nk + rows - 1) / rows);
@@ -685,8 +617,13 @@ size_t partial_bytes(int64_t BH, int64_t Nq, int64_t D, int64_t P) {
     return (r * static_cast<size_t>(D) * sizeof(float) + 255) / 256 * 256 + (r * sizeof(float) + 255) / 256 * 256;
 }
 
+// Two or more new queries in bf16/fp16 at head width 64 run on the tensor-core kernel
+// (attn_decode_tc.cu): groups of up to 128 queries as one M128 tile, 128-key tiles, one CTA per SM.
+bool use_tc(int dtype, int64_t d, int64_t Nq) { return dtype != ATTN_F32 && d == 64 && Nq >= 2; }
+
 // Builds the plan of a call: the kernel's tile rows and occupancy come from its configuration.
 bool plan_for(int64_t BH, int64_t Nq, int64_t Nk, int64_t D, int splits, int dtype, int num_sms, Plan* pl) {
+    if (use_tc(dtype, D, Nq)) return make_plan(BH, Nq, Nk, 128, splits, num_sms, 1, 128, pl);
     int rows = 0, per_sm = 0;
     visit_cfg(dtype, D, queries_per_group(Nq), [&](auto t, auto qg, auto dd) -> int {
         using T = typename decltype(t)::type;
@@ -695,7 +632,27 @@ bool plan_for(int64_t BH, int64_t Nq, int64_t Nk, int64_t D, int splits, int dty
         return 0;
     });
     if (per_sm <= 0) return false;
-    return make_plan(BH, Nq, Nk, rows, splits, num_sms, per_sm, pl);
+    return make_plan(BH, Nq, Nk, rows, splits, num_sms, per_sm, queries_per_group(Nq), pl);
+}
+
+// Programmatic stream serialisation: the merge grid may start while the main grid runs (it is
+// released by the main kernel's launch_dependents) and waits in griddepcontrol.wait until that
+// grid has completed and its memory is visible.
+template <typename T, int QG, int D>
+int launch_merge(const DecodeParams& prm, cudaStream_t stream) {
+    const int64_t rows = static_cast<int64_t>(prm.BH) * prm.Nq;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_decode_merge_kernel<T, QG, D>, prm, rows) == cudaSuccess ? ATTN_OK
+                                                                                                  : ATTN_ERR_LAUNCH;
 }
 
 }  // namespace
@@ -764,6 +721,14 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
     CUtensorMap mk, mv;
     if (!make_map(&mk, k, BH, Nk, d, dtype, pl.rows) || !make_map(&mv, v, BH, Nk, d, dtype, pl.rows))
         return ATTN_ERR_DEVICE;
+    if (use_tc(dtype, d, Nq)) {
+        CUtensorMap mq;
+        if (!make_map(&mq, q, BH, Nq, d, dtype, 128)) return ATTN_ERR_DEVICE;
+        const int st = launch_decode_tc_main(mq, mk, mv, prm, dtype == ATTN_BF16, stream);
+        if (st != ATTN_OK || !pl.merge) return st;
+        return dtype == ATTN_BF16 ? launch_merge<__nv_bfloat16, 128, 64>(prm, stream)
+                                  : launch_merge<__half, 128, 64>(prm, stream);
+    }
     return visit_cfg(dtype, d, pl.qg, [&](auto t, auto qg, auto dd) -> int {
         using T = typename decltype(t)::type;
         constexpr int QG = decltype(qg)::value, D = decltype(dd)::value;
@@ -776,23 +741,7 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
                                        stream>>>(mk, mv, prm);
         if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
         if (!pl.merge) return ATTN_OK;
-        // Programmatic stream serialisation: the merge grid may start while the main grid runs
-        // (it is released by the main kernel's launch_dependents) and waits in griddepcontrol.wait
-        // until that grid has completed and its memory is visible.
-        const int64_t rows = static_cast<int64_t>(prm.BH) * prm.Nq;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
-        cfg.blockDim = dim3(128);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, attn_decode_merge_kernel<T, QG, D>, prm, rows) != cudaSuccess)
-            return ATTN_ERR_LAUNCH;
-        return ATTN_OK;
+        return launch_merge<T, QG, D>(prm, stream);
     });
 }
 

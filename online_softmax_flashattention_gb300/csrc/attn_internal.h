@@ -113,4 +113,7 @@ int launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream);
 // Reads (and optionally clears) the decode kernel's device error word.
 int decode_device_error(bool clear, unsigned* err);
 
+// Reads (and optionally clears) the tensor-core decode kernel's device error word.
+int decode_tc_device_error(bool clear, unsigned* err);
+
 }  // namespace attn

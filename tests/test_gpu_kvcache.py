@@ -212,3 +212,29 @@ def test_kvcache_noncausal_ignores_key_order():
     o2 = fa.attn_fwd_kvcache(qd, kd[:, :, perm].contiguous(), vd[:, :, perm].contiguous(), causal=False)
     torch.cuda.synchronize()
     assert float((o1 - o2).abs().max()) <= 1e-5
+
+
+@pytest.mark.parametrize("Nq", [2, 4, 8])
+def test_kvcache_tensor_core_decode_shape(Nq):
+    # A few new tokens per sequence against an 8192-key cache, B16 H12: 16-bit inputs at d = 64
+    # with two or more queries run on the tensor-core kernel (queries padded to a 128-row tile);
+    # balanced plan, every query row against the oracle.
+    B, H, Nk = 16, 12, 8192
+    q, k, v = _inputs(0xCAC3E000 + Nq, B, H, Nq, Nk, "bf16")
+    qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
+    o, lse = fa.attn_fwd_kvcache(qd, kd, vd, causal=True, lse=True)
+    torch.cuda.synchronize()
+    assert fa.attn_device_status(clear=True) == 0
+    ref_o, ref_lse = oracle.attn_fwd_kv(q, k, v, True)
+    check(o.float().cpu().numpy().astype(np.float64), ref_o, "bf16", Nk, f"decode B16H12 Nq{Nq} Nk8192")
+    assert float(np.max(np.abs(lse.cpu().numpy() - ref_lse))) <= _lse_bound(ref_lse)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(127, 300), (128, 128), (129, 1000), (200, 200), (300, 5000)])
+@pytest.mark.parametrize("splits", [0, 2])
+def test_kvcache_query_groups_of_128(dtype, causal, Nq, Nk, splits):
+    # The tensor-core kernel takes a head's queries 128 at a time: a group filling the tile, a
+    # ragged last group, several groups with the causal diagonal inside the cache, Nq == Nk.
+    _run(0xCAC3F000 + Nq * 7919 + Nk, 2, 2, Nq, Nk, dtype, causal, splits)
