@@ -70,6 +70,12 @@ TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_tc_bf16_causal_B1H12N
 DECODE = {"workload": "key-value cache decode, bf16, B16 H12 Nq1 Nk8192 d64 (one new token per sequence)",
           "B": 16, "H": 12, "Nq": 1, "Nk": 8192, "d": 64, "causal": True, "dtype": "bf16"}
 DECODE_SOURCE = os.path.join(ROOT, "online_softmax_flashattention_gb300", "csrc", "attn_decode.cu")
+# The same cache with eight new tokens per sequence (speculative or chunked decoding): 16-bit
+# inputs at d64 with two or more queries run on the tensor-core kernel.
+DECODE8 = {"workload": "key-value cache decode, bf16, B16 H12 Nq8 Nk8192 d64 (eight new tokens per sequence)",
+           "B": 16, "H": 12, "Nq": 8, "Nk": 8192, "d": 64, "causal": True, "dtype": "bf16"}
+DECODE8_SOURCE = os.path.join(ROOT, "online_softmax_flashattention_gb300", "csrc", "attn_decode_tc.cu")
+DECODE8_PROFILE = os.path.join(ROOT, "profiles", "attn_decode_tc_bf16_B16H12Nq8Nk8192.md")
 # Head width 128, reported beside the headline: the same causal forward at B1 H12 N8192 d128 bf16.
 WIDE = {"workload": "causal attention forward, bf16 in/out, fp32 accumulate, B1 H12 N8192 d128",
         "B": 1, "H": 12, "N": 8192, "d": 128, "causal": True, "dtype": "bf16"}
@@ -277,24 +283,22 @@ def cpu_baseline_leg(q, k, v, o_dev_rows_fn, target_s=15.0):
             {"rows_checked": int(len(flat)), "max_abs_err": err, "tolerance": 2e-2, "pass": bool(err <= 2e-2)})
 
 
-def make_decode_inputs(dev):
-    """Seeded N(0,1) inputs of the decode workload, drawn on the device (403 MB)."""
+def make_decode_inputs(dev, w=DECODE):
+    """Seeded N(0,1) inputs of a decode workload, drawn on the device (403 MB of K and V)."""
     import torch
 
-    w = DECODE
-    g = torch.Generator(device=dev).manual_seed(SEED + 11)
+    g = torch.Generator(device=dev).manual_seed(SEED + 11 + w["Nq"])
     q = torch.randn(w["B"], w["H"], w["Nq"], w["d"], generator=g, device=dev).to(torch.bfloat16)
     k = torch.randn(w["B"], w["H"], w["Nk"], w["d"], generator=g, device=dev).to(torch.bfloat16)
     v = torch.randn(w["B"], w["H"], w["Nk"], w["d"], generator=g, device=dev).to(torch.bfloat16)
     return q, k, v
 
 
-def decode_cpu_leg(q, k, v, o, lse, target_s=10.0):
-    """The oracle on a bounded sample of the decode workload's heads, timed on this host's
+def decode_cpu_leg(q, k, v, o, lse, target_s=10.0, w=DECODE):
+    """The oracle on a bounded sample of a decode workload's heads, timed on this host's
     cores; the GPU's o and lse at the same heads are compared on the side."""
     import oracle
 
-    w = DECODE
     bh = w["B"] * w["H"]
     qf = q.float().reshape(bh, w["Nq"], w["d"])
     kf = k.float().reshape(bh, w["Nk"], w["d"])
@@ -322,15 +326,15 @@ def decode_cpu_leg(q, k, v, o, lse, target_s=10.0):
              "max_abs_err_lse": err_l, "tolerance_lse": tol_l, "pass": bool(err_o <= 2e-2 and err_l <= tol_l)})
 
 
-def decode_leg(dev, stream, steps, warmup, with_cpu, cpu_seconds):
-    """The key-value cache path on the decode workload: K steps back to back between two events
+def decode_leg(dev, stream, steps, warmup, with_cpu, cpu_seconds, w=DECODE, source=DECODE_SOURCE,
+               profile=DECODE_PROFILE):
+    """The key-value cache path on a decode workload: K steps back to back between two events
     (inputs larger than L2, so no flush), balanced plan (num_splits = 0)."""
     import torch
 
     import online_softmax_flashattention_gb300 as fa
 
-    w = DECODE
-    q, k, v = make_decode_inputs(dev)
+    q, k, v = make_decode_inputs(dev, w)
     ws_bytes = fa.attn_kvcache_workspace_bytes(w["B"], w["H"], w["Nq"], w["Nk"], 0, torch.bfloat16, device=dev)
     ws = torch.empty(max(1, ws_bytes), dtype=torch.uint8, device=dev)
     o = torch.empty_like(q)
@@ -375,8 +379,8 @@ def decode_leg(dev, stream, steps, warmup, with_cpu, cpu_seconds):
     nbytes = decode_bytes(w["B"], w["H"], w["Nq"], w["Nk"], w["d"])
     peaks, peak_src = load_peaks()
     gbs = nbytes / (us * 1e-6) / 1e9
-    traffic, traffic_src = recorded_traffic(DECODE_PROFILE, DECODE_SOURCE)
-    out = {"config": dict(DECODE), "steps": steps, "us_per_step": us, "value": gbs, "unit": "GB/s",
+    traffic, traffic_src = recorded_traffic(profile, source)
+    out = {"config": dict(w), "steps": steps, "us_per_step": us, "value": gbs, "unit": "GB/s",
            "graph_replay": {"us_per_step": graph_us, "value": nbytes / (graph_us * 1e-6) / 1e9, "unit": "GB/s"},
            "l2": "not flushed: K and V (403 MB) exceed L2; steps run back to back",
            "launches_per_step": 2 if ws_bytes > 0 else 1,
@@ -385,7 +389,7 @@ def decode_leg(dev, stream, steps, warmup, with_cpu, cpu_seconds):
                         "peak_source": f"{peak_src} HBM copy", "traffic_source": traffic_src,
                         "algorithmic_bytes_per_launch": nbytes}}
     if with_cpu:
-        out["cpu_baseline"], out["parity"] = decode_cpu_leg(q, k, v, o, lse, cpu_seconds)
+        out["cpu_baseline"], out["parity"] = decode_cpu_leg(q, k, v, o, lse, cpu_seconds, w)
     del q, k, v, o, lse, ws
     return out
 
@@ -738,11 +742,13 @@ def run_ours(args, rank, world, local):
                                  "peak_source": "measured bf16 dense (burst)"}}
         del dout, ob, lse
 
-    decode = wide = fp32 = long_ctx = None
+    decode = decode8 = wide = fp32 = long_ctx = None
     if rank == 0 and not args.no_ablation:
         fp32 = fp32_leg(dev, stream, flush, 20, args.warmup, not args.no_cpu_baseline)
         long_ctx = long_context_leg(dev, stream, flush, not args.no_cpu_baseline)
         decode = decode_leg(dev, stream, 50, args.warmup, not args.no_cpu_baseline, min(args.cpu_seconds, 10.0))
+        decode8 = decode_leg(dev, stream, 50, args.warmup, not args.no_cpu_baseline, min(args.cpu_seconds, 5.0),
+                             DECODE8, DECODE8_SOURCE, DECODE8_PROFILE)
         wide = wide_leg(dev, stream, 30, args.warmup, flush, not args.no_cpu_baseline, min(args.cpu_seconds, 8.0))
 
     cpu = parity = None
@@ -784,6 +790,7 @@ def run_ours(args, rank, world, local):
         "ablation": ablation,
         "backward": backward,
         "decode": decode,
+        "decode_nq8": decode8,
         "d128": wide,
         "fp32": fp32,
         "long_context": long_ctx,
@@ -840,9 +847,9 @@ def run_profile(args):
 
     import online_softmax_flashattention_gb300 as fa
 
-    if args.profile_kernel == "decode":
-        w = DECODE
-        q, k, v = make_decode_inputs(torch.device("cuda", 0))
+    if args.profile_kernel in ("decode", "decode8"):
+        w = DECODE if args.profile_kernel == "decode" else DECODE8
+        q, k, v = make_decode_inputs(torch.device("cuda", 0), w)
         nb = fa.attn_kvcache_workspace_bytes(w["B"], w["H"], w["Nq"], w["Nk"], 0, torch.bfloat16)
         ws = torch.empty(max(1, nb), dtype=torch.uint8, device="cuda")
         o = torch.empty_like(q)
@@ -903,7 +910,7 @@ def main(argv=None):
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--profile", action="store_true", help="only launch the timed kernel (for ncu)")
     ap.add_argument("--profile-launches", type=int, default=4)
-    ap.add_argument("--profile-kernel", choices=["forward", "decode", "d128", "backward"], default="forward",
+    ap.add_argument("--profile-kernel", choices=["forward", "decode", "decode8", "d128", "backward"], default="forward",
                     help="which path --profile launches")
     args = ap.parse_args(argv)
     if args.warmup < 3:
