@@ -617,13 +617,13 @@ size_t partial_bytes(int64_t BH, int64_t Nq, int64_t D, int64_t P) {
     return (r * static_cast<size_t>(D) * sizeof(float) + 255) / 256 * 256 + (r * sizeof(float) + 255) / 256 * 256;
 }
 
-// Two or more new queries in bf16/fp16 at head width 64 run on the tensor-core kernel
-// (attn_decode_tc.cu): groups of up to 128 queries as one M128 tile, 128-key tiles, one CTA per SM.
-bool use_tc(int dtype, int64_t d, int64_t Nq) { return dtype != ATTN_F32 && d == 64 && Nq >= 2; }
+// Two or more new queries in bf16/fp16 run on the tensor-core kernel (attn_decode_tc.cu): groups
+// of up to 128 queries as one M128 tile, key tiles of 128 (d = 64) or 64 (d = 128), one CTA per SM.
+bool use_tc(int dtype, int64_t d, int64_t Nq) { return dtype != ATTN_F32 && (d == 64 || d == 128) && Nq >= 2; }
 
 // Builds the plan of a call: the kernel's tile rows and occupancy come from its configuration.
 bool plan_for(int64_t BH, int64_t Nq, int64_t Nk, int64_t D, int splits, int dtype, int num_sms, Plan* pl) {
-    if (use_tc(dtype, D, Nq)) return make_plan(BH, Nq, Nk, 128, splits, num_sms, 1, 128, pl);
+    if (use_tc(dtype, D, Nq)) return make_plan(BH, Nq, Nk, D == 64 ? 128 : 64, splits, num_sms, 1, 128, pl);
     int rows = 0, per_sm = 0;
     visit_cfg(dtype, D, queries_per_group(Nq), [&](auto t, auto qg, auto dd) -> int {
         using T = typename decltype(t)::type;
@@ -724,10 +724,13 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
     if (use_tc(dtype, d, Nq)) {
         CUtensorMap mq;
         if (!make_map(&mq, q, BH, Nq, d, dtype, 128)) return ATTN_ERR_DEVICE;
-        const int st = launch_decode_tc_main(mq, mk, mv, prm, dtype == ATTN_BF16, stream);
+        const int st = launch_decode_tc_main(mq, mk, mv, prm, dtype == ATTN_BF16, static_cast<int>(d), stream);
         if (st != ATTN_OK || !pl.merge) return st;
-        return dtype == ATTN_BF16 ? launch_merge<__nv_bfloat16, 128, 64>(prm, stream)
-                                  : launch_merge<__half, 128, 64>(prm, stream);
+        if (d == 64)
+            return dtype == ATTN_BF16 ? launch_merge<__nv_bfloat16, 128, 64>(prm, stream)
+                                      : launch_merge<__half, 128, 64>(prm, stream);
+        return dtype == ATTN_BF16 ? launch_merge<__nv_bfloat16, 128, 128>(prm, stream)
+                                  : launch_merge<__half, 128, 128>(prm, stream);
     }
     return visit_cfg(dtype, d, pl.qg, [&](auto t, auto qg, auto dd) -> int {
         using T = typename decltype(t)::type;

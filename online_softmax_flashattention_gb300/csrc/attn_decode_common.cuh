@@ -79,9 +79,10 @@ __device__ inline bool get_piece(const DecodeParams& p, int cta, int k, Piece& p
 }
 
 // Tensor-core decode (attn_decode_tc.cu): launches its main kernel over prm.C CTAs (query groups of
-// 128 rows, key tiles of 128) with tensor maps of q ([BH][Nq][64], 128-row boxes) and k, v
-// ([BH][Nk][64], 128-row boxes); bf16 or fp16, head width 64.
+// 128 rows; key tiles of 128 keys at d = 64, 64 at d = 128) with tensor maps of q ([BH][Nq][d],
+// boxes of 128 rows x 64 values) and k, v ([BH][Nk][d], boxes of a key tile's rows x 64 values);
+// bf16 or fp16.
 int launch_decode_tc_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& prm,
-                          bool bf16, cudaStream_t stream);
+                          bool bf16, int d, cudaStream_t stream);
 
 }  // namespace attn

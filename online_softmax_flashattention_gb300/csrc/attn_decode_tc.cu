@@ -1,5 +1,5 @@
 // Key-value cache attention on tcgen05 tensor cores, for 2 or more new queries (bf16 / fp16,
-// head width 64): the same operation and work split as attn_decode.cu (query i at position
+// head width 64 or 128): the same operation and work split as attn_decode.cu (query i at position
 // Nk - Nq + i; the keys of a head cut into pieces on different CTAs, merged by their
 // log-sum-exps; the "Backwards, and training with it" section of "Flash attention in PyTorch,
 // then in Triton" names this generation case and leaves it out of its kernel), with the products
@@ -7,9 +7,10 @@
 //
 // A head's group of up to 128 new queries is one 128-row Q tile (rows past the group zero-filled
 // by the tensor map), so S = Q K^T and O += P V are M128 products like the forward's, with every
-// padded row wasted; the arithmetic has room for that: a 128-key K and V tile (32 KB) takes the
-// SM about 1500 cycles to receive at the HBM rate, the products about 600. Softmax warps whose
-// 32 rows are all padding skip the exponentials and write zero probabilities.
+// padded row wasted; the arithmetic has room for that: a K and V tile pair (32 KB: 128 keys at
+// d = 64, 64 at d = 128) takes the SM about 1500 cycles to receive at the HBM rate, the products
+// about 600. Softmax warps whose 32 rows are all padding skip the exponentials and write zero
+// probabilities.
 //
 // Pipeline (one CTA per SM, persistent over the pieces of its run): the TMA producer streams the
 // pieces' K and V tiles through 4-stage rings and the group's Q tile into one of two buffers; S(g)
@@ -34,8 +35,7 @@ namespace {
 
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr uint64_t kDrainTimeoutNs = 100000000ull;
-constexpr float kLazyLog2 = 8.f;    // keep a stale max until a tile exceeds it by 2^8
-constexpr float kLazyBound = 256.f;
+constexpr float kLazyLog2 = 8.f;  // keep a stale max until a tile exceeds it by 2^8
 
 __device__ unsigned int g_dtc_error = 0;
 
@@ -49,19 +49,10 @@ constexpr int kRegsLaunch = 168;
 constexpr int kRegsSm = 216;
 constexpr int kRegsOt = 72;
 static_assert(256 * kRegsSm + 128 * kRegsOt <= kThreads * kRegsLaunch, "register split must fit the launch");
-constexpr int kBN = 128;               // keys per tile
 constexpr int kQRows = 128;            // queries per group (one Q tile)
-constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 16-bit values
+constexpr int kBlkQ = 128 * 128;       // one 64-value column block of a Q tile: 128 rows x 128 bytes
 constexpr int kStages = 4;
 constexpr uint32_t kTmemCols = 512;
-// Tensor memory per step parity e: S_e (fp32, 128 columns), P_e (16-bit pairs, 64), O_e (64).
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColP = 256;
-constexpr uint32_t kColO = 384;
-constexpr int kOffQ = 0;  // two Q buffers
-constexpr int kOffK = kOffQ + 2 * kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
 constexpr int kBarQFull = 0;
 constexpr int kBarQEmpty = 2;
 constexpr int kBarKFull = 4;
@@ -75,15 +66,37 @@ constexpr int kBarPVDone = kBarPFull + 2;         // [2]
 constexpr int kBarDrain = kBarPVDone + 2;         // [2] S issuer, PV issuer
 constexpr int kBarX = kBarDrain + 2;              // [4] per row quarter: both parities' m, l posted (64 threads)
 constexpr int kNumBars = kBarX + 4;
-// Per-piece exchange of m and l, [piece parity][m | l][step parity][row]: double-buffered by
-// piece so that one barrier a piece suffices (a warp writes a buffer again two pieces later,
-// after its partner's arrival for the piece between, which follows the partner's reads).
-constexpr int kOffX = kOffBar + 8 * kNumBars;
-constexpr int kOffSlot = kOffX + 4 * 2 * 2 * 2 * 128;
-constexpr int kOffAbort = kOffSlot + 4;
-constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // slack to align the base to 1024
-static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
-static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+
+// What depends on the head width D. Keys per tile BN: 128 at d = 64, 64 at d = 128, so that
+// S_e (BN fp32 columns), P_e (BN/2) and O_e (D) of both parities fit the 512 TMEM columns
+// (512 and 448). Tiles are D/64 column blocks of rows x 128 bytes, one TMA box each. Tensor
+// memory: S_e at BN e, P_e at 2 BN + BN/2 e, O_e at 512 - 2 D + D e.
+template <int D>
+struct DLay {
+    static_assert(D == 64 || D == 128, "head width 64 or 128");
+    static constexpr int kBN = D == 64 ? 128 : 64;
+    static constexpr int kBlocks = D / 64;
+    static constexpr int kQTile = kBlocks * kBlkQ;      // 16 or 32 KB
+    static constexpr int kKVBlock = kBN * 128;          // one column block of a K or V tile
+    static constexpr int kKVTile = kBlocks * kKVBlock;  // 16 KB
+    static constexpr uint32_t kColS = 0;
+    static constexpr uint32_t kColP = 2 * kBN;
+    static constexpr uint32_t kColO = kTmemCols - 2 * D;
+    static_assert(kColP + kBN <= kColO, "tensor-memory budget");
+    static constexpr int kOffQ = 0;  // two Q buffers
+    static constexpr int kOffK = kOffQ + 2 * kQTile;
+    static constexpr int kOffV = kOffK + kStages * kKVTile;
+    static constexpr int kOffBar = kOffV + kStages * kKVTile;
+    // Per-piece exchange of m and l, [piece parity][m | l][step parity][row]: double-buffered by
+    // piece so that one barrier a piece suffices (a warp writes a buffer again two pieces later,
+    // after its partner's arrival for the piece between, which follows the partner's reads).
+    static constexpr int kOffX = kOffBar + 8 * kNumBars;
+    static constexpr int kOffSlot = kOffX + 4 * 2 * 2 * 2 * 128;
+    static constexpr int kOffAbort = kOffSlot + 4;
+    static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // slack to align the base to 1024
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
+    static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+};
 
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag) {
     *abort_flag = 1;
@@ -126,18 +139,19 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[
         : "memory");
 }
 
-// Row maximum of 128 scores: eight independent chains of 3-input max, then a tree.
-__device__ __forceinline__ float row_max128(const uint32_t (&su)[kBN]) {
+// Row maximum of BN (64 or 128) scores: eight independent chains of 3-input max, then a tree.
+template <int BN>
+__device__ __forceinline__ float row_max_t(const uint32_t (&su)[BN]) {
     float mx[8];
 #pragma unroll
     for (int g = 0; g < 8; ++g)
         mx[g] = fmax3(__uint_as_float(su[g]), __uint_as_float(su[g + 8]), __uint_as_float(su[g + 16]));
 #pragma unroll
-    for (int t = 3; t < kBN / 8 - 1; t += 2)
+    for (int t = 3; t < BN / 8 - 1; t += 2)
 #pragma unroll
         for (int g = 0; g < 8; ++g) mx[g] = fmax3(mx[g], __uint_as_float(su[g + 8 * t]), __uint_as_float(su[g + 8 * t + 8]));
 #pragma unroll
-    for (int g = 0; g < 8; ++g) mx[g] = fmaxf(mx[g], __uint_as_float(su[g + kBN - 8]));
+    for (int g = 0; g < 8; ++g) mx[g] = fmaxf(mx[g], __uint_as_float(su[g + BN - 8]));
     return fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
 }
 
@@ -146,11 +160,13 @@ __device__ __forceinline__ float row_max128(const uint32_t (&su)[kBN]) {
 // warps of its parity) frees the buffer; once PV(g-2) has finished with P_e and O_e, takes the row
 // maximum, moves this parity's reference m when the tile exceeds it by more than 2^8 (rescaling
 // O_e; any reference common to l and O gives the same O / l), and writes P(g) = 2^(s c - m) into
-// P_e in four 32-key pieces. A warp whose rows are all padding (active = false) writes zeros.
-template <bool BF16>
+// P_e in 32-key pieces. A warp whose rows are all padding (active = false) writes zeros.
+template <bool BF16, int D>
 __device__ __forceinline__ bool dtc_step(uint32_t tmem_lane, uint32_t bar0, uint32_t g, bool first, bool masked,
                                          bool active, int key0, int limit, float c, float& m, float& l,
                                          volatile int* abort_flag) {
+    using L = DLay<D>;
+    constexpr int kBN = L::kBN;
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
     const uint32_t e = g & 1u;
     if (!warp_wait(bar(kBarSFull + static_cast<int>(e)), (g >> 1) & 1u, abort_flag)) return false;
@@ -158,7 +174,8 @@ __device__ __forceinline__ bool dtc_step(uint32_t tmem_lane, uint32_t bar0, uint
     uint32_t su[kBN];
     if (active) {
 #pragma unroll
-        for (int cc = 0; cc < kBN / 32; ++cc) ATTN_TMEM_LD_X32(tmem_lane + kColS + 128u * e + 32u * cc, (su + 32 * cc));
+        for (int cc = 0; cc < kBN / 32; ++cc)
+            ATTN_TMEM_LD_X32(tmem_lane + L::kColS + kBN * e + 32u * cc, (su + 32 * cc));
         tmem_ld_wait();
     }
     tc_fence_before();
@@ -174,7 +191,7 @@ __device__ __forceinline__ bool dtc_step(uint32_t tmem_lane, uint32_t bar0, uint
 #pragma unroll
             for (int i = 0; i < kBN; ++i) su[i] = (i < nvalid) ? su[i] : 0xFF800000u;
         }
-        const float mt = row_max128(su) * c;
+        const float mt = row_max_t<kBN>(su) * c;
         float alpha = 1.f;
         if (mt > m + kLazyLog2) {
             alpha = ex2_approx(m - mt);  // 0 on the first tile (m = -inf)
@@ -185,7 +202,7 @@ __device__ __forceinline__ bool dtc_step(uint32_t tmem_lane, uint32_t bar0, uint
         const float2 c2 = make_float2(c, c), nm = make_float2(-m_use, -m_use);
         float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = 0; ch < kBN / 32; ++ch) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -195,16 +212,16 @@ __device__ __forceinline__ bool dtc_step(uint32_t tmem_lane, uint32_t bar0, uint
                 acc = fadd2(acc, pp);
                 pk[i] = pack2<BF16>(pp.x, pp.y);
             }
-            tmem_st_x16(tmem_lane + kColP + 64u * e + 16u * ch, pk);
+            tmem_st_x16(tmem_lane + L::kColP + (kBN / 2) * e + 16u * ch, pk);
         }
         tile_sum = acc.x + acc.y;
         if (!first && __any_sync(0xffffffffu, alpha != 1.f)) {
             // O_e <- alpha O_e (rare); PV(g-2), the last product into O_e, is complete.
             const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
-            for (int qq = 0; qq < 4; ++qq) {
+            for (int qq = 0; qq < D / 16; ++qq) {
                 uint32_t ou[16];
-                tmem_ld_x16(tmem_lane + kColO + 64u * e + 16u * qq, ou);
+                tmem_ld_x16(tmem_lane + L::kColO + D * e + 16u * qq, ou);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; i += 2) {
@@ -212,7 +229,7 @@ __device__ __forceinline__ bool dtc_step(uint32_t tmem_lane, uint32_t bar0, uint
                     ou[i] = __float_as_uint(v.x);
                     ou[i + 1] = __float_as_uint(v.y);
                 }
-                tmem_st_x16(tmem_lane + kColO + 64u * e + 16u * qq, ou);
+                tmem_st_x16(tmem_lane + L::kColO + D * e + 16u * qq, ou);
             }
         }
     } else {
@@ -220,7 +237,7 @@ __device__ __forceinline__ bool dtc_step(uint32_t tmem_lane, uint32_t bar0, uint
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) tmem_st_x16(tmem_lane + kColP + 64u * e + 16u * ch, z);
+        for (int ch = 0; ch < kBN / 32; ++ch) tmem_st_x16(tmem_lane + L::kColP + (kBN / 2) * e + 16u * ch, z);
     }
     l += tile_sum;
     tmem_st_wait();
@@ -230,41 +247,52 @@ __device__ __forceinline__ bool dtc_step(uint32_t tmem_lane, uint32_t bar0, uint
     return true;
 }
 
-// S = Q K^T: M=128 (queries), N=128 (keys), K=64 as four K=16 steps, both operands in shared
-// memory; warp-wide (one elected lane issues).
-template <bool BF16>
+// S = Q K^T: M=128 (queries), N=BN (keys), K=D as D/16 steps of K=16 (32 bytes of a 128-byte
+// row; steps 4..7 at D = 128 read the second column block), both operands in shared memory;
+// warp-wide (one elected lane issues).
+template <bool BF16, int D>
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t sQ, uint32_t sK) {
-    constexpr uint32_t kIdesc = idesc_f16(BF16, 128, kBN, false, false);
+    using L = DLay<D>;
+    constexpr uint32_t kIdesc = idesc_f16(BF16, 128, L::kBN, false, false);
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-        umma_ss_elect(d_tmem, smem_desc_sw128(sQ + 32 * kk, 16, 1024), smem_desc_sw128(sK + 32 * kk, 16, 1024), kIdesc,
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t a_off = static_cast<uint32_t>((kk >> 2) * kBlkQ + 32 * (kk & 3));
+        const uint32_t b_off = static_cast<uint32_t>((kk >> 2) * L::kKVBlock + 32 * (kk & 3));
+        umma_ss_elect(d_tmem, smem_desc_sw128(sQ + a_off, 16, 1024), smem_desc_sw128(sK + b_off, 16, 1024), kIdesc,
                       kk > 0 ? 1u : 0u);
+    }
 }
 
-// O_e += P_e V: M=128, N=64, K=128 as eight K=16 steps, P from tensor memory, V MN-major.
-template <bool BF16>
+// O_e += P_e V: M=128, N=D, K=BN as BN/16 steps of K=16 (16 keys = 2048 bytes of each column
+// block), P from tensor memory, V MN-major (dims contiguous; at D = 128 its two 64-dim column
+// blocks are one block apart, the descriptor's leading byte offset).
+template <bool BF16, int D>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t sV, bool accumulate) {
-    constexpr uint32_t kIdesc = idesc_f16(BF16, 128, 64, false, true);
+    using L = DLay<D>;
+    constexpr uint32_t kIdesc = idesc_f16(BF16, 128, D, false, true);
+    constexpr uint32_t kLbo = D == 64 ? 16u : static_cast<uint32_t>(L::kKVBlock);
 #pragma unroll
-    for (int kk = 0; kk < kBN / 16; ++kk)
-        umma_ts_elect(o_tmem, p_tmem + 8u * kk, smem_desc_sw128(sV + 2048 * kk, 16, 1024), kIdesc,
+    for (int kk = 0; kk < L::kBN / 16; ++kk)
+        umma_ts_elect(o_tmem, p_tmem + 8u * kk, smem_desc_sw128(sV + 2048 * kk, kLbo, 1024), kIdesc,
                       (accumulate || kk > 0) ? 1u : 0u);
 }
 
-template <bool BF16>
+template <bool BF16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+    using L = DLay<D>;
+    constexpr int kBN = L::kBN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
-    const uint32_t bar0 = base + kOffBar;
+    const uint32_t sQ = base + L::kOffQ, sK = base + L::kOffK, sV = base + L::kOffV;
+    const uint32_t bar0 = base + L::kOffBar;
     auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
-    float* const xch = reinterpret_cast<float*>(gbase + kOffX);  // [m | l][parity][row]
-    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffSlot);
-    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + kOffAbort);
+    float* const xch = reinterpret_cast<float*>(gbase + L::kOffX);  // [piece parity][m | l][step parity][row]
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kOffSlot);
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + L::kOffAbort);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = static_cast<int>(blockIdx.x);
 
@@ -322,14 +350,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j0 = static_cast<int>((g0 & 1u) ^ e);  // this parity's first step of the piece
             for (int j = j0; ok && j < n; j += 2) {
                 const int key0 = (pc.t0 + j) * kBN;
-                ok = dtc_step<BF16>(tmem_lane, bar0, g0 + static_cast<uint32_t>(j), j < 2, key0 + kBN > lim0, active,
+                ok = dtc_step<BF16, D>(tmem_lane, bar0, g0 + static_cast<uint32_t>(j), j < 2, key0 + kBN > lim0, active,
                                     key0, limit, p.c, m, l, abort_flag);
             }
             if (!ok) break;
             if (active) {
                 // ---- merge the two parities, O = (2^(m0-M) O_0 + 2^(m1-M) O_1) / (2^(m0-M) l0 +
-                // 2^(m1-M) l1); this thread writes columns 32 e .. 32 e + 31 of its row. Both warps
-                // wait for the piece's last products before the exchange. ----
+                // 2^(m1-M) l1); this thread writes columns D/2 e .. D/2 e + D/2 - 1 of its row. Both
+                // warps wait for the piece's last products before the exchange. ----
                 if (n >= 1) {
                     const uint32_t gl = g0 + static_cast<uint32_t>(n) - 1;
                     if (!(ok = warp_wait(bar(kBarPVDone + static_cast<int>(gl & 1u)), (gl >> 1) & 1u, abort_flag))) break;
@@ -360,10 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t row = static_cast<int64_t>(pc.bh) * p.Nq + qi;
                 const bool real = r < pc.ng;
 #pragma unroll 1
-                for (int cc = 0; cc < 2; ++cc) {
+                for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t u0[16], u1[16];
-                    tmem_ld_x16(tmem_lane + kColO + 32u * e + 16u * cc, u0);
-                    tmem_ld_x16(tmem_lane + kColO + 64u + 32u * e + 16u * cc, u1);
+                    tmem_ld_x16(tmem_lane + L::kColO + (D / 2) * e + 16u * cc, u0);
+                    tmem_ld_x16(tmem_lane + L::kColO + D + (D / 2) * e + 16u * cc, u1);
                     tmem_ld_wait();
                     float x[16];
 #pragma unroll
@@ -376,16 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         x[i + 1] = xx.y;
                     }
                     if (!real) continue;
-                    const int c0 = static_cast<int>(32u * e) + 16 * cc;
+                    const int c0 = static_cast<int>((D / 2) * e) + 16 * cc;
                     if (pc.nslots == 1) {
                         uint32_t pk[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) pk[i] = pack2<BF16>(x[2 * i], x[2 * i + 1]);
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + row * 64 + c0);
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + row * D + c0);
                         dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                         dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                     } else {
-                        float4* dst = reinterpret_cast<float4*>(p.part_o + (row * p.P + pc.slot) * 64 + c0);
+                        float4* dst = reinterpret_cast<float4*>(p.part_o + (row * p.P + pc.slot) * D + c0);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) dst[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
                     }
@@ -418,8 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_v = [&](int bh, int t) -> bool {
             const int s = static_cast<int>(vq % kStages);
             if (!wait_s(bar(kBarVEmpty + s), ((vq / kStages) & 1u) ^ 1u, abort_flag, kWaitTimeoutNs)) return false;
-            mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
-            tma_load_3d(sV + s * kTileBytes, &tmap_v, 0, t * kBN, bh, bar(kBarVFull + s));
+            mbar_arrive_expect_tx(bar(kBarVFull + s), L::kKVTile);
+#pragma unroll
+            for (int c = 0; c < L::kBlocks; ++c)
+                tma_load_3d(sV + s * L::kKVTile + c * L::kKVBlock, &tmap_v, 64 * c, t * kBN, bh, bar(kBarVFull + s));
             ++vq;
             return true;
         };
@@ -428,14 +458,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (pc.t1 <= pc.t0) continue;
             const int qb = static_cast<int>(qi & 1u);
             if (!(ok = wait_s(bar(kBarQEmpty + qb), ((qi >> 1) & 1u) ^ 1u, abort_flag, kWaitTimeoutNs))) break;
-            mbar_arrive_expect_tx(bar(kBarQFull + qb), kTileBytes);
-            tma_load_3d(sQ + qb * kTileBytes, &tmap_q, 0, pc.g0, pc.bh, bar(kBarQFull + qb));
+            mbar_arrive_expect_tx(bar(kBarQFull + qb), L::kQTile);
+#pragma unroll
+            for (int c = 0; c < L::kBlocks; ++c)
+                tma_load_3d(sQ + qb * L::kQTile + c * kBlkQ, &tmap_q, 64 * c, pc.g0, pc.bh, bar(kBarQFull + qb));
             ++qi;
             for (int t = pc.t0; ok && t < pc.t1; ++t) {
                 const int s = static_cast<int>(kv % kStages);
                 if (!(ok = wait_s(bar(kBarKEmpty + s), ((kv / kStages) & 1u) ^ 1u, abort_flag, kWaitTimeoutNs))) break;
-                mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
-                tma_load_3d(sK + s * kTileBytes, &tmap_k, 0, t * kBN, pc.bh, bar(kBarKFull + s));
+                mbar_arrive_expect_tx(bar(kBarKFull + s), L::kKVTile);
+#pragma unroll
+                for (int c = 0; c < L::kBlocks; ++c)
+                    tma_load_3d(sK + s * L::kKVTile + c * L::kKVBlock, &tmap_k, 64 * c, t * kBN, pc.bh,
+                                bar(kBarKFull + s));
                 ++kv;
                 if (pend_bh >= 0 && !(ok = issue_v(pend_bh, pend_t))) break;
                 pend_bh = pc.bh;
@@ -471,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     !(ok = warp_wait(bar(kBarSFree + static_cast<int>(gs & 1u)), ((gs - 2) >> 1) & 1u, abort_flag)))
                     break;
                 tc_fence_after();
-                issue_s<BF16>(tmem + kColS + 128u * (gs & 1u), sQ + qb * kTileBytes, sK + s * kTileBytes);
+                issue_s<BF16, D>(tmem + L::kColS + kBN * (gs & 1u), sQ + qb * L::kQTile, sK + s * L::kKVTile);
                 umma_commit_elect(bar(kBarSFull + static_cast<int>(gs & 1u)));
                 umma_commit_elect(bar(kBarKEmpty + s));
                 if (j == n - 1) {
@@ -499,8 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = warp_wait(bar(kBarVFull + s), (kvp / kStages) & 1u, abort_flag))) break;
                 if (!(ok = warp_wait(bar(kBarPFull + static_cast<int>(gp & 1u)), (gp >> 1) & 1u, abort_flag))) break;
                 tc_fence_after();
-                issue_pv<BF16>(tmem + kColO + 64u * (gp & 1u), tmem + kColP + 64u * (gp & 1u), sV + s * kTileBytes,
-                               j >= 2);
+                issue_pv<BF16, D>(tmem + L::kColO + D * (gp & 1u), tmem + L::kColP + (kBN / 2) * (gp & 1u),
+                                  sV + s * L::kKVTile, j >= 2);
                 umma_commit_elect(bar(kBarPVDone + static_cast<int>(gp & 1u)));
                 umma_commit_elect(bar(kBarVEmpty + s));
                 ++gp;
@@ -523,21 +558,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int launch_decode_tc_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& prm,
-                          bool bf16, cudaStream_t stream) {
+namespace {
+template <bool BF16, int D>
+int launch_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& prm,
+              cudaStream_t stream) {
     static uint64_t ready = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
-    auto kern = bf16 ? attn_decode_tc_kernel<true> : attn_decode_tc_kernel<false>;
     if (!once_per_device(&ready, dev, [] {
-            return cudaFuncSetAttribute(attn_decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kSmemBytes) == cudaSuccess &&
-                   cudaFuncSetAttribute(attn_decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kSmemBytes) == cudaSuccess;
+            return cudaFuncSetAttribute(attn_decode_tc_kernel<BF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        DLay<D>::kSmemBytes) == cudaSuccess;
         }))
         return ATTN_ERR_LAUNCH;
-    kern<<<static_cast<unsigned>(prm.C), kThreads, kSmemBytes, stream>>>(mq, mk, mv, prm);
+    attn_decode_tc_kernel<BF16, D><<<static_cast<unsigned>(prm.C), kThreads, DLay<D>::kSmemBytes, stream>>>(mq, mk, mv,
+                                                                                                            prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+}  // namespace
+
+int launch_decode_tc_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& prm,
+                          bool bf16, int d, cudaStream_t stream) {
+    if (d == 64)
+        return bf16 ? launch_tc<true, 64>(mq, mk, mv, prm, stream) : launch_tc<false, 64>(mq, mk, mv, prm, stream);
+    if (d == 128)
+        return bf16 ? launch_tc<true, 128>(mq, mk, mv, prm, stream) : launch_tc<false, 128>(mq, mk, mv, prm, stream);
+    return ATTN_ERR_UNSUPPORTED;
 }
 
 int decode_tc_device_error(bool clear, unsigned* err) {

@@ -238,3 +238,13 @@ def test_kvcache_query_groups_of_128(dtype, causal, Nq, Nk, splits):
     # The tensor-core kernel takes a head's queries 128 at a time: a group filling the tile, a
     # ragged last group, several groups with the causal diagonal inside the cache, Nq == Nk.
     _run(0xCAC3F000 + Nq * 7919 + Nk, 2, 2, Nq, Nk, dtype, causal, splits)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(2, 65), (8, 8192), (129, 1000), (200, 200)])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_kvcache_tensor_cores_head_width_128(dtype, causal, Nq, Nk, splits):
+    # At d = 128 the tensor-core kernel streams 64-key tiles (two 64-value column blocks per
+    # row): a ragged single key past one tile, a long cache, several query groups, Nq == Nk.
+    _run(0xCAC3F800 + Nq * 7919 + Nk, 2, 2, Nq, Nk, dtype, causal, splits, d=128)
