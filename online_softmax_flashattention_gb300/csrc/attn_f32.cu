@@ -8,13 +8,13 @@
 // Triton"). Causal key tiles past a block's last query are skipped and ragged N is guarded
 // on every load and store (the page's kernel masks rows and keys past T).
 //
-// Layout per CTA: BM query rows (64, or 32 when the grid would not fill the GPU) against
-// key tiles of 64, head width D = 64 or 128, BM/4 x 16 threads. Thread (ty, tx) holds a 4 x 4
-// score micro-tile — rows ty*4 + i, keys tx + 16 j — and a 4 x D/16 output micro-tile — rows
-// ty*4 + i, dims 64 g + tx*4 + j. Rows of shared tiles are padded to D + 4 floats so that every
-// float4 read of a key row, every P store and every V read is free of bank conflicts. The 16
-// threads that share a row sit in one half-warp, so row max and row sum are 4-step xor
-// shuffles.
+// Layout per CTA: BM query rows (64; 32 when the grid would not fill the GPU; 16 for causal
+// grids that split the keys, below) against key tiles of 64, head width D = 64 or 128, BM/4 x 16
+// threads. Thread (ty, tx) holds a 4 x 4 score micro-tile — rows ty*4 + i, keys tx + 16 j — and a
+// 4 x D/16 output micro-tile — rows ty*4 + i, dims 64 g + tx*4 + j. Rows of shared tiles are
+// padded to D + 4 floats so that every float4 read of a key row, every P store and every V read
+// is free of bank conflicts. The 16 threads that share a row sit in one half-warp, so row max
+// and row sum are 4-step xor shuffles.
 // With an `lse` pointer each row's log-sum-exp is stored too, in base 2 as the page's
 // forward kernel keeps it for the backward pass (m + log2 l, "Backwards, and training with
 // it").
@@ -34,8 +34,6 @@
 
 namespace attn {
 namespace {
-
-constexpr int kBN = 64;
 
 // Padded row stride (floats) of every shared tile.
 template <int D>
@@ -57,7 +55,7 @@ __device__ __forceinline__ void group_sync(int grp) {
     }
 }
 
-template <int BM, int D, int G>
+template <int BM, int D, int G, int kBN>
 __global__ void __launch_bounds__(BM * 4 * G)
     attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                         const float* __restrict__ v, float* __restrict__ o, float* __restrict__ lse,
@@ -66,6 +64,7 @@ __global__ void __launch_bounds__(BM * 4 * G)
     constexpr int kLd = ld_of<D>();
     constexpr int kD4 = D / 4;   // float4 per row
     constexpr int kG = D / 64;   // 64-dim groups of this thread's output columns
+    constexpr int kJ = kBN / 16;  // keys of this thread's score micro-tile
     extern __shared__ float4 smem4[];
     const int grp = static_cast<int>(threadIdx.x) / kThreads;
     float* const Qs = reinterpret_cast<float*>(smem4);
@@ -122,22 +121,22 @@ __global__ void __launch_bounds__(BM * 4 * G)
         group_sync<G, kThreads>(grp);
 
         // S micro-tile: rows ty*4+i, keys tx+16j.
-        float s[4][4];
+        float s[4][kJ];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+            for (int j = 0; j < kJ; ++j) s[i][j] = 0.f;
 #pragma unroll 4
         for (int e = 0; e < D; e += 4) {
-            float4 qa[4], kb[4];
+            float4 qa[4], kb[kJ];
 #pragma unroll
             for (int i = 0; i < 4; ++i) qa[i] = *reinterpret_cast<const float4*>(Qs + (ty * 4 + i) * kLd + e);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) kb[j] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * j) * kLd + e);
+            for (int j = 0; j < kJ; ++j) kb[j] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * j) * kLd + e);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < kJ; ++j) {
                     s[i][j] = fmaf(qa[i].x, kb[j].x, s[i][j]);
                     s[i][j] = fmaf(qa[i].y, kb[j].y, s[i][j]);
                     s[i][j] = fmaf(qa[i].z, kb[j].z, s[i][j]);
@@ -152,7 +151,7 @@ __global__ void __launch_bounds__(BM * 4 * G)
                 const int row = row0 + ty * 4 + i;
                 const int lim = causal ? min(row + 1, N) : N;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < kJ; ++j)
                     if (kbase + tx + 16 * j >= lim) s[i][j] = -INFINITY;
             }
         }
@@ -160,7 +159,9 @@ __global__ void __launch_bounds__(BM * 4 * G)
         // Online update per row.
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float mx = fmaxf(fmaxf(s[i][0], s[i][1]), fmaxf(s[i][2], s[i][3]));
+            float mx = s[i][0];
+#pragma unroll
+            for (int j = 1; j < kJ; ++j) mx = fmaxf(mx, s[i][j]);
 #pragma unroll
             for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
             const float m_new = fmaxf(m[i], mx * c);
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(BM * 4 * G)
             const float alpha = ex2f(m[i] - m_ref);
             float ps = 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kJ; ++j) {
                 const float pv = ex2f(fmaf(s[i][j], c, -m_ref));
                 ps += pv;
                 Ps[(ty * 4 + i) * kLd + tx + 16 * j] = pv;
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(BM * 4 * G)
     }
 }
 
-template <int BM, int D, int G>
+template <int BM, int D, int G, int kBN = 64>
 int launch_bm(const float* q, const float* k, const float* v, float* o, float* lse, int64_t BH,
               int64_t N, bool causal, cudaStream_t stream) {
     // Q, then per group K, V and P tiles; the groups' merge records reuse the K/V/P space.
@@ -283,7 +284,7 @@ int launch_bm(const float* q, const float* k, const float* v, float* o, float* l
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
     if (!once_per_device(&ready, dev, [] {
-            return cudaFuncSetAttribute(attn_fwd_f32_kernel<BM, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            return cudaFuncSetAttribute(attn_fwd_f32_kernel<BM, D, G, kBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         smem) == cudaSuccess;
         }))
         return ATTN_ERR_LAUNCH;
@@ -291,7 +292,7 @@ int launch_bm(const float* q, const float* k, const float* v, float* o, float* l
     const int64_t blocks = nblk * BH;
     if (blocks > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
     const float c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-    attn_fwd_f32_kernel<BM, D, G><<<static_cast<unsigned>(blocks), BM * 4 * G, smem, stream>>>(
+    attn_fwd_f32_kernel<BM, D, G, kBN><<<static_cast<unsigned>(blocks), BM * 4 * G, smem, stream>>>(
         q, k, v, o, lse, static_cast<int>(N), static_cast<int>(BH), static_cast<int>(nblk), causal ? 1 : 0, c);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
@@ -301,14 +302,18 @@ int launch_bm(const float* q, const float* k, const float* v, float* o, float* l
 int launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int64_t BH,
                    int64_t N, int64_t d, bool causal, int num_sms, cudaStream_t stream) {
     if (N > 0x7FFFFFFFll - 64 || BH > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+    constexpr int kBN = 64;
     // Grids that fill the GPU run 64-row blocks; smaller ones 32-row blocks, and when even those
     // leave most SMs with a single block, the keys are split over G groups inside each block.
     const int64_t blocks64 = ((N + 63) / 64) * BH;
     const int64_t blocks32 = ((N + 31) / 32) * BH;
     const bool small = blocks64 < 2 * static_cast<int64_t>(num_sms);
     const bool split = blocks32 < 2 * static_cast<int64_t>(num_sms) && N > 2 * kBN;
+    // Causal small grids take 16-row blocks: the heaviest block (the last rows, which see every
+    // key) bounds the call, and it runs on one SM, so halving its rows halves the critical path.
     if (d == 64)
-        return split ? launch_bm<32, 64, 4>(q, k, v, o, lse, BH, N, causal, stream)
+        return split ? (causal ? launch_bm<16, 64, 4>(q, k, v, o, lse, BH, N, causal, stream)
+                               : launch_bm<32, 64, 4>(q, k, v, o, lse, BH, N, causal, stream))
                : small ? launch_bm<32, 64, 1>(q, k, v, o, lse, BH, N, causal, stream)
                        : launch_bm<64, 64, 1>(q, k, v, o, lse, BH, N, causal, stream);
     if (d == 128)
