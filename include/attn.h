@@ -139,12 +139,15 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  *     o[b,h,i,:] = sum_{j in vis(i)} softmax_j( q[b,h,i,:] . k[b,h,j,:] / sqrt(d) ) v[b,h,j,:]
  *
  * with vis(i) = {0 .. Nk-1}, or {0 .. Nk-Nq+i} when causal (with Nq == Nk this is attn_fwd's
- * mask). The keys of each (head, group of up to 8 queries) are cut into pieces that run on
+ * mask). The keys of each (head, group of queries) are cut into pieces that run on
  * different CTAs; every piece runs the page's online softmax (section "Flash attention") over
  * its keys and leaves its normalised output O_p and base-2 log-sum-exp lse_p, and a second
  * kernel merges the pieces the way the online softmax merges tiles: lse = log2 sum_p 2^lse_p,
  * o = sum_p 2^(lse_p - lse) O_p. A piece that covers all of its head's keys writes o directly.
- * All arithmetic is fp32 on CUDA cores (the work is bound by reading the cache); o is rounded
+ * The work is bound by reading the cache. One new query, and fp32 inputs, run in groups of up
+ * to 8 queries with all arithmetic fp32 on CUDA cores; two or more bf16/f16 queries run in
+ * groups of up to 128 on tcgen05 tensor cores (S = q k^T and o += P v with bf16/f16 operands
+ * and fp32 accumulation, P rounded to dtype before it weighs v, as attn_fwd does). o is rounded
  * to dtype (RNE). Nothing is allocated.
  *
  *   q, o          : device pointers, [B, H, Nq, d] of dtype, 16-byte aligned; o must not
@@ -161,7 +164,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  *   Nq, Nk        : 0 <= Nq <= Nk <= ATTN_MAX_N, Nq <= 8 * 65535; Nq == 0 or B*H == 0 is a
  *                   successful no-op
  *   num_splits    : 0 — balanced: a persistent grid of as many CTAs as the device holds, each
- *                   streaming the same number of 128-key tiles (within one) of all heads' keys,
+ *                   streaming the same number of key tiles (within one; 128 keys, or 64 on
+ *                   tensor cores at d = 128) of all heads' keys,
  *                   cut at head boundaries; 1 .. ATTN_KV_MAX_SPLITS — every (head, query
  *                   group) is cut into that many equal shares (shares past the last key are
  *                   empty and carry weight 0 in the merge).

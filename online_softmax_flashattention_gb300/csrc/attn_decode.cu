@@ -11,12 +11,15 @@
 // combines the pieces the way the online softmax combines tiles:
 //     lse2 = log2 sum_p 2^lse2_p,   O = sum_p 2^(lse2_p - lse2) O_p.
 // A query does one product of d terms per cached row of 2d values, so the work is bound by
-// reading the cache from HBM. The kernel streams K and V once per group of up to eight
-// queries through a ring of shared-memory stages filled by TMA, and keeps the arithmetic on
-// CUDA cores.
+// reading the cache from HBM. This file's kernel streams K and V once per group of up to eight
+// queries through a ring of shared-memory stages filled by TMA, with the arithmetic on CUDA
+// cores; it serves one new query, fp32, and everything the tensor-core kernel does not take.
+// Two or more 16-bit queries go to attn_decode_tc.cu (groups of up to 128 queries as M128
+// tensor-core tiles) under the same work split and the same merge kernel.
 //
-// Work split. The queries are cut into groups of QG (1, 2, 4 or 8); a segment is one
-// (head, query group) with Tn tiles of 128 keys. Two ways to cut segments into pieces:
+// Work split. The queries are cut into groups of QG (1, 2, 4 or 8 here, 128 on tensor cores);
+// a segment is one (head, query group) with Tn tiles of ROWS keys (128 here; 128 or 64 on
+// tensor cores). Two ways to cut segments into pieces:
 //   balanced (num_splits == 0): the grid is persistent (as many CTAs as fit on the GPU, or
 //     fewer when there is less work) and CTA c takes the contiguous run of tiles
 //     [c G / C, (c+1) G / C) of all G = segments * Tn tiles, cut at segment boundaries, so
