@@ -70,8 +70,8 @@ TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_tc_bf16_causal_B1H12N
 DECODE = {"workload": "key-value cache decode, bf16, B16 H12 Nq1 Nk8192 d64 (one new token per sequence)",
           "B": 16, "H": 12, "Nq": 1, "Nk": 8192, "d": 64, "causal": True, "dtype": "bf16"}
 DECODE_SOURCE = os.path.join(ROOT, "online_softmax_flashattention_gb300", "csrc", "attn_decode.cu")
-# The same cache with eight new tokens per sequence (speculative or chunked decoding): 16-bit
-# inputs at d64 with two or more queries run on the tensor-core kernel.
+# The same cache with eight new tokens per sequence (speculative or chunked decoding), which runs
+# on the tensor-core cache kernel.
 DECODE8 = {"workload": "key-value cache decode, bf16, B16 H12 Nq8 Nk8192 d64 (eight new tokens per sequence)",
            "B": 16, "H": 12, "Nq": 8, "Nk": 8192, "d": 64, "causal": True, "dtype": "bf16"}
 DECODE8_SOURCE = os.path.join(ROOT, "online_softmax_flashattention_gb300", "csrc", "attn_decode_tc.cu")

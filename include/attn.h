@@ -144,11 +144,13 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  * its keys and leaves its normalised output O_p and base-2 log-sum-exp lse_p, and a second
  * kernel merges the pieces the way the online softmax merges tiles: lse = log2 sum_p 2^lse_p,
  * o = sum_p 2^(lse_p - lse) O_p. A piece that covers all of its head's keys writes o directly.
- * The work is bound by reading the cache. One new query, and fp32 inputs, run in groups of up
- * to 8 queries with all arithmetic fp32 on CUDA cores; two or more bf16/f16 queries run in
- * groups of up to 128 on tcgen05 tensor cores (S = q k^T and o += P v with bf16/f16 operands
- * and fp32 accumulation, P rounded to dtype before it weighs v, as attn_fwd does). o is rounded
- * to dtype (RNE). Nothing is allocated.
+ * The work is bound by reading the cache. Two or more bf16/f16 queries run in groups of up to
+ * 128 on tcgen05 tensor cores (S = q k^T and o += P v with bf16/f16 operands and fp32
+ * accumulation, P rounded to dtype before it weighs v, as attn_fwd does) where that measured
+ * faster: always at d = 128; at d = 64 from 8 queries, from 3 on caches of 1024 keys or more
+ * (and 2^18 cached rows in the call), and from 2 on caches of 32768 keys or more. Everything
+ * else (one query, fp32, the short cases) runs in groups of up to 8 queries with all arithmetic
+ * fp32 on CUDA cores. o is rounded to dtype (RNE). Nothing is allocated.
  *
  *   q, o          : device pointers, [B, H, Nq, d] of dtype, 16-byte aligned; o must not
  *                   overlap q, k, v, lse or the workspace

@@ -620,13 +620,25 @@ size_t partial_bytes(int64_t BH, int64_t Nq, int64_t D, int64_t P) {
     return (r * static_cast<size_t>(D) * sizeof(float) + 255) / 256 * 256 + (r * sizeof(float) + 255) / 256 * 256;
 }
 
-// Two or more new queries in bf16/fp16 run on the tensor-core kernel (attn_decode_tc.cu): groups
-// of up to 128 queries as one M128 tile, key tiles of 128 (d = 64) or 64 (d = 128), one CTA per SM.
-bool use_tc(int dtype, int64_t d, int64_t Nq) { return dtype != ATTN_F32 && (d == 64 || d == 128) && Nq >= 2; }
+// Two or more new queries in bf16/fp16 may run on the tensor-core kernel (attn_decode_tc.cu):
+// groups of up to 128 queries as one M128 tile, key tiles of 128 (d = 64) or 64 (d = 128), one CTA
+// per SM. It costs more per piece (a Q tile, the exchange of the two step parities) and its
+// floor per call is a couple of microseconds higher, while the CUDA-core kernel slows with every
+// query of a group (3 queries run as a group of 4). Measured on GB300 (bf16, causal): at d = 128
+// the tensor-core kernel is never slower; at d = 64 it wins from 8 queries on (B64 H12 Nk256: 35
+// against 41 us), for 3 to 7 once the cache holds 1024 keys and the call 2^18 cached rows in all
+// (B64 H12 Nk1024 Nq4: 55 against 67 us; B16 H12 Nk8192 Nq3: 73 against 102; B4 H8 Nk2048 Nq4:
+// 19 against 16), and for 2 only on long caches (B1 H1 Nk100000: 35 against 52 us; B16 H12
+// Nk8192: 72.5 against 69.3).
+bool use_tc(int dtype, int64_t d, int64_t BH, int64_t Nq, int64_t Nk) {
+    if (dtype == ATTN_F32 || Nq < 2 || (d != 64 && d != 128)) return false;
+    if (d == 128 || Nq >= 8 || Nk >= 32768) return true;
+    return Nq >= 3 && Nk >= 1024 && BH * Nk >= (int64_t{1} << 18);
+}
 
 // Builds the plan of a call: the kernel's tile rows and occupancy come from its configuration.
 bool plan_for(int64_t BH, int64_t Nq, int64_t Nk, int64_t D, int splits, int dtype, int num_sms, Plan* pl) {
-    if (use_tc(dtype, D, Nq)) return make_plan(BH, Nq, Nk, D == 64 ? 128 : 64, splits, num_sms, 1, 128, pl);
+    if (use_tc(dtype, D, BH, Nq, Nk)) return make_plan(BH, Nq, Nk, D == 64 ? 128 : 64, splits, num_sms, 1, 128, pl);
     int rows = 0, per_sm = 0;
     visit_cfg(dtype, D, queries_per_group(Nq), [&](auto t, auto qg, auto dd) -> int {
         using T = typename decltype(t)::type;
@@ -724,7 +736,7 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
     CUtensorMap mk, mv;
     if (!make_map(&mk, k, BH, Nk, d, dtype, pl.rows) || !make_map(&mv, v, BH, Nk, d, dtype, pl.rows))
         return ATTN_ERR_DEVICE;
-    if (use_tc(dtype, d, Nq)) {
+    if (use_tc(dtype, d, BH, Nq, Nk)) {
         CUtensorMap mq;
         if (!make_map(&mq, q, BH, Nq, d, dtype, 128)) return ATTN_ERR_DEVICE;
         const int st = launch_decode_tc_main(mq, mk, mv, prm, dtype == ATTN_BF16, static_cast<int>(d), stream);

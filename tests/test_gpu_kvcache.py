@@ -214,11 +214,11 @@ def test_kvcache_noncausal_ignores_key_order():
     assert float((o1 - o2).abs().max()) <= 1e-5
 
 
-@pytest.mark.parametrize("Nq", [2, 4, 8])
+@pytest.mark.parametrize("Nq", [2, 3, 4, 8])
 def test_kvcache_tensor_core_decode_shape(Nq):
-    # A few new tokens per sequence against an 8192-key cache, B16 H12: 16-bit inputs at d = 64
-    # with two or more queries run on the tensor-core kernel (queries padded to a 128-row tile);
-    # balanced plan, every query row against the oracle.
+    # A few new tokens per sequence against an 8192-key cache, B16 H12: at d = 64, 3 to 8 queries
+    # run on the tensor-core kernel (queries padded to a 128-row tile), 2 on CUDA cores; balanced
+    # plan, every query row against the oracle.
     B, H, Nk = 16, 12, 8192
     q, k, v = _inputs(0xCAC3E000 + Nq, B, H, Nq, Nk, "bf16")
     qd, kd, vd = (to_dev(x, "bf16") for x in (q, k, v))
@@ -248,3 +248,12 @@ def test_kvcache_tensor_cores_head_width_128(dtype, causal, Nq, Nk, splits):
     # At d = 128 the tensor-core kernel streams 64-key tiles (two 64-value column blocks per
     # row): a ragged single key past one tile, a long cache, several query groups, Nq == Nk.
     _run(0xCAC3F800 + Nq * 7919 + Nk, 2, 2, Nq, Nk, dtype, causal, splits, d=128)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,Nq,Nk,splits", [(1, 2, 2, 40000, 0), (1, 1, 3, 33000, 0), (1, 1, 2, 33000, 7)])
+def test_kvcache_tensor_cores_long_cache_few_queries(B, H, Nq, Nk, splits, causal):
+    # Two 16-bit queries at d = 64 take the tensor-core kernel only on long caches (32768 keys or
+    # more); three take it from 1024 keys: balanced and explicit shares over a cache of a few
+    # hundred tiles.
+    _run(0xCAC3FC00 + Nq * 7919 + Nk, B, H, Nq, Nk, "bf16", causal, splits)
