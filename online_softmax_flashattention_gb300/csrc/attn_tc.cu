@@ -36,6 +36,10 @@
 //     tensor memory and V (dims contiguous, "MN-major") from shared memory.
 //   * S_X(j+1) is issued as soon as softmax X has copied S_X(j) into registers, so the
 //     next QK^T overlaps the exponentials, and the two groups' products interleave.
+//   * Epilogue: each tile's softmax warps write O / l, rounded to the output type, into the
+//     tile's Q buffer (free once its last S product has completed) in the 128-byte-swizzled
+//     layout of the output's TMA box, and one thread stores the box with a TMA bulk store; the
+//     tensor map clips rows >= N.
 //   * With an `lse` pointer the epilogue also stores each row's log-sum-exp in base 2,
 //     m + log2 l, as the page's forward kernel keeps it for the backward pass ("Backwards,
 //     and training with it"); any common reference m gives the same value.
@@ -121,7 +125,8 @@ struct Lay {
     static constexpr int kBarPFull = kBarSFree + 2;          // [2] softmax X wrote P_X(j) (4 warps)
     static constexpr int kBarOReady = kBarPFull + 2;         // [2] PV_X(j) done: O_X stable, P_X reusable
     static constexpr int kBarDrain = kBarOReady + 2;         // [2] every MMA of issuer 0 (S) / 1 (PV) done
-    static constexpr int kNumBars = kBarDrain + 2;
+    static constexpr int kBarEpi = kBarDrain + 2;            // [2] tile X's output rows are in shared memory (4 warps)
+    static constexpr int kNumBars = kBarEpi + 2;
     static constexpr int kOffSlot = kOffBar + 8 * kNumBars;  // TMEM base address written by tcgen05.alloc
     static constexpr int kOffAbort = kOffSlot + 4;
     static constexpr int kSmemUsed = kOffAbort + 4;
@@ -362,7 +367,8 @@ template <bool BF16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                        const __grid_constant__ CUtensorMap tmap_k,
-                       const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
+                       const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
+                       const TcParams p) {
     using L = Lay<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -417,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::kBarPFull + x), 4);
             mbar_init(bar(L::kBarOReady + x), 1);
             mbar_init(bar(L::kBarDrain + x), 1);
+            mbar_init(bar(L::kBarEpi + x), 4);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -469,13 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (; ok && j < nX; ++j) ok = softmax_step<BF16, true, D>(cx, su, m, l, j, nX);
         }
 
-        // ---- epilogue: O / l, rounded to the output type, rows >= N not stored ----
+        // ---- epilogue: O / l, rounded to the output type, written into this tile's Q buffer (the
+        // tile's last S product has completed) in the 128-byte-swizzled layout of the output's TMA
+        // box; then one thread stores the box, which drops rows >= N. ----
         if (ok && nX > 0) {
             if (warp_wait(cx.bar_o_ready, (nX - 1) & 1, abort_flag)) {
                 tc_fence_after();
                 const float inv = 1.f / l;
-                uint16_t* const orow = reinterpret_cast<uint16_t*>(p.o) +
-                                       (static_cast<int64_t>(bh) * N + row) * D;
+                const int r = ((warp & 3) << 5) + lane;  // row of the tile
+                const uint32_t sO = sQ + static_cast<uint32_t>(X) * L::kTileBytes;
 #pragma unroll 1
                 for (int h = 0; h < D / 16; ++h) {
                     uint32_t ou[16];
@@ -486,13 +495,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 8; ++i)
                         pk[i] = pack2<BF16>(__uint_as_float(ou[2 * i]) * inv,
                                             __uint_as_float(ou[2 * i + 1]) * inv);
-                    if (row < N) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + 16 * h);
-                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    // 16-byte chunk c of row r sits at chunk c ^ (r mod 8) of the row's 128 bytes.
+                    const uint32_t rowb = sO + static_cast<uint32_t>(((2 * h) >> 3) * kBlockBytes + r * 128);
+#pragma unroll
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const int c = (2 * h + c2) & 7;
+                        st_shared_v4(rowb + static_cast<uint32_t>((c ^ (r & 7)) * 16), pk[4 * c2], pk[4 * c2 + 1],
+                                     pk[4 * c2 + 2], pk[4 * c2 + 3]);
                     }
                 }
                 if (p.lse != nullptr && row < N) p.lse[static_cast<int64_t>(bh) * N + row] = m + log2f(l);
+                fence_proxy_async_smem();
+                __syncwarp();
+                mbar_arrive_elect(bar(L::kBarEpi + X));
+                if ((warp & 3) == 0) {
+                    ok = warp_wait(bar(L::kBarEpi + X), 0, abort_flag);
+                    if (ok && lane == 0) {
+#pragma unroll
+                        for (int c = 0; c < L::kBlocks; ++c)
+                            tma_store_3d(&tmap_o, sO + c * kBlockBytes, 64 * c, X ? rowB : rowA, bh);
+                        bulk_commit_group();
+                        bulk_wait_group_read0();  // the box has left shared memory before the CTA exits
+                    }
+                    __syncwarp();
+                }
             } else {
                 ok = false;
             }
@@ -709,14 +735,15 @@ struct FwdMaps {
     const void* q;
     const void* k;
     const void* v;
+    const void* o;
     int64_t BH, N;
     int D;
     bool bf16;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
 };
 
-bool fwd_maps(const void* q, const void* k, const void* v, int64_t BH, int64_t N, int D, int kv_rows, bool bf16,
-              CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv) {
+bool fwd_maps(const void* q, const void* k, const void* v, const void* o, int64_t BH, int64_t N, int D, int kv_rows,
+              bool bf16, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* mo) {
     constexpr int kSlots = 8;
     static std::mutex mu;
     static FwdMaps slots[kSlots];
@@ -724,16 +751,17 @@ bool fwd_maps(const void* q, const void* k, const void* v, int64_t BH, int64_t N
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i) {
         const FwdMaps& e = slots[i];
-        if (e.q == q && e.k == k && e.v == v && e.BH == BH && e.N == N && e.D == D && e.bf16 == bf16) {
+        if (e.q == q && e.k == k && e.v == v && e.o == o && e.BH == BH && e.N == N && e.D == D && e.bf16 == bf16) {
             *mq = e.mq;
             *mk = e.mk;
             *mv = e.mv;
+            *mo = e.mo;
             return true;
         }
     }
-    FwdMaps e{q, k, v, BH, N, D, bf16, {}, {}, {}};
+    FwdMaps e{q, k, v, o, BH, N, D, bf16, {}, {}, {}, {}};
     if (!make_map(&e.mq, q, BH, N, D, kBM, bf16) || !make_map(&e.mk, k, BH, N, D, kv_rows, bf16) ||
-        !make_map(&e.mv, v, BH, N, D, kv_rows, bf16))
+        !make_map(&e.mv, v, BH, N, D, kv_rows, bf16) || !make_map(&e.mo, o, BH, N, D, kBM, bf16))
         return false;
     slots[next] = e;
     next = (next + 1) % kSlots;
@@ -741,6 +769,7 @@ bool fwd_maps(const void* q, const void* k, const void* v, int64_t BH, int64_t N
     *mq = e.mq;
     *mk = e.mk;
     *mv = e.mv;
+    *mo = e.mo;
     return true;
 }
 
@@ -770,8 +799,8 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
         return aerr == cudaSuccess;
     });
     if (!ok) return ATTN_ERR_LAUNCH;
-    CUtensorMap mq, mk, mv;
-    if (!fwd_maps(q, k, v, BH, N, D, Lay<D>::kBN, BF16, &mq, &mk, &mv)) return ATTN_ERR_DEVICE;
+    CUtensorMap mq, mk, mv, mo;
+    if (!fwd_maps(q, k, v, o, BH, N, D, Lay<D>::kBN, BF16, &mq, &mk, &mv, &mo)) return ATTN_ERR_DEVICE;
     TcParams prm;
     prm.o = o;
     prm.lse = lse;
@@ -801,7 +830,7 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
         }, prm.order);
     }
     attn_fwd_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, kSmemBytes, stream>>>(
-        mq, mk, mv, prm);
+        mq, mk, mv, mo, prm);
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess && std::getenv("ATTN_DEBUG"))
         std::fprintf(stderr, "attn: tensor-core kernel launch failed: %s\n", cudaGetErrorString(err));
