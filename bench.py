@@ -480,6 +480,33 @@ def ffma_peak(dev, stream, launches=5, iters=8192):
     return best
 
 
+def sfu_peak(dev, stream, launches=5, iters=16384):
+    """The rate of ex2.approx on this GPU from the library's own probe kernel (attn_probe_sfu_ex2:
+    one 1024-thread block per SM, 8 independent chains a = 2^(-a) a thread): best of `launches`
+    launches, in exponentials per second, with the median SM clock NVML read meanwhile and the
+    rate per SM per clock at that clock."""
+    import torch
+
+    import online_softmax_flashattention_gb300 as fa
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = torch.empty(sms * 1024, dtype=torch.float32, device=dev)
+    fa.attn_probe_sfu_ex2(sink, 64, stream=stream)
+    torch.cuda.synchronize(dev)
+    best = None
+    with ClockSampler(dev.index) as cs:
+        for _ in range(launches):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ops = fa.attn_probe_sfu_ex2(sink, iters, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            rate = ops / (e0.elapsed_time(e1) * 1e-3)
+            best = rate if best is None else max(best, rate)
+    mhz = cs.summary()["sm_mhz"]
+    return best, (best / (sms * mhz * 1e6) if mhz else None), mhz
+
+
 def fp32_leg(dev, stream, flush, steps, warmup, with_cpu):
     """The FFMA forward (dtype float32) on attention.cu's largest case, one head of N = 4096,
     causal and not: per-launch CUDA events with the L2 flushed between launches, TFLOP/s as a
@@ -756,6 +783,17 @@ def run_ours(args, rank, world, local):
         o_rows = od.float().cpu().numpy().reshape(-1, w["d"]).astype(np.float64)
         cpu, parity = cpu_baseline_leg(q, k, v, lambda flat: o_rows[flat], args.cpu_seconds)
 
+    sfu = None
+    if rank == 0:
+        # The softmax's second bound at d = 64: one exp2 per visible (query, key) pair.
+        ex_rate, ex_per_clk, ex_mhz = sfu_peak(dev, stream)
+        n_exp = float(w["B"] * w["H"]) * (w["N"] * (w["N"] + 1) / 2 if w["causal"] else w["N"] ** 2)
+        sfu = {"bound": "sfu", "unit": "exp2/s", "exp2_per_launch": n_exp, "achieved": n_exp / (ms * 1e-3),
+               "peak": ex_rate, "frac": n_exp / (ms * 1e-3) / ex_rate,
+               "peak_per_sm_per_clk": ex_per_clk, "peak_sm_mhz": ex_mhz,
+               "peak_source": "measured: attn_probe_sfu_ex2 (ex2.approx chains, one 1024-thread block per SM), "
+                              "best of 5 launches"}
+
     grp.close()
     if rank != 0:
         return
@@ -785,6 +823,7 @@ def run_ours(args, rank, world, local):
         "rounds_ms_per_step": {"rounds": len(rounds), "mean": statistics.fmean(all_ms),
                                "median": statistics.median(all_ms)},
         "host_us_per_call": host_us,
+        "sfu": sfu,
         "cpu_baseline": cpu,
         "parity": parity,
         "ablation": ablation,

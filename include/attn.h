@@ -291,13 +291,22 @@ int attn_plan_launch_order(const int32_t* weights, int64_t n, int32_t fixed, int
  */
 int attn_probe_fp32_fma(float* sink, int64_t sink_floats, int64_t iters, double* flop, void* stream);
 
+/*
+ * attn_probe_sfu_ex2 — the rate of the exponential the softmax uses (ex2.approx, base 2), which
+ * co-bounds the tensor-core forward at d = 64 (one exponential per 256 flop of its products).
+ * Same grid and arguments as attn_probe_fp32_fma: every thread runs 8 independent chains of
+ * `iters` steps a = 2^(-a), and *ops receives the launch's count of exponentials. Not a step of
+ * the attention path.
+ */
+int attn_probe_sfu_ex2(float* sink, int64_t sink_floats, int64_t iters, double* ops, void* stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* attn_status_string(int status);
 
 /* ABI version of this header: (major << 16) | minor (1.1 added attn_fwd_lse, 1.2 attn_bwd,
  * 1.3 attn_fwd_kvcache, 1.4 head width 128 for the forward entry points, 1.5
  * attn_selftest_wait_timeout, 1.6 head width 128 for attn_bwd, 1.7 attn_plan_launch_order, 1.8
- * attn_probe_fp32_fma). */
+ * attn_probe_fp32_fma, 1.9 attn_probe_sfu_ex2). */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

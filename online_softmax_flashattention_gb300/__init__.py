@@ -27,6 +27,7 @@ __all__ = [
     "attn_status_string", "attn_abi_version", "raw", "attn_fwd_materialized_noalloc",
     "ATTN_NOALLOC_MAX_N", "attn_fwd_lse", "attn_bwd", "attn_fwd_kvcache", "attn_kvcache_workspace_bytes",
     "ATTN_KV_MAX_SPLITS", "attn_selftest_wait_timeout", "attn_plan_launch_order", "attn_probe_fp32_fma",
+    "attn_probe_sfu_ex2",
 ]
 
 ATTN_F32, ATTN_BF16, ATTN_F16 = 0, 1, 2
@@ -91,6 +92,8 @@ def raw():
             lib.attn_plan_launch_order.restype = ci
             lib.attn_probe_fp32_fma.argtypes = [vp, i64, i64, ctypes.POINTER(ctypes.c_double), vp]
             lib.attn_probe_fp32_fma.restype = ci
+            lib.attn_probe_sfu_ex2.argtypes = [vp, i64, i64, ctypes.POINTER(ctypes.c_double), vp]
+            lib.attn_probe_sfu_ex2.restype = ci
             _lib = lib
     return _lib
 
@@ -107,6 +110,20 @@ def attn_probe_fp32_fma(sink: torch.Tensor, iters: int, stream=None) -> float:
     if st != 0:
         raise AttnError(st, "attn_probe_fp32_fma")
     return float(flop.value)
+
+
+def attn_probe_sfu_ex2(sink: torch.Tensor, iters: int, stream=None) -> float:
+    """Enqueue the exponential (ex2) throughput probe (see attn_probe_sfu_ex2 in include/attn.h)
+    on `stream` and return the launch's count of exponentials; the caller times the launch with
+    CUDA events. sink: float32 CUDA tensor of >= SMs x 1024."""
+    if sink.dtype != torch.float32 or not sink.is_cuda or not sink.is_contiguous():
+        raise ValueError("sink must be a contiguous float32 CUDA tensor")
+    ops = ctypes.c_double(0.0)
+    st = raw().attn_probe_sfu_ex2(sink.data_ptr(), sink.numel(), int(iters), ctypes.byref(ops),
+                                  _stream(sink.device, stream))
+    if st != 0:
+        raise AttnError(st, "attn_probe_sfu_ex2")
+    return float(ops.value)
 
 
 def attn_status_string(status: int) -> str:

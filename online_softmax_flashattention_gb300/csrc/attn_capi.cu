@@ -304,6 +304,6 @@ int attn_plan_launch_order(const int32_t* weights, int64_t n, int32_t fixed, int
     return ATTN_OK;
 }
 
-int attn_abi_version(void) { return (1 << 16) | 8; }
+int attn_abi_version(void) { return (1 << 16) | 9; }
 
 }  // extern "C"

@@ -188,3 +188,14 @@ def test_fma_probe_checks_before_the_device(lib):
     assert lib.attn_probe_fp32_fma(P, 1 << 20, 0, fp, None) == 1          # iters < 1
     assert lib.attn_probe_fp32_fma(P, 1 << 20, (1 << 24) + 1, fp, None) == 1
     assert lib.attn_probe_fp32_fma(P, 1 << 20, 16, None, None) == 1       # no flop out
+
+
+def test_sfu_probe_checks_before_the_device(lib):
+    import ctypes
+
+    ops = ctypes.c_double(0.0)
+    op = ctypes.byref(ops)
+    assert lib.attn_probe_sfu_ex2(None, 1 << 20, 16, op, None) == 1      # no sink
+    assert lib.attn_probe_sfu_ex2(P, 1 << 20, 0, op, None) == 1          # iters < 1
+    assert lib.attn_probe_sfu_ex2(P, 1 << 20, (1 << 24) + 1, op, None) == 1
+    assert lib.attn_probe_sfu_ex2(P, 1 << 20, 16, None, None) == 1       # no count out
