@@ -665,17 +665,17 @@ def run_ours(args, rank, world, local):
     for _ in range(args.warmup):
         flush.zero_()
         fa.attn_fwd(qd, kd, vd, causal=True, out=od)
-    # The K timed steps (round 1, the reported measurement), then the same K steps repeated in
-    # back-to-back rounds while NVML samples the SM clock, so that the clock record holds enough
-    # samples (a round of K ~0.15 ms steps is shorter than NVML's update interval). The number of
-    # rounds depends only on K, so every rank runs the same number.
-    extra_rounds = min(60, max(0, math.ceil(0.06 / (args.steps * 0.15e-3)) - 1))
+    # The K timed steps (pass 1, the reported measurement), then the same K steps repeated in
+    # back-to-back passes while NVML samples the SM clock, so that the clock record holds enough
+    # samples (a pass of K ~0.15 ms steps is shorter than NVML's update interval). The number of
+    # passes depends only on K, so every rank runs the same number.
+    extra_passes = min(60, max(0, math.ceil(0.06 / (args.steps * 0.15e-3)) - 1))
     sampler = ClockSampler(local)
-    rounds = []
+    passes = []
     grp.barrier()
     torch.cuda.synchronize(dev)
     with sampler:
-        for rnd in range(1 + extra_rounds):
+        for _ in range(1 + extra_passes):
             starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
             ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
             for i in range(args.steps):
@@ -684,12 +684,12 @@ def run_ours(args, rank, world, local):
                 fa.attn_fwd(qd, kd, vd, causal=True, out=od)
                 ends[i].record(stream)
             torch.cuda.synchronize(dev)
-            rounds.append([s.elapsed_time(e) for s, e in zip(starts, ends)])
+            passes.append([s.elapsed_time(e) for s, e in zip(starts, ends)])
     grp.barrier()
-    launch_ms = rounds[0]
+    launch_ms = passes[0]
     ms = statistics.fmean(launch_ms)
     ms_max = grp.max(ms)
-    all_ms = [t for r in rounds for t in r]
+    all_ms = [t for r in passes for t in r]
     status = fa.attn_device_status(clear=True, device=dev)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed steps")
@@ -818,9 +818,9 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": world * flop / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps,
-        "clocks": {**clk, "window": f"round 1 (the {args.steps} timed steps) and {extra_rounds} identical rounds "
+        "clocks": {**clk, "window": f"pass 1 (the {args.steps} timed steps) and {extra_passes} identical passes "
                                     "right after it", "cycles_per_step": (clk["sm_mhz"] or 0) * 1e3 * ms},
-        "rounds_ms_per_step": {"rounds": len(rounds), "mean": statistics.fmean(all_ms),
+        "passes_ms_per_step": {"passes": len(passes), "mean": statistics.fmean(all_ms),
                                "median": statistics.median(all_ms)},
         "host_us_per_call": host_us,
         "sfu": sfu,
