@@ -24,12 +24,16 @@
 //   * One CTA owns two query tiles A and B of 128 rows (rows 256c .. 256c+255 of one head)
 //     and streams K/V tiles of BN keys past both (BN = 128 at head width 64, 64 at 128), so
 //     each K/V tile is fetched once for 256 queries.
-//   * Warp 8 issues TMA loads (128-byte swizzle) into a 3-stage K/V ring guarded by
-//     full/empty mbarriers. Warp 9 owns the tensor memory and issues every tcgen05.mma from
-//     one thread, in whatever order their inputs become ready. Warps 0-3 (tile A) and 4-7
-//     (tile B) are the softmax warpgroups: thread t of a group owns query row t, which is
-//     TMEM lane t, so row reductions need no shuffles. The third warpgroup (warps 8-11)
-//     gives up registers so the softmax groups can hold a whole row of scores.
+//   * Warp 8 issues TMA loads (128-byte swizzle) into a 4-stage K ring and a 3-stage V ring
+//     guarded by full/empty mbarriers. Warp 9 owns the tensor memory and issues the S = Q K^T
+//     products, warp 10 the O += P V products, each from one thread and for whichever tile's
+//     inputs are ready first. Warps 0-3 (tile A) and 4-7 (tile B) are the softmax warpgroups:
+//     thread t of a group owns query row t, which is TMEM lane t, so row reductions need no
+//     shuffles. The third warpgroup (warps 8-11) gives up registers so the softmax groups can
+//     hold a whole row of scores.
+//   * Causal grids launch their blocks in the order of a best-fit-decreasing packing of the
+//     work items into one bin per SM (plan_launch_order), so the hardware's first-free-SM
+//     dispatch balances the uneven causal items.
 //   * Tensor memory (512 columns x 128 lanes x 32 bit): S_A, S_B fp32 scores (BN columns
 //     each), O_A, O_B fp32 outputs (d each), P_A, P_B probabilities as 16-bit pairs (BN/2
 //     each). S = Q K^T runs with both operands in shared memory; O += P V takes P from
