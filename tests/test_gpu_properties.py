@@ -191,3 +191,28 @@ def test_calls_capture_into_a_cuda_graph_and_replay_bit_identically():
     assert fa.attn_device_status(clear=True) == 0
     for a, b in zip(eager, (*grads, o, lse, od)):
         assert torch.equal(a, b)
+
+
+def test_throughput_probes_run_and_report_plausible_rates():
+    # The roofline probes: FFMA chains and ex2.approx chains on every SM. Their counts follow
+    # from the grid (SMs x 1024 threads x 8 chains x iters), and the measured rates sit between
+    # a tenth of and twice the GB300's nominal figures (128 FMA lanes and 32 ex2 per SM per
+    # clock at up to 2.07 GHz), which catches a probe that stops doing its work.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    sink = torch.empty(sms * 1024, dtype=torch.float32, device="cuda")
+    iters = 4096
+    for probe, per_item, nominal in ((fa.attn_probe_fp32_fma, 2.0, 128 * 2 * 2.07e9 * sms),
+                                     (fa.attn_probe_sfu_ex2, 1.0, 32 * 2.07e9 * sms)):
+        probe(sink, 64)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        count = probe(sink, iters)
+        e1.record()
+        torch.cuda.synchronize()
+        assert count == per_item * sms * 1024 * 8 * iters
+        rate = count / (e0.elapsed_time(e1) * 1e-3)
+        assert 0.1 * nominal < rate < 2.0 * nominal, (probe.__name__, rate, nominal)
+        assert bool(torch.isfinite(sink).all())
+    with pytest.raises(fa.AttnError):
+        fa.attn_probe_sfu_ex2(sink[:-1], 16)  # one float short of SMs x 1024
