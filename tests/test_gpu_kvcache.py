@@ -257,3 +257,11 @@ def test_kvcache_tensor_cores_long_cache_few_queries(B, H, Nq, Nk, splits, causa
     # more); three take it from 1024 keys: balanced and explicit shares over a cache of a few
     # hundred tiles.
     _run(0xCAC3FC00 + Nq * 7919 + Nk, B, H, Nq, Nk, "bf16", causal, splits)
+
+
+@pytest.mark.parametrize("H,Nk", [(256, 1024), (255, 1024), (256, 1023)])
+def test_kvcache_kernel_choice_boundary(H, Nk):
+    # Three 16-bit queries at d = 64 move to the tensor-core kernel at 1024 keys and 2^18 cached
+    # rows in the call (H256 Nk1024); one head fewer, or one key fewer, stays on CUDA cores. Both
+    # sides of the boundary against the oracle.
+    _run(0xCAC3FE00 + H * 7 + Nk, 1, H, 3, Nk, "bf16", True, 0)
