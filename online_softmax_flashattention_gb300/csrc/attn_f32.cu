@@ -107,16 +107,32 @@ __global__ void __launch_bounds__(BM * 4 * G)
     for (int t = grp; t < ntiles; t += G) {
         const int kbase = t * kBN;
         group_sync<G, kThreads>(grp);  // the previous tile's products are done with Ks, Vs and Ps
-        for (int idx = tid; idx < kBN * kD4; idx += kThreads) {
-            const int r = idx / kD4, e4 = idx % kD4;
-            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-            if (kbase + r < N) {
-                const int64_t off = static_cast<int64_t>(kbase + r) * D + 4 * e4;
-                kv = *reinterpret_cast<const float4*>(kh + off);
-                vv = *reinterpret_cast<const float4*>(vh + off);
+        // The tile's K and V rows, kPer float4 of each per thread, in batches whose loads are all
+        // issued before their stores, so a thread waits for one load latency a batch.
+        static_assert(kBN * kD4 % kThreads == 0, "whole float4 per thread");
+        constexpr int kPer = kBN * kD4 / kThreads;
+        constexpr int kBatch = kPer < 8 ? kPer : 8;
+#pragma unroll
+        for (int b0 = 0; b0 < kPer; b0 += kBatch) {
+            float4 kr[kBatch], vr[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int idx = tid + (b0 + u) * kThreads;
+                const int r = idx / kD4, e4 = idx % kD4;
+                kr[u] = vr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (kbase + r < N) {
+                    const int64_t off = static_cast<int64_t>(kbase + r) * D + 4 * e4;
+                    kr[u] = *reinterpret_cast<const float4*>(kh + off);
+                    vr[u] = *reinterpret_cast<const float4*>(vh + off);
+                }
             }
-            *reinterpret_cast<float4*>(Ks + r * kLd + 4 * e4) = kv;
-            *reinterpret_cast<float4*>(Vs + r * kLd + 4 * e4) = vv;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int idx = tid + (b0 + u) * kThreads;
+                const int r = idx / kD4, e4 = idx % kD4;
+                *reinterpret_cast<float4*>(Ks + r * kLd + 4 * e4) = kr[u];
+                *reinterpret_cast<float4*>(Vs + r * kLd + 4 * e4) = vr[u];
+            }
         }
         group_sync<G, kThreads>(grp);
 
