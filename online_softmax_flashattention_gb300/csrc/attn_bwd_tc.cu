@@ -8,7 +8,9 @@
 // As on the page the work is split into two kernels so that no program adds into another's
 // rows: one CTA per block of 128 keys keeps dK and dV while the blocks of 128 queries that see
 // those keys go past; one CTA per block of 128 queries keeps dQ while its key blocks go past.
-// Both recompute the scores and dP (the page's trade: no atomics, that work done twice).
+// Both recompute the scores and dP (the page's trade: no atomics, that work done twice). The
+// dQ grid is launched with programmatic stream serialisation: its CTAs take SMs as the dK/dV
+// grid's last CTAs finish and wait for that grid only before they write dq.
 //
 // GB300 mapping. Every product is a tcgen05.mma (bf16/fp16 operands, fp32 accumulate) with
 // the forward kernel's two shapes: SS (both operands K-major tiles as TMA writes them, 128-byte
@@ -341,6 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The dQ kernel may take SMs as this grid's last CTAs finish; it waits for this grid before it
+    // writes dq, whose rows hold the delta values read here.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp < kElemWarps) {
         // ===================== elementwise warps: thread = key (TMEM lane) =====================
@@ -686,6 +691,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && nk > 0) {
             if ((ok = warp_wait(bar(L::kDone), (nk - 1) & 1, abort_flag))) {
                 tc_fence_after();
+                // dq's rows hold the delta values the dK/dV grid reads: wait for that grid to
+                // complete (launched with programmatic serialisation, this grid may start before).
+                asm volatile("griddepcontrol.wait;" ::: "memory");
                 uint16_t* const dq = reinterpret_cast<uint16_t*>(p.grad0) + (static_cast<int64_t>(bh) * N + query) * D;
 #pragma unroll 1
                 for (int h = g * (D / 32); h < (g + 1) * (D / 32); ++h) {
@@ -888,9 +896,18 @@ int launch_impl(const void* q, const void* k, const void* v, const void* o, cons
             return w;
         }, prm.order);
     }
-    attn_bwd_dq_tc_kernel<BF16, D><<<static_cast<unsigned>(blocks), kThreads, QLay<D>::kSmem, stream>>>(
-        mq, mk, mv, mdo, prm);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = QLay<D>::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_bwd_dq_tc_kernel<BF16, D>, mq, mk, mv, mdo, prm) == cudaSuccess ? ATTN_OK
+                                                                                                : ATTN_ERR_LAUNCH;
 }
 
 }  // namespace
