@@ -162,18 +162,22 @@ def test_calls_capture_into_a_cuda_graph_and_replay_bit_identically():
     q, k, v, do = (torch.randn(2, 3, 300, 64, device="cuda", dtype=torch.bfloat16) for _ in range(4))
     kc, vc = (torch.randn(2, 3, 5000, 64, device="cuda", dtype=torch.bfloat16) for _ in range(2))
     q1 = torch.randn(2, 3, 1, 64, device="cuda", dtype=torch.bfloat16)
+    q8 = torch.randn(2, 3, 8, 64, device="cuda", dtype=torch.bfloat16)  # eight queries: tensor-core cache kernel
     ws = torch.empty(max(1, fa.attn_kvcache_workspace_bytes(2, 3, 1, 5000, 0, torch.bfloat16)), dtype=torch.uint8,
                      device="cuda")
+    ws8 = torch.empty(max(1, fa.attn_kvcache_workspace_bytes(2, 3, 8, 5000, 0, torch.bfloat16)), dtype=torch.uint8,
+                      device="cuda")
     o, lse = torch.empty_like(q), torch.empty(2, 3, 300, device="cuda")
-    od = torch.empty_like(q1)
+    od, od8 = torch.empty_like(q1), torch.empty_like(q8)
 
     def step():
         fa.attn_fwd_lse(q, k, v, causal=True, out=o, lse=lse)
         grads = fa.attn_bwd(q, k, v, o, do, lse, causal=True)
         fa.attn_fwd_kvcache(q1, kc, vc, causal=True, workspace=ws, out=od)
+        fa.attn_fwd_kvcache(q8, kc, vc, causal=True, workspace=ws8, out=od8)
         return grads
 
-    eager = [x.clone() for x in (*step(), o, lse, od)]
+    eager = [x.clone() for x in (*step(), o, lse, od, od8)]
     torch.cuda.synchronize()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -184,12 +188,12 @@ def test_calls_capture_into_a_cuda_graph_and_replay_bit_identically():
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         grads = step()
-    for x in (o, lse, od, *grads):
+    for x in (o, lse, od, od8, *grads):
         x.zero_()
     g.replay()
     torch.cuda.synchronize()
     assert fa.attn_device_status(clear=True) == 0
-    for a, b in zip(eager, (*grads, o, lse, od)):
+    for a, b in zip(eager, (*grads, o, lse, od, od8)):
         assert torch.equal(a, b)
 
 
