@@ -45,6 +45,35 @@ __device__ __forceinline__ float ex2f(float x) {
     return y;
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async, cached in L2 only); with `valid` false
+// nothing is read and the 16 bytes are filled with zeros.
+__device__ __forceinline__ void cp_async16(float* smem_dst, const float* gsrc, bool valid) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gsrc), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's most recent copy groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// One 64-key tile of K or V (rows kbase .. kbase + kBN - 1 of a head, rows >= N as zeros) into a
+// padded shared tile, kBN * D / 4 16-byte copies spread over the group's threads.
+template <int kBN, int D, int kThreads>
+__device__ __forceinline__ void load_tile_async(float* dst, const float* src, int kbase, int N, int tid) {
+    constexpr int kD4 = D / 4;
+    constexpr int kLd = D + 4;
+    static_assert(kBN * kD4 % kThreads == 0, "whole 16-byte copies per thread");
+#pragma unroll
+    for (int u = 0; u < kBN * kD4 / kThreads; ++u) {
+        const int idx = tid + u * kThreads;
+        const int r = idx / kD4, e4 = idx % kD4;
+        const bool ok = kbase + r < N;
+        cp_async16(dst + r * kLd + 4 * e4, ok ? src + static_cast<int64_t>(kbase + r) * D + 4 * e4 : src, ok);
+    }
+}
+
 // Group-local barrier (G > 1) or the whole CTA (G = 1).
 template <int G, int kThreads>
 __device__ __forceinline__ void group_sync(int grp) {
@@ -104,37 +133,21 @@ __global__ void __launch_bounds__(BM * 4 * G)
     if constexpr (G > 1) __syncthreads();  // Q is in
     const int kend = causal ? min(N, row0 + BM) : N;
     const int ntiles = (kend + kBN - 1) / kBN;
+    // K and V stream through one shared tile each, software-pipelined with asynchronous copies:
+    // tile t + G's keys load while tile t's softmax and P V run, its values while tile t + G's
+    // scores are formed. Copy groups are committed K, V, K, V, ... so that "all but the newest
+    // group" is always the tile about to be read.
+    if (grp < ntiles) {
+        load_tile_async<kBN, D, kThreads>(Ks, kh, grp * kBN, N, tid);
+        cp_async_commit();
+        load_tile_async<kBN, D, kThreads>(Vs, vh, grp * kBN, N, tid);
+        cp_async_commit();
+    }
     for (int t = grp; t < ntiles; t += G) {
         const int kbase = t * kBN;
-        group_sync<G, kThreads>(grp);  // the previous tile's products are done with Ks, Vs and Ps
-        // The tile's K and V rows, kPer float4 of each per thread, in batches whose loads are all
-        // issued before their stores, so a thread waits for one load latency a batch.
-        static_assert(kBN * kD4 % kThreads == 0, "whole float4 per thread");
-        constexpr int kPer = kBN * kD4 / kThreads;
-        constexpr int kBatch = kPer < 8 ? kPer : 8;
-#pragma unroll
-        for (int b0 = 0; b0 < kPer; b0 += kBatch) {
-            float4 kr[kBatch], vr[kBatch];
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int idx = tid + (b0 + u) * kThreads;
-                const int r = idx / kD4, e4 = idx % kD4;
-                kr[u] = vr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (kbase + r < N) {
-                    const int64_t off = static_cast<int64_t>(kbase + r) * D + 4 * e4;
-                    kr[u] = *reinterpret_cast<const float4*>(kh + off);
-                    vr[u] = *reinterpret_cast<const float4*>(vh + off);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int idx = tid + (b0 + u) * kThreads;
-                const int r = idx / kD4, e4 = idx % kD4;
-                *reinterpret_cast<float4*>(Ks + r * kLd + 4 * e4) = kr[u];
-                *reinterpret_cast<float4*>(Vs + r * kLd + 4 * e4) = vr[u];
-            }
-        }
-        group_sync<G, kThreads>(grp);
+        const bool next = t + G < ntiles;
+        cp_async_wait<1>();            // this thread's copies of K(t) have landed
+        group_sync<G, kThreads>(grp);  // everyone's have
 
         // S micro-tile: rows ty*4+i, keys tx+16j.
         float s[4][kJ];
@@ -159,6 +172,10 @@ __global__ void __launch_bounds__(BM * 4 * G)
                     s[i][j] = fmaf(qa[i].w, kb[j].w, s[i][j]);
                 }
         }
+
+        group_sync<G, kThreads>(grp);  // K(t) is read: the next tile's keys may overwrite it
+        if (next) load_tile_async<kBN, D, kThreads>(Ks, kh, kbase + G * kBN, N, tid);
+        cp_async_commit();
 
         // Mask keys past N and, when causal, keys after the query.
         if (kbase + kBN > N || (causal && kbase + kBN - 1 > row0)) {
@@ -195,7 +212,8 @@ __global__ void __launch_bounds__(BM * 4 * G)
 #pragma unroll
             for (int j = 0; j < 4 * kG; ++j) acc[i][j] *= alpha;
         }
-        group_sync<G, kThreads>(grp);
+        cp_async_wait<1>();            // V(t) has landed (K(t + G) may still be in flight)
+        group_sync<G, kThreads>(grp);  // V(t) and P are visible to the group
 
         // O micro-tile += P V: rows ty*4+i, dims 64g + tx*4+j.
 #pragma unroll 4
@@ -222,7 +240,11 @@ __global__ void __launch_bounds__(BM * 4 * G)
                 }
             }
         }
+        group_sync<G, kThreads>(grp);  // V(t) and P are read
+        if (next) load_tile_async<kBN, D, kThreads>(Vs, vh, kbase + G * kBN, N, tid);
+        cp_async_commit();
     }
+    cp_async_wait<0>();
 
     // Row totals across the 16 threads of the row.
     float tot[4];
