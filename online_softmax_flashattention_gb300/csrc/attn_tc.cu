@@ -164,6 +164,21 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag) {
     atomicOr(&g_tc_error, 1u);
 }
 
+// A decision of an issuer loop: with kWarp the whole warp runs the loop, so the lanes' results
+// are combined into one (every lane reads the same barrier or flag in the same instruction, so
+// they agree anyway; the vote makes the branch provably uniform for elect.sync); a single-lane
+// issuer passes its own result through.
+template <bool kWarp>
+__device__ __forceinline__ bool warp_vote(bool v) {
+    if constexpr (kWarp) return __all_sync(0xffffffffu, v);
+    return v;
+}
+template <bool kWarp>
+__device__ __forceinline__ bool warp_vote_any(bool v) {
+    if constexpr (kWarp) return __any_sync(0xffffffffu, v);
+    return v;
+}
+
 // All lanes of a warp wait; the result is the same in every lane, so a warp never splits
 // in front of a warp-collective tcgen05.ld / tcgen05.st.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -335,20 +350,29 @@ __device__ __forceinline__ bool softmax_step(const SoftmaxCtx& cx, uint32_t (&su
 }
 
 // S_X(j) = Q_X K_j^T : M=128, N=BN, K=D as D/16 steps of K=16 (32 bytes of a 128-byte row;
-// steps 4..7 of D = 128 read the second column block of each tile).
-template <bool BF16, int D>
+// steps 4..7 of D = 128 read the second column block of each tile). kWarp: issued by a whole
+// converged warp, elect.sync picking the lane (see the S issuer); else by the calling thread.
+template <bool BF16, int D, bool kWarp>
 __device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sQx, uint32_t sKs, int X, uint32_t bar_s_full) {
     using L = Lay<D>;
     constexpr uint32_t kIdescQK = idesc_f16(BF16, kBM, L::kBN, false, false);
+    // The descriptors of the K=16 steps differ only in their start address (bits 0-13, in
+    // 16-byte units; shared addresses stay below 2^18 bytes, so the field cannot carry over).
+    const uint64_t a0 = smem_desc_sw128(sQx, 16, 1024);
+    const uint64_t b0 = smem_desc_sw128(sKs, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t a_off = static_cast<uint32_t>((kk >> 2) * kBlockBytes + 32 * (kk & 3));
-        const uint32_t b_off = static_cast<uint32_t>((kk >> 2) * L::kKVBlockBytes + 32 * (kk & 3));
-        const uint64_t a = smem_desc_sw128(sQx + a_off, 16, 1024);
-        const uint64_t b = smem_desc_sw128(sKs + b_off, 16, 1024);
-        umma_ss(tmem + L::colS(X), a, b, kIdescQK, kk > 0 ? 1u : 0u);
+        const uint64_t a = a0 + static_cast<uint64_t>(((kk >> 2) * kBlockBytes + 32 * (kk & 3)) >> 4);
+        const uint64_t b = b0 + static_cast<uint64_t>(((kk >> 2) * L::kKVBlockBytes + 32 * (kk & 3)) >> 4);
+        if constexpr (kWarp)
+            umma_ss_elect(tmem + L::colS(X), a, b, kIdescQK, kk > 0 ? 1u : 0u);
+        else
+            umma_ss(tmem + L::colS(X), a, b, kIdescQK, kk > 0 ? 1u : 0u);
     }
-    umma_commit(bar_s_full);
+    if constexpr (kWarp)
+        umma_commit_elect(bar_s_full);
+    else
+        umma_commit(bar_s_full);
 }
 
 // O_X += P_X V_j : M=128, N=D, K=BN as BN/16 steps of K=16 (16 keys = 2048 bytes of each V
@@ -359,9 +383,10 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sVs, int X, boo
     using L = Lay<D>;
     constexpr uint32_t kIdescPV = idesc_f16(BF16, kBM, D, false, true);
     constexpr uint32_t kLbo = D == 64 ? 16u : static_cast<uint32_t>(L::kKVBlockBytes);
+    const uint64_t b0 = smem_desc_sw128(sVs, kLbo, 1024);
 #pragma unroll
     for (int kk = 0; kk < L::kBN / 16; ++kk) {
-        const uint64_t b = smem_desc_sw128(sVs + 2048 * kk, kLbo, 1024);
+        const uint64_t b = b0 + static_cast<uint64_t>((2048 * kk) >> 4);
         umma_ts(tmem + L::colO(X), tmem + L::colP(X) + 8u * kk, b, kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
     }
     umma_commit(bar_o_ready);
@@ -374,6 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
                        const TcParams p) {
     using L = Lay<D>;
+    // Who issues S = Q K^T. At D = 128 a step's S is eight N = 64 products, and issuing them
+    // from a whole converged warp (operands in uniform registers, elect.sync picking the lane)
+    // is what keeps them fed: B1 H12 N8192 causal 1153 -> 1383 TFLOP/s. At D = 64 (four N = 128
+    // products a step, the softmax warps heavier) the single-lane issuer measured faster
+    // (981 against 953).
+    constexpr bool kWarpS = D == 128;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -585,13 +616,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(bar(L::kBarKFull + j % L::kKStages), (j / L::kKStages) & 1, nullptr, kDrainTimeoutNs);
             for (int j = max(0, vissued - L::kVStages); j < vissued; ++j)
                 mbar_wait(bar(L::kBarVFull + j % L::kVStages), (j / L::kVStages) & 1, nullptr, kDrainTimeoutNs);
-        } else if (warp == kSIssuerWarp && lane == 0) {
+        } else if (warp == kSIssuerWarp && (kWarpS || lane == 0)) {
             // ============================ S issuer: QK^T ============================
             // S_X(j) goes out as soon as K_j has landed and (j > 0) softmax X has copied
             // S_X(j-1) out of tensor memory; the two tiles progress independently. K_j's stage
             // is released by the later of the two tiles' products (the only one when the other
-            // tile does not read K_j).
-            bool ok = mbar_wait(bar(L::kBarQFull), 0, abort_flag, kWaitTimeoutNs);
+            // tile does not read K_j). At D = 128 (kWarpS) the whole warp runs this loop and
+            // elect.sync issues: every decision is a warp vote, so the warp never splits.
+            bool ok = warp_vote<kWarpS>(mbar_wait(bar(L::kBarQFull), 0, abort_flag, kWaitTimeoutNs));
             int ns0 = 0, ns1 = 0;
             uint64_t idle_since = 0;
             uint32_t polls = 0;
@@ -607,14 +639,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int nX = X ? nB : nA, nO = X ? nA : nB, other = X ? ns0 : ns1;
                     // The usually-late condition first: barrier tests are slow while products
                     // stream their operands out of shared memory.
-                    if (j < nX && (j == 0 || mbar_test(bar(L::kBarSFree + X), (j - 1) & 1)) &&
-                        mbar_test(bar(L::kBarKFull + j % L::kKStages), (j / L::kKStages) & 1)) {
+                    if (j < nX && warp_vote<kWarpS>((j == 0 || mbar_test(bar(L::kBarSFree + X), (j - 1) & 1)) &&
+                                                    mbar_test(bar(L::kBarKFull + j % L::kKStages), (j / L::kKStages) & 1))) {
                         tc_fence_after();
-                        issue_s<BF16, D>(tmem, sQ + X * L::kTileBytes, sK + (j % L::kKStages) * L::kKVTileBytes, X,
-                                      bar(L::kBarSFull + X));
+                        issue_s<BF16, D, kWarpS>(tmem, sQ + X * L::kTileBytes, sK + (j % L::kKStages) * L::kKVTileBytes,
+                                                 X, bar(L::kBarSFull + X));
                         // K_j is released once, after the last product that reads it (a commit
                         // covers every earlier product of this thread).
-                        if (other > j || j >= nO) umma_commit(bar(L::kBarKEmpty + j % L::kKStages));
+                        if (other > j || j >= nO) {
+                            if constexpr (kWarpS)
+                                umma_commit_elect(bar(L::kBarKEmpty + j % L::kKStages));
+                            else
+                                umma_commit(bar(L::kBarKEmpty + j % L::kKStages));
+                        }
                         ++j;
                         progressed = true;
                     }
@@ -627,12 +664,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if ((++polls & 15u) == 0) {
                         const uint64_t now = global_timer_ns();
                         if (idle_since == 0) idle_since = now;
-                        if (*abort_flag || now - idle_since > kWaitTimeoutNs) ok = false;
+                        if (warp_vote_any<kWarpS>(*abort_flag != 0 || now - idle_since > kWaitTimeoutNs)) ok = false;
                     }
                 }
             }
-            if (!ok) raise_abort(abort_flag);
-            umma_commit(bar(L::kBarDrain + 0));  // no S product may still run at teardown
+            if (!ok && lane == 0) raise_abort(abort_flag);
+            if constexpr (kWarpS)
+                umma_commit_elect(bar(L::kBarDrain + 0));  // no S product may still run at teardown
+            else
+                umma_commit(bar(L::kBarDrain + 0));
             mbar_wait(bar(L::kBarDrain + 0), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         } else if (warp == kPVIssuerWarp && lane == 0) {
             // ============================== PV issuer ==============================
