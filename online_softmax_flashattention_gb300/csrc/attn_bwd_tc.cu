@@ -185,28 +185,54 @@ __global__ void __launch_bounds__(256)
 // 128 x NB product over K = D of two K-major tiles (D/64 column blocks of 128-byte rows each,
 // kABlk and kBBlk bytes apart in A and B) into TMEM columns `d`: D/16 steps of K = 16, the ones
 // past 64 in the second column block.
-template <bool BF16, int D, int NB, int kABlk, int kBBlk>
+template <bool BF16, int D, int NB, int kABlk, int kBBlk, bool kWarp = false>
 __device__ __forceinline__ void mma_ss_kmajor(uint32_t d, uint32_t sA, uint32_t sB) {
     constexpr uint32_t kIdesc = idesc_f16(BF16, kBlk, NB, false, false);
+    // The steps' descriptors differ only in the start address field (16-byte units).
+    const uint64_t a0 = smem_desc_sw128(sA, 16, 1024);
+    const uint64_t b0 = smem_desc_sw128(sB, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t a_off = static_cast<uint32_t>((kk >> 2) * kABlk + 32 * (kk & 3));
-        const uint32_t b_off = static_cast<uint32_t>((kk >> 2) * kBBlk + 32 * (kk & 3));
-        umma_ss(d, smem_desc_sw128(sA + a_off, 16, 1024), smem_desc_sw128(sB + b_off, 16, 1024), kIdesc,
-                kk > 0 ? 1u : 0u);
+        const uint64_t a = a0 + static_cast<uint64_t>(((kk >> 2) * kABlk + 32 * (kk & 3)) >> 4);
+        const uint64_t b = b0 + static_cast<uint64_t>(((kk >> 2) * kBBlk + 32 * (kk & 3)) >> 4);
+        if constexpr (kWarp)
+            umma_ss_elect(d, a, b, kIdesc, kk > 0 ? 1u : 0u);
+        else
+            umma_ss(d, a, b, kIdesc, kk > 0 ? 1u : 0u);
     }
 }
 
 // 128 x D product over K = 16 KSTEPS with A (128 lanes, K-step kk at column a + 8 kk) in TMEM
 // and B an MN-major tile (rows = K, 16 rows = 2048 bytes a step; D/64 column blocks kBBlk bytes
 // apart, the descriptor's leading byte offset), accumulated into TMEM columns `d`.
-template <bool BF16, int D, int KSTEPS, int kBBlk>
+template <bool BF16, int D, int KSTEPS, int kBBlk, bool kWarp = false>
 __device__ __forceinline__ void mma_ts_mn(uint32_t d, uint32_t a, uint32_t sB, bool accumulate) {
     constexpr uint32_t kIdesc = idesc_f16(BF16, kBlk, D, false, true);
     constexpr uint32_t kLbo = D == 64 ? 16u : static_cast<uint32_t>(kBBlk);
+    const uint64_t b0 = smem_desc_sw128(sB, kLbo, 1024);
 #pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk)
-        umma_ts(d, a + 8u * kk, smem_desc_sw128(sB + 2048 * kk, kLbo, 1024), kIdesc, (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+        const uint64_t b = b0 + static_cast<uint64_t>((2048 * kk) >> 4);
+        if constexpr (kWarp)
+            umma_ts_elect(d, a + 8u * kk, b, kIdesc, (accumulate || kk > 0) ? 1u : 0u);
+        else
+            umma_ts(d, a + 8u * kk, b, kIdesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+// An issuer's decision: with kWarp the whole warp runs the issuing loop (elect.sync picks the
+// lane that issues), so each lane's result is combined into one and the warp never splits.
+template <bool kWarp>
+__device__ __forceinline__ bool issuer_vote(bool v) {
+    if constexpr (kWarp) return __all_sync(0xffffffffu, v);
+    return v;
+}
+template <bool kWarp>
+__device__ __forceinline__ void issuer_commit(uint32_t bar) {
+    if constexpr (kWarp)
+        umma_commit_elect(bar);
+    else
+        umma_commit(bar);
 }
 
 // TMA copy of one tile of a [BH][N][D] tensor: D/64 boxes of 64 values (the map's box rows),
@@ -296,6 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const BwdParams p) {
     using L = KvLay<D>;
     constexpr int kTile = L::kTile;
+    // Which issuers run as a whole converged warp (elect.sync issues, operands in uniform
+    // registers) rather than as one lane. Measured (B1 H12 N8192 causal, L2 flushed, outputs
+    // bit-identical): the dV/dK issuer warp-wide at D = 64, 808 -> 851 TFLOP/s for the pair of
+    // grids (N4096 non-causal 701 -> 742); at D = 128 no gain (882 -> 879); the S^T/dP^T issuer
+    // warp-wide lost at both widths (795, 845).
+    constexpr bool kWarpA = false;
+    constexpr bool kWarpB = D == 64;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -456,53 +489,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(bar(L::kKV), 0, nullptr, kDrainTimeoutNs);
             for (int i = (issued > L::kStages ? issued - L::kStages : 0); i < issued; ++i)
                 mbar_wait(bar(L::kQFull + i % L::kStages), (i / L::kStages) & 1, nullptr, kDrainTimeoutNs);
-        } else if (warp == kMmaWarp && lane == 0) {
+        } else if (warp == kMmaWarp && (kWarpA || lane == 0)) {
             // ============================ MMA issuer: S^T, dP^T ============================
             // S^T(0), dP^T(0); then block i+1's once block i's were copied out (d = 128: once
             // block i's dV, dK products are done, as P^T and dS^T sit over S^T and dP^T). The
             // products that take P^T and dS^T come from another warp: a thread's barrier waits
             // queue behind the tensor-core instructions it issued before, so one issuer would
             // let the pipe drain at every hand-off.
-            bool ok = mbar_wait(bar(L::kKV), 0, abort_flag, kWaitTimeoutNs);
+            bool ok = issuer_vote<kWarpA>(mbar_wait(bar(L::kKV), 0, abort_flag, kWaitTimeoutNs));
             auto issue_sdp = [&](int i) {
                 const uint32_t stage = base + L::kOffStage + (i % L::kStages) * L::kStageBytes;
-                if (!mbar_wait(bar(L::kQFull + i % L::kStages), (i / L::kStages) & 1, abort_flag, kWaitTimeoutNs))
+                if (!issuer_vote<kWarpA>(
+                        mbar_wait(bar(L::kQFull + i % L::kStages), (i / L::kStages) & 1, abort_flag, kWaitTimeoutNs)))
                     return false;
                 tc_fence_after();
-                mma_ss_kmajor<BF16, D, BQ, kBlockBytes, L::kQBlockBytes>(tmem + L::kColS, base + L::kOffK,
-                                                                         stage);  // S^T = K Q^T
-                mma_ss_kmajor<BF16, D, BQ, kBlockBytes, L::kQBlockBytes>(tmem + L::kColDP, base + L::kOffV,
-                                                                         stage + L::kTileQ);  // dP^T = V dO^T
-                umma_commit(bar(L::kDPFull));
+                mma_ss_kmajor<BF16, D, BQ, kBlockBytes, L::kQBlockBytes, kWarpA>(tmem + L::kColS, base + L::kOffK,
+                                                                                 stage);  // S^T = K Q^T
+                mma_ss_kmajor<BF16, D, BQ, kBlockBytes, L::kQBlockBytes, kWarpA>(tmem + L::kColDP, base + L::kOffV,
+                                                                                 stage + L::kTileQ);  // dP^T = V dO^T
+                issuer_commit<kWarpA>(bar(L::kDPFull));
                 return true;
             };
             if (ok && nq > 0) ok = issue_sdp(0);
             for (int i = 0; ok && i + 1 < nq; ++i) {
-                if (!(ok = mbar_wait(bar(L::kSdPFree), i & 1, abort_flag, kWaitTimeoutNs))) break;
+                if (!(ok = issuer_vote<kWarpA>(mbar_wait(bar(L::kSdPFree), i & 1, abort_flag, kWaitTimeoutNs)))) break;
                 tc_fence_after();
                 if (!(ok = issue_sdp(i + 1))) break;
             }
-            if (!ok) raise_abort(abort_flag);
-            umma_commit(bar(L::kDrain));
+            if (!ok && lane == 0) raise_abort(abort_flag);
+            issuer_commit<kWarpA>(bar(L::kDrain));
             mbar_wait(bar(L::kDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
-        } else if (warp == kMma2Warp && lane == 0) {
+        } else if (warp == kMma2Warp && (kWarpB || lane == 0)) {
             // ============================ MMA issuer: dV, dK ============================
             // dV, dK += block i's P^T dO, dS^T Q once P^T and dS^T are in TMEM (block i's
             // S^T, dP^T products are then done, so the stage's tiles have landed).
             bool ok = true;
             for (int i = 0; ok && i < nq; ++i) {
-                if (!(ok = mbar_wait(bar(L::kPdSFull), i & 1, abort_flag, kWaitTimeoutNs))) break;
+                if (!(ok = issuer_vote<kWarpB>(mbar_wait(bar(L::kPdSFull), i & 1, abort_flag, kWaitTimeoutNs)))) break;
                 tc_fence_after();
                 const uint32_t stage = base + L::kOffStage + (i % L::kStages) * L::kStageBytes;
-                mma_ts_mn<BF16, D, BQ / 16, L::kQBlockBytes>(tmem + L::kColDV, tmem + L::kColP, stage + L::kTileQ,
-                                                             i > 0);  // dV += P^T dO
-                mma_ts_mn<BF16, D, BQ / 16, L::kQBlockBytes>(tmem + L::kColDK, tmem + L::kColDS, stage,
-                                                             i > 0);  // dK += dS^T Q
-                umma_commit(bar(L::kDone));
-                umma_commit(bar(L::kQEmpty + i % L::kStages));
+                mma_ts_mn<BF16, D, BQ / 16, L::kQBlockBytes, kWarpB>(tmem + L::kColDV, tmem + L::kColP, stage + L::kTileQ,
+                                                                     i > 0);  // dV += P^T dO
+                mma_ts_mn<BF16, D, BQ / 16, L::kQBlockBytes, kWarpB>(tmem + L::kColDK, tmem + L::kColDS, stage,
+                                                                     i > 0);  // dK += dS^T Q
+                issuer_commit<kWarpB>(bar(L::kDone));
+                issuer_commit<kWarpB>(bar(L::kQEmpty + i % L::kStages));
             }
-            if (!ok) raise_abort(abort_flag);
-            umma_commit(bar(L::kDrain2));
+            if (!ok && lane == 0) raise_abort(abort_flag);
+            issuer_commit<kWarpB>(bar(L::kDrain2));
             mbar_wait(bar(L::kDrain2), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         } else if (warp == kLoaderWarp) {
             // ==================== warp 11: each query block's lse and delta ====================
@@ -595,6 +629,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = QLay<D>;
     constexpr int kTile = L::kTile;
     constexpr int S = L::kStages;
+    // As in the dK/dV kernel: the dQ issuer warp-wide at D = 64, the S/dP issuer one lane.
+    constexpr bool kWarpA = false;
+    constexpr bool kWarpB = D == 64;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -739,47 +776,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(bar(qQ), 0, nullptr, kDrainTimeoutNs);
             for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
                 mbar_wait(bar(qKVFull + j % S), (j / S) & 1, nullptr, kDrainTimeoutNs);
-        } else if (warp == kMmaWarp && lane == 0) {
+        } else if (warp == kMmaWarp && (kWarpA || lane == 0)) {
             // ============================= MMA issuer: S, dP =============================
             // S(0), dP(0); then key block j+1's once block j's were copied out. dQ comes from
             // another warp (see the dK/dV kernel).
-            bool ok = mbar_wait(bar(qQ), 0, abort_flag, kWaitTimeoutNs);
+            bool ok = issuer_vote<kWarpA>(mbar_wait(bar(qQ), 0, abort_flag, kWaitTimeoutNs));
             auto issue_sdp = [&](int j) {
                 const int st = j % S;
                 const uint32_t stage = base + L::kOffKV + st * L::kStageBytes;
-                if (!mbar_wait(bar(qKVFull + st), (j / S) & 1, abort_flag, kWaitTimeoutNs)) return false;
+                if (!issuer_vote<kWarpA>(mbar_wait(bar(qKVFull + st), (j / S) & 1, abort_flag, kWaitTimeoutNs)))
+                    return false;
                 tc_fence_after();
-                mma_ss_kmajor<BF16, D, kBlk, kBlockBytes, kBlockBytes>(tmem + L::kColS, base + L::kOffQ,
-                                                                       stage);  // S = Q K^T
-                mma_ss_kmajor<BF16, D, kBlk, kBlockBytes, kBlockBytes>(tmem + L::kColDP, base + L::kOffDO,
-                                                                       stage + kTile);  // dP = dO V^T
-                umma_commit(bar(L::kDPFull));
+                mma_ss_kmajor<BF16, D, kBlk, kBlockBytes, kBlockBytes, kWarpA>(tmem + L::kColS, base + L::kOffQ,
+                                                                               stage);  // S = Q K^T
+                mma_ss_kmajor<BF16, D, kBlk, kBlockBytes, kBlockBytes, kWarpA>(tmem + L::kColDP, base + L::kOffDO,
+                                                                               stage + kTile);  // dP = dO V^T
+                issuer_commit<kWarpA>(bar(L::kDPFull));
                 return true;
             };
             if (ok && nk > 0) ok = issue_sdp(0);
             for (int j = 0; ok && j + 1 < nk; ++j) {
-                if (!(ok = mbar_wait(bar(L::kSdPFree), j & 1, abort_flag, kWaitTimeoutNs))) break;
+                if (!(ok = issuer_vote<kWarpA>(mbar_wait(bar(L::kSdPFree), j & 1, abort_flag, kWaitTimeoutNs)))) break;
                 tc_fence_after();
                 if (!(ok = issue_sdp(j + 1))) break;
             }
-            if (!ok) raise_abort(abort_flag);
-            umma_commit(bar(L::kDrain));
+            if (!ok && lane == 0) raise_abort(abort_flag);
+            issuer_commit<kWarpA>(bar(L::kDrain));
             mbar_wait(bar(L::kDrain), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
-        } else if (warp == kMma2Warp && lane == 0) {
+        } else if (warp == kMma2Warp && (kWarpB || lane == 0)) {
             // ============================== MMA issuer: dQ ==============================
             // dQ += dS K once block j's dS is in TMEM (its S, dP products are then done).
             bool ok = true;
             for (int j = 0; ok && j < nk; ++j) {
-                if (!(ok = mbar_wait(bar(L::kDSFull), j & 1, abort_flag, kWaitTimeoutNs))) break;
+                if (!(ok = issuer_vote<kWarpB>(mbar_wait(bar(L::kDSFull), j & 1, abort_flag, kWaitTimeoutNs)))) break;
                 tc_fence_after();
                 const uint32_t stage = base + L::kOffKV + (j % S) * L::kStageBytes;
-                mma_ts_mn<BF16, D, kBlk / 16, kBlockBytes>(tmem + L::kColDQ, tmem + L::kColDS, stage,
-                                                           j > 0);  // dQ += dS K
-                umma_commit(bar(L::kDone));
-                umma_commit(bar(L::kKVEmpty + j % S));
+                mma_ts_mn<BF16, D, kBlk / 16, kBlockBytes, kWarpB>(tmem + L::kColDQ, tmem + L::kColDS, stage,
+                                                                   j > 0);  // dQ += dS K
+                issuer_commit<kWarpB>(bar(L::kDone));
+                issuer_commit<kWarpB>(bar(L::kKVEmpty + j % S));
             }
-            if (!ok) raise_abort(abort_flag);
-            umma_commit(bar(L::kDrain2));
+            if (!ok && lane == 0) raise_abort(abort_flag);
+            issuer_commit<kWarpB>(bar(L::kDrain2));
             mbar_wait(bar(L::kDrain2), 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         }
     }
