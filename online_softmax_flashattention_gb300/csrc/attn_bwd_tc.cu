@@ -497,24 +497,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             // queue behind the tensor-core instructions it issued before, so one issuer would
             // let the pipe drain at every hand-off.
             bool ok = issuer_vote<kWarpA>(mbar_wait(bar(L::kKV), 0, abort_flag, kWaitTimeoutNs));
+            // Block i's (Q, dO) tiles are waited for before the release of block i-1's S^T and
+            // dP^T, which comes last: the products then go out one barrier test after it.
+            auto wait_tiles = [&](int i) {
+                return issuer_vote<kWarpA>(
+                    mbar_wait(bar(L::kQFull + i % L::kStages), (i / L::kStages) & 1, abort_flag, kWaitTimeoutNs));
+            };
             auto issue_sdp = [&](int i) {
                 const uint32_t stage = base + L::kOffStage + (i % L::kStages) * L::kStageBytes;
-                if (!issuer_vote<kWarpA>(
-                        mbar_wait(bar(L::kQFull + i % L::kStages), (i / L::kStages) & 1, abort_flag, kWaitTimeoutNs)))
-                    return false;
                 tc_fence_after();
                 mma_ss_kmajor<BF16, D, BQ, kBlockBytes, L::kQBlockBytes, kWarpA>(tmem + L::kColS, base + L::kOffK,
                                                                                  stage);  // S^T = K Q^T
                 mma_ss_kmajor<BF16, D, BQ, kBlockBytes, L::kQBlockBytes, kWarpA>(tmem + L::kColDP, base + L::kOffV,
                                                                                  stage + L::kTileQ);  // dP^T = V dO^T
                 issuer_commit<kWarpA>(bar(L::kDPFull));
-                return true;
             };
-            if (ok && nq > 0) ok = issue_sdp(0);
+            if (ok && nq > 0 && (ok = wait_tiles(0))) issue_sdp(0);
             for (int i = 0; ok && i + 1 < nq; ++i) {
+                if (!(ok = wait_tiles(i + 1))) break;
                 if (!(ok = issuer_vote<kWarpA>(mbar_wait(bar(L::kSdPFree), i & 1, abort_flag, kWaitTimeoutNs)))) break;
-                tc_fence_after();
-                if (!(ok = issue_sdp(i + 1))) break;
+                issue_sdp(i + 1);
             }
             if (!ok && lane == 0) raise_abort(abort_flag);
             issuer_commit<kWarpA>(bar(L::kDrain));
@@ -781,24 +783,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S(0), dP(0); then key block j+1's once block j's were copied out. dQ comes from
             // another warp (see the dK/dV kernel).
             bool ok = issuer_vote<kWarpA>(mbar_wait(bar(qQ), 0, abort_flag, kWaitTimeoutNs));
+            // Key block j's tiles are waited for before the release of block j-1's S and dP (as
+            // in the dK/dV kernel).
+            auto wait_tiles = [&](int j) {
+                return issuer_vote<kWarpA>(mbar_wait(bar(qKVFull + j % S), (j / S) & 1, abort_flag, kWaitTimeoutNs));
+            };
             auto issue_sdp = [&](int j) {
-                const int st = j % S;
-                const uint32_t stage = base + L::kOffKV + st * L::kStageBytes;
-                if (!issuer_vote<kWarpA>(mbar_wait(bar(qKVFull + st), (j / S) & 1, abort_flag, kWaitTimeoutNs)))
-                    return false;
+                const uint32_t stage = base + L::kOffKV + (j % S) * L::kStageBytes;
                 tc_fence_after();
                 mma_ss_kmajor<BF16, D, kBlk, kBlockBytes, kBlockBytes, kWarpA>(tmem + L::kColS, base + L::kOffQ,
                                                                                stage);  // S = Q K^T
                 mma_ss_kmajor<BF16, D, kBlk, kBlockBytes, kBlockBytes, kWarpA>(tmem + L::kColDP, base + L::kOffDO,
                                                                                stage + kTile);  // dP = dO V^T
                 issuer_commit<kWarpA>(bar(L::kDPFull));
-                return true;
             };
-            if (ok && nk > 0) ok = issue_sdp(0);
+            if (ok && nk > 0 && (ok = wait_tiles(0))) issue_sdp(0);
             for (int j = 0; ok && j + 1 < nk; ++j) {
+                if (!(ok = wait_tiles(j + 1))) break;
                 if (!(ok = issuer_vote<kWarpA>(mbar_wait(bar(L::kSdPFree), j & 1, abort_flag, kWaitTimeoutNs)))) break;
-                tc_fence_after();
-                if (!(ok = issue_sdp(j + 1))) break;
+                issue_sdp(j + 1);
             }
             if (!ok && lane == 0) raise_abort(abort_flag);
             issuer_commit<kWarpA>(bar(L::kDrain));
