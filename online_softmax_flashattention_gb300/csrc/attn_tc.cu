@@ -26,8 +26,9 @@
 //     each K/V tile is fetched once for 256 queries.
 //   * Warp 8 issues TMA loads (128-byte swizzle) into a 4-stage K ring and a 3-stage V ring
 //     guarded by full/empty mbarriers. Warp 9 owns the tensor memory and issues the S = Q K^T
-//     products, warp 10 the O += P V products, each from one thread and for whichever tile's
-//     inputs are ready first. Warps 0-3 (tile A) and 4-7 (tile B) are the softmax warpgroups:
+//     products, warp 10 the O += P V products, each for whichever tile's inputs are ready
+//     first: the PV products from one thread, the S products from one thread at head width 64
+//     and from the whole warp (elect.sync) at 128. Warps 0-3 (tile A) and 4-7 (tile B) are the softmax warpgroups:
 //     thread t of a group owns query row t, which is TMEM lane t, so row reductions need no
 //     shuffles. The third warpgroup (warps 8-11) gives up registers so the softmax groups can
 //     hold a whole row of scores.
