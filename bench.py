@@ -570,6 +570,87 @@ def sfu_peak(dev, stream, launches=5, iters=16384):
     return best, (best / (sms * mhz * 1e6) if mhz else None), mhz
 
 
+SMALL = [  # the fp32 configurations of the pages' own tests: (name, B, H, N, causal)
+    ("config1 B1 H1 N256 non-causal", 1, 1, 256, False),
+    ("config2 B1 H1 N1024 causal", 1, 1, 1024, True),
+    ("config2 B1 H1 N1024 non-causal", 1, 1, 1024, False),
+    ("config3 B2 H3 N1 causal", 2, 3, 1, True),
+    ("config3 B2 H3 N100 causal", 2, 3, 100, True),
+    ("config3 B2 H3 N256 causal", 2, 3, 256, True),
+    ("config3 B2 H3 N1000 causal", 2, 3, 1000, True),
+]
+
+
+def small_configs_leg(dev, stream, launches, warmup, with_cpu):
+    """The small fp32 configurations (d = 64, i.i.d. N(0,1)). Each call is a few microseconds of
+    GPU work, less than the host's time to make it, so calls timed one by one measure the host.
+    Instead `launches` calls are captured in a CUDA graph and the replay is timed with CUDA events
+    (inputs L2-resident): GPU time per call. The host-side wall time of one call through the
+    Python binding is reported beside it. Every row is checked against the oracle under the
+    contract's fp32 rule (1e-5 N max|ref|). For config 1 the oracle's own time on one host thread
+    and on all of them is reported too."""
+    import torch
+
+    import online_softmax_flashattention_gb300 as fa
+    import seeded_inputs as si
+
+    out = {"timing": f"CUDA graph of {launches} calls replayed, CUDA events around the replay, best of 5 replays "
+                     "(inputs L2-resident)", "dtype": "f32", "d": 64}
+    for i, (name, B, H, N, causal) in enumerate(SMALL):
+        q, k, v = si.qkv(SEED + 41 + i, B, H, N, 64, "f32")
+        qd, kd, vd = (torch.from_numpy(x).to(dev) for x in (q, k, v))
+        od = torch.empty_like(qd)
+        for _ in range(warmup):
+            fa.attn_fwd(qd, kd, vd, causal=causal, out=od)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(launches):
+            fa.attn_fwd(qd, kd, vd, causal=causal, out=od)
+        torch.cuda.synchronize(dev)
+        host_us = (time.perf_counter() - t0) / launches * 1e6
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=cap):
+            for _ in range(launches):
+                fa.attn_fwd(qd, kd, vd, causal=causal, out=od)
+        stream.wait_stream(cap)
+        best = None
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            t = e0.elapsed_time(e1) * 1e3 / launches
+            best = t if best is None else min(best, t)
+        if fa.attn_device_status(clear=True, device=dev) != 0:
+            raise RuntimeError("device-side timeout in the small-configuration leg")
+        del graph
+        us = best
+        flop = workload_flops(B, H, N, 64, causal)
+        leg = {"us_per_call": us, "value": flop / (us * 1e-6) / 1e12 if N > 1 else None, "unit": UNIT,
+               "algorithmic_flop": flop, "host_wall_us_per_call": host_us}
+        if with_cpu:
+            import oracle
+
+            t0 = time.perf_counter()
+            ref = oracle.attn_fwd(q, k, v, causal, threads=oracle.default_threads())
+            secs = time.perf_counter() - t0
+            got = od.double().cpu().numpy()
+            err = float(np.max(np.abs(got - ref)))
+            tol = 1e-5 * N * float(np.max(np.abs(ref)))
+            leg["parity"] = {"rows_checked": B * H * N, "max_abs_err": err, "tolerance": tol, "pass": bool(err <= tol)}
+            if i == 0:
+                t0 = time.perf_counter()
+                oracle.attn_fwd(q, k, v, causal, threads=1)
+                one = time.perf_counter() - t0
+                leg["cpu_oracle_us"] = {"one_thread": one * 1e6, "all_threads": secs * 1e6,
+                                        "threads": oracle.default_threads()}
+        out[name] = leg
+    return out
+
+
 def fp32_leg(dev, stream, flush, steps, warmup, with_cpu):
     """The FFMA forward (dtype float32) on attention.cu's largest case, one head of N = 4096,
     causal and not: per-launch CUDA events with the L2 flushed between launches, TFLOP/s as a
@@ -833,9 +914,10 @@ def run_ours(args, rank, world, local):
                                  "peak_source": "measured bf16 dense (burst)"}}
         del dout, ob, lse
 
-    decode = decode8 = wide = fp32 = long_ctx = None
+    decode = decode8 = wide = fp32 = long_ctx = small = None
     if rank == 0 and not args.no_ablation:
         fp32 = fp32_leg(dev, stream, flush, 20, args.warmup, not args.no_cpu_baseline)
+        small = small_configs_leg(dev, stream, 50, args.warmup, not args.no_cpu_baseline)
         long_ctx = long_context_leg(dev, stream, flush, not args.no_cpu_baseline)
         decode = decode_leg(dev, stream, 50, args.warmup, not args.no_cpu_baseline, min(args.cpu_seconds, 10.0))
         decode8 = decode_leg(dev, stream, 50, args.warmup, not args.no_cpu_baseline, min(args.cpu_seconds, 5.0),
@@ -903,6 +985,7 @@ def run_ours(args, rank, world, local):
         "decode_nq8": decode8,
         "d128": wide,
         "fp32": fp32,
+        "small_configs": small,
         "long_context": long_ctx,
         "launch_ms": {"min": min(launch_ms), "median": statistics.median(launch_ms), "max": max(launch_ms)},
     }
