@@ -15,6 +15,7 @@ Build with ``python -m online_softmax_flashattention_gb300.build`` (or
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -59,6 +60,8 @@ def library_path() -> str:
 def raw():
     """The loaded ctypes library, with argument types declared (for C-ABI level tests)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(_LIB_PATH):
@@ -160,10 +163,25 @@ def _check(q, k, v):
         raise ValueError("q, k, v must be on one device")
 
 
+# The current stream's handle without building a Stream object (PyTorch's own raw accessor);
+# the public call when a build of PyTorch lacks it.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(dev, stream):
     if stream is None:
+        if _raw_stream is not None:
+            return ctypes.c_void_p(_raw_stream(dev.index if dev.index is not None else torch.cuda.current_device()))
         stream = torch.cuda.current_stream(dev)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _device(dev):
+    """The tensors' device made current for the call (the library launches on the current
+    device); no switch when it already is."""
+    if dev.index is None or dev.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(dev)
 
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
@@ -176,7 +194,7 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
         raise ValueError("out must be a contiguous tensor like q")
     B, H, N, d = q.shape
     lib = raw()
-    with torch.cuda.device(q.device):
+    with _device(q.device):
         st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, d,
                           int(bool(causal)), _DTYPES[q.dtype], _stream(q.device, stream))
     if st != 0:
@@ -200,7 +218,7 @@ def attn_fwd_lse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool
     elif lse.shape != (B, H, N) or lse.dtype != torch.float32 or lse.device != q.device or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 tensor [B, H, N] on q's device")
     lib = raw()
-    with torch.cuda.device(q.device):
+    with _device(q.device):
         st = lib.attn_fwd_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                               B, H, N, d, int(bool(causal)), _DTYPES[q.dtype], _stream(q.device, stream))
     if st != 0:
@@ -223,7 +241,7 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
         raise ValueError("lse must be a contiguous float32 tensor [B, H, N] on q's device")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     lib = raw()
-    with torch.cuda.device(q.device):
+    with _device(q.device):
         st = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, int(bool(causal)),
                           _DTYPES[q.dtype], _stream(q.device, stream))
@@ -244,7 +262,7 @@ def attn_kvcache_workspace_bytes(B: int, H: int, Nq: int, Nk: int, num_splits: i
         if num_splits == 0 else None
     if dev is None:
         return int(raw().attn_kvcache_workspace_bytes(B, H, Nq, Nk, d, num_splits, _DTYPES[dtype]))
-    with torch.cuda.device(dev):
+    with _device(dev):
         return int(raw().attn_kvcache_workspace_bytes(B, H, Nq, Nk, d, num_splits, _DTYPES[dtype]))
 
 
@@ -282,7 +300,7 @@ def attn_fwd_kvcache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: 
                        or not lse.is_contiguous()):
         raise ValueError("lse must be a contiguous float32 tensor [B, H, Nq] on q's device")
     lib = raw()
-    with torch.cuda.device(q.device):
+    with _device(q.device):
         if workspace is None:
             need = int(lib.attn_kvcache_workspace_bytes(B, H, Nq, Nk, d, int(num_splits), _DTYPES[q.dtype]))
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
@@ -312,7 +330,7 @@ def attn_fwd_materialized(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cau
         workspace = torch.empty(max(1, attn_materialized_workspace_bytes(B, H, N)), dtype=torch.uint8,
                                 device=q.device)
     lib = raw()
-    with torch.cuda.device(q.device):
+    with _device(q.device):
         st = lib.attn_fwd_materialized(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                        B, H, N, d, int(bool(causal)), _DTYPES[q.dtype],
@@ -327,7 +345,7 @@ def attn_selftest_wait_timeout(timeout_ns: int = 1_000_000, stream: torch.cuda.S
     """Launches the library's timeout self-test: one warp whose only wait runs out after
     ``timeout_ns``; afterwards :func:`attn_device_status` reports ATTN_ERR_TIMEOUT (7)."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index or 0)
-    with torch.cuda.device(dev):
+    with _device(dev):
         st = raw().attn_selftest_wait_timeout(int(timeout_ns), _stream(dev, stream))
     if st != 0:
         raise AttnError(st, "attn_selftest_wait_timeout")
@@ -337,7 +355,7 @@ def attn_device_status(clear: bool = True, stream: torch.cuda.Stream | None = No
                        device: torch.device | int | None = None) -> int:
     """Synchronises the stream and returns ATTN_OK (0) or ATTN_ERR_TIMEOUT (7)."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index or 0)
-    with torch.cuda.device(dev):
+    with _device(dev):
         return int(raw().attn_device_status(_stream(dev, stream), int(bool(clear))))
 
 
@@ -361,7 +379,7 @@ def attn_fwd_materialized_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Ten
     vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     fn.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ci, ci, vp]
     fn.restype = ci
-    with torch.cuda.device(q.device):
+    with _device(q.device):
         st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, d, int(bool(causal)),
                 _DTYPES[q.dtype], _stream(q.device, stream))
     if st != 0:
