@@ -917,7 +917,10 @@ def run_ours(args, rank, world, local):
     decode = decode8 = wide = fp32 = long_ctx = small = None
     if rank == 0 and not args.no_ablation:
         fp32 = fp32_leg(dev, stream, flush, 20, args.warmup, not args.no_cpu_baseline)
-        small = small_configs_leg(dev, stream, 50, args.warmup, not args.no_cpu_baseline)
+        try:
+            small = small_configs_leg(dev, stream, 50, args.warmup, not args.no_cpu_baseline)
+        except RuntimeError as exc:  # a device-side timeout or a failed graph capture: reported, not fatal
+            small = {"error": str(exc)}
         long_ctx = long_context_leg(dev, stream, flush, not args.no_cpu_baseline)
         decode = decode_leg(dev, stream, 50, args.warmup, not args.no_cpu_baseline, min(args.cpu_seconds, 10.0))
         decode8 = decode_leg(dev, stream, 50, args.warmup, not args.no_cpu_baseline, min(args.cpu_seconds, 5.0),
